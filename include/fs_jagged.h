@@ -1,0 +1,233 @@
+/*
+ * fs_jagged.h -- C ABI of the GB300 (sm_103a) jagged index + embedding library.
+ *
+ * The library runs the data-parallel hot path of one FreeScale training
+ * iteration ("FreeScale: Distributed Training for Sequence Recommendation
+ * Models with Minimal Scaling Cost", arXiv 2604.24073) over n logical ranks
+ * held in one GPU's memory:
+ *
+ *   balance (FBS or VBS, §4.1)  ->  jagged sample permutation (Algorithm 1,
+ *   Stage III; §4.2 indexed permute)  ->  row-wise bucketize into shard-major
+ *   form (§3.2, Algorithm 2 line 8; §4.2 ranged dispatch)  ->  collision /
+ *   exclusive split between iterations t and t+1 (Algorithm 2 line 10)  ->
+ *   embedding gather into batch-major jagged output (Algorithm 2 lines 12
+ *   and 15; ranged combine)  ->  gradient segment-reduce + row update
+ *   (Algorithm 2 lines 7, 18 and 20).
+ *
+ * Conventions shared by every call:
+ *  - Pointers are DEVICE pointers owned by the caller unless stated otherwise.
+ *    Nothing is allocated, freed or synchronised inside a call; every call is
+ *    asynchronous on `stream` (NULL = the legacy default stream).
+ *  - Argument errors (bad sizes, NULL pointers, misalignment, workspace too
+ *    small) are found on the host and returned at once; nothing is launched.
+ *  - Data errors (an ID outside [0, num_rows), malformed offsets or
+ *    permutation, an output capacity that is too small, a bounded wait that
+ *    gave up) are written by the kernels into the caller's device word
+ *    `*err` (int32, first error wins; the caller zeroes it).  fs_check() reads
+ *    it.  After a data error the outputs of that call are unspecified, but
+ *    every write stays inside the buffers described here.
+ *  - Scratch memory comes from the caller: `ws` / `ws_bytes`, at least the
+ *    size the matching *_workspace_size() query returns, 256-byte aligned.
+ *  - Sizes of data-dependent outputs (list lengths, selected counts) stay on
+ *    the device; the host never needs them to launch the next call.
+ *  - Positions are int32: T (IDs per batch) must be < 2^31.
+ */
+#ifndef FS_JAGGED_H
+#define FS_JAGGED_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* fs_stream_t; /* same handle as cudaStream_t */
+
+typedef enum {
+  FS_OK = 0,
+  FS_ERR_INVALID_ARG = 1, /* host: bad size, NULL pointer, unsupported dim/dtype; device: bad length */
+  FS_ERR_ID_RANGE = 2,    /* device: an ID < 0 or >= num_rows */
+  FS_ERR_BAD_OFFSETS = 3, /* device: offsets not monotone / permutation entry out of range */
+  FS_ERR_CAPACITY = 4,    /* device: an output would exceed the capacity passed in */
+  FS_ERR_WORKSPACE = 5,   /* host: ws_bytes smaller than the workspace query */
+  FS_ERR_TIMEOUT = 6,     /* device: a bounded inter-block wait gave up (no hang) */
+  FS_ERR_CUDA = 7,        /* host: a CUDA runtime call or launch failed */
+  FS_ERR_ALIGNMENT = 8    /* host: a pointer is not aligned as documented */
+} fs_status;
+
+typedef enum { FS_F32 = 0, FS_BF16 = 1 } fs_dtype;
+typedef enum { FS_SGD = 0, FS_ROWWISE_ADAGRAD = 1 } fs_optim;
+typedef enum { FS_PHASE_ALL = 0, FS_PHASE_COLLISION = 1, FS_PHASE_EXCLUSIVE = 2 } fs_phase;
+
+/* ------------------------------------------------------------------------
+ * FBS partition -- FreeScale §4.1 (Partitioning Algorithms), FBS paragraph.
+ * Sorts the S samples by UIH length (ascending, ties by global index g, so the
+ * partition is deterministic as Algorithm 1 requires) and deals the sorted
+ * positions to the n ranks in snake order: sorted position p is in round
+ * rho = p / n at place k = p % n and goes to rank k (rho even) or n-1-k (rho
+ * odd); a rank lists its samples by round.  (The printed index list
+ * [i, 2n-i, 2n+i, 4n-i, ...] is this rule with an off-by-one.)  Every rank
+ * gets floor(S/n) or ceil(S/n) samples (exactly S/n when n divides S).
+ *   uih_len      [S]   int32, >= 0 (negative -> FS_ERR_INVALID_ARG in *err)
+ *   perm         [S]   int32 out: perm[new position] = g
+ *   rank_offsets [n+1] int64 out: rank r owns new positions [ro[r], ro[r+1])
+ * S in [0, 2^31), n >= 1.
+ * ---------------------------------------------------------------------- */
+size_t fs_balance_fbs_workspace_size(int64_t S, int32_t n);
+fs_status fs_balance_fbs(const int32_t* uih_len, int64_t S, int32_t n, int32_t* perm, int64_t* rank_offsets,
+                         int32_t* err, void* ws, size_t ws_bytes, fs_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * VBS partition -- FreeScale §4.1, VBS paragraph.  Sample weight L^alpha,
+ * kept in fixed point w = round_half_even(256 * L^alpha) (uint64; L^alpha is
+ * L*sqrt(L) for alpha = 1.5 and the matching exact products for alpha in
+ * {0.5, 1, 2, 2.5, 3}, pow() otherwise).  The order is the (L, g)-sorted order
+ * when sort_by_len != 0 ("partitions globally sorted samples"), else the
+ * original rank-major order.  With P_j the exclusive prefix of the weights
+ * along that order and W their total, sample j goes to rank
+ * min(n-1, floor(n * P_j / W)); segments are contiguous and may be empty, and
+ * the heaviest weighs at most W/n + max w.  If W = 0 the rank is
+ * min(n-1, floor(n * j / S)).
+ *   perm       [S]   int32 out: the order; rank r owns [ro[r], ro[r+1])
+ *   seg_weight [n]   uint64 out: sum of w over rank r
+ * S * max(w) must stay below 2^62 (else FS_ERR_INVALID_ARG in *err).
+ * ---------------------------------------------------------------------- */
+size_t fs_balance_vbs_workspace_size(int64_t S, int32_t n);
+fs_status fs_balance_vbs(const int32_t* uih_len, int64_t S, int32_t n, double alpha, int32_t sort_by_len,
+                         int32_t* perm, int64_t* rank_offsets, uint64_t* seg_weight, int32_t* err, void* ws,
+                         size_t ws_bytes, fs_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Jagged sample permutation ("indexed permute") -- FreeScale Algorithm 1
+ * Stage III (shuffle samples to match the partition) and §4.2.  Output sample
+ * k is input sample perm[k] with all its IDs ([UIH | candidates]):
+ *   out_offsets[k+1] - out_offsets[k] = offsets[perm[k]+1] - offsets[perm[k]]
+ *   out_values[out_offsets[k] + i]    = values[offsets[perm[k]] + i]
+ *   offsets     [S+1] int64, offsets[0] = 0, non-decreasing
+ *   values      [offsets[S]] int64
+ *   perm        [S]   int32 in [0, S)
+ *   out_offsets [S+1] int64 out
+ *   out_values  [capacity] int64 out; offsets[S] > capacity -> FS_ERR_CAPACITY
+ * Optional (rank_offsets != NULL): rank_id_offsets[r] = out_offsets[rank_offsets[r]]
+ * for r = 0..n, the ID range of each destination rank (input of the bucketize).
+ * ---------------------------------------------------------------------- */
+size_t fs_permute_jagged_workspace_size(int64_t S);
+fs_status fs_permute_jagged(const int64_t* offsets, const int64_t* values, int64_t S, const int32_t* perm,
+                            int64_t* out_offsets, int64_t* out_values, int64_t capacity,
+                            const int64_t* rank_offsets, int32_t n, int64_t* rank_id_offsets, int32_t* err,
+                            void* ws, size_t ws_bytes, fs_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Row-wise bucketize ("ranged dispatch") -- FreeScale §3.2 (batch-major and
+ * shard-major forms), Algorithm 2 line 8, §4.2.  The table of num_rows rows is
+ * row-wise sharded into n ranges of block = ceil(num_rows / n) rows; ID x
+ * belongs to shard x / block.  Shard-major order is the stable sort of the
+ * batch-major positions by shard (inside a shard: source rank, then position).
+ *   ids             [T]   int64 batch-major, in [0, num_rows)
+ *   rank_id_offsets [n+1] int64: source rank r owns positions [rio[r], rio[r+1]),
+ *                         rio[0] = 0, rio[n] = T
+ *   sm_ids          [T]   int64 out: shard-major IDs
+ *   pos             [T]   int32 out: batch-major position of shard-major entry j
+ *   splits          [n*n] int64 out: splits[r*n + s] = IDs of source rank r in shard s
+ *                         (the AllToAll send splits)
+ *   shard_offsets   [n+1] int64 out
+ * n in [1, 512].
+ * ---------------------------------------------------------------------- */
+size_t fs_bucketize_rowwise_workspace_size(int64_t T, int32_t n);
+fs_status fs_bucketize_rowwise(const int64_t* ids, int64_t T, const int64_t* rank_id_offsets, int32_t n,
+                               int64_t num_rows, int64_t* sm_ids, int32_t* pos, int64_t* splits,
+                               int64_t* shard_offsets, int32_t* err, void* ws, size_t ws_bytes,
+                               fs_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Collision / exclusive split -- FreeScale Algorithm 2 line 10
+ * (compute_collision) and the notation paragraph after Algorithm 2: a
+ * collision row is used by both iteration t and t+1, an exclusive row by one
+ * of them.  Sets are of rows, so the result does not depend on whether the
+ * inputs are given batch-major or shard-major.
+ *   co      = uniq(ids_t) & uniq(ids_next)    ascending int64
+ *   ex_t    = uniq(ids_t) - uniq(ids_next)    ascending int64
+ *   ex_next = uniq(ids_next) - uniq(ids_t)    ascending int64
+ *   counts  [3] int64 out: |co|, |ex_t|, |ex_next|; a list longer than cap_rows
+ *           sets FS_ERR_CAPACITY and is truncated
+ *   *_shard_off [n+1] int64 out: list entries below k * ceil(num_rows/n)
+ *   is_co_t [T_t], is_co_next [T_next] uint8 out, aligned with the inputs:
+ *           1 when that entry's row is a collision row, else 0
+ * num_rows < 2^32.
+ * ---------------------------------------------------------------------- */
+size_t fs_collision_split_workspace_size(int64_t T_t, int64_t T_next, int64_t num_rows, int32_t n);
+fs_status fs_collision_split(const int64_t* ids_t, int64_t T_t, const int64_t* ids_next, int64_t T_next,
+                             int64_t num_rows, int32_t n, int64_t* co, int64_t* ex_t, int64_t* ex_next,
+                             int64_t cap_rows, int64_t* counts, int64_t* co_shard_off, int64_t* ex_t_shard_off,
+                             int64_t* ex_next_shard_off, uint8_t* is_co_t, uint8_t* is_co_next, int32_t* err,
+                             void* ws, size_t ws_bytes, fs_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Embedding gather -- FreeScale Algorithm 2 line 12 (Lookup, then back to
+ * batch-major: the ranged combine is fused, rows land directly at their
+ * batch-major position) and line 15 (merge of the prefetched exclusive rows
+ * and the collision rows into one batch); §2.1 (an ID list becomes a
+ * sequence of embeddings, no pooling).
+ *   out[p, :] = table[ids[p], :]  (a byte copy of one row)
+ * With mask != NULL only positions p with mask[p] == sel are written; the
+ * other rows of out are left untouched.
+ *   table [num_rows, dim] of dtype, row-major;  out [T, dim] of dtype.
+ * Row bytes must be a multiple of 4; multiples of 16 with 16-byte aligned
+ * table and out take the vector path.
+ * ---------------------------------------------------------------------- */
+fs_status fs_emb_gather(const void* table, int64_t num_rows, int32_t dim, fs_dtype dtype, const int64_t* ids,
+                        int64_t T, const uint8_t* mask, uint8_t sel, void* out, int32_t* err,
+                        fs_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Embedding backward: gradient segment-reduce per row + row update --
+ * FreeScale Algorithm 2 lines 7 and 20 (update_embedding on the exclusive and
+ * the collision rows) and line 18 (split of the gradients).  The pages name
+ * no optimizer; this implements
+ *   g_r = sum of grads[p] over positions p with ids[p] = r selected by phase
+ *         (fp32 accumulation in a fixed order: the result is identical run to run)
+ *   FS_SGD:             W_r -= lr * g_r
+ *   FS_ROWWISE_ADAGRAD: s_r += mean_d(g_{r,d}^2);  W_r -= lr * g_r / (sqrt(s_r) + eps)
+ * bf16 tables read bf16 grads, accumulate in fp32 and store round-to-nearest-
+ * even.  phase selects positions: ALL every position, COLLISION those with
+ * is_co[p] == 1, EXCLUSIVE those with is_co[p] == 0.  Collision is a property
+ * of the row, so COLLISION then EXCLUSIVE updates every row of the batch once,
+ * collision rows first.
+ *   table [num_rows, dim] in place;  state [num_rows] fp32 in place (NULL for SGD)
+ *   ids [T] int64;  grads [T, dim] of dtype (batch-major);  is_co [T] (NULL for ALL)
+ * Supported: dim in {32, 64, 128} (fp32) or {32, 64, 128, 256} (bf16);
+ * num_rows < 2^32.
+ * ---------------------------------------------------------------------- */
+size_t fs_emb_backward_adagrad_workspace_size(int64_t T, int64_t num_rows, int32_t dim, fs_dtype dtype);
+fs_status fs_emb_backward_adagrad(void* table, float* state, int64_t num_rows, int32_t dim, fs_dtype dtype,
+                                  fs_optim optim, const int64_t* ids, const void* grads, int64_t T,
+                                  const uint8_t* is_co, fs_phase phase, float lr, float eps, int32_t* err,
+                                  void* ws, size_t ws_bytes, fs_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Utilities.
+ * fs_check: waits for `stream`, then returns the code in *err (FS_OK if 0),
+ *   or FS_ERR_CUDA if the stream reports an error.  Host-synchronous: meant for
+ *   tests and benchmarks, not for the hot loop.
+ * fs_set_spin_limit: polls before a bounded inter-block wait gives up with
+ *   FS_ERR_TIMEOUT (default 1<<22, roughly a second).  Applies to later calls.
+ * fs_launch_count: kernels this library has launched in this process.
+ * fs_debug_skip_publish: test hook for the bounded waits.  Tile `tile` of the
+ *   single-pass scans (VBS weights, permute offsets, collision compaction)
+ *   skips publishing its look-back status, so every later tile's wait runs out
+ *   and the call reports FS_ERR_TIMEOUT instead of hanging.  -1 (the default)
+ *   turns it off.  Never used outside tests.
+ * ---------------------------------------------------------------------- */
+fs_status fs_check(const int32_t* err, fs_stream_t stream);
+const char* fs_status_string(fs_status s);
+void fs_set_spin_limit(int64_t polls);
+void fs_debug_skip_publish(int64_t tile);
+int64_t fs_launch_count(void);
+const char* fs_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FS_JAGGED_H */

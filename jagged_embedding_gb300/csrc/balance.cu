@@ -1,0 +1,274 @@
+// Sequence load balancing: FBS and VBS partitions.
+// FreeScale (arXiv 2604.24073) §4.1 "Partitioning Algorithms"; §3.1 /
+// Algorithm 1 (a deterministic partition function over the gathered lengths).
+//
+// Both partitions start from the samples ordered by (UIH length, global
+// index): a stable LSD radix sort of the lengths with the index as value
+// (onesweep passes).  FBS then deals sorted positions to ranks in snake order
+// with a closed form per position; VBS scans fixed-point weights L^alpha with
+// a single-pass decoupled look-back scan and cuts the prefix into n segments.
+#include "onesweep.cuh"
+
+namespace fs {
+namespace {
+
+using onesweep::kThreads;
+
+// Length array as a sort source: key = L[g] (negative lengths flagged), value = g.
+struct SrcLen {
+  using Key = uint32_t;
+  const int32_t* L;
+  __device__ __forceinline__ bool load(int64_t i, Key& key, uint32_t& val, int32_t* err) const {
+    int32_t l = L[i];
+    if (l < 0) {
+      if (err) set_err(err, FS_ERR_INVALID_ARG);
+      l = 0;
+    }
+    key = static_cast<uint32_t>(l);
+    val = static_cast<uint32_t>(i);
+    return true;
+  }
+  __device__ __forceinline__ uint32_t digit(Key key, int shift, int bits) const {
+    return (key >> shift) & ((1u << bits) - 1u);
+  }
+};
+
+// rank_offsets of the snake deal: F = S / n full rounds, rem = S % n samples in
+// the last round, dealt left to right when F is even, right to left when odd.
+__device__ __forceinline__ int64_t fbs_rank_offset(int64_t r, int64_t S, int64_t n) {
+  const int64_t F = S / n, rem = S % n;
+  int64_t extra_before;
+  if ((F & 1) == 0) {
+    extra_before = r < rem ? r : rem;                      // ranks 0..rem-1 get one more
+  } else {
+    int64_t first = n - rem;                               // ranks n-rem..n-1 get one more
+    extra_before = r > first ? r - first : 0;
+  }
+  return r * F + extra_before;
+}
+
+__global__ void fbs_assign_kernel(const uint32_t* sorted_g, int64_t S, int32_t n, int32_t* perm,
+                                  int64_t* rank_offsets) {
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  for (int64_t p = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; p < S; p += stride) {
+    const int64_t rho = p / n, k = p % n;
+    const int64_t r = (rho & 1) ? (n - 1 - k) : k;
+    perm[fbs_rank_offset(r, S, n) + rho] = static_cast<int32_t>(sorted_g[p]);
+  }
+  for (int64_t r = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; r <= n; r += stride)
+    rank_offsets[r] = fbs_rank_offset(r, S, n);
+}
+
+// ------------------------------------------------------------------- VBS
+
+// Fixed-point weight round_half_even(256 * L^alpha); L^alpha evaluated with
+// IEEE-exact operations where alpha allows (a product of L's and at most one
+// correctly rounded square root), pow() otherwise.
+__device__ __forceinline__ uint64_t vbs_weight(int32_t L, double alpha) {
+  const double x = static_cast<double>(L < 0 ? 0 : L);
+  double p;
+  if (alpha == 1.0) {
+    p = x;
+  } else if (alpha == 1.5) {
+    p = __dmul_rn(x, __dsqrt_rn(x));
+  } else if (alpha == 2.0) {
+    p = __dmul_rn(x, x);
+  } else if (alpha == 0.5) {
+    p = __dsqrt_rn(x);
+  } else if (alpha == 2.5) {
+    p = __dmul_rn(__dmul_rn(x, x), __dsqrt_rn(x));
+  } else if (alpha == 3.0) {
+    p = __dmul_rn(__dmul_rn(x, x), x);
+  } else {
+    p = pow(x, alpha);
+  }
+  return static_cast<uint64_t>(rint(__dmul_rn(p, 256.0)));
+}
+
+constexpr int kVbsItems = 8;
+constexpr int kVbsTile = kThreads * kVbsItems;
+
+// Exclusive prefix of the weights along the order (order == nullptr: identity).
+// P[j] for j < S, P[S] = W.  Tiles claim their index dynamically.
+__global__ void __launch_bounds__(kThreads) vbs_scan_kernel(const int32_t* L, const uint32_t* order, int64_t S,
+                                                            double alpha, uint64_t* P, uint64_t* status,
+                                                            int* tile_counter, int32_t* err, int64_t limit,
+                                                            int64_t skip_tile) {
+  __shared__ uint64_t tmp[32];
+  __shared__ int64_t s_tile;
+  __shared__ uint64_t s_excl;
+  if (threadIdx.x == 0) s_tile = atomicAdd(tile_counter, 1);
+  __syncthreads();
+  const int64_t tile = s_tile;
+  const int64_t base = tile * kVbsTile + int64_t(threadIdx.x) * kVbsItems;
+  const uint64_t wmax = ((1ull << 62) - 1) / static_cast<uint64_t>(S > 0 ? S : 1);
+  uint64_t w[kVbsItems];
+  uint64_t sum = 0;
+#pragma unroll
+  for (int i = 0; i < kVbsItems; ++i) {
+    int64_t j = base + i;
+    w[i] = 0;
+    if (j < S) {
+      int64_t g = order ? int64_t(order[j]) : j;
+      int32_t l = L[g];
+      if (l < 0) set_err(err, FS_ERR_INVALID_ARG);
+      w[i] = vbs_weight(l, alpha);
+      if (w[i] > wmax) {
+        set_err(err, FS_ERR_INVALID_ARG);
+        w[i] = 0;
+      }
+    }
+    sum += w[i];
+  }
+  uint64_t tot;
+  uint64_t ex = block_exclusive_scan<uint64_t>(sum, tmp, &tot);
+  if (tile == skip_tile) return;  // test hook: this tile never publishes
+  if (threadIdx.x < 32) {
+    uint64_t e = warp_lookback(status, 1, tile, tot, err, limit);
+    if (threadIdx.x == 0) s_excl = e;
+  }
+  __syncthreads();
+  uint64_t run = s_excl + ex;
+#pragma unroll
+  for (int i = 0; i < kVbsItems; ++i) {
+    int64_t j = base + i;
+    if (j < S) P[j] = run;
+    run += w[i];
+    if (j == S - 1) P[S] = run;
+  }
+}
+
+__device__ __forceinline__ int64_t vbs_rank(uint64_t Pj, uint64_t W, int64_t j, int64_t S, int64_t n) {
+  int64_t r;
+  if (W == 0) {
+    r = static_cast<int64_t>((static_cast<unsigned __int128>(j) * static_cast<unsigned __int128>(n)) /
+                             static_cast<unsigned __int128>(S));
+  } else {
+    r = static_cast<int64_t>((static_cast<unsigned __int128>(Pj) * static_cast<unsigned __int128>(n)) /
+                             static_cast<unsigned __int128>(W));
+  }
+  return r > n - 1 ? n - 1 : r;
+}
+
+__global__ void vbs_assign_kernel(const uint32_t* order, const uint64_t* P, int64_t S, int32_t n, int32_t* perm,
+                                  int64_t* rank_offsets) {
+  const uint64_t W = P[S];
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  for (int64_t j = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; j < S; j += stride) {
+    perm[j] = order ? static_cast<int32_t>(order[j]) : static_cast<int32_t>(j);
+    const int64_t r = vbs_rank(P[j], W, j, S, n);
+    const int64_t rp = (j == 0) ? -1 : vbs_rank(P[j - 1], W, j - 1, S, n);
+    for (int64_t q = rp + 1; q <= r; ++q) rank_offsets[q] = j;  // first sample of ranks rp+1..r
+    if (j == S - 1)
+      for (int64_t q = r + 1; q <= n; ++q) rank_offsets[q] = S;
+  }
+}
+
+__global__ void vbs_segment_weight_kernel(const uint64_t* P, const int64_t* rank_offsets, int32_t n,
+                                          uint64_t* seg_weight) {
+  for (int64_t r = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; r < n; r += int64_t(gridDim.x) * blockDim.x)
+    seg_weight[r] = P[rank_offsets[r + 1]] - P[rank_offsets[r]];
+}
+
+__global__ void fill_i64_kernel(int64_t* p, int64_t count, int64_t v) {
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < count; i += int64_t(gridDim.x) * blockDim.x)
+    p[i] = v;
+}
+
+unsigned grid_for(int64_t items, int per_block = kThreads) {
+  int64_t g = (items + per_block - 1) / per_block;
+  int64_t cap = int64_t(sm_count()) * 8;
+  if (g > cap) g = cap;
+  return unsigned(g < 1 ? 1 : g);
+}
+
+constexpr int kLenKeyBits = 31;  // int32 lengths >= 0
+
+size_t vbs_extra_bytes(int64_t S) {
+  int64_t tiles = (S + kVbsTile - 1) / kVbsTile;
+  return align_up(size_t(S + 1) * sizeof(uint64_t)) + align_up(size_t(tiles) * sizeof(uint64_t) + 256);
+}
+
+}  // namespace
+}  // namespace fs
+
+using namespace fs;
+
+extern "C" size_t fs_balance_fbs_workspace_size(int64_t S, int32_t n) {
+  (void)n;
+  if (S < 0) return 0;
+  return onesweep::SortPlan(S, kLenKeyBits).bytes() + 256;
+}
+
+extern "C" fs_status fs_balance_fbs(const int32_t* uih_len, int64_t S, int32_t n, int32_t* perm,
+                                    int64_t* rank_offsets, int32_t* err, void* ws, size_t ws_bytes,
+                                    fs_stream_t stream) {
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (n < 1 || S < 0 || S > INT32_MAX || !rank_offsets || !err) return FS_ERR_INVALID_ARG;
+  if (S > 0 && (!uih_len || !perm)) return FS_ERR_INVALID_ARG;
+  if (!aligned(rank_offsets, 8) || !aligned(err, 4)) return FS_ERR_ALIGNMENT;
+  if (ws_bytes < fs_balance_fbs_workspace_size(S, n) || (S > 0 && !ws)) return FS_ERR_WORKSPACE;
+  int launches = 0;
+  if (S == 0) {
+    fill_i64_kernel<<<1, kThreads, 0, st>>>(rank_offsets, int64_t(n) + 1, 0);
+    count_launch(1);
+    return launch_status();
+  }
+  onesweep::SortPlan P(S, kLenKeyBits);
+  WsCursor cur(ws, ws_bytes);
+  onesweep::SortWs W;
+  if (!onesweep::carve_sort_ws(P, cur, W)) return FS_ERR_WORKSPACE;
+  uint32_t *sk = nullptr, *sv = nullptr;
+  fs_status s = onesweep::run_sort(SrcLen{uih_len}, P, W, err, st, &sk, &sv, &launches);
+  if (s != FS_OK) return s;
+  fbs_assign_kernel<<<grid_for(S > n ? S : n + 1), kThreads, 0, st>>>(sv, S, n, perm, rank_offsets);
+  count_launch(launches + 1);
+  return launch_status();
+}
+
+extern "C" size_t fs_balance_vbs_workspace_size(int64_t S, int32_t n) {
+  return fs_balance_fbs_workspace_size(S, n) + vbs_extra_bytes(S) + 256;
+}
+
+extern "C" fs_status fs_balance_vbs(const int32_t* uih_len, int64_t S, int32_t n, double alpha, int32_t sort_by_len,
+                                    int32_t* perm, int64_t* rank_offsets, uint64_t* seg_weight, int32_t* err,
+                                    void* ws, size_t ws_bytes, fs_stream_t stream) {
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (n < 1 || S < 0 || S > INT32_MAX || !rank_offsets || !err || !seg_weight || !(alpha >= 0.0))
+    return FS_ERR_INVALID_ARG;
+  if (S > 0 && (!uih_len || !perm)) return FS_ERR_INVALID_ARG;
+  if (!aligned(rank_offsets, 8) || !aligned(seg_weight, 8) || !aligned(err, 4)) return FS_ERR_ALIGNMENT;
+  if (ws_bytes < fs_balance_vbs_workspace_size(S, n) || (S > 0 && !ws)) return FS_ERR_WORKSPACE;
+  if (S == 0) {
+    fill_i64_kernel<<<1, kThreads, 0, st>>>(rank_offsets, int64_t(n) + 1, 0);
+    fill_i64_kernel<<<1, kThreads, 0, st>>>(reinterpret_cast<int64_t*>(seg_weight), n, 0);
+    count_launch(2);
+    return launch_status();
+  }
+  int launches = 0;
+  WsCursor cur(ws, ws_bytes);
+  const int64_t vtiles = (S + kVbsTile - 1) / kVbsTile;
+  uint64_t* P = cur.take<uint64_t>(size_t(S + 1));
+  unsigned char* vzero = cur.take<unsigned char>(size_t(vtiles) * sizeof(uint64_t) + 256);
+  if (!cur.ok) return FS_ERR_WORKSPACE;
+  uint64_t* vstatus = reinterpret_cast<uint64_t*>(vzero + 256);
+  int* vcounter = reinterpret_cast<int*>(vzero);
+  if (cudaMemsetAsync(vzero, 0, size_t(vtiles) * sizeof(uint64_t) + 256, st) != cudaSuccess) return FS_ERR_CUDA;
+
+  const uint32_t* order = nullptr;
+  if (sort_by_len) {
+    onesweep::SortPlan SP(S, kLenKeyBits);
+    onesweep::SortWs W;
+    if (!onesweep::carve_sort_ws(SP, cur, W)) return FS_ERR_WORKSPACE;
+    uint32_t *sk = nullptr, *sv = nullptr;
+    fs_status s = onesweep::run_sort(SrcLen{uih_len}, SP, W, err, st, &sk, &sv, &launches);
+    if (s != FS_OK) return s;
+    order = sv;
+  }
+  vbs_scan_kernel<<<unsigned(vtiles), kThreads, 0, st>>>(uih_len, order, S, alpha, P, vstatus, vcounter, err,
+                                                         spin_limit(), debug_skip_tile());
+  vbs_assign_kernel<<<grid_for(S), kThreads, 0, st>>>(order, P, S, n, perm, rank_offsets);
+  vbs_segment_weight_kernel<<<grid_for(n), kThreads, 0, st>>>(P, rank_offsets, n, seg_weight);
+  count_launch(launches + 3);
+  return launch_status();
+}

@@ -1,0 +1,220 @@
+// Collision / exclusive row split between consecutive iterations.
+// FreeScale (arXiv 2604.24073) Algorithm 2 line 10 (compute_collision on the
+// shard-major I^i, I^{i+1}) and the notation paragraph after Algorithm 2.
+//
+// Rows are sets, so the split is computed on two presence bitmaps over the
+// num_rows rows (R/8 bytes each: 12.5 MB for 100M rows, resident in the 129 MB
+// L2):
+//   1. mark: one pass over each ID array sets the row's bit (a load of the
+//      bitmap word first, so hot rows that are already marked cost no atomic);
+//   2. compact: one pass over the bitmap words with a decoupled look-back
+//      scan of three popcounts (co = A&B, ex_t = A&~B, ex_next = B&~A); rows
+//      come out ascending, i.e. shard-major, and the shard offsets fall out of
+//      the same scan;
+//   3. masks: one pass over each ID array tests the other iteration's bitmap.
+#include "fs_common.cuh"
+
+namespace fs {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWordsPerThread = 8;
+constexpr int kWordsPerTile = kThreads * kWordsPerThread;
+
+__global__ void __launch_bounds__(kThreads) mark_kernel(const int64_t* ids_t, int64_t T_t, const int64_t* ids_next,
+                                                        int64_t T_next, int64_t R, uint32_t* bm_t, uint32_t* bm_next,
+                                                        int32_t* err) {
+  const int64_t total = T_t + T_next;
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += stride) {
+    const bool first = i < T_t;
+    const int64_t id = first ? __ldcs(ids_t + i) : __ldcs(ids_next + (i - T_t));
+    if (id < 0 || id >= R) {
+      set_err(err, FS_ERR_ID_RANGE);
+      continue;
+    }
+    uint32_t* bm = first ? bm_t : bm_next;
+    const uint64_t w = uint64_t(id) >> 5;
+    const uint32_t bit = 1u << (uint32_t(id) & 31u);
+    if ((bm[w] & bit) == 0) atomicOr(bm + w, bit);
+  }
+}
+
+// Three counters packed in one 64-bit word, 21 bits each (a tile holds at most
+// kWordsPerTile * 32 = 65536 rows per counter).
+__device__ __forceinline__ uint64_t pack3(uint32_t a, uint32_t b, uint32_t c) {
+  return uint64_t(a) | (uint64_t(b) << 21) | (uint64_t(c) << 42);
+}
+__device__ __forceinline__ uint32_t unpack3(uint64_t v, int k) { return uint32_t((v >> (21 * k)) & 0x1FFFFFu); }
+
+__global__ void __launch_bounds__(kThreads) compact_kernel(const uint32_t* bm_t, const uint32_t* bm_next, int64_t nwords,
+                                                           int64_t R, int32_t n, int64_t block, int64_t* co,
+                                                           int64_t* ex_t, int64_t* ex_next, int64_t cap,
+                                                           int64_t* counts, int64_t* co_off, int64_t* ex_t_off,
+                                                           int64_t* ex_next_off, uint64_t* status, int* tile_counter,
+                                                           int32_t* err, int64_t limit, int64_t skip_tile) {
+  __shared__ uint64_t tmp[32];
+  __shared__ int64_t s_tile;
+  __shared__ int64_t s_excl[3];
+  if (threadIdx.x == 0) s_tile = atomicAdd(tile_counter, 1);
+  __syncthreads();
+  const int64_t tile = s_tile;
+  const int64_t w0 = tile * kWordsPerTile + int64_t(threadIdx.x) * kWordsPerThread;
+  uint32_t m[3][kWordsPerThread];
+  uint32_t c[3] = {0, 0, 0};
+#pragma unroll
+  for (int i = 0; i < kWordsPerThread; ++i) {
+    const int64_t w = w0 + i;
+    uint32_t a = 0, b = 0;
+    if (w < nwords) {
+      a = bm_t[w];
+      b = bm_next[w];
+    }
+    m[0][i] = a & b;
+    m[1][i] = a & ~b;
+    m[2][i] = b & ~a;
+#pragma unroll
+    for (int k = 0; k < 3; ++k) c[k] += __popc(m[k][i]);
+  }
+  uint64_t tot;
+  uint64_t ex = block_exclusive_scan<uint64_t>(pack3(c[0], c[1], c[2]), tmp, &tot);
+  if (tile == skip_tile) return;  // test hook: this tile never publishes
+  const int warp = threadIdx.x >> 5;
+  if (warp < 3) {
+    uint64_t e = warp_lookback(status + warp, 3, tile, unpack3(tot, warp), err, limit);
+    if ((threadIdx.x & 31) == 0) s_excl[warp] = int64_t(e);
+  }
+  __syncthreads();
+  int64_t* lists[3] = {co, ex_t, ex_next};
+  int64_t* offs[3] = {co_off, ex_t_off, ex_next_off};
+  const int64_t last_word = nwords - 1;
+#pragma unroll
+  for (int k = 0; k < 3; ++k) {
+    int64_t at = s_excl[k] + int64_t(unpack3(ex, k));
+    for (int i = 0; i < kWordsPerThread; ++i) {
+      const int64_t w = w0 + i;
+      if (w >= nwords) break;
+      uint32_t bits = m[k][i];
+      // shard boundaries k_s * block that fall inside this word (rows < R)
+      const int64_t row0 = w * 32;
+      int64_t s_lo = (row0 + block - 1) / block;
+      for (int64_t s = s_lo; s <= n && s * block < row0 + 32 && s * block < R; ++s) {
+        const uint32_t below = uint32_t(s * block - row0);
+        offs[k][s] = at + __popc(bits & ((below == 0) ? 0u : (0xFFFFFFFFu >> (32 - below))));
+      }
+      while (bits) {
+        const int b = __ffs(bits) - 1;
+        bits &= bits - 1;
+        if (at < cap) lists[k][at] = row0 + b;
+        ++at;
+      }
+      if (w == last_word) {
+        counts[k] = at;
+        if (at > cap) set_err(err, FS_ERR_CAPACITY);
+        // boundaries at or beyond R hold the full list length
+        int64_t s_first = (R + block - 1) / block;
+        for (int64_t s = s_first; s <= n; ++s) offs[k][s] = at;
+      }
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) mask_kernel(const int64_t* ids_t, int64_t T_t, const int64_t* ids_next,
+                                                        int64_t T_next, int64_t R, const uint32_t* bm_t,
+                                                        const uint32_t* bm_next, uint8_t* is_co_t,
+                                                        uint8_t* is_co_next) {
+  const int64_t total = T_t + T_next;
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += stride) {
+    const bool first = i < T_t;
+    const int64_t j = first ? i : i - T_t;
+    const int64_t id = first ? __ldcs(ids_t + j) : __ldcs(ids_next + j);
+    const uint32_t* other = first ? bm_next : bm_t;
+    uint8_t v = 0;
+    if (id >= 0 && id < R) v = (__ldg(other + (uint64_t(id) >> 5)) >> (uint32_t(id) & 31u)) & 1u;
+    if (first) is_co_t[j] = v; else is_co_next[j] = v;
+  }
+}
+
+struct CollLayout {
+  int64_t nwords, tiles;
+  size_t bitmap_bytes() const { return align_up(size_t(nwords) * sizeof(uint32_t)); }
+  size_t zero_bytes() const { return 2 * bitmap_bytes() + align_up(size_t(tiles) * 3 * sizeof(uint64_t) + 256); }
+};
+
+CollLayout coll_layout(int64_t R) {
+  CollLayout L;
+  L.nwords = (R + 31) / 32;
+  L.tiles = (L.nwords + kWordsPerTile - 1) / kWordsPerTile;
+  if (L.tiles < 1) L.tiles = 1;
+  return L;
+}
+
+unsigned grid_for(int64_t items) {
+  int64_t g = (items + kThreads - 1) / kThreads, cap = int64_t(sm_count()) * 8;
+  if (g > cap) g = cap;
+  return unsigned(g < 1 ? 1 : g);
+}
+
+}  // namespace
+}  // namespace fs
+
+using namespace fs;
+
+extern "C" size_t fs_collision_split_workspace_size(int64_t T_t, int64_t T_next, int64_t num_rows, int32_t n) {
+  (void)T_t;
+  (void)T_next;
+  (void)n;
+  if (num_rows < 1) return 0;
+  return coll_layout(num_rows).zero_bytes() + 256;
+}
+
+extern "C" fs_status fs_collision_split(const int64_t* ids_t, int64_t T_t, const int64_t* ids_next, int64_t T_next,
+                                        int64_t num_rows, int32_t n, int64_t* co, int64_t* ex_t, int64_t* ex_next,
+                                        int64_t cap_rows, int64_t* counts, int64_t* co_shard_off,
+                                        int64_t* ex_t_shard_off, int64_t* ex_next_shard_off, uint8_t* is_co_t,
+                                        uint8_t* is_co_next, int32_t* err, void* ws, size_t ws_bytes,
+                                        fs_stream_t stream) {
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (T_t < 0 || T_next < 0 || T_t > INT32_MAX || T_next > INT32_MAX || num_rows < 1 ||
+      num_rows > (int64_t(1) << 32) || n < 1 || cap_rows < 0 || !counts || !co_shard_off || !ex_t_shard_off ||
+      !ex_next_shard_off || !err)
+    return FS_ERR_INVALID_ARG;
+  if ((T_t > 0 && (!ids_t || !is_co_t)) || (T_next > 0 && (!ids_next || !is_co_next))) return FS_ERR_INVALID_ARG;
+  if (cap_rows > 0 && (!co || !ex_t || !ex_next)) return FS_ERR_INVALID_ARG;
+  if ((ids_t && !aligned(ids_t, 8)) || (ids_next && !aligned(ids_next, 8)) || !aligned(counts, 8) ||
+      (co && !aligned(co, 8)) || (ex_t && !aligned(ex_t, 8)) || (ex_next && !aligned(ex_next, 8)))
+    return FS_ERR_ALIGNMENT;
+  if (ws_bytes < fs_collision_split_workspace_size(T_t, T_next, num_rows, n) || !ws) return FS_ERR_WORKSPACE;
+
+  CollLayout L = coll_layout(num_rows);
+  WsCursor cur(ws, ws_bytes);
+  unsigned char* zero = cur.take<unsigned char>(L.zero_bytes());
+  if (!cur.ok) return FS_ERR_WORKSPACE;
+  uint32_t* bm_t = reinterpret_cast<uint32_t*>(zero);
+  uint32_t* bm_next = reinterpret_cast<uint32_t*>(zero + L.bitmap_bytes());
+  unsigned char* tail = zero + 2 * L.bitmap_bytes();
+  int* counter = reinterpret_cast<int*>(tail);
+  uint64_t* status = reinterpret_cast<uint64_t*>(tail + 256);
+  if (cudaMemsetAsync(zero, 0, L.zero_bytes(), st) != cudaSuccess) return FS_ERR_CUDA;
+
+  const int64_t block = (num_rows + n - 1) / n;
+  int launches = 0;
+  if (T_t + T_next > 0) {
+    mark_kernel<<<grid_for(T_t + T_next), kThreads, 0, st>>>(ids_t, T_t, ids_next, T_next, num_rows, bm_t, bm_next,
+                                                             err);
+    ++launches;
+  }
+  compact_kernel<<<unsigned(L.tiles), kThreads, 0, st>>>(bm_t, bm_next, L.nwords, num_rows, n, block, co, ex_t,
+                                                         ex_next, cap_rows, counts, co_shard_off, ex_t_shard_off,
+                                                         ex_next_shard_off, status, counter, err, spin_limit(),
+                                                         debug_skip_tile());
+  ++launches;
+  if (T_t + T_next > 0) {
+    mask_kernel<<<grid_for(T_t + T_next), kThreads, 0, st>>>(ids_t, T_t, ids_next, T_next, num_rows, bm_t, bm_next,
+                                                             is_co_t, is_co_next);
+    ++launches;
+  }
+  count_launch(launches);
+  return launch_status();
+}

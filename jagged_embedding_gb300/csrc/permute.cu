@@ -1,0 +1,212 @@
+// Jagged sample permutation ("indexed permute").
+// FreeScale (arXiv 2604.24073) §3.1 Algorithm 1 Stage III (shuffle the samples
+// to the ranks the partition chose) and §4.2 (jagged kernels).  On one GPU
+// the AllToAll of Stage III is this device-memory permutation.
+//
+// Kernel 1 (one pass over the S samples): permuted lengths, their exclusive
+// scan (decoupled look-back) into out_offsets, the source start of each output
+// sample, and for every 4096-ID output tile the first sample that covers it.
+// Kernel 2 (one pass over the T IDs, ID-balanced): each block copies a fixed
+// 4096-ID window of the output, whatever the sample lengths (a 16K-ID sample
+// is spread over several blocks, so long samples do not straggle).
+#include "fs_common.cuh"
+
+namespace fs {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kScanItems = 8;
+constexpr int kScanTile = kThreads * kScanItems;
+constexpr int kCopyItems = 16;
+constexpr int kCopyTile = kThreads * kCopyItems;  // output IDs per copy tile
+
+__global__ void __launch_bounds__(kThreads) permute_scan_kernel(const int64_t* offsets, int64_t S, const int32_t* perm,
+                                                                int64_t* out_offsets, int64_t* src_start,
+                                                                int32_t* first_sample, int64_t n_copy_tiles,
+                                                                int64_t capacity, uint64_t* status, int* tile_counter,
+                                                                int32_t* err, int64_t limit, int64_t skip_tile) {
+  __shared__ int64_t tmp[32];
+  __shared__ int64_t s_tile;
+  __shared__ int64_t s_excl;
+  if (threadIdx.x == 0) s_tile = atomicAdd(tile_counter, 1);
+  __syncthreads();
+  const int64_t tile = s_tile;
+  const int64_t base = tile * kScanTile + int64_t(threadIdx.x) * kScanItems;
+  const int64_t total_in = offsets[S];
+  int64_t len[kScanItems], src[kScanItems];
+  int64_t sum = 0;
+#pragma unroll
+  for (int i = 0; i < kScanItems; ++i) {
+    const int64_t k = base + i;
+    len[i] = 0;
+    src[i] = 0;
+    if (k < S) {
+      int64_t g = perm[k];
+      if (g < 0 || g >= S) {
+        set_err(err, FS_ERR_BAD_OFFSETS);
+      } else {
+        int64_t a = offsets[g], b = offsets[g + 1];
+        if (b < a || a < 0 || b > total_in) {
+          set_err(err, FS_ERR_BAD_OFFSETS);
+        } else {
+          len[i] = b - a;
+          src[i] = a;
+        }
+      }
+    }
+    sum += len[i];
+  }
+  int64_t tot;
+  int64_t ex = block_exclusive_scan<int64_t>(sum, tmp, &tot);
+  if (tile == skip_tile) return;  // test hook: this tile never publishes
+  if (threadIdx.x < 32) {
+    uint64_t e = warp_lookback(status, 1, tile, static_cast<uint64_t>(tot), err, limit);
+    if (threadIdx.x == 0) s_excl = static_cast<int64_t>(e);
+  }
+  __syncthreads();
+  int64_t run = s_excl + ex;
+#pragma unroll
+  for (int i = 0; i < kScanItems; ++i) {
+    const int64_t k = base + i;
+    if (k < S) {
+      out_offsets[k] = run;
+      src_start[k] = src[i];
+      if (len[i] > 0) {
+        // output tiles whose first position falls inside this sample
+        int64_t t0 = (run + kCopyTile - 1) / kCopyTile;
+        int64_t t1 = (run + len[i] + kCopyTile - 1) / kCopyTile;
+        if (t1 > n_copy_tiles) t1 = n_copy_tiles;
+        for (int64_t t = t0; t < t1; ++t) first_sample[t] = static_cast<int32_t>(k);
+      }
+    }
+    run += len[i];
+    if (k == S - 1) {
+      out_offsets[S] = run;
+      if (run > capacity) set_err(err, FS_ERR_CAPACITY);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) permute_copy_kernel(const int64_t* values, const int64_t* out_offsets,
+                                                                const int64_t* src_start, const int32_t* first_sample,
+                                                                int64_t S, int64_t capacity, int64_t* out_values,
+                                                                const int64_t* rank_offsets, int32_t n,
+                                                                int64_t* rank_id_offsets, int32_t* err) {
+  if (rank_offsets && blockIdx.x == 0) {
+    for (int r = threadIdx.x; r <= n; r += blockDim.x) {
+      int64_t q = rank_offsets[r];
+      bool bad = q < 0 || q > S || (r > 0 && rank_offsets[r - 1] > q) || (r == 0 && q != 0) || (r == n && q != S);
+      if (bad) set_err(err, FS_ERR_BAD_OFFSETS);
+      rank_id_offsets[r] = out_offsets[bad ? (q < 0 ? 0 : (q > S ? S : q)) : q];
+    }
+  }
+  int64_t total = out_offsets[S];
+  if (total > capacity) total = capacity;
+  const int64_t ntiles = (total + kCopyTile - 1) / kCopyTile;
+  for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
+    const int64_t j0 = t * kCopyTile;
+    int64_t k = first_sample[t];
+    int64_t k_hi = (t + 1 < ntiles) ? int64_t(first_sample[t + 1]) : S - 1;  // last sample touching this tile
+    int64_t srcidx[kCopyItems];
+#pragma unroll
+    for (int i = 0; i < kCopyItems; ++i) {
+      const int64_t j = j0 + int64_t(i) * kThreads + threadIdx.x;
+      srcidx[i] = -1;
+      if (j < total) {
+        // largest k' in [k, k_hi] with out_offsets[k'] <= j
+        int64_t lo = k, hi = k_hi;
+        while (lo < hi) {
+          int64_t mid = (lo + hi + 1) >> 1;
+          if (__ldg(out_offsets + mid) <= j) lo = mid; else hi = mid - 1;
+        }
+        k = lo;
+        srcidx[i] = __ldg(src_start + k) + (j - __ldg(out_offsets + k));
+      }
+    }
+    int64_t v[kCopyItems];
+#pragma unroll
+    for (int i = 0; i < kCopyItems; ++i) v[i] = srcidx[i] >= 0 ? __ldcs(values + srcidx[i]) : 0;
+#pragma unroll
+    for (int i = 0; i < kCopyItems; ++i) {
+      const int64_t j = j0 + int64_t(i) * kThreads + threadIdx.x;
+      if (srcidx[i] >= 0) __stcs(out_values + j, v[i]);
+    }
+  }
+}
+
+__global__ void permute_empty_kernel(int64_t* out_offsets, const int64_t* rank_offsets, int32_t n,
+                                     int64_t* rank_id_offsets, int32_t* err) {
+  if (threadIdx.x == 0) out_offsets[0] = 0;
+  if (rank_offsets)
+    for (int r = threadIdx.x; r <= n; r += blockDim.x) {
+      if (rank_offsets[r] != 0) set_err(err, FS_ERR_BAD_OFFSETS);
+      rank_id_offsets[r] = 0;
+    }
+}
+
+struct PermuteLayout {
+  int64_t scan_tiles, copy_tiles;
+  size_t zero_bytes() const { return align_up(size_t(scan_tiles) * sizeof(uint64_t) + 256); }
+};
+
+PermuteLayout layout(int64_t S, int64_t capacity) {
+  PermuteLayout L;
+  L.scan_tiles = (S + kScanTile - 1) / kScanTile;
+  L.copy_tiles = (capacity + kCopyTile - 1) / kCopyTile;
+  return L;
+}
+
+}  // namespace
+}  // namespace fs
+
+using namespace fs;
+
+// The copy-tile map depends on the output capacity; the query assumes the
+// worst case of one tile per 4096 IDs of a capacity up to 2^31.
+extern "C" size_t fs_permute_jagged_workspace_size(int64_t S) {
+  if (S < 0) return 0;
+  PermuteLayout L = layout(S, int64_t(INT32_MAX));
+  return L.zero_bytes() + align_up(size_t(S) * sizeof(int64_t)) + align_up(size_t(L.copy_tiles + 1) * sizeof(int32_t)) +
+         256;
+}
+
+extern "C" fs_status fs_permute_jagged(const int64_t* offsets, const int64_t* values, int64_t S, const int32_t* perm,
+                                       int64_t* out_offsets, int64_t* out_values, int64_t capacity,
+                                       const int64_t* rank_offsets, int32_t n, int64_t* rank_id_offsets,
+                                       int32_t* err, void* ws, size_t ws_bytes, fs_stream_t stream) {
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (S < 0 || S > INT32_MAX || capacity < 0 || capacity > INT32_MAX || !out_offsets || !err)
+    return FS_ERR_INVALID_ARG;
+  if (S > 0 && (!offsets || !perm)) return FS_ERR_INVALID_ARG;
+  if (capacity > 0 && (!values || !out_values)) return FS_ERR_INVALID_ARG;
+  if (rank_offsets && (n < 1 || !rank_id_offsets)) return FS_ERR_INVALID_ARG;
+  if (!aligned(out_offsets, 8) || (S > 0 && !aligned(offsets, 8)) || (out_values && !aligned(out_values, 8)) ||
+      (values && !aligned(values, 8)))
+    return FS_ERR_ALIGNMENT;
+  if (ws_bytes < fs_permute_jagged_workspace_size(S) || !ws) return FS_ERR_WORKSPACE;
+  if (S == 0) {
+    permute_empty_kernel<<<1, kThreads, 0, st>>>(out_offsets, rank_offsets, n, rank_id_offsets, err);
+    count_launch(1);
+    return launch_status();
+  }
+  PermuteLayout L = layout(S, capacity);
+  WsCursor cur(ws, ws_bytes);
+  unsigned char* zero = cur.take<unsigned char>(L.zero_bytes());
+  int64_t* src_start = cur.take<int64_t>(size_t(S));
+  int32_t* first_sample = cur.take<int32_t>(size_t(L.copy_tiles + 1));
+  if (!cur.ok) return FS_ERR_WORKSPACE;
+  if (cudaMemsetAsync(zero, 0, L.zero_bytes(), st) != cudaSuccess) return FS_ERR_CUDA;
+  int* counter = reinterpret_cast<int*>(zero);
+  uint64_t* status = reinterpret_cast<uint64_t*>(zero + 256);
+  permute_scan_kernel<<<unsigned(L.scan_tiles), kThreads, 0, st>>>(offsets, S, perm, out_offsets, src_start,
+                                                                   first_sample, L.copy_tiles, capacity, status,
+                                                                   counter, err, spin_limit(), debug_skip_tile());
+  int64_t grid = L.copy_tiles;
+  int64_t cap = int64_t(sm_count()) * 8;
+  if (grid > cap) grid = cap;
+  if (grid < 1) grid = 1;
+  permute_copy_kernel<<<unsigned(grid), kThreads, 0, st>>>(values, out_offsets, src_start, first_sample, S, capacity,
+                                                           out_values, rank_offsets, n, rank_id_offsets, err);
+  count_launch(2);
+  return launch_status();
+}

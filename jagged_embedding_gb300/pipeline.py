@@ -1,0 +1,163 @@
+"""One FreeScale training iteration's jagged index + embedding path on one GPU.
+
+Sequences the C-ABI calls of binding.py over preallocated device buffers
+(FreeScale, arXiv 2604.24073: Algorithm 1 for the balance + shuffle,
+Algorithm 2 for the collision split, lookups and updates).  n logical ranks
+live in one GPU's memory, so the AllGathers of Algorithm 1 are the identity
+and every AllToAll is a device-memory permutation done by the kernels.
+
+Two orders are provided:
+  * step_sync   -- gather of iteration t, then the update of t (collision rows
+                   first, then exclusive rows); the IDs of t+1 are prepared
+                   and split against t before the update, as Algorithm 2 does.
+  * run_prioritized -- Algorithm 2's order: exclusive rows of t+1 prefetched
+                   before the update of t, collision rows of t updated first,
+                   then gathered for t+1; exclusive updates of t deferred to
+                   the next forward.  It needs a second output buffer.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import binding as B
+
+
+class Slot:
+    """Device buffers of one prepared batch (balance, permute, bucketize)."""
+
+    def __init__(self, w, max_S, max_T, device):
+        n = w.n
+        self.perm = torch.empty(max_S, dtype=torch.int32, device=device)
+        self.rank_offsets = torch.empty(n + 1, dtype=torch.int64, device=device)
+        self.seg_weight = torch.empty(n, dtype=torch.int64, device=device)
+        self.offsets = torch.empty(max_S + 1, dtype=torch.int64, device=device)
+        self.ids = torch.empty(max_T, dtype=torch.int64, device=device)
+        self.rank_id_offsets = torch.empty(n + 1, dtype=torch.int64, device=device)
+        self.sm_ids = torch.empty(max_T, dtype=torch.int64, device=device)
+        self.pos = torch.empty(max_T, dtype=torch.int32, device=device)
+        self.splits = torch.empty(n, n, dtype=torch.int64, device=device)
+        self.shard_offsets = torch.empty(n + 1, dtype=torch.int64, device=device)
+        self.T = 0
+
+
+class Pipeline:
+    def __init__(self, w, device, max_T, table, state=None, max_S=None, two_outputs=False):
+        self.w = w
+        self.dev = torch.device(device)
+        self.max_T = int(max_T)
+        self.max_S = int(max_S or w.S)
+        self.table = table
+        self.state = state
+        dev = self.dev
+        self.slots = [Slot(w, self.max_S, self.max_T, dev), Slot(w, self.max_S, self.max_T, dev)]
+        cap = min(2 * self.max_T, w.R)
+        self.cap_rows = cap
+        self.coll = {
+            "co": torch.empty(cap, dtype=torch.int64, device=dev),
+            "ex_t": torch.empty(cap, dtype=torch.int64, device=dev),
+            "ex_next": torch.empty(cap, dtype=torch.int64, device=dev),
+            "counts": torch.zeros(3, dtype=torch.int64, device=dev),
+            "co_off": torch.empty(w.n + 1, dtype=torch.int64, device=dev),
+            "ex_t_off": torch.empty(w.n + 1, dtype=torch.int64, device=dev),
+            "ex_next_off": torch.empty(w.n + 1, dtype=torch.int64, device=dev),
+        }
+        self.masks = [torch.zeros(self.max_T, dtype=torch.uint8, device=dev) for _ in range(2)]
+        self.out = [torch.empty(self.max_T, w.D, dtype=table.dtype, device=dev)]
+        if two_outputs:
+            self.out.append(torch.empty(self.max_T, w.D, dtype=table.dtype, device=dev))
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        L = B.lib()
+        ws_bytes = max(
+            L.fs_balance_vbs_workspace_size(self.max_S, w.n),
+            L.fs_balance_fbs_workspace_size(self.max_S, w.n),
+            L.fs_permute_jagged_workspace_size(self.max_S),
+            L.fs_bucketize_rowwise_workspace_size(self.max_T, w.n),
+            L.fs_collision_split_workspace_size(self.max_T, self.max_T, w.R, w.n),
+            B.backward_workspace_size(self.max_T, w.R, w.D, B.dtype_code(table)) if w.has_update else 0,
+        )
+        # one workspace, reused by every call (calls on one stream run in order)
+        self.ws = B.workspace(ws_bytes, dev)
+
+    # -------------------------------------------------------------- stages
+    def prepare(self, batch, slot):
+        """Balance + permute + bucketize one batch into slot (Algorithm 1; Algorithm 2 line 8)."""
+        w, s = self.w, self.slots[slot]
+        if w.balance == "fbs":
+            B.fs_balance_fbs(batch["uih_len"], w.n, perm=s.perm, rank_offsets=s.rank_offsets, err=self.err, ws=self.ws)
+        else:
+            B.fs_balance_vbs(batch["uih_len"], w.n, w.alpha, w.sort_by_len, perm=s.perm, rank_offsets=s.rank_offsets,
+                             seg_weight=s.seg_weight, err=self.err, ws=self.ws)
+        T = int(batch["T"])
+        B.fs_permute_jagged(batch["offsets"], batch["ids"], s.perm[: batch["uih_len"].numel()], capacity=self.max_T,
+                            rank_offsets=s.rank_offsets, out_offsets=s.offsets[: batch["offsets"].numel()],
+                            out_values=s.ids, rank_id_offsets=s.rank_id_offsets, err=self.err, ws=self.ws)
+        B.fs_bucketize_rowwise(s.ids, s.rank_id_offsets, w.R, sm_ids=s.sm_ids, pos=s.pos, splits=s.splits,
+                               shard_offsets=s.shard_offsets, err=self.err, ws=self.ws, T=T)
+        s.T = T
+
+    def collision(self, slot_t, slot_next):
+        """Collision / exclusive split of (t, t+1) (Algorithm 2 line 10); masks are batch-major."""
+        a, b = self.slots[slot_t], self.slots[slot_next]
+        out = dict(self.coll)
+        out["is_co_t"] = self.masks[slot_t]
+        out["is_co_next"] = self.masks[slot_next]
+        B.fs_collision_split(a.ids, b.ids, self.w.R, self.w.n, cap_rows=self.cap_rows, out=out, err=self.err,
+                             ws=self.ws, T_t=a.T, T_next=b.T)
+
+    def gather(self, slot, out_idx=0, mask=None, sel=1):
+        s = self.slots[slot]
+        B.fs_emb_gather(self.table, s.ids, out=self.out[out_idx], mask=mask, sel=sel, err=self.err, T=s.T)
+
+    def backward(self, slot, grads, phase=B.PHASE_ALL):
+        w, s = self.w, self.slots[slot]
+        B.fs_emb_backward_adagrad(self.table, self.state, s.ids, grads, w.optim, w.lr, w.eps,
+                                  is_co=self.masks[slot] if phase != B.PHASE_ALL else None, phase=phase,
+                                  err=self.err, ws=self.ws, T=s.T)
+
+    # -------------------------------------------------------------- orders
+    def step_sync(self, cur, nxt_batch, grads, has_next=True):
+        """One iteration in the synchronous order; slot `cur` holds iteration t already prepared.
+
+        Returns the slot that now holds t+1.
+        """
+        nxt = 1 - cur
+        if has_next:
+            self.prepare(nxt_batch, nxt)
+            self.collision(cur, nxt)
+        self.gather(cur)
+        if self.w.has_update:
+            if has_next:
+                self.backward(cur, grads, B.PHASE_COLLISION)
+                self.backward(cur, grads, B.PHASE_EXCLUSIVE)
+            else:
+                self.backward(cur, grads, B.PHASE_ALL)
+        return nxt
+
+    def run_prioritized(self, batches, grads_list, on_output=None):
+        """Algorithm 2 order over len(batches) iterations.  on_output(t, out_tensor) sees each batch's output."""
+        K = len(batches)
+        assert len(self.out) == 2
+        self.prepare(batches[0], 0)
+        self.gather(0, out_idx=0)
+        pending_ex = None
+        for t in range(K):
+            cur, nxt = t % 2, (t + 1) % 2
+            if pending_ex is not None:                                   # line 7
+                self.backward(pending_ex[0], pending_ex[1], B.PHASE_EXCLUSIVE)
+                pending_ex = None
+            if t + 1 < K:                                                # lines 8-12
+                self.prepare(batches[t + 1], nxt)
+                self.collision(cur, nxt)
+                self.gather(nxt, out_idx=nxt, mask=self.masks[nxt], sel=0)
+            if on_output is not None:
+                on_output(t, self.out[cur][: self.slots[cur].T])
+            if self.w.has_update:                                        # lines 18-20
+                if t + 1 < K:
+                    self.backward(cur, grads_list[t], B.PHASE_COLLISION)
+                    pending_ex = (cur, grads_list[t])
+                else:
+                    self.backward(cur, grads_list[t], B.PHASE_ALL)
+            if t + 1 < K:                                                # line 21
+                self.gather(nxt, out_idx=nxt, mask=self.masks[nxt], sel=1)
+        if pending_ex is not None:
+            self.backward(pending_ex[0], pending_ex[1], B.PHASE_EXCLUSIVE)

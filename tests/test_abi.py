@@ -1,0 +1,91 @@
+"""The C-ABI library loads, exports every symbol the header declares, and rejects
+bad arguments on the host (no GPU needed: nothing is launched for these)."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+from jagged_embedding_gb300 import binding as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fs_jagged.h")
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(fs_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_declares_the_hot_path_calls():
+    names = _declared()
+    for n in ["fs_balance_fbs", "fs_balance_vbs", "fs_permute_jagged", "fs_bucketize_rowwise", "fs_collision_split",
+              "fs_emb_gather", "fs_emb_backward_adagrad"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol():
+    L = B.lib()
+    missing = [n for n in _declared() if not hasattr(L, n)]
+    assert missing == []
+    assert sorted(_declared()) == sorted(B.EXPORTS)
+
+
+def test_status_strings_and_version():
+    L = B.lib()
+    for code, text in B.STATUS.items():
+        assert L.fs_status_string(code).decode() == text
+    assert "sm_103a" in B.version()
+
+
+def test_workspace_queries():
+    L = B.lib()
+    assert L.fs_balance_fbs_workspace_size(131072, 256) > 4 * 131072 * 4
+    assert L.fs_balance_vbs_workspace_size(32768, 512) > L.fs_balance_fbs_workspace_size(32768, 512)
+    assert L.fs_permute_jagged_workspace_size(131072) >= 131072 * 8
+    assert L.fs_bucketize_rowwise_workspace_size(10 ** 6, 256) > 0
+    # two presence bitmaps of R bits
+    assert L.fs_collision_split_workspace_size(0, 0, 10 ** 8, 256) >= 2 * 10 ** 8 // 8
+    # key/value ping-pong of the backward sort: 16 bytes per ID at least
+    assert L.fs_emb_backward_adagrad_workspace_size(10 ** 6, 10 ** 7, 64, 0) >= 16 * 10 ** 6
+    assert L.fs_balance_fbs_workspace_size(-1, 4) == 0
+
+
+NULL = None
+
+
+def test_host_argument_errors_return_without_launching():
+    L = B.lib()
+    err = C.c_void_p(0x1000)  # never dereferenced: every call below fails host checks first
+    ws = C.c_void_p(0x2000)
+    assert L.fs_balance_fbs(NULL, 10, 0, NULL, NULL, err, ws, 1 << 30, NULL) == 1            # n < 1
+    assert L.fs_balance_fbs(NULL, 10, 4, NULL, C.c_void_p(0x3000), err, ws, 1 << 30, NULL) == 1  # NULL input
+    assert L.fs_balance_fbs(C.c_void_p(0x10), 10, 4, C.c_void_p(0x20), C.c_void_p(0x3000), err, ws, 16, NULL) == 5
+    assert L.fs_balance_vbs(C.c_void_p(0x10), 10, 4, -1.0, 0, C.c_void_p(0x20), C.c_void_p(0x3000),
+                            C.c_void_p(0x4000), err, ws, 1 << 30, NULL) == 1                   # alpha < 0
+    assert L.fs_bucketize_rowwise(C.c_void_p(0x10), 10, C.c_void_p(0x100), 513, 100, C.c_void_p(0x20),
+                                  C.c_void_p(0x30), C.c_void_p(0x40), C.c_void_p(0x50), err, ws, 1 << 30, NULL) == 1
+    assert L.fs_bucketize_rowwise(C.c_void_p(0x13), 10, C.c_void_p(0x100), 4, 100, C.c_void_p(0x20),
+                                  C.c_void_p(0x30), C.c_void_p(0x40), C.c_void_p(0x50), err, ws, 1 << 30, NULL) == 8
+    assert L.fs_emb_gather(C.c_void_p(0x100), 10, 0, 0, C.c_void_p(0x200), 5, NULL, 1, C.c_void_p(0x300), err,
+                           NULL) == 1                                                           # dim < 1
+    assert L.fs_emb_gather(C.c_void_p(0x100), 10, 64, 7, C.c_void_p(0x200), 5, NULL, 1, C.c_void_p(0x300), err,
+                           NULL) == 1                                                           # bad dtype
+    # backward: dim 48 unsupported, Adagrad without state, phase without mask
+    args = dict(table=C.c_void_p(0x100), R=10, ids=C.c_void_p(0x200), grads=C.c_void_p(0x300), T=4)
+    assert L.fs_emb_backward_adagrad(args["table"], C.c_void_p(0x400), 10, 48, 0, 1, args["ids"], args["grads"], 4,
+                                     NULL, 0, C.c_float(0.01), C.c_float(1e-8), err, ws, 1 << 30, NULL) == 1
+    assert L.fs_emb_backward_adagrad(args["table"], NULL, 10, 64, 0, 1, args["ids"], args["grads"], 4,
+                                     NULL, 0, C.c_float(0.01), C.c_float(1e-8), err, ws, 1 << 30, NULL) == 1
+    assert L.fs_emb_backward_adagrad(args["table"], C.c_void_p(0x400), 10, 64, 0, 1, args["ids"], args["grads"], 4,
+                                     NULL, 1, C.c_float(0.01), C.c_float(1e-8), err, ws, 1 << 30, NULL) == 1
+    assert L.fs_collision_split(C.c_void_p(0x10), 5, C.c_void_p(0x20), 5, (1 << 32) + 1, 4, NULL, NULL, NULL, 0,
+                                C.c_void_p(0x30), C.c_void_p(0x40), C.c_void_p(0x50), C.c_void_p(0x60),
+                                C.c_void_p(0x70), C.c_void_p(0x80), err, ws, 1 << 30, NULL) == 1
+
+
+def test_binding_refuses_cpu_tensors():
+    import torch
+    with pytest.raises(B.FsError):
+        B.fs_balance_fbs(torch.zeros(4, dtype=torch.int32), 2)

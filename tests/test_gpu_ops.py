@@ -1,0 +1,374 @@
+"""Parity of every C-ABI call with the CPU oracle, element by element (GPU).
+
+Bit-exact for partitions, permutations, bucketize, collision lists / masks and
+gathers; toleranced (see helpers.assert_table_close) for updated embeddings.
+Inputs are seeded and synthetic; sizes span several tiles plus a ragged tail.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from jagged_embedding_gb300 import binding as B
+from jagged_embedding_gb300 import synthetic
+from tests.helpers import assert_state_close, assert_table_close, to_np, update_scale
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _check(err):
+    B.check(err)
+
+
+def _lens(rng, S, mu=5.0, sigma=1.2, lmax=2048):
+    return np.clip(np.round(rng.lognormal(mu, sigma, S)), 1, lmax).astype(np.int32)
+
+
+# ------------------------------------------------------------------ balance
+
+@pytest.mark.parametrize("n,S", [(8, 512), (64, 16384), (256, 131072), (3, 12), (5, 23), (1, 100), (7, 3), (4, 0),
+                                 (512, 32768), (13, 4097)])
+def test_fbs_matches_oracle(n, S):
+    rng = np.random.default_rng(n * 7 + S)
+    L = _lens(rng, S, 6.8, 1.5, 16384)
+    perm, ro, err = B.fs_balance_fbs(torch.from_numpy(L).to(DEV), n)
+    _check(err)
+    p_ref, ro_ref = oracle.balance_fbs(L, n)
+    assert np.array_equal(to_np(perm), p_ref)
+    assert np.array_equal(to_np(ro), ro_ref)
+
+
+def test_fbs_ties_and_extremes():
+    L = np.array([5] * 1000 + [0] * 50 + [2 ** 31 - 1] * 3 + [7] * 4000, np.int32)
+    perm, ro, err = B.fs_balance_fbs(torch.from_numpy(L).to(DEV), 6)
+    _check(err)
+    p_ref, ro_ref = oracle.balance_fbs(L, 6)
+    assert np.array_equal(to_np(perm), p_ref) and np.array_equal(to_np(ro), ro_ref)
+
+
+def test_fbs_negative_length_sets_error():
+    L = torch.tensor([3, -1, 4], dtype=torch.int32, device=DEV)
+    _, _, err = B.fs_balance_fbs(L, 2)
+    with pytest.raises(B.FsError) as e:
+        _check(err)
+    assert e.value.code == 1
+
+
+@pytest.mark.parametrize("n,S,sort_by_len", [(16, 2048, 0), (512, 32768, 1), (16, 2048, 1), (3, 7, 1), (1, 50, 0),
+                                             (64, 20000, 0), (7, 0, 1)])
+def test_vbs_matches_oracle(n, S, sort_by_len):
+    rng = np.random.default_rng(n + S + sort_by_len)
+    L = _lens(rng, S, 7.0, 1.6, 16384)
+    perm, ro, sw, err = B.fs_balance_vbs(torch.from_numpy(L).to(DEV), n, 1.5, sort_by_len)
+    _check(err)
+    p_ref, ro_ref, sw_ref = oracle.balance_vbs(L, n, 1.5, sort_by_len)
+    assert np.array_equal(to_np(perm), p_ref)
+    assert np.array_equal(to_np(ro), ro_ref)
+    assert np.array_equal(to_np(sw).astype(np.uint64), sw_ref)
+
+
+@pytest.mark.parametrize("alpha", [1.5, 1.0, 2.0, 0.5, 2.5, 3.0])
+def test_vbs_weight_table_exact(alpha):
+    """Every L in [1, 16384] (4096 for alpha = 3), shuffled, one rank per sample: the cut and every
+    segment weight (a sum of fixed-point weights) equal the oracle's bit for bit."""
+    lmax = 4096 if alpha >= 3.0 else 16384            # S * max weight must stay below 2^62
+    L = np.random.default_rng(1).permutation(np.arange(1, lmax + 1, dtype=np.int32))
+    S = L.size
+    perm, ro, sw, err = B.fs_balance_vbs(torch.from_numpy(L).to(DEV), S, alpha, 0)
+    _check(err)
+    p_ref, ro_ref, sw_ref = oracle.balance_vbs(L, S, alpha, 0)
+    assert np.array_equal(to_np(ro), ro_ref)
+    assert np.array_equal(to_np(sw).astype(np.uint64), sw_ref)
+
+
+def test_vbs_general_alpha_total():
+    """alpha = 1.3 goes through pow(); device and host pow may differ by an ulp, which the
+    fixed-point rounding absorbs except next to a half-integer: totals within 16 units."""
+    L = np.arange(1, 16385, dtype=np.int32)
+    _, _, sw, err = B.fs_balance_vbs(torch.from_numpy(L).to(DEV), 1, 1.3, 0)
+    _check(err)
+    ref = sum(oracle.vbs_weight(int(l), 1.3) for l in L)
+    assert abs(int(to_np(sw)[0]) - ref) <= 16
+
+
+# ------------------------------------------------------------------ permute
+
+def _jagged(rng, S, R, mu=5.0, sigma=1.2, lmax=2048):
+    lens = _lens(rng, S, mu, sigma, lmax).astype(np.int64)
+    off = np.zeros(S + 1, np.int64)
+    off[1:] = np.cumsum(lens)
+    ids = rng.integers(0, R, int(off[-1])).astype(np.int64)
+    return off, ids
+
+
+@pytest.mark.parametrize("S", [1, 7, 512, 4096, 16384, 40000])
+def test_permute_matches_oracle(S):
+    rng = np.random.default_rng(S)
+    off, ids = _jagged(rng, S, 10 ** 6)
+    perm = rng.permutation(S).astype(np.int32)
+    n = max(1, S // 64)
+    cuts = np.sort(rng.integers(0, S + 1, n - 1))
+    ro = np.concatenate([[0], cuts, [S]]).astype(np.int64)
+    o2, v2, rio, err = B.fs_permute_jagged(torch.from_numpy(off).to(DEV), torch.from_numpy(ids).to(DEV),
+                                           torch.from_numpy(perm).to(DEV), rank_offsets=torch.from_numpy(ro).to(DEV))
+    _check(err)
+    o_ref, v_ref = oracle.permute_jagged(off, ids, perm)
+    assert np.array_equal(to_np(o2), o_ref) and np.array_equal(to_np(v2), v_ref)
+    assert np.array_equal(to_np(rio), o_ref[ro])
+
+
+def test_permute_with_empty_samples_and_long_samples():
+    rng = np.random.default_rng(3)
+    S = 3000
+    lens = rng.integers(0, 3, S).astype(np.int64)
+    lens[rng.integers(0, S, 20)] = 16384          # a few very long samples span many copy tiles
+    lens[:100] = 0
+    off = np.zeros(S + 1, np.int64)
+    off[1:] = np.cumsum(lens)
+    ids = rng.integers(0, 1 << 40, int(off[-1])).astype(np.int64)
+    perm = rng.permutation(S).astype(np.int32)
+    o2, v2, _, err = B.fs_permute_jagged(torch.from_numpy(off).to(DEV), torch.from_numpy(ids).to(DEV),
+                                         torch.from_numpy(perm).to(DEV))
+    _check(err)
+    o_ref, v_ref = oracle.permute_jagged(off, ids, perm)
+    assert np.array_equal(to_np(o2), o_ref) and np.array_equal(to_np(v2), v_ref)
+
+
+def test_permute_errors():
+    off = torch.tensor([0, 2, 5], dtype=torch.int64, device=DEV)
+    val = torch.arange(5, dtype=torch.int64, device=DEV)
+    _, _, _, err = B.fs_permute_jagged(off, val, torch.tensor([0, 2], dtype=torch.int32, device=DEV))
+    with pytest.raises(B.FsError) as e:
+        _check(err)
+    assert e.value.code == 3
+    _, _, _, err = B.fs_permute_jagged(off, val, torch.tensor([1, 0], dtype=torch.int32, device=DEV), capacity=4)
+    with pytest.raises(B.FsError) as e:
+        _check(err)
+    assert e.value.code == 4
+
+
+def test_permute_empty_batch():
+    off = torch.zeros(1, dtype=torch.int64, device=DEV)
+    o2, v2, rio, err = B.fs_permute_jagged(off, torch.zeros(0, dtype=torch.int64, device=DEV),
+                                           torch.zeros(0, dtype=torch.int32, device=DEV),
+                                           rank_offsets=torch.zeros(4, dtype=torch.int64, device=DEV))
+    _check(err)
+    assert to_np(o2).tolist() == [0] and to_np(rio).tolist() == [0, 0, 0, 0]
+
+
+# ------------------------------------------------------------------ bucketize
+
+@pytest.mark.parametrize("n,R,T", [(8, 100_000, 150_000), (64, 10_000_000, 500_000), (512, 50_000_000, 300_001),
+                                   (256, 100_000_000, 70_000), (1, 1000, 5000), (13, 12, 4097), (7, 100, 0)])
+def test_bucketize_matches_oracle(n, R, T):
+    rng = np.random.default_rng(n + T)
+    ids = rng.integers(0, R, T).astype(np.int64)
+    cuts = np.sort(rng.integers(0, T + 1, n - 1))
+    rio = np.concatenate([[0], cuts, [T]]).astype(np.int64)
+    sm, pos, splits, so, err = B.fs_bucketize_rowwise(torch.from_numpy(ids).to(DEV), torch.from_numpy(rio).to(DEV), R)
+    _check(err)
+    sm_ref, pos_ref, splits_ref, so_ref = oracle.bucketize_rowwise(ids, rio, n, R)
+    assert np.array_equal(to_np(sm), sm_ref)
+    assert np.array_equal(to_np(pos), pos_ref)
+    assert np.array_equal(to_np(splits), splits_ref)
+    assert np.array_equal(to_np(so), so_ref)
+
+
+def test_bucketize_zipf_hot_rows():
+    w = synthetic.WORKLOADS["mid-full-step"]
+    rng = torch.Generator(device="cpu").manual_seed(5)
+    ids = synthetic.zipf_rows(w.R, w.zipf_s, 400_000, rng, "cpu")
+    n = w.n
+    rio = np.linspace(0, ids.numel(), n + 1).astype(np.int64)
+    sm, pos, splits, so, err = B.fs_bucketize_rowwise(ids.to(DEV), torch.from_numpy(rio).to(DEV), w.R)
+    _check(err)
+    sm_ref, pos_ref, splits_ref, so_ref = oracle.bucketize_rowwise(ids.numpy(), rio, n, w.R)
+    assert np.array_equal(to_np(sm), sm_ref) and np.array_equal(to_np(pos), pos_ref)
+    assert np.array_equal(to_np(splits), splits_ref)
+
+
+def test_bucketize_id_out_of_range():
+    ids = torch.tensor([1, 5, 100], dtype=torch.int64, device=DEV)
+    rio = torch.tensor([0, 3], dtype=torch.int64, device=DEV)
+    *_, err = B.fs_bucketize_rowwise(ids, rio, 50)
+    with pytest.raises(B.FsError) as e:
+        _check(err)
+    assert e.value.code == 2
+
+
+# ------------------------------------------------------------------ collision
+
+@pytest.mark.parametrize("R,n,Tt,Tn", [(100_000, 8, 70_000, 80_000), (20, 4, 6, 6), (10_000_000, 64, 300_000, 250_000),
+                                       (100_000_000, 256, 200_000, 200_000), (50_000_000, 512, 0, 1000),
+                                       (33, 5, 1000, 0), (1_000_003, 7, 123_457, 98_765)])
+def test_collision_matches_oracle(R, n, Tt, Tn):
+    rng = np.random.default_rng(R + Tt)
+    a = rng.integers(0, R, Tt).astype(np.int64)
+    b = rng.integers(0, R, Tn).astype(np.int64)
+    if Tt and Tn:
+        b[: Tn // 2] = a[rng.integers(0, Tt, Tn // 2)]      # plenty of collisions
+    out, err = B.fs_collision_split(torch.from_numpy(a).to(DEV), torch.from_numpy(b).to(DEV), R, n)
+    _check(err)
+    ref = oracle.collision_split(a, b, R, n)
+    counts = to_np(out["counts"])
+    assert counts.tolist() == [ref["co"].size, ref["ex_t"].size, ref["ex_next"].size]
+    for k, c in (("co", 0), ("ex_t", 1), ("ex_next", 2)):
+        assert np.array_equal(to_np(out[k])[: counts[c]], ref[k]), k
+        assert np.array_equal(to_np(out[k + "_off"]), ref[k + "_off"]), k
+    assert np.array_equal(to_np(out["is_co_t"]), ref["is_co_t"])
+    assert np.array_equal(to_np(out["is_co_next"]), ref["is_co_next"])
+
+
+def test_collision_capacity_error():
+    a = torch.arange(100, dtype=torch.int64, device=DEV)
+    out, err = B.fs_collision_split(a, a.flip(0).contiguous(), 1000, 4, cap_rows=10)
+    with pytest.raises(B.FsError) as e:
+        _check(err)
+    assert e.value.code == 4
+
+
+# ------------------------------------------------------------------ gather
+
+@pytest.mark.parametrize("dtype,D", [("f32", 64), ("bf16", 128), ("f32", 128), ("f32", 3), ("bf16", 6), ("f32", 20)])
+def test_gather_bit_exact(dtype, D):
+    rng = np.random.default_rng(D)
+    R, T = 5000, 77_777
+    tt = torch.float32 if dtype == "f32" else torch.bfloat16
+    table = torch.randn(R, D, generator=torch.Generator().manual_seed(1)).to(tt)
+    ids = rng.integers(0, R, T).astype(np.int64)
+    out, err = B.fs_emb_gather(table.to(DEV), torch.from_numpy(ids).to(DEV))
+    _check(err)
+    ref = oracle.emb_gather(to_np(table), ids)
+    assert np.array_equal(to_np(out), ref)
+
+
+def test_gather_masked_merge():
+    rng = np.random.default_rng(9)
+    R, D, T = 3000, 64, 50_000
+    table = torch.randn(R, D, generator=torch.Generator().manual_seed(2))
+    ids = rng.integers(0, R, T).astype(np.int64)
+    mask = rng.integers(0, 2, T).astype(np.uint8)
+    out = torch.full((T, D), -3.5, device=DEV)
+    tdev, idev, mdev = table.to(DEV), torch.from_numpy(ids).to(DEV), torch.from_numpy(mask).to(DEV)
+    _, err = B.fs_emb_gather(tdev, idev, out=out, mask=mdev, sel=0)
+    _check(err)
+    got = to_np(out)
+    assert np.array_equal(got[mask == 0], to_np(table)[ids[mask == 0]])
+    assert (got[mask == 1] == -3.5).all()
+    B.fs_emb_gather(tdev, idev, out=out, mask=mdev, sel=1, err=err)
+    _check(err)
+    assert np.array_equal(to_np(out), to_np(table)[ids])
+
+
+def test_gather_bad_id():
+    _, err = B.fs_emb_gather(torch.zeros(10, 64, device=DEV), torch.tensor([3, 10], dtype=torch.int64, device=DEV))
+    with pytest.raises(B.FsError) as e:
+        _check(err)
+    assert e.value.code == 2
+
+
+# ------------------------------------------------------------------ backward
+
+def _bwd_case(seed, R, D, T, dtype, s=1.1):
+    g = torch.Generator().manual_seed(seed)
+    ids = synthetic.zipf_rows(R, s, T, g, "cpu")
+    tt = torch.float32 if dtype == "f32" else torch.bfloat16
+    W = (torch.randn(R, D, generator=g) * 0.01).to(tt)
+    G = torch.randn(T, D, generator=g).to(tt)
+    return ids, W, G
+
+
+@pytest.mark.parametrize("dtype,D,optim,T,R", [
+    ("f32", 64, "sgd", 150_000, 100_000),
+    ("f32", 64, "adagrad", 300_000, 1_000_000),
+    ("bf16", 128, "adagrad", 200_000, 10_000_000),
+    ("f32", 32, "adagrad", 50_000, 3000),
+    ("f32", 128, "sgd", 40_000, 100),
+    ("bf16", 64, "sgd", 60_000, 70_000),
+    ("bf16", 256, "adagrad", 20_000, 5000),
+    ("f32", 64, "adagrad", 5, 10),
+])
+def test_backward_matches_oracle(dtype, D, optim, T, R):
+    ids, W, G = _bwd_case(T + D, R, D, T, dtype)
+    state = torch.rand(R, generator=torch.Generator().manual_seed(3)) if optim == "adagrad" else None
+    Wd = W.to(DEV)
+    sd = state.to(DEV) if state is not None else None
+    err = B.fs_emb_backward_adagrad(Wd, sd, ids.to(DEV), G.to(DEV), optim, 0.01, 1e-8)
+    _check(err)
+    W_ref = to_np(W)
+    s_ref = state.numpy().copy() if state is not None else None
+    oracle.emb_backward(W_ref, s_ref, ids.numpy(), to_np(G), optim, 0.01, 1e-8)
+    scale = update_scale(ids.numpy(), to_np(G), R, optim, 0.01, 1e-8, s_ref)
+    assert_table_close(to_np(Wd), W_ref, dtype, 0.01, scale=scale)
+    if state is not None:
+        assert_state_close(to_np(sd), s_ref)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_backward_phases_and_determinism(dtype):
+    R, D, T = 200_000, 64 if dtype == "f32" else 128, 250_000
+    ids, W, G = _bwd_case(11, R, D, T, dtype, s=1.05)
+    rng = np.random.default_rng(4)
+    nxt = synthetic.zipf_rows(R, 1.05, 200_000, torch.Generator().manual_seed(12), "cpu").numpy()
+    is_co = np.isin(ids.numpy(), nxt).astype(np.uint8)
+    results = []
+    for _ in range(2):
+        Wd, sd = W.to(DEV), torch.zeros(R, device=DEV)
+        idd, Gd, md = ids.to(DEV), G.to(DEV), torch.from_numpy(is_co).to(DEV)
+        err = B.fs_emb_backward_adagrad(Wd, sd, idd, Gd, "adagrad", 0.01, 1e-8, is_co=md, phase=B.PHASE_COLLISION)
+        B.fs_emb_backward_adagrad(Wd, sd, idd, Gd, "adagrad", 0.01, 1e-8, is_co=md, phase=B.PHASE_EXCLUSIVE, err=err)
+        _check(err)
+        results.append((to_np(Wd), to_np(sd)))
+    assert np.array_equal(results[0][0], results[1][0]) and np.array_equal(results[0][1], results[1][1])
+    W_ref, s_ref = to_np(W), np.zeros(R, np.float32)
+    oracle.emb_backward(W_ref, s_ref, ids.numpy(), to_np(G), "adagrad", 0.01, 1e-8, is_co=is_co, phase=1)
+    oracle.emb_backward(W_ref, s_ref, ids.numpy(), to_np(G), "adagrad", 0.01, 1e-8, is_co=is_co, phase=2)
+    assert_table_close(results[0][0], W_ref, dtype, 0.01)
+    assert_state_close(results[0][1], s_ref)
+
+
+def test_backward_single_hot_row_spans_many_tiles():
+    """One row owns most positions: its sum crosses hundreds of reduce tiles (carry chain)."""
+    R, D, T = 1000, 64, 1_000_000
+    g = torch.Generator().manual_seed(21)
+    ids = torch.where(torch.rand(T, generator=g) < 0.9, torch.tensor(7), torch.randint(0, R, (T,), generator=g))
+    W = torch.randn(R, D, generator=g) * 0.01
+    G = torch.randn(T, D, generator=g)
+    s = torch.zeros(R)
+    Wd, sd = W.to(DEV), s.to(DEV)
+    err = B.fs_emb_backward_adagrad(Wd, sd, ids.to(DEV), G.to(DEV), "adagrad", 0.01, 1e-8)
+    _check(err)
+    W_ref, s_ref = W.numpy().copy(), s.numpy().copy()
+    oracle.emb_backward(W_ref, s_ref, ids.numpy(), G.numpy(), "adagrad", 0.01, 1e-8)
+    assert_table_close(to_np(Wd), W_ref, "f32", 0.01)
+    assert_state_close(to_np(sd), s_ref)
+
+
+def test_backward_rejects_unsupported_dim():
+    with pytest.raises(B.FsError):
+        B.fs_emb_backward_adagrad(torch.zeros(10, 48, device=DEV), torch.zeros(10, device=DEV),
+                                  torch.zeros(4, dtype=torch.int64, device=DEV), torch.zeros(4, 48, device=DEV),
+                                  "adagrad", 0.01, 1e-8)
+
+
+# ------------------------------------------------------------------ bounded waits
+
+def test_lookback_wait_gives_up_with_timeout_status():
+    """A scan tile that never publishes: later tiles stop waiting and report FS_ERR_TIMEOUT."""
+    rng = np.random.default_rng(0)
+    S = 40_000                                             # 20 scan tiles of 2048
+    L = _lens(rng, S)
+    B.set_spin_limit(1 << 14)
+    B.debug_skip_publish(3)
+    try:
+        _, _, _, err = B.fs_balance_vbs(torch.from_numpy(L).to(DEV), 16, 1.5, 0)
+        with pytest.raises(B.FsError) as e:
+            _check(err)
+        assert e.value.code == 6
+    finally:
+        B.debug_skip_publish(-1)
+        B.set_spin_limit(1 << 22)
+    # the context is still usable
+    _, _, _, err = B.fs_balance_vbs(torch.from_numpy(L).to(DEV), 16, 1.5, 0)
+    _check(err)
