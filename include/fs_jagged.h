@@ -153,7 +153,9 @@ fs_status fs_bucketize_rowwise(const int64_t* ids, int64_t T, const int64_t* ran
  *           sets FS_ERR_CAPACITY and is truncated
  *   *_shard_off [n+1] int64 out: list entries below k * ceil(num_rows/n)
  *   is_co_t [T_t], is_co_next [T_next] uint8 out, aligned with the inputs:
- *           1 when that entry's row is a collision row, else 0
+ *           1 when that entry's row is a collision row, else 0.  Either may be
+ *           NULL when the caller does not need it (the synchronous order
+ *           needs only is_co_t); its pass over the IDs is then skipped.
  * num_rows < 2^32.
  * ---------------------------------------------------------------------- */
 size_t fs_collision_split_workspace_size(int64_t T_t, int64_t T_next, int64_t num_rows, int32_t n);

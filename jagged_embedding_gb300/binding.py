@@ -229,7 +229,7 @@ def fs_bucketize_rowwise(ids, rank_id_offsets, num_rows, sm_ids=None, pos=None, 
 
 
 def fs_collision_split(ids_t, ids_next, num_rows, n, cap_rows=None, out=None, err=None, ws=None, T_t=None,
-                       T_next=None):
+                       T_next=None, want_next_mask=True):
     """Returns dict with co/ex_t/ex_next (capacity-sized; counts on device), shard offsets and masks."""
     dev = ids_t.device
     _need(ids_t, torch.int64, "ids_t")
@@ -255,8 +255,9 @@ def fs_collision_split(ids_t, ids_next, num_rows, n, cap_rows=None, out=None, er
     o = out
     _ok(lib().fs_collision_split(_ptr(ids_t), Tt, _ptr(ids_next), Tn, int(num_rows), n, _ptr(o["co"]),
                                  _ptr(o["ex_t"]), _ptr(o["ex_next"]), cap, _ptr(o["counts"]), _ptr(o["co_off"]),
-                                 _ptr(o["ex_t_off"]), _ptr(o["ex_next_off"]), _ptr(o["is_co_t"]),
-                                 _ptr(o["is_co_next"]), _ptr(err), _ptr(ws), ws.numel(), _stream(dev)),
+                                 _ptr(o["ex_t_off"]), _ptr(o["ex_next_off"]), _ptr(o.get("is_co_t")),
+                                 _ptr(o.get("is_co_next") if want_next_mask else None), _ptr(err), _ptr(ws),
+                                 ws.numel(), _stream(dev)),
         "fs_collision_split")
     return out, err
 

@@ -23,6 +23,7 @@
 #include <cuda_bf16.h>
 
 #include "onesweep.cuh"
+#include "tma.cuh"
 
 namespace fs {
 namespace {
@@ -34,6 +35,7 @@ constexpr uint32_t kNoKey = 0xFFFFFFFFu;     // rows are < num_rows < 2^32
 // Sort source: the selected positions of the batch, key = row, value = position.
 struct SrcRows {
   using Key = uint32_t;
+  static constexpr bool kIndexValue = true;  // value = item index
   const int64_t* ids;
   const uint8_t* is_co;
   int phase;
@@ -154,15 +156,15 @@ __device__ __forceinline__ void prefetch_l2(const void* p) {
 }
 
 template <bool BF16, int EPL>
-__global__ void __launch_bounds__(kThreads) reduce_kernel(const uint32_t* __restrict__ keys,
-                                                          const uint32_t* __restrict__ vals, const int64_t* n_dev,
-                                                          const void* __restrict__ grads, UpdateArgs u,
-                                                          float* carry_head, float* carry_tail, uint8_t* head_cont,
-                                                          uint8_t* tail_flag) {
+__global__ void __launch_bounds__(kThreads, 4) reduce_kernel(const uint32_t* __restrict__ keys,
+                                                             const uint32_t* __restrict__ vals, const int64_t* n_dev,
+                                                             const void* __restrict__ grads, UpdateArgs u,
+                                                             float* carry_head, float* carry_tail, uint8_t* head_cont,
+                                                             uint8_t* tail_flag) {
   constexpr int ESZ = BF16 ? 2 : 4;
   constexpr int D = 32 * EPL;
   constexpr int RB = D * ESZ;
-  constexpr int G = (32 / EPL) > 16 ? 16 : (32 / EPL);  // gradient rows in flight per warp
+  constexpr int G = (16 / EPL) > 8 ? 8 : (16 / EPL);  // gradient rows in flight per warp (64-register budget)
   const int64_t n = *n_dev;
   const int64_t ntiles = (n + kChunk - 1) / kChunk;
   const int lane = threadIdx.x & 31;
@@ -178,12 +180,18 @@ __global__ void __launch_bounds__(kThreads) reduce_kernel(const uint32_t* __rest
 #pragma unroll
     for (int i = 0; i < EPL; ++i) acc[i] = 0.f;
 
+    // keys / positions of the next batch are loaded one batch ahead
+    uint32_t pre_k = (s0 + lane < s1) ? __ldcs(keys + s0 + lane) : kNoKey;
+    uint32_t pre_p = (s0 + lane < s1) ? __ldcs(vals + s0 + lane) : 0u;
     for (int64_t j = s0; j < s1; j += 32) {
       const int cnt = (s1 - j < 32) ? int(s1 - j) : 32;
-      const uint32_t my_k = lane < cnt ? __ldcs(keys + j + lane) : kNoKey;
-      const uint32_t my_p = lane < cnt ? __ldcs(vals + j + lane) : 0u;
+      const uint32_t my_k = pre_k, my_p = pre_p;
+      const int64_t jn = j + 32;
+      pre_k = (jn + lane < s1) ? __ldcs(keys + jn + lane) : kNoKey;
+      pre_p = (jn + lane < s1) ? __ldcs(vals + jn + lane) : 0u;
       uint32_t nk = __shfl_down_sync(0xffffffffu, my_k, 1);
-      if (lane == cnt - 1) nk = (j + cnt < s1) ? keys[j + cnt] : next_key;
+      const uint32_t first_next = __shfl_sync(0xffffffffu, pre_k, 0);
+      if (lane == cnt - 1) nk = (j + cnt < s1) ? first_next : next_key;
       if (lane < cnt && nk != my_k) {  // a row ends at this entry: bring its table row and state to L2
         const char* rp = static_cast<const char*>(u.table) + int64_t(my_k) * RB;
 #pragma unroll
@@ -249,6 +257,186 @@ __global__ void __launch_bounds__(kThreads) reduce_kernel(const uint32_t* __rest
   }
 }
 
+// Shared-memory plan of the staged reduce: per warp NST stages, each holding
+// the 32 gradient rows of one batch of sorted entries and the table rows of
+// the rows that end (and get updated) in that batch, plus keys, flags and the
+// stage's mbarrier.
+template <bool BF16, int EPL>
+struct Staged {
+  static constexpr int ESZ = BF16 ? 2 : 4;
+  static constexpr int D = 32 * EPL;
+  static constexpr int RB = D * ESZ;
+  static constexpr int NST = 3;
+  static constexpr int STAGE = 2 * 32 * RB;
+  static constexpr int META = NST * (32 * 4 + 32) + NST * 8;
+  static constexpr int WARP_BYTES = NST * STAGE + ((META + 127) / 128) * 128;
+  static constexpr int WPB_RAW = (196 * 1024) / WARP_BYTES;
+  static constexpr int WPB = WPB_RAW < 1 ? 1 : (WPB_RAW > 8 ? 8 : WPB_RAW);
+  static constexpr int SMEM = WPB * WARP_BYTES;
+};
+
+// Staged variant of the reduce: gradient rows and the table rows to update are
+// brought into shared memory by bulk asynchronous copies (cp.async.bulk, one
+// 256-byte row per lane, completion on an mbarrier), NST batches of 32 entries
+// ahead of the warp that sums them.  Same tiling, carries and summation order
+// as reduce_kernel.
+template <bool BF16, int EPL>
+__global__ void __launch_bounds__(Staged<BF16, EPL>::WPB * 32, 1)
+    reduce_staged_kernel(const uint32_t* __restrict__ keys, const uint32_t* __restrict__ vals, const int64_t* n_dev,
+                         const void* __restrict__ grads, UpdateArgs u, float* carry_head, float* carry_tail,
+                         uint8_t* head_cont, uint8_t* tail_flag, int32_t* err, int64_t limit) {
+  using P = Staged<BF16, EPL>;
+  constexpr int ESZ = P::ESZ, D = P::D, RB = P::RB, NST = P::NST;
+  using V = typename Raw<EPL * ESZ>::T;
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  unsigned char* wb = smem + warp * P::WARP_BYTES;
+  uint32_t* skeys = reinterpret_cast<uint32_t*>(wb + NST * P::STAGE);
+  uint8_t* sflags = reinterpret_cast<uint8_t*>(skeys + NST * 32);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sflags + NST * 32);
+  if (lane == 0) {
+    for (int s = 0; s < NST; ++s) tma::mbar_init(bars + s, 1);
+    tma::fence_barrier_init();
+  }
+  __syncwarp();
+  uint32_t phase = 0;  // bit s: parity of the next completion of stage s
+  const char* gbytes = static_cast<const char*>(grads);
+  const char* tbytes = static_cast<const char*>(u.table);
+
+  const int64_t n = *n_dev;
+  const int64_t ntiles = (n + kChunk - 1) / kChunk;
+  const int64_t nwarps = int64_t(gridDim.x) * P::WPB;
+  for (int64_t t = int64_t(blockIdx.x) * P::WPB + warp; t < ntiles; t += nwarps) {
+    const int64_t s0 = t * kChunk;
+    const int64_t s1 = (s0 + kChunk < n) ? s0 + kChunk : n;
+    const uint32_t prev_key = s0 > 0 ? keys[s0 - 1] : kNoKey;
+    const uint32_t next_key = s1 < n ? keys[s1] : kNoKey;
+    const uint32_t first_key = keys[s0];
+    const bool from_prev_tile = (first_key == prev_key);
+    const int nb = int((s1 - s0 + 31) / 32);
+
+    // Stage batch b: its keys / flags to shared memory, its rows in flight.
+    auto issue = [&](int b) {
+      const int st = b % NST;
+      const int64_t j = s0 + int64_t(b) * 32;
+      const int cnt = (s1 - j < 32) ? int(s1 - j) : 32;
+      const uint32_t k = lane < cnt ? __ldcs(keys + j + lane) : kNoKey;
+      const uint32_t p = lane < cnt ? __ldcs(vals + j + lane) : 0u;
+      uint32_t nk = __shfl_down_sync(0xffffffffu, k, 1);
+      if (lane == cnt - 1) nk = (j + cnt < s1) ? keys[j + cnt] : next_key;
+      const bool ends = lane < cnt && nk != k;
+      const bool carry = ends && from_prev_tile && k == first_key;
+      const bool upd = ends && !carry;
+      if (lane < cnt) {
+        skeys[st * 32 + lane] = k;
+        sflags[st * 32 + lane] = uint8_t((ends ? 1 : 0) | (upd ? 2 : 0));
+      }
+      const unsigned updm = __ballot_sync(0xffffffffu, upd);
+      if (lane == 0) tma::mbar_arrive_expect_tx(bars + st, uint32_t(cnt + __popc(updm)) * RB);
+      __syncwarp();
+      unsigned char* gs = wb + st * P::STAGE;
+      if (lane < cnt) tma::bulk_g2s(gs + lane * RB, gbytes + int64_t(p) * RB, RB, bars + st);
+      if (upd) {
+        tma::bulk_g2s(gs + 32 * RB + lane * RB, tbytes + int64_t(k) * RB, RB, bars + st);
+        if (u.state) prefetch_l2(u.state + k);
+      }
+    };
+
+    for (int b = 0; b < NST && b < nb; ++b) issue(b);
+    bool from_prev = from_prev_tile;
+    float acc[EPL];
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) acc[i] = 0.f;
+
+    for (int b = 0; b < nb; ++b) {
+      const int st = b % NST;
+      const int64_t j = s0 + int64_t(b) * 32;
+      const int cnt = (s1 - j < 32) ? int(s1 - j) : 32;
+      if (!tma::mbar_wait(bars + st, (phase >> st) & 1u, limit)) {
+        if (lane == 0) set_err(err, FS_ERR_TIMEOUT);
+        return;  // never seen in practice: the copies are a few microseconds long
+      }
+      phase ^= 1u << st;
+      const unsigned char* gs = wb + st * P::STAGE;
+      // Adagrad state of the rows updated in this batch, one load per lane
+      const uint8_t myf = sflags[st * 32 + lane];
+      float my_state = 0.f;
+      if (lane < cnt && (myf & 2) && u.state) my_state = u.state[skeys[st * 32 + lane]];
+      for (int e = 0; e < cnt; ++e) {
+        float g[EPL];
+        {
+          const V v = *reinterpret_cast<const V*>(gs + e * RB + lane * EPL * ESZ);
+          uint32_t w[(EPL * ESZ + 3) / 4];
+          if constexpr (EPL * ESZ >= 4) memcpy(w, &v, EPL * ESZ);
+          else w[0] = uint32_t(*reinterpret_cast<const unsigned short*>(&v));
+#pragma unroll
+          for (int i = 0; i < EPL; ++i)
+            g[i] = BF16 ? __uint_as_float(((w[i / 2] >> ((i & 1) * 16)) & 0xFFFFu) << 16) : __uint_as_float(w[i]);
+        }
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) acc[i] += g[i];
+        const uint8_t f = sflags[st * 32 + e];
+        const float s_old = __shfl_sync(0xffffffffu, my_state, e);
+        if (f & 1) {
+          if (f & 2) {
+            const uint32_t row = skeys[st * 32 + e];
+            float w[EPL];
+            {
+              const V v = *reinterpret_cast<const V*>(gs + 32 * RB + e * RB + lane * EPL * ESZ);
+              uint32_t x[(EPL * ESZ + 3) / 4];
+              if constexpr (EPL * ESZ >= 4) memcpy(x, &v, EPL * ESZ);
+              else x[0] = uint32_t(*reinterpret_cast<const unsigned short*>(&v));
+#pragma unroll
+              for (int i = 0; i < EPL; ++i)
+                w[i] = BF16 ? __uint_as_float(((x[i / 2] >> ((i & 1) * 16)) & 0xFFFFu) << 16) : __uint_as_float(x[i]);
+            }
+            if (u.optim == FS_ROWWISE_ADAGRAD) {
+              float ss = 0.f;
+#pragma unroll
+              for (int i = 0; i < EPL; ++i) ss = __fmaf_rn(acc[i], acc[i], ss);
+#pragma unroll
+              for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+              ss = __shfl_sync(0xffffffffu, ss, 0);
+              const float snew = s_old + ss / float(D);
+              const float denom = sqrtf(snew) + u.eps;
+              if (lane == 0) u.state[row] = snew;
+#pragma unroll
+              for (int i = 0; i < EPL; ++i) w[i] = w[i] - u.lr * acc[i] / denom;
+            } else {
+#pragma unroll
+              for (int i = 0; i < EPL; ++i) w[i] = w[i] - u.lr * acc[i];
+            }
+            store_slice<BF16, EPL>(u.table, row, lane, w);
+          } else {  // the row began in an earlier tile and ends here
+#pragma unroll
+            for (int i = 0; i < EPL; ++i) carry_head[t * D + lane * EPL + i] = acc[i];
+            if (lane == 0) head_cont[t] = 0;
+          }
+          from_prev = false;
+#pragma unroll
+          for (int i = 0; i < EPL; ++i) acc[i] = 0.f;
+        }
+      }
+      __syncwarp();
+      tma::fence_proxy_async();
+      if (b + NST < nb) issue(b + NST);
+    }
+    // the tile's last row, if it continues past the tile
+    const bool open = (keys[s1 - 1] == next_key);
+    if (open) {
+      if (from_prev) {
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) carry_head[t * D + lane * EPL + i] = acc[i];
+        if (lane == 0) head_cont[t] = 1;
+      } else {
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) carry_tail[t * D + lane * EPL + i] = acc[i];
+      }
+    }
+    if (lane == 0) tail_flag[t] = (open && !from_prev) ? 1 : 0;
+  }
+}
+
 // Rows that cross tile boundaries: carry of the starting tile, then the head
 // carries of the following tiles in order.
 template <bool BF16, int EPL>
@@ -269,10 +457,29 @@ __global__ void __launch_bounds__(kThreads) fixup_kernel(const uint32_t* __restr
     double acc64[EPL];
 #pragma unroll
     for (int i = 0; i < EPL; ++i) acc64[i] = double(carry_tail[t * D + lane * EPL + i]);
-    for (int64_t v = t + 1; v < ntiles; ++v) {
+    // the chain ends at the first following tile whose head does not continue;
+    // read 32 continuation flags at a time, then sum that window's carries in
+    // tile order with several loads in flight
+    for (int64_t v = t + 1; v < ntiles; v += 32) {
+      const uint8_t hc = (v + lane < ntiles) ? head_cont[v + lane] : uint8_t(0);
+      const unsigned stop = __ballot_sync(0xffffffffu, hc == 0);
+      const int last = stop ? (__ffs(stop) - 1) : 31;
+      int j = 0;
+      for (; j + 8 <= last + 1; j += 8) {
+        float c[8][EPL];
 #pragma unroll
-      for (int i = 0; i < EPL; ++i) acc64[i] += double(carry_head[v * D + lane * EPL + i]);
-      if (!head_cont[v]) break;
+        for (int q = 0; q < 8; ++q)
+#pragma unroll
+          for (int i = 0; i < EPL; ++i) c[q][i] = carry_head[(v + j + q) * D + lane * EPL + i];
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+#pragma unroll
+          for (int i = 0; i < EPL; ++i) acc64[i] += double(c[q][i]);
+      }
+      for (; j <= last; ++j)
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) acc64[i] += double(carry_head[(v + j) * D + lane * EPL + i]);
+      if (stop) break;
     }
     float acc[EPL];
 #pragma unroll
@@ -283,9 +490,16 @@ __global__ void __launch_bounds__(kThreads) fixup_kernel(const uint32_t* __restr
 
 template <bool BF16, int EPL>
 void launch_reduce(const uint32_t* k, const uint32_t* v, const int64_t* n_dev, const void* grads, UpdateArgs u,
-                   float* ch, float* ct, uint8_t* hc, uint8_t* tf, cudaStream_t st) {
+                   float* ch, float* ct, uint8_t* hc, uint8_t* tf, int32_t* err, bool staged, cudaStream_t st) {
   const unsigned grid = unsigned(sm_count()) * (2048 / kThreads);
-  reduce_kernel<BF16, EPL><<<grid, kThreads, 0, st>>>(k, v, n_dev, grads, u, ch, ct, hc, tf);
+  if (staged) {
+    using P = Staged<BF16, EPL>;
+    cudaFuncSetAttribute(reduce_staged_kernel<BF16, EPL>, cudaFuncAttributeMaxDynamicSharedMemorySize, P::SMEM);
+    reduce_staged_kernel<BF16, EPL><<<unsigned(sm_count()), P::WPB * 32, P::SMEM, st>>>(
+        k, v, n_dev, grads, u, ch, ct, hc, tf, err, spin_limit());
+  } else {
+    reduce_kernel<BF16, EPL><<<unsigned(sm_count()) * 4, kThreads, 0, st>>>(k, v, n_dev, grads, u, ch, ct, hc, tf);
+  }
   fixup_kernel<BF16, EPL><<<grid, kThreads, 0, st>>>(k, n_dev, u, ch, ct, hc, tf);
 }
 
@@ -304,6 +518,8 @@ BwdLayout bwd_layout(int64_t T, int64_t R, int32_t dim) {
   return L;
 }
 
+bool g_force_unstaged = true;  // measured: the register path beats bulk-copy staging for 256-byte rows
+
 int epl_for(int32_t dim, fs_dtype dtype) {
   if (dim % 32 != 0) return 0;
   int e = dim / 32;
@@ -316,6 +532,8 @@ int epl_for(int32_t dim, fs_dtype dtype) {
 }  // namespace fs
 
 using namespace fs;
+
+extern "C" void fs_debug_reduce_variant(int32_t staged) { fs::g_force_unstaged = staged == 0; }
 
 extern "C" size_t fs_emb_backward_adagrad_workspace_size(int64_t T, int64_t num_rows, int32_t dim, fs_dtype dtype) {
   (void)dtype;
@@ -359,19 +577,17 @@ extern "C" fs_status fs_emb_backward_adagrad(void* table, float* state, int64_t 
   if (s != FS_OK) return s;
   UpdateArgs u{table, optim == FS_ROWWISE_ADAGRAD ? state : nullptr, int(optim), lr, eps};
   const bool bf = dtype == FS_BF16;
+  // bulk copies need 16-byte aligned rows; otherwise the register-staged kernel runs
+  const bool staged = aligned(grads, 16) && aligned(table, 16) && !g_force_unstaged;
+#define FS_REDUCE(BF, E) launch_reduce<BF, E>(sk, sv, W.n_valid, grads, u, carry_head, carry_tail, head_cont, \
+                                               tail_flag, err, staged, st)
   switch (epl) {
-    case 1: bf ? launch_reduce<true, 1>(sk, sv, W.n_valid, grads, u, carry_head, carry_tail, head_cont, tail_flag, st)
-               : launch_reduce<false, 1>(sk, sv, W.n_valid, grads, u, carry_head, carry_tail, head_cont, tail_flag, st);
-      break;
-    case 2: bf ? launch_reduce<true, 2>(sk, sv, W.n_valid, grads, u, carry_head, carry_tail, head_cont, tail_flag, st)
-               : launch_reduce<false, 2>(sk, sv, W.n_valid, grads, u, carry_head, carry_tail, head_cont, tail_flag, st);
-      break;
-    case 4: bf ? launch_reduce<true, 4>(sk, sv, W.n_valid, grads, u, carry_head, carry_tail, head_cont, tail_flag, st)
-               : launch_reduce<false, 4>(sk, sv, W.n_valid, grads, u, carry_head, carry_tail, head_cont, tail_flag, st);
-      break;
-    default: launch_reduce<true, 8>(sk, sv, W.n_valid, grads, u, carry_head, carry_tail, head_cont, tail_flag, st);
-      break;
+    case 1: if (bf) FS_REDUCE(true, 1); else FS_REDUCE(false, 1); break;
+    case 2: if (bf) FS_REDUCE(true, 2); else FS_REDUCE(false, 2); break;
+    case 4: if (bf) FS_REDUCE(true, 4); else FS_REDUCE(false, 4); break;
+    default: FS_REDUCE(true, 8); break;
   }
+#undef FS_REDUCE
   count_launch(launches + 2);
   return launch_status();
 }

@@ -17,6 +17,7 @@ using onesweep::kThreads;
 // Length array as a sort source: key = L[g] (negative lengths flagged), value = g.
 struct SrcLen {
   using Key = uint32_t;
+  static constexpr bool kIndexValue = true;  // value = item index
   const int32_t* L;
   __device__ __forceinline__ bool load(int64_t i, Key& key, uint32_t& val, int32_t* err) const {
     int32_t l = L[i];

@@ -18,6 +18,7 @@ using onesweep::kThreads;
 
 struct SrcShard {
   using Key = int64_t;
+  static constexpr bool kIndexValue = true;  // value = item index
   const int64_t* ids;
   int64_t R;
   int64_t block;

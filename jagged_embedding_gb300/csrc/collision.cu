@@ -136,6 +136,18 @@ __global__ void __launch_bounds__(kThreads) mask_kernel(const int64_t* ids_t, in
   }
 }
 
+// Mask of one array only (the other mask was not requested).
+__global__ void __launch_bounds__(kThreads) mask_one_kernel(const int64_t* ids, int64_t T, int64_t R,
+                                                            const uint32_t* other, uint8_t* is_co) {
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  for (int64_t j = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; j < T; j += stride) {
+    const int64_t id = __ldcs(ids + j);
+    uint8_t v = 0;
+    if (id >= 0 && id < R) v = (__ldg(other + (uint64_t(id) >> 5)) >> (uint32_t(id) & 31u)) & 1u;
+    is_co[j] = v;
+  }
+}
+
 struct CollLayout {
   int64_t nwords, tiles;
   size_t bitmap_bytes() const { return align_up(size_t(nwords) * sizeof(uint32_t)); }
@@ -180,7 +192,7 @@ extern "C" fs_status fs_collision_split(const int64_t* ids_t, int64_t T_t, const
       num_rows > (int64_t(1) << 32) || n < 1 || cap_rows < 0 || !counts || !co_shard_off || !ex_t_shard_off ||
       !ex_next_shard_off || !err)
     return FS_ERR_INVALID_ARG;
-  if ((T_t > 0 && (!ids_t || !is_co_t)) || (T_next > 0 && (!ids_next || !is_co_next))) return FS_ERR_INVALID_ARG;
+  if ((T_t > 0 && !ids_t) || (T_next > 0 && !ids_next)) return FS_ERR_INVALID_ARG;
   if (cap_rows > 0 && (!co || !ex_t || !ex_next)) return FS_ERR_INVALID_ARG;
   if ((ids_t && !aligned(ids_t, 8)) || (ids_next && !aligned(ids_next, 8)) || !aligned(counts, 8) ||
       (co && !aligned(co, 8)) || (ex_t && !aligned(ex_t, 8)) || (ex_next && !aligned(ex_next, 8)))
@@ -210,9 +222,16 @@ extern "C" fs_status fs_collision_split(const int64_t* ids_t, int64_t T_t, const
                                                          ex_next_shard_off, status, counter, err, spin_limit(),
                                                          debug_skip_tile());
   ++launches;
-  if (T_t + T_next > 0) {
+  // masks: either may be NULL (not wanted); then that pass over its IDs is skipped
+  if (is_co_t && is_co_next && T_t + T_next > 0) {
     mask_kernel<<<grid_for(T_t + T_next), kThreads, 0, st>>>(ids_t, T_t, ids_next, T_next, num_rows, bm_t, bm_next,
                                                              is_co_t, is_co_next);
+    ++launches;
+  } else if (is_co_t && T_t > 0) {
+    mask_one_kernel<<<grid_for(T_t), kThreads, 0, st>>>(ids_t, T_t, num_rows, bm_next, is_co_t);
+    ++launches;
+  } else if (is_co_next && T_next > 0) {
+    mask_one_kernel<<<grid_for(T_next), kThreads, 0, st>>>(ids_next, T_next, num_rows, bm_t, is_co_next);
     ++launches;
   }
   count_launch(launches);

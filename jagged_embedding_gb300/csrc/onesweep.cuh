@@ -45,13 +45,21 @@ __global__ void __launch_bounds__(kThreads) histogram_kernel(Src src, int64_t co
   if (threadIdx.x == 0) s_valid = 0;
   __syncthreads();
   uint32_t my_valid = 0;
+  const int lane = threadIdx.x & 31;
   const int64_t stride = int64_t(gridDim.x) * blockDim.x;
   for (int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; idx < count; idx += stride) {
+    const unsigned act = __activemask();
     typename Src::Key k;
     uint32_t v;
-    if (!src.load(idx, k, v, err)) continue;
-    ++my_valid;
-    for (int p = 0; p < npasses; ++p) atomicAdd(&sh[p * nb + src.digit(k, p * bits, bits)], 1u);
+    const bool ok = src.load(idx, k, v, err);
+    my_valid += ok ? 1u : 0u;
+    // warp-aggregated increments: one shared atomic per distinct digit of the warp
+    // (Zipf-hot keys would otherwise serialise on one counter)
+    for (int p = 0; p < npasses; ++p) {
+      const uint32_t d = ok ? src.digit(k, p * bits, bits) : 0xFFFFFFFFu;
+      const unsigned peers = __match_any_sync(act, d);
+      if (ok && (__ffs(peers) - 1) == lane) atomicAdd(&sh[p * nb + d], uint32_t(__popc(peers)));
+    }
   }
   for (int o = 16; o > 0; o >>= 1) my_valid += __shfl_xor_sync(0xffffffffu, my_valid, o);
   if ((threadIdx.x & 31) == 0 && my_valid) atomicAdd(&s_valid, my_valid);
@@ -85,7 +93,7 @@ static __global__ void __launch_bounds__(kThreads) digit_scan_kernel(const uint3
 // tile_counter: zeroed int (dynamic tile order = launch order, so a tile
 // only ever waits on tiles that have already started).
 template <class Src, class Dst>
-__global__ void __launch_bounds__(kThreads) pass_kernel(Src src, Dst dst, int shift, int bits, int nb,
+__global__ void __launch_bounds__(kThreads, 3) pass_kernel(Src src, Dst dst, int shift, int bits, int nb,
                                                         const uint32_t* digit_offsets, uint64_t* status,
                                                         int* tile_counter, const int64_t* count_dev,
                                                         int64_t count_host, int32_t* err, int64_t limit) {
@@ -111,15 +119,20 @@ __global__ void __launch_bounds__(kThreads) pass_kernel(Src src, Dst dst, int sh
   const int64_t base = tile * kTile;
   if (base >= count) return;  // trailing tile: no later valid tile looks back at it
 
+  // Registers per item: the key, one packed word (digit in bits 20..31, rank /
+  // local position in bits 0..19) and, only for sources whose value is not the
+  // item index, the value.
   KeyT key[kItems];
-  uint32_t val[kItems];
-  uint32_t dig[kItems];
-  uint32_t rank[kItems];
+  uint32_t val[Src::kIndexValue ? 1 : kItems];
+  uint32_t pk[kItems];
+  constexpr uint32_t kSkipPk = 0xFFF00000u;
 #pragma unroll
   for (int i = 0; i < kItems; ++i) {
     int64_t idx = base + int64_t(warp) * 32 * kItems + i * 32 + lane;
-    bool ok = idx < count && src.load(idx, key[i], val[i], nullptr);
-    dig[i] = ok ? src.digit(key[i], shift, bits) : kSkip;
+    uint32_t v = 0;
+    bool ok = idx < count && src.load(idx, key[i], v, nullptr);
+    if constexpr (!Src::kIndexValue) val[i] = v;
+    pk[i] = ok ? (src.digit(key[i], shift, bits) << 20) : kSkipPk;
   }
   for (int j = threadIdx.x; j < kWarps * nb; j += kThreads) warp_hist[j] = 0;
   __syncthreads();
@@ -128,13 +141,14 @@ __global__ void __launch_bounds__(kThreads) pass_kernel(Src src, Dst dst, int sh
   uint32_t* wh = warp_hist + warp * nb;
 #pragma unroll
   for (int i = 0; i < kItems; ++i) {
-    const uint32_t d = dig[i];
-    const unsigned peers = __match_any_sync(0xffffffffu, d);
+    const uint32_t d = pk[i] >> 20;
+    const bool skip = pk[i] == kSkipPk;
+    const unsigned peers = __match_any_sync(0xffffffffu, pk[i]);
     const unsigned lt = __popc(peers & lanemask_lt());
-    const uint32_t b = (d != kSkip) ? wh[d] : 0u;
-    rank[i] = b + lt;
+    const uint32_t b = skip ? 0u : wh[d];
+    if (!skip) pk[i] |= b + lt;
     __syncwarp();
-    if (d != kSkip && lt == 0) wh[d] = b + __popc(peers);
+    if (!skip && lt == 0) wh[d] = b + __popc(peers);
     __syncwarp();
   }
   __syncthreads();
@@ -168,17 +182,22 @@ __global__ void __launch_bounds__(kThreads) pass_kernel(Src src, Dst dst, int sh
     if (threadIdx.x == 0) scratch[40] = tot;
   }
   __syncthreads();
-  uint32_t lpos[kItems];
 #pragma unroll
   for (int i = 0; i < kItems; ++i)
-    lpos[i] = (dig[i] != kSkip) ? local_start[dig[i]] + warp_hist[warp * nb + dig[i]] + rank[i] : 0u;
+    if (pk[i] != kSkipPk) {
+      const uint32_t d = pk[i] >> 20;
+      pk[i] = local_start[d] + warp_hist[warp * nb + d] + (pk[i] & 0xFFFFFu);  // tile-local position
+    }
   const uint32_t nvalid = scratch[40];
   __syncthreads();  // warp_hist is dead; its space becomes the staging area
 #pragma unroll
   for (int i = 0; i < kItems; ++i)
-    if (dig[i] != kSkip) {
-      stage_k[lpos[i]] = key[i];
-      stage_v[lpos[i]] = val[i];
+    if (pk[i] != kSkipPk) {
+      stage_k[pk[i]] = key[i];
+      if constexpr (Src::kIndexValue)
+        stage_v[pk[i]] = uint32_t(base + int64_t(warp) * 32 * kItems + i * 32 + lane);
+      else
+        stage_v[pk[i]] = val[i];
     }
   __syncthreads();
   for (uint32_t j = threadIdx.x; j < nvalid; j += kThreads) {
@@ -194,6 +213,7 @@ __global__ void __launch_bounds__(kThreads) pass_kernel(Src src, Dst dst, int sh
 // Plain (uint32 key, uint32 value) arrays; digit = bits [shift, shift+bits).
 struct SrcU32 {
   using Key = uint32_t;
+  static constexpr bool kIndexValue = false;
   const uint32_t* k;
   const uint32_t* v;
   __device__ __forceinline__ bool load(int64_t i, Key& key, uint32_t& val, int32_t*) const {

@@ -95,14 +95,18 @@ class Pipeline:
                                shard_offsets=s.shard_offsets, err=self.err, ws=self.ws, T=T)
         s.T = T
 
-    def collision(self, slot_t, slot_next):
-        """Collision / exclusive split of (t, t+1) (Algorithm 2 line 10); masks are batch-major."""
+    def collision(self, slot_t, slot_next, want_next_mask=True):
+        """Collision / exclusive split of (t, t+1) (Algorithm 2 line 10); masks are batch-major.
+
+        The mask of t+1 only serves the prioritized order's masked gathers of t+1;
+        the synchronous order skips it.
+        """
         a, b = self.slots[slot_t], self.slots[slot_next]
         out = dict(self.coll)
         out["is_co_t"] = self.masks[slot_t]
         out["is_co_next"] = self.masks[slot_next]
         B.fs_collision_split(a.ids, b.ids, self.w.R, self.w.n, cap_rows=self.cap_rows, out=out, err=self.err,
-                             ws=self.ws, T_t=a.T, T_next=b.T)
+                             ws=self.ws, T_t=a.T, T_next=b.T, want_next_mask=want_next_mask)
 
     def gather(self, slot, out_idx=0, mask=None, sel=1):
         s = self.slots[slot]
@@ -123,7 +127,7 @@ class Pipeline:
         nxt = 1 - cur
         if has_next:
             self.prepare(nxt_batch, nxt)
-            self.collision(cur, nxt)
+            self.collision(cur, nxt, want_next_mask=False)
         self.gather(cur)
         if self.w.has_update:
             if has_next:

@@ -220,6 +220,20 @@ def test_collision_matches_oracle(R, n, Tt, Tn):
     assert np.array_equal(to_np(out["is_co_next"]), ref["is_co_next"])
 
 
+def test_collision_single_mask():
+    """Either mask may be omitted; the other one is unchanged."""
+    rng = np.random.default_rng(77)
+    R = 500_000
+    a = rng.integers(0, R, 200_000).astype(np.int64)
+    b = rng.integers(0, R, 150_000).astype(np.int64)
+    ref = oracle.collision_split(a, b, R, 16)
+    out, err = B.fs_collision_split(torch.from_numpy(a).to(DEV), torch.from_numpy(b).to(DEV), R, 16,
+                                    want_next_mask=False)
+    _check(err)
+    assert np.array_equal(to_np(out["is_co_t"]), ref["is_co_t"])
+    assert np.array_equal(to_np(out["co"])[: to_np(out["counts"])[0]], ref["co"])
+
+
 def test_collision_capacity_error():
     a = torch.arange(100, dtype=torch.int64, device=DEV)
     out, err = B.fs_collision_split(a, a.flip(0).contiguous(), 1000, 4, cap_rows=10)
