@@ -378,7 +378,7 @@ def run_gpu(args):
                    "parallelism": f"replicas x{ws}"},
         "hbm_roofline_frac_step": step_bytes / secs / (hbm_gbs * 1e9),
         "algorithmic_bytes_per_step": step_bytes / K,
-        "roofline": {"kernel": "fs_emb_gather (gather_vec16_kernel)", "bound": "hbm", "achieved": achieved,
+        "roofline": {"kernel": "fs_emb_gather (gather_rows_kernel<16>)", "bound": "hbm", "achieved": achieved,
                      "peak": hbm_gbs, "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / hbm_gbs,
                      "traffic": traffic, "algorithmic_bytes_per_launch": gbytes, "avg_launch_ms": gather_ms},
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clk,

@@ -6,8 +6,9 @@
 //
 // Pipeline (all on `stream`, sizes stay on the device):
 //   1. stable LSD radix sort of (row, position) over the positions the phase
-//      selects (onesweep passes; the first pass reads the int64 IDs and the
-//      collision mask directly, so unselected positions are never copied);
+//      selects (reduce-then-scan counting passes of at most 9 bits; the first
+//      pass reads the int64 IDs and the collision mask directly, so
+//      unselected positions are never copied);
 //   2. reduce: the sorted array is cut into fixed 2048-entry tiles, one warp
 //      per tile, so a Zipf-hot row with millions of positions is spread over
 //      many warps and a long tail of single-position rows costs the same per
@@ -22,13 +23,13 @@
 // are bit-identical from run to run.
 #include <cuda_bf16.h>
 
-#include "onesweep.cuh"
+#include "radix.cuh"
 #include "tma.cuh"
 
 namespace fs {
 namespace {
 
-using onesweep::kThreads;
+using radix::kThreads;
 constexpr int kChunk = 2048;                 // sorted entries per reduce tile
 constexpr uint32_t kNoKey = 0xFFFFFFFFu;     // rows are < num_rows < 2^32
 
@@ -504,14 +505,14 @@ void launch_reduce(const uint32_t* k, const uint32_t* v, const int64_t* n_dev, c
 }
 
 struct BwdLayout {
-  onesweep::SortPlan plan;
+  radix::SortPlan plan;
   int64_t max_tiles = 0;
   size_t carry_bytes = 0, flag_bytes = 0;
 };
 
 BwdLayout bwd_layout(int64_t T, int64_t R, int32_t dim) {
   BwdLayout L;
-  L.plan = onesweep::SortPlan(T, onesweep::bits_for(uint64_t(R > 0 ? R - 1 : 0)));
+  L.plan = radix::SortPlan(T, radix::bits_for(uint64_t(R > 0 ? R - 1 : 0)));
   L.max_tiles = (T + kChunk - 1) / kChunk;
   L.carry_bytes = align_up(size_t(L.max_tiles) * size_t(dim) * sizeof(float));
   L.flag_bytes = align_up(size_t(L.max_tiles));
@@ -562,8 +563,8 @@ extern "C" fs_status fs_emb_backward_adagrad(void* table, float* state, int64_t 
 
   BwdLayout L = bwd_layout(T, num_rows, dim);
   WsCursor cur(ws, ws_bytes);
-  onesweep::SortWs W;
-  if (!onesweep::carve_sort_ws(L.plan, cur, W)) return FS_ERR_WORKSPACE;
+  radix::SortWs W;
+  if (!radix::carve_sort_ws(L.plan, cur, W)) return FS_ERR_WORKSPACE;
   float* carry_head = cur.take<float>(size_t(L.max_tiles) * dim);
   float* carry_tail = cur.take<float>(size_t(L.max_tiles) * dim);
   uint8_t* head_cont = cur.take<uint8_t>(size_t(L.max_tiles));
@@ -573,13 +574,13 @@ extern "C" fs_status fs_emb_backward_adagrad(void* table, float* state, int64_t 
   int launches = 0;
   uint32_t *sk = nullptr, *sv = nullptr;
   SrcRows src{ids, is_co, int(phase), num_rows};
-  fs_status s = onesweep::run_sort(src, L.plan, W, err, st, &sk, &sv, &launches);
+  fs_status s = radix::run_sort(src, L.plan, W, err, st, &sk, &sv, &launches);
   if (s != FS_OK) return s;
   UpdateArgs u{table, optim == FS_ROWWISE_ADAGRAD ? state : nullptr, int(optim), lr, eps};
   const bool bf = dtype == FS_BF16;
   // bulk copies need 16-byte aligned rows; otherwise the register-staged kernel runs
   const bool staged = aligned(grads, 16) && aligned(table, 16) && !g_force_unstaged;
-#define FS_REDUCE(BF, E) launch_reduce<BF, E>(sk, sv, W.n_valid, grads, u, carry_head, carry_tail, head_cont, \
+#define FS_REDUCE(BF, E) launch_reduce<BF, E>(sk, sv, W.pass.n_valid, grads, u, carry_head, carry_tail, head_cont, \
                                                tail_flag, err, staged, st)
   switch (epl) {
     case 1: if (bf) FS_REDUCE(true, 1); else FS_REDUCE(false, 1); break;

@@ -4,15 +4,15 @@
 //
 // Both partitions start from the samples ordered by (UIH length, global
 // index): a stable LSD radix sort of the lengths with the index as value
-// (onesweep passes).  FBS then deals sorted positions to ranks in snake order
+// (reduce-then-scan counting passes).  FBS then deals sorted positions to ranks in snake order
 // with a closed form per position; VBS scans fixed-point weights L^alpha with
 // a single-pass decoupled look-back scan and cuts the prefix into n segments.
-#include "onesweep.cuh"
+#include "radix.cuh"
 
 namespace fs {
 namespace {
 
-using onesweep::kThreads;
+using radix::kThreads;
 
 // Length array as a sort source: key = L[g] (negative lengths flagged), value = g.
 struct SrcLen {
@@ -198,7 +198,7 @@ using namespace fs;
 extern "C" size_t fs_balance_fbs_workspace_size(int64_t S, int32_t n) {
   (void)n;
   if (S < 0) return 0;
-  return onesweep::SortPlan(S, kLenKeyBits).bytes() + 256;
+  return radix::SortPlan(S, kLenKeyBits).bytes() + 256;
 }
 
 extern "C" fs_status fs_balance_fbs(const int32_t* uih_len, int64_t S, int32_t n, int32_t* perm,
@@ -215,12 +215,12 @@ extern "C" fs_status fs_balance_fbs(const int32_t* uih_len, int64_t S, int32_t n
     count_launch(1);
     return launch_status();
   }
-  onesweep::SortPlan P(S, kLenKeyBits);
+  radix::SortPlan P(S, kLenKeyBits);
   WsCursor cur(ws, ws_bytes);
-  onesweep::SortWs W;
-  if (!onesweep::carve_sort_ws(P, cur, W)) return FS_ERR_WORKSPACE;
+  radix::SortWs W;
+  if (!radix::carve_sort_ws(P, cur, W)) return FS_ERR_WORKSPACE;
   uint32_t *sk = nullptr, *sv = nullptr;
-  fs_status s = onesweep::run_sort(SrcLen{uih_len}, P, W, err, st, &sk, &sv, &launches);
+  fs_status s = radix::run_sort(SrcLen{uih_len}, P, W, err, st, &sk, &sv, &launches);
   if (s != FS_OK) return s;
   fbs_assign_kernel<<<grid_for(S > n ? S : n + 1), kThreads, 0, st>>>(sv, S, n, perm, rank_offsets);
   count_launch(launches + 1);
@@ -258,11 +258,11 @@ extern "C" fs_status fs_balance_vbs(const int32_t* uih_len, int64_t S, int32_t n
 
   const uint32_t* order = nullptr;
   if (sort_by_len) {
-    onesweep::SortPlan SP(S, kLenKeyBits);
-    onesweep::SortWs W;
-    if (!onesweep::carve_sort_ws(SP, cur, W)) return FS_ERR_WORKSPACE;
+    radix::SortPlan SP(S, kLenKeyBits);
+    radix::SortWs W;
+    if (!radix::carve_sort_ws(SP, cur, W)) return FS_ERR_WORKSPACE;
     uint32_t *sk = nullptr, *sv = nullptr;
-    fs_status s = onesweep::run_sort(SrcLen{uih_len}, SP, W, err, st, &sk, &sv, &launches);
+    fs_status s = radix::run_sort(SrcLen{uih_len}, SP, W, err, st, &sk, &sv, &launches);
     if (s != FS_OK) return s;
     order = sv;
   }

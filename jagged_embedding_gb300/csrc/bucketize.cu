@@ -3,18 +3,18 @@
 // Algorithm 2 line 8 (IDs AllToAll to shard-major) and §4.2.
 //
 // Shard-major order is one stable counting-sort pass keyed by the shard of
-// each ID (one onesweep digit pass with n digit values): per-tile warp
-// multisplit, decoupled look-back across tiles, shared-memory staging so that
-// the writes of every shard run are coalesced.  The send-splits matrix is
+// each ID (n digit values): per-tile shard counts, their scan, then a per-tile
+// warp multisplit with shared-memory staging so that the writes of every shard
+// run are coalesced.  The send-splits matrix is
 // computed afterwards from the sorted positions (inside a shard they are
 // ascending, so each (source rank, shard) count is two binary searches),
 // which is the local recomputation of the AllToAll metadata.
-#include "onesweep.cuh"
+#include "radix.cuh"
 
 namespace fs {
 namespace {
 
-using onesweep::kThreads;
+using radix::kThreads;
 
 struct SrcShard {
   using Key = int64_t;
@@ -78,11 +78,7 @@ __global__ void splits_kernel(const int32_t* pos, const int64_t* shard_offsets, 
   }
 }
 
-size_t bucketize_bytes(int64_t T, int32_t n) {
-  const int64_t tiles = onesweep::num_tiles(T);
-  return align_up(4 * onesweep::kMaxBins * sizeof(uint32_t)) + align_up(sizeof(int64_t) + 4 * sizeof(int)) +
-         align_up(size_t(tiles) * size_t(n) * sizeof(uint64_t)) + align_up(4 * onesweep::kMaxBins * sizeof(uint32_t));
-}
+size_t bucketize_bytes(int64_t T, int32_t n) { return radix::pass_ws_bytes(T, n); }
 
 }  // namespace
 }  // namespace fs
@@ -99,7 +95,7 @@ extern "C" fs_status fs_bucketize_rowwise(const int64_t* ids, int64_t T, const i
                                           int64_t* shard_offsets, int32_t* err, void* ws, size_t ws_bytes,
                                           fs_stream_t stream) {
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if (T < 0 || T > INT32_MAX || n < 1 || n > onesweep::kMaxBins || num_rows < 1 || !rank_id_offsets || !splits ||
+  if (T < 0 || T > INT32_MAX || n < 1 || n > radix::kMaxBins || num_rows < 1 || !rank_id_offsets || !splits ||
       !shard_offsets || !err)
     return FS_ERR_INVALID_ARG;
   if (T > 0 && (!ids || !sm_ids || !pos)) return FS_ERR_INVALID_ARG;
@@ -108,38 +104,18 @@ extern "C" fs_status fs_bucketize_rowwise(const int64_t* ids, int64_t T, const i
     return FS_ERR_ALIGNMENT;
   if (ws_bytes < fs_bucketize_rowwise_workspace_size(T, n) || !ws) return FS_ERR_WORKSPACE;
 
-  const int64_t tiles = onesweep::num_tiles(T);
   WsCursor cur(ws, ws_bytes);
-  const size_t zero_bytes = align_up(4 * onesweep::kMaxBins * sizeof(uint32_t)) +
-                            align_up(sizeof(int64_t) + 4 * sizeof(int)) +
-                            align_up(size_t(tiles) * size_t(n) * sizeof(uint64_t));
-  unsigned char* zero = cur.take<unsigned char>(zero_bytes);
-  uint32_t* offs = cur.take<uint32_t>(4 * onesweep::kMaxBins);
-  if (!cur.ok) return FS_ERR_WORKSPACE;
-  uint32_t* hist = reinterpret_cast<uint32_t*>(zero);
-  unsigned char* p = zero + align_up(4 * onesweep::kMaxBins * sizeof(uint32_t));
-  int64_t* n_valid = reinterpret_cast<int64_t*>(p);
-  int* counter = reinterpret_cast<int*>(p + sizeof(int64_t));
-  uint64_t* status = reinterpret_cast<uint64_t*>(p + align_up(sizeof(int64_t) + 4 * sizeof(int)));
-  if (cudaMemsetAsync(zero, 0, zero_bytes, st) != cudaSuccess) return FS_ERR_CUDA;
-
+  radix::PassWs P;
+  if (!radix::carve_pass_ws(T, n, cur, P)) return FS_ERR_WORKSPACE;
   const int64_t block = (num_rows + n - 1) / n;
   SrcShard src{ids, num_rows, block, 1.0 / static_cast<double>(block), n};
   int launches = 0;
   if (T > 0) {
-    int64_t hgrid = (T + kThreads - 1) / kThreads, hcap = int64_t(sm_count()) * 8;
-    if (hgrid > hcap) hgrid = hcap;
-    onesweep::histogram_kernel<SrcShard><<<unsigned(hgrid), kThreads, 0, st>>>(src, T, 1, 0, n, hist, n_valid, err);
-    onesweep::digit_scan_kernel<<<1, kThreads, 0, st>>>(hist, offs, n);
-    const size_t smem = onesweep::pass_smem_bytes<int64_t>();
-    onesweep::set_pass_smem(onesweep::pass_kernel<SrcShard, DstShardMajor>, smem);
-    onesweep::pass_kernel<SrcShard, DstShardMajor><<<unsigned(tiles), kThreads, smem, st>>>(
-        src, DstShardMajor{sm_ids, pos}, 0, 0, n, offs, status, counter, nullptr, T, err, spin_limit());
-    launches += 3;
+    radix::run_pass(src, DstShardMajor{sm_ids, pos}, 0, 0, n, nullptr, T, P, err, st, &launches);
   } else {
-    if (cudaMemsetAsync(offs, 0, size_t(n) * sizeof(uint32_t), st) != cudaSuccess) return FS_ERR_CUDA;
+    if (cudaMemsetAsync(P.digit_base, 0, size_t(n) * sizeof(uint32_t), st) != cudaSuccess) return FS_ERR_CUDA;
   }
-  shard_offsets_kernel<<<1, kThreads, 0, st>>>(offs, n, T, shard_offsets);
+  shard_offsets_kernel<<<1, kThreads, 0, st>>>(P.digit_base, n, T, shard_offsets);
   int64_t nn = int64_t(n) * n;
   int64_t g = (nn + kThreads - 1) / kThreads;
   if (g > int64_t(sm_count()) * 8) g = int64_t(sm_count()) * 8;

@@ -124,56 +124,6 @@ __device__ __forceinline__ uint64_t warp_lookback(uint64_t* status, int64_t stri
   return excl;
 }
 
-// Look-back by one thread (used per digit / per counter when many counters
-// are scanned at once).  Same contract as warp_lookback.  The predecessors'
-// words are read kWin at a time (independent loads), so a walk over tiles
-// that have published only their aggregate costs one memory latency per kWin
-// tiles instead of one per tile.
-__device__ __forceinline__ uint64_t thread_lookback(uint64_t* status, int64_t stride, int64_t tile, uint64_t aggregate,
-                                                    int32_t* err, int64_t limit, bool publish = true) {
-  constexpr int kWin = 8;
-  if (tile == 0) {
-    if (publish) st_volatile_u64(status, kFlagInc | aggregate);
-    return 0;
-  }
-  if (publish) st_volatile_u64(status + tile * stride, kFlagAgg | aggregate);
-  uint64_t excl = 0;
-  int64_t pred = tile - 1;
-  int64_t polls = 0;
-  bool done = false;
-  while (!done) {
-    uint64_t w[kWin];
-#pragma unroll
-    for (int i = 0; i < kWin; ++i) w[i] = (pred - i >= 0) ? ld_volatile_u64(status + (pred - i) * stride) : kFlagInc;
-    int used = 0;
-#pragma unroll
-    for (int i = 0; i < kWin; ++i) {
-      const uint64_t flag = w[i] >> 62;
-      if (flag == 0) break;                   // stop at the first word that is not ready
-      excl += w[i] & kValMask;
-      used = i + 1;
-      if (flag == 2) {
-        done = true;
-        break;
-      }
-    }
-    if (done) break;
-    if (used > 0) {
-      pred -= used;
-      polls = 0;
-      continue;
-    }
-    if (++polls > limit || (polls % 1024 == 0 && read_err(err) != 0)) {
-      set_err(err, FS_ERR_TIMEOUT);
-      excl = 0;
-      break;
-    }
-    __nanosleep(32);
-  }
-  if (publish) st_volatile_u64(status + tile * stride, kFlagInc | ((excl + aggregate) & kValMask));
-  return excl;
-}
-
 // Block-wide exclusive scan of one value per thread (blockDim.x <= 1024,
 // multiple of 32).  `smem` needs 32 slots.  Returns exclusive prefix, sets
 // *total (same in all threads).
