@@ -79,6 +79,27 @@ fs_status fs_balance_fbs(const int32_t* uih_len, int64_t S, int32_t n, int32_t* 
                          int32_t* err, void* ws, size_t ws_bytes, fs_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * FBS partition without caller workspace (no counterpart on the pages: the
+ * method itself says nothing about memory ownership).
+ * For callers that cannot allocate device memory when they partition a batch
+ * -- code running while a memory pool is frozen or torn down, a plugin inside
+ * another framework's process whose allocator it does not own, a step with a
+ * fixed memory plan.  Same result as fs_balance_fbs; the sort's scratch is a
+ * fixed array inside the library (about 4.7 MB of device memory, held on every
+ * device that loads the library until the process exits), so this call
+ * allocates nothing.
+ *   S must be <= 262144 (FS_ERR_INVALID_ARG otherwise).
+ *   The first call on a device looks the array's device address up
+ *   (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   Every call shares the one array: calls that overlap on the GPU (two
+ *   streams, two host threads) race and must be serialised by the caller.
+ *   The call clears the counters it needs itself; leftovers of earlier calls
+ *   do not matter.
+ * ---------------------------------------------------------------------- */
+fs_status fs_balance_fbs_noalloc(const int32_t* uih_len, int64_t S, int32_t n, int32_t* perm, int64_t* rank_offsets,
+                                 int32_t* err, fs_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * VBS partition -- FreeScale §4.1, VBS paragraph.  Sample weight L^alpha,
  * kept in fixed point w = round_half_even(256 * L^alpha) (uint64; L^alpha is
  * L*sqrt(L) for alpha = 1.5 and the matching exact products for alpha in

@@ -30,7 +30,8 @@ STATUS = {0: "ok", 1: "invalid argument", 2: "ID outside [0, num_rows)", 3: "mal
           7: "CUDA runtime error", 8: "misaligned pointer"}
 
 EXPORTS = [
-    "fs_balance_fbs_workspace_size", "fs_balance_fbs", "fs_balance_vbs_workspace_size", "fs_balance_vbs",
+    "fs_balance_fbs_workspace_size", "fs_balance_fbs", "fs_balance_fbs_noalloc", "fs_balance_vbs_workspace_size",
+    "fs_balance_vbs",
     "fs_permute_jagged_workspace_size", "fs_permute_jagged", "fs_bucketize_rowwise_workspace_size",
     "fs_bucketize_rowwise", "fs_collision_split_workspace_size", "fs_collision_split", "fs_emb_gather",
     "fs_emb_backward_adagrad_workspace_size", "fs_emb_backward_adagrad", "fs_check", "fs_status_string",
@@ -59,6 +60,7 @@ def lib():
     sig = {
         "fs_balance_fbs_workspace_size": ([i64, i32], sz),
         "fs_balance_fbs": ([P, i64, i32, P, P, P, P, sz, P], C.c_int),
+        "fs_balance_fbs_noalloc": ([P, i64, i32, P, P, P, P], C.c_int),
         "fs_balance_vbs_workspace_size": ([i64, i32], sz),
         "fs_balance_vbs": ([P, i64, i32, f64, i32, P, P, P, P, P, sz, P], C.c_int),
         "fs_permute_jagged_workspace_size": ([i64], sz),
@@ -163,6 +165,19 @@ def fs_balance_fbs(uih_len, n, perm=None, rank_offsets=None, err=None, ws=None):
     ws = workspace(need, dev) if ws is None else ws
     _ok(lib().fs_balance_fbs(_ptr(uih_len), S, n, _ptr(perm), _ptr(rank_offsets), _ptr(err), _ptr(ws), ws.numel(),
                              _stream(dev)), "fs_balance_fbs")
+    return perm, rank_offsets, err
+
+
+def fs_balance_fbs_noalloc(uih_len, n, perm, rank_offsets, err):
+    """FBS partition that allocates nothing: the caller passes every output, the
+    scratch is a fixed array inside the library (S <= 262144; calls must not overlap)."""
+    dev = uih_len.device
+    _need(uih_len, torch.int32, "uih_len")
+    _need(perm, torch.int32, "perm", uih_len.numel())
+    _need(rank_offsets, torch.int64, "rank_offsets", n + 1)
+    _need(err, torch.int32, "err", 1)
+    _ok(lib().fs_balance_fbs_noalloc(_ptr(uih_len), uih_len.numel(), n, _ptr(perm), _ptr(rank_offsets), _ptr(err),
+                                     _stream(dev)), "fs_balance_fbs_noalloc")
     return perm, rank_offsets, err
 
 

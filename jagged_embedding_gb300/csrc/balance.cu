@@ -7,6 +7,8 @@
 // (reduce-then-scan counting passes).  FBS then deals sorted positions to ranks in snake order
 // with a closed form per position; VBS scans fixed-point weights L^alpha with
 // a single-pass decoupled look-back scan and cuts the prefix into n segments.
+#include <mutex>
+
 #include "radix.cuh"
 
 namespace fs {
@@ -225,6 +227,66 @@ extern "C" fs_status fs_balance_fbs(const int32_t* uih_len, int64_t S, int32_t n
   fbs_assign_kernel<<<grid_for(S > n ? S : n + 1), kThreads, 0, st>>>(sv, S, n, perm, rank_offsets);
   count_launch(launches + 1);
   return launch_status();
+}
+
+// ---------------------------------------------------------------------------
+// FBS without caller workspace.  Some callers cannot allocate device memory
+// at the moment they need the partition: code that runs while a memory pool
+// is frozen or being torn down, a runtime whose allocator they do not own
+// (for example a plugin inside another framework's process), or a step whose
+// memory plan is fixed in advance.  For them this variant keeps the sort's
+// scratch in a fixed array in the library's own device memory, so the call
+// itself allocates nothing.
+namespace fs {
+namespace {
+
+constexpr int64_t kNoAllocMaxS = int64_t(1) << 18;  // 262144 samples
+
+// Same layout arithmetic as radix::SortPlan::bytes() for S = kNoAllocMaxS and
+// 31-bit keys (4 passes of 8 bits: 256 digit values), at compile time.
+constexpr size_t ce_align(size_t x) { return (x + 255) / 256 * 256; }
+constexpr size_t kNoAllocTiles = size_t((kNoAllocMaxS + radix::kTile - 1) / radix::kTile);
+constexpr size_t kNoAllocScratchBytes = ce_align(256 * kNoAllocTiles * sizeof(uint32_t)) +
+                                        2 * ce_align(radix::kMaxBins * sizeof(uint32_t)) + ce_align(sizeof(int64_t)) +
+                                        4 * ce_align(size_t(kNoAllocMaxS) * sizeof(uint32_t));
+
+// Lives for as long as the library is loaded, on every device that uses it.
+static __device__ __align__(256) unsigned char g_fbs_scratch[kNoAllocScratchBytes + 256];
+
+std::mutex g_scratch_mu;
+void* g_scratch_ptr[64] = {nullptr};
+
+// Device address of g_fbs_scratch on the current device, looked up once per
+// device (host code only sees a stand-in symbol, never a device address).
+fs_status scratch_for_current_device(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FS_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_scratch_mu);
+  if (g_scratch_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_fbs_scratch) != cudaSuccess || p == nullptr) return FS_ERR_CUDA;
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return FS_OK;
+}
+
+}  // namespace
+}  // namespace fs
+
+extern "C" fs_status fs_balance_fbs_noalloc(const int32_t* uih_len, int64_t S, int32_t n, int32_t* perm,
+                                            int64_t* rank_offsets, int32_t* err, fs_stream_t stream) {
+  if (S > kNoAllocMaxS) return FS_ERR_INVALID_ARG;  // beyond the fixed scratch array
+  if (n < 1 || S < 0 || !rank_offsets || !err) return FS_ERR_INVALID_ARG;
+  if (S > 0 && (!uih_len || !perm)) return FS_ERR_INVALID_ARG;
+  void* scratch = nullptr;
+  fs_status s = scratch_for_current_device(&scratch);
+  if (s != FS_OK) return s;
+  const size_t need = radix::SortPlan(S, kLenKeyBits).bytes();
+  if (need > kNoAllocScratchBytes) return FS_ERR_INVALID_ARG;
+  // the sort clears its counters and look-back words itself (cudaMemsetAsync
+  // on this array), so stale contents of a previous call do no harm
+  return fs_balance_fbs(uih_len, S, n, perm, rank_offsets, err, scratch, sizeof(g_fbs_scratch), stream);
 }
 
 extern "C" size_t fs_balance_vbs_workspace_size(int64_t S, int32_t n) {
