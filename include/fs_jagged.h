@@ -187,6 +187,27 @@ fs_status fs_collision_split(const int64_t* ids_t, int64_t T_t, const int64_t* i
                              void* ws, size_t ws_bytes, fs_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * The same split in two steps, so that a batch's row set is built once and
+ * used by both pairs it belongs to ((t-1, t) and (t, t+1)).
+ * fs_row_bitmap: presence bitmap of the rows of one batch,
+ *   fs_row_bitmap_words(num_rows) uint32 words, bit (r % 32) of word r / 32;
+ *   cleared and filled by the call (an ID outside [0, num_rows) sets
+ *   FS_ERR_ID_RANGE).
+ * fs_collision_split_bitmaps: the outputs of fs_collision_split from the two
+ *   bitmaps; ids_t / ids_next are only read for the masks that are asked for.
+ * ---------------------------------------------------------------------- */
+size_t fs_row_bitmap_words(int64_t num_rows);
+fs_status fs_row_bitmap(const int64_t* ids, int64_t T, int64_t num_rows, uint32_t* bitmap, int32_t* err,
+                        fs_stream_t stream);
+size_t fs_collision_split_bitmaps_workspace_size(int64_t num_rows);
+fs_status fs_collision_split_bitmaps(const int64_t* ids_t, int64_t T_t, const uint32_t* bm_t, const int64_t* ids_next,
+                                     int64_t T_next, const uint32_t* bm_next, int64_t num_rows, int32_t n,
+                                     int64_t* co, int64_t* ex_t, int64_t* ex_next, int64_t cap_rows, int64_t* counts,
+                                     int64_t* co_shard_off, int64_t* ex_t_shard_off, int64_t* ex_next_shard_off,
+                                     uint8_t* is_co_t, uint8_t* is_co_next, int32_t* err, void* ws, size_t ws_bytes,
+                                     fs_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Embedding gather -- FreeScale Algorithm 2 line 12 (Lookup, then back to
  * batch-major: the ranged combine is fused, rows land directly at their
  * batch-major position) and line 15 (merge of the prefetched exclusive rows

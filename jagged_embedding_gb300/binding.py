@@ -33,7 +33,8 @@ EXPORTS = [
     "fs_balance_fbs_workspace_size", "fs_balance_fbs", "fs_balance_fbs_noalloc", "fs_balance_vbs_workspace_size",
     "fs_balance_vbs",
     "fs_permute_jagged_workspace_size", "fs_permute_jagged", "fs_bucketize_rowwise_workspace_size",
-    "fs_bucketize_rowwise", "fs_collision_split_workspace_size", "fs_collision_split", "fs_emb_gather",
+    "fs_bucketize_rowwise", "fs_collision_split_workspace_size", "fs_collision_split", "fs_row_bitmap_words",
+    "fs_row_bitmap", "fs_collision_split_bitmaps_workspace_size", "fs_collision_split_bitmaps", "fs_emb_gather",
     "fs_emb_backward_adagrad_workspace_size", "fs_emb_backward_adagrad", "fs_check", "fs_status_string",
     "fs_set_spin_limit", "fs_debug_skip_publish", "fs_launch_count", "fs_version",
 ]
@@ -69,6 +70,11 @@ def lib():
         "fs_bucketize_rowwise": ([P, i64, P, i32, i64, P, P, P, P, P, P, sz, P], C.c_int),
         "fs_collision_split_workspace_size": ([i64, i64, i64, i32], sz),
         "fs_collision_split": ([P, i64, P, i64, i64, i32, P, P, P, i64, P, P, P, P, P, P, P, P, sz, P], C.c_int),
+        "fs_row_bitmap_words": ([i64], sz),
+        "fs_row_bitmap": ([P, i64, i64, P, P, P], C.c_int),
+        "fs_collision_split_bitmaps_workspace_size": ([i64], sz),
+        "fs_collision_split_bitmaps": ([P, i64, P, P, i64, P, i64, i32, P, P, P, i64, P, P, P, P, P, P, P, P, sz, P],
+                                       C.c_int),
         "fs_emb_gather": ([P, i64, i32, C.c_int, P, i64, P, u8, P, P, P], C.c_int),
         "fs_emb_backward_adagrad_workspace_size": ([i64, i64, i32, C.c_int], sz),
         "fs_emb_backward_adagrad": ([P, P, i64, i32, C.c_int, C.c_int, P, P, i64, P, C.c_int, f32, f32, P, P, sz, P],
@@ -274,6 +280,36 @@ def fs_collision_split(ids_t, ids_next, num_rows, n, cap_rows=None, out=None, er
                                  _ptr(o.get("is_co_next") if want_next_mask else None), _ptr(err), _ptr(ws),
                                  ws.numel(), _stream(dev)),
         "fs_collision_split")
+    return out, err
+
+
+def fs_row_bitmap(ids, num_rows, bitmap=None, err=None, T=None):
+    dev = ids.device
+    _need(ids, torch.int64, "ids")
+    T = ids.numel() if T is None else int(T)
+    words = int(lib().fs_row_bitmap_words(int(num_rows)))
+    bitmap = torch.empty(words, dtype=torch.int32, device=dev) if bitmap is None else bitmap
+    err = new_err(dev) if err is None else err
+    _ok(lib().fs_row_bitmap(_ptr(ids), T, int(num_rows), _ptr(bitmap), _ptr(err), _stream(dev)), "fs_row_bitmap")
+    return bitmap, err
+
+
+def fs_collision_split_bitmaps(ids_t, bm_t, ids_next, bm_next, num_rows, n, out, cap_rows, err=None, ws=None,
+                               T_t=None, T_next=None, want_t_mask=True, want_next_mask=True):
+    """Same outputs as fs_collision_split (into the caller's `out` dict), from two row bitmaps."""
+    dev = bm_t.device
+    Tt = ids_t.numel() if T_t is None else int(T_t)
+    Tn = ids_next.numel() if T_next is None else int(T_next)
+    err = new_err(dev) if err is None else err
+    need = lib().fs_collision_split_bitmaps_workspace_size(int(num_rows))
+    ws = workspace(need, dev) if ws is None else ws
+    o = out
+    _ok(lib().fs_collision_split_bitmaps(
+        _ptr(ids_t), Tt, _ptr(bm_t), _ptr(ids_next), Tn, _ptr(bm_next), int(num_rows), n, _ptr(o["co"]),
+        _ptr(o["ex_t"]), _ptr(o["ex_next"]), int(cap_rows), _ptr(o["counts"]), _ptr(o["co_off"]), _ptr(o["ex_t_off"]),
+        _ptr(o["ex_next_off"]), _ptr(o.get("is_co_t") if want_t_mask else None),
+        _ptr(o.get("is_co_next") if want_next_mask else None), _ptr(err), _ptr(ws), ws.numel(), _stream(dev)),
+        "fs_collision_split_bitmaps")
     return out, err
 
 

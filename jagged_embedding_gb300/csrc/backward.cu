@@ -31,6 +31,8 @@ namespace {
 
 using radix::kThreads;
 constexpr int kChunk = 2048;                 // sorted entries per reduce tile
+bool g_force_unstaged = true;  // measured: the register path beats bulk-copy staging for 256-byte rows
+int g_reduce_variant = 0;      // launch shape of the register path (see launch_reduce)
 constexpr uint32_t kNoKey = 0xFFFFFFFFu;     // rows are < num_rows < 2^32
 
 // Sort source: the selected positions of the batch, key = row, value = position.
@@ -42,11 +44,12 @@ struct SrcRows {
   int phase;
   int64_t R;
   __device__ __forceinline__ bool load(int64_t i, Key& key, uint32_t& val, int32_t* err) const {
+    // the ID and the mask byte are loaded independently (no load-to-load dependency)
+    const int64_t id = __ldcs(ids + i);
     if (phase != FS_PHASE_ALL) {
-      const uint8_t m = is_co[i];
+      const uint8_t m = __ldcs(is_co + i);
       if ((phase == FS_PHASE_COLLISION) ? (m != 1) : (m != 0)) return false;
     }
-    const int64_t id = ids[i];
     if (id < 0 || id >= R) {
       if (err) set_err(err, FS_ERR_ID_RANGE);
       return false;
@@ -156,8 +159,8 @@ __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
-template <bool BF16, int EPL>
-__global__ void __launch_bounds__(kThreads, 4) reduce_kernel(const uint32_t* __restrict__ keys,
+template <bool BF16, int EPL, int GROWS, int MINB>
+__global__ void __launch_bounds__(kThreads, MINB) reduce_kernel(const uint32_t* __restrict__ keys,
                                                              const uint32_t* __restrict__ vals, const int64_t* n_dev,
                                                              const void* __restrict__ grads, UpdateArgs u,
                                                              float* carry_head, float* carry_tail, uint8_t* head_cont,
@@ -165,7 +168,7 @@ __global__ void __launch_bounds__(kThreads, 4) reduce_kernel(const uint32_t* __r
   constexpr int ESZ = BF16 ? 2 : 4;
   constexpr int D = 32 * EPL;
   constexpr int RB = D * ESZ;
-  constexpr int G = (16 / EPL) > 8 ? 8 : (16 / EPL);  // gradient rows in flight per warp (64-register budget)
+  constexpr int G = GROWS;  // gradient rows in flight per warp
   const int64_t n = *n_dev;
   const int64_t ntiles = (n + kChunk - 1) / kChunk;
   const int lane = threadIdx.x & 31;
@@ -241,6 +244,303 @@ __global__ void __launch_bounds__(kThreads, 4) reduce_kernel(const uint32_t* __r
           tail_flag[t] = 0;
         }
       } else {  // starts here, continues in the next tile
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) carry_tail[t * D + lane * EPL + i] = acc[i];
+        if (lane == 0) tail_flag[t] = 1;
+      }
+    } else {
+      if (from_prev) {
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) carry_head[t * D + lane * EPL + i] = acc[i];
+        if (lane == 0) head_cont[t] = 0;
+      } else {
+        update_row<BF16, EPL>(u, cur, acc, lane);
+      }
+      if (lane == 0) tail_flag[t] = 0;
+    }
+  }
+}
+
+// Reduce with batched updates: within a group of G sorted entries, every row
+// that ends in the group has its sum completed first (sequentially, entry by
+// entry, the same order as reduce_kernel), then the table-row loads of all
+// those rows are issued together and the updates applied.  A run of
+// single-position rows (the Zipf tail) thus keeps up to G table rows in
+// flight per warp instead of waiting for one row at a time.
+template <bool BF16, int EPL, int G, int MINB>
+__global__ void __launch_bounds__(kThreads, MINB) reduce_batched_kernel(const uint32_t* __restrict__ keys,
+                                                                        const uint32_t* __restrict__ vals,
+                                                                        const int64_t* n_dev,
+                                                                        const void* __restrict__ grads, UpdateArgs u,
+                                                                        float* carry_head, float* carry_tail,
+                                                                        uint8_t* head_cont, uint8_t* tail_flag) {
+  constexpr int ESZ = BF16 ? 2 : 4;
+  constexpr int D = 32 * EPL;
+  static_assert(32 % G == 0, "groups tile a batch of 32 entries");
+  const int64_t n = *n_dev;
+  const int64_t ntiles = (n + kChunk - 1) / kChunk;
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
+  (void)ESZ;
+  for (int64_t t = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; t < ntiles; t += nwarps) {
+    const int64_t s0 = t * kChunk;
+    const int64_t s1 = (s0 + kChunk < n) ? s0 + kChunk : n;
+    const uint32_t prev_key = s0 > 0 ? keys[s0 - 1] : kNoKey;
+    const uint32_t next_key = s1 < n ? keys[s1] : kNoKey;
+    const uint32_t first_key = keys[s0];
+    bool from_prev = (first_key == prev_key);  // the open row began in an earlier tile
+    float acc[EPL];
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) acc[i] = 0.f;
+
+    uint32_t pre_k = (s0 + lane < s1) ? __ldcs(keys + s0 + lane) : kNoKey;
+    uint32_t pre_p = (s0 + lane < s1) ? __ldcs(vals + s0 + lane) : 0u;
+    uint32_t last_key = first_key;
+    for (int64_t j = s0; j < s1; j += 32) {
+      const int cnt = (s1 - j < 32) ? int(s1 - j) : 32;
+      const uint32_t my_k = pre_k, my_p = pre_p;
+      const int64_t jn = j + 32;
+      pre_k = (jn + lane < s1) ? __ldcs(keys + jn + lane) : kNoKey;
+      pre_p = (jn + lane < s1) ? __ldcs(vals + jn + lane) : 0u;
+      const uint32_t first_next = (j + cnt < s1) ? __shfl_sync(0xffffffffu, pre_k, 0) : next_key;
+      // key of the entry after mine (for "a row ends at my entry")
+      uint32_t nk = __shfl_down_sync(0xffffffffu, my_k, 1);
+      if (lane == cnt - 1) nk = first_next;
+      const bool my_end = lane < cnt && nk != my_k;
+      if (my_end) {  // bring the table row and the state of a row that ends here to L2
+        const char* rp = static_cast<const char*>(u.table) + int64_t(my_k) * (D * ESZ);
+#pragma unroll
+        for (int b = 0; b < D * ESZ; b += 128) prefetch_l2(rp + b);
+        if (u.state) prefetch_l2(u.state + my_k);
+      }
+      const unsigned ends = __ballot_sync(0xffffffffu, my_end);
+      // state of the row ending at each entry, one load per lane
+      float my_state = 0.f;
+      if (my_end && u.state) my_state = u.state[my_k];
+
+      for (int e0 = 0; e0 < cnt; e0 += G) {
+        float g[G][EPL];
+#pragma unroll
+        for (int q = 0; q < G; ++q) {
+          const int e = e0 + q;
+          const uint32_t p = __shfl_sync(0xffffffffu, my_p, e & 31);
+          if (e < cnt) load_slice<BF16, EPL, true>(grads, p, lane, g[q]);
+        }
+        // sums of the rows that end in this group, in entry order
+        bool upd[G];
+#pragma unroll
+        for (int q = 0; q < G; ++q) {
+          const int e = e0 + q;
+          upd[q] = false;
+          if (e < cnt) {
+#pragma unroll
+            for (int i = 0; i < EPL; ++i) acc[i] += g[q][i];
+            if ((ends >> e) & 1u) {
+              const uint32_t k = __shfl_sync(0xffffffffu, my_k, e);
+              if (from_prev && k == first_key) {  // began in an earlier tile: leave a carry
+#pragma unroll
+                for (int i = 0; i < EPL; ++i) carry_head[t * D + lane * EPL + i] = acc[i];
+                if (lane == 0) head_cont[t] = 0;
+                from_prev = false;
+              } else {
+                upd[q] = true;
+#pragma unroll
+                for (int i = 0; i < EPL; ++i) g[q][i] = acc[i];
+              }
+#pragma unroll
+              for (int i = 0; i < EPL; ++i) acc[i] = 0.f;
+            }
+          }
+        }
+        // table rows of all rows ending here, loads in flight together
+        float w[G][EPL];
+#pragma unroll
+        for (int q = 0; q < G; ++q)
+          if (upd[q]) load_slice<BF16, EPL, false>(u.table, __shfl_sync(0xffffffffu, my_k, e0 + q), lane, w[q]);
+#pragma unroll
+        for (int q = 0; q < G; ++q) {
+          const int e = e0 + q;
+          const float s_old = __shfl_sync(0xffffffffu, my_state, e & 31);
+          if (upd[q]) {
+            const uint32_t row = __shfl_sync(0xffffffffu, my_k, e);
+            if (u.optim == FS_ROWWISE_ADAGRAD) {
+              float ss = 0.f;
+#pragma unroll
+              for (int i = 0; i < EPL; ++i) ss = __fmaf_rn(g[q][i], g[q][i], ss);
+#pragma unroll
+              for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+              ss = __shfl_sync(0xffffffffu, ss, 0);
+              const float snew = s_old + ss / float(D);
+              const float denom = sqrtf(snew) + u.eps;
+              if (lane == 0) u.state[row] = snew;
+#pragma unroll
+              for (int i = 0; i < EPL; ++i) w[q][i] = w[q][i] - u.lr * g[q][i] / denom;
+            } else {
+#pragma unroll
+              for (int i = 0; i < EPL; ++i) w[q][i] = w[q][i] - u.lr * g[q][i];
+            }
+            store_slice<BF16, EPL>(u.table, row, lane, w[q]);
+          }
+        }
+      }
+      last_key = __shfl_sync(0xffffffffu, my_k, cnt - 1);
+    }
+    // the tile's last row, if it did not end inside the tile
+    if (last_key == next_key) {
+      if (from_prev) {
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) carry_head[t * D + lane * EPL + i] = acc[i];
+        if (lane == 0) head_cont[t] = 1;
+      } else {
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) carry_tail[t * D + lane * EPL + i] = acc[i];
+      }
+    }
+    if (lane == 0) tail_flag[t] = (last_key == next_key && !from_prev) ? 1 : 0;
+  }
+}
+
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst))),
+               "l"(gsrc)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Reduce with the gradient rows streamed into a per-warp shared-memory ring by
+// asynchronous copies (cp.async, 16 bytes per lane, no registers held while
+// in flight): the rows of groups g+1 .. g+NST-1 are on their way while group g
+// is summed, so a warp keeps (NST-1) * G rows in flight even while it waits
+// on a table row to update.  Same tiling, carries and summation order as
+// reduce_kernel (entries in sorted order, fp32 per tile, fixed per lane).
+template <bool BF16, int EPL, int G, int NST, int MINB>
+__global__ void __launch_bounds__(kThreads, MINB)
+    reduce_async_kernel(const uint32_t* __restrict__ keys, const uint32_t* __restrict__ vals, const int64_t* n_dev,
+                        const void* __restrict__ grads, UpdateArgs u, float* carry_head, float* carry_tail,
+                        uint8_t* head_cont, uint8_t* tail_flag) {
+  constexpr int ESZ = BF16 ? 2 : 4;
+  constexpr int D = 32 * EPL;
+  constexpr int RB = D * ESZ;
+  constexpr int CPR = RB / 16;                  // 16-byte chunks per row
+  constexpr int CPL = (G * CPR + 31) / 32;      // chunks per lane per group
+  static_assert(32 % G == 0, "groups tile a batch of 32 entries");
+  static_assert((NST - 1) * G <= 32, "copies run at most one batch ahead");
+  using V = typename Raw<EPL * ESZ>::T;
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  unsigned char* ring = smem + warp * (NST * G * RB);
+  const char* gb = static_cast<const char*>(grads);
+  const int64_t n = *n_dev;
+  const int64_t ntiles = (n + kChunk - 1) / kChunk;
+  const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t t = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; t < ntiles; t += nwarps) {
+    const int64_t s0 = t * kChunk;
+    const int64_t s1 = (s0 + kChunk < n) ? s0 + kChunk : n;
+    const int ne = int(s1 - s0);
+    const int ngroups = (ne + G - 1) / G;
+    const uint32_t prev_key = s0 > 0 ? keys[s0 - 1] : kNoKey;
+    const uint32_t next_key = s1 < n ? keys[s1] : kNoKey;
+    // keys / positions of two consecutive batches of 32 entries live in registers
+    uint32_t bk[2], bp[2];
+    bk[0] = lane < ne ? __ldcs(keys + s0 + lane) : kNoKey;
+    bp[0] = lane < ne ? __ldcs(vals + s0 + lane) : 0u;
+    bk[1] = 32 + lane < ne ? __ldcs(keys + s0 + 32 + lane) : kNoKey;
+    bp[1] = 32 + lane < ne ? __ldcs(vals + s0 + 32 + lane) : 0u;
+    int loaded_batch = 1;  // index of the batch held in slot (loaded_batch & 1)
+
+    auto issue = [&](int g) {
+      if (g < ngroups) {
+        unsigned char* dst = ring + (g % NST) * (G * RB);
+#pragma unroll
+        for (int i = 0; i < CPL; ++i) {
+          const int c = lane + 32 * i;
+          const int cc = c < G * CPR ? c : 0;
+          const int r = cc / CPR, part = cc % CPR;
+          const int e = g * G + r;
+          // every lane shuffles both batch slots and picks the one its entry is in
+          const uint32_t p0 = __shfl_sync(0xffffffffu, bp[0], e & 31);
+          const uint32_t p1 = __shfl_sync(0xffffffffu, bp[1], e & 31);
+          const uint32_t p = ((e >> 5) & 1) ? p1 : p0;
+          if (c < G * CPR && e < ne) cp_async16(dst + r * RB + part * 16, gb + int64_t(p) * RB + part * 16);
+        }
+      }
+      cp_async_commit();  // one group per call, empty past the end, so wait counts stay exact
+    };
+
+    for (int g = 0; g < NST - 1; ++g) issue(g);
+    uint32_t cur = __shfl_sync(0xffffffffu, bk[0], 0);
+    bool from_prev = (cur == prev_key);
+    float acc[EPL];
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) acc[i] = 0.f;
+
+    for (int g = 0; g < ngroups; ++g) {
+      cp_async_wait<NST - 2>();  // group g has landed (for this lane)
+      __syncwarp();              // ... and for every lane of the warp
+      const unsigned char* src = ring + (g % NST) * (G * RB);
+      const int bslot = ((g * G) >> 5) & 1;
+      // segment ends of this group: an entry ends its row when the next key differs
+#pragma unroll
+      for (int r = 0; r < G; ++r) {
+        const int e = g * G + r;
+        if (e < ne) {
+          const uint32_t k0 = __shfl_sync(0xffffffffu, bk[0], e & 31);
+          const uint32_t k1 = __shfl_sync(0xffffffffu, bk[1], e & 31);
+          const uint32_t k = bslot ? k1 : k0;
+          if (k != cur) {
+            if (from_prev) {
+#pragma unroll
+              for (int i = 0; i < EPL; ++i) carry_head[t * D + lane * EPL + i] = acc[i];
+              if (lane == 0) head_cont[t] = 0;
+            } else {
+              update_row<BF16, EPL>(u, cur, acc, lane);
+            }
+            cur = k;
+            from_prev = false;
+#pragma unroll
+            for (int i = 0; i < EPL; ++i) acc[i] = 0.f;
+          }
+          const V v = *reinterpret_cast<const V*>(src + r * RB + lane * EPL * ESZ);
+          uint32_t w[(EPL * ESZ + 3) / 4];
+          if constexpr (EPL * ESZ >= 4) memcpy(w, &v, EPL * ESZ);
+          else w[0] = uint32_t(*reinterpret_cast<const unsigned short*>(&v));
+#pragma unroll
+          for (int i = 0; i < EPL; ++i)
+            acc[i] += BF16 ? __uint_as_float(((w[i / 2] >> ((i & 1) * 16)) & 0xFFFFu) << 16) : __uint_as_float(w[i]);
+        }
+      }
+      __syncwarp();  // every lane is done with this stage before it is refilled
+      // batch bookkeeping: when group g finishes a batch, the batch after the
+      // next one is loaded into the slot just freed (the issue-ahead window
+      // never reaches more than one batch ahead)
+      if (((g + 1) * G) % 32 == 0) {
+        const int finished = ((g + 1) * G) / 32 - 1;
+        if (finished + 2 > loaded_batch) {
+          const int nb = finished + 2;
+          const int64_t base = s0 + int64_t(nb) * 32;
+          bk[nb & 1] = base + lane < s1 ? __ldcs(keys + base + lane) : kNoKey;
+          bp[nb & 1] = base + lane < s1 ? __ldcs(vals + base + lane) : 0u;
+          loaded_batch = nb;
+        }
+      }
+      issue(g + NST - 1);
+    }
+    cp_async_wait<0>();
+    __syncwarp();
+    // the tile's last row
+    if (cur == next_key) {
+      if (from_prev) {
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) carry_head[t * D + lane * EPL + i] = acc[i];
+        if (lane == 0) {
+          head_cont[t] = 1;
+          tail_flag[t] = 0;
+        }
+      } else {
 #pragma unroll
         for (int i = 0; i < EPL; ++i) carry_tail[t * D + lane * EPL + i] = acc[i];
         if (lane == 0) tail_flag[t] = 1;
@@ -489,6 +789,16 @@ __global__ void __launch_bounds__(kThreads) fixup_kernel(const uint32_t* __restr
   }
 }
 
+template <bool BF16, int EPL, int G, int NST, int MINB>
+void launch_async(const uint32_t* k, const uint32_t* v, const int64_t* n_dev, const void* grads, UpdateArgs u,
+                  float* ch, float* ct, uint8_t* hc, uint8_t* tf, cudaStream_t st) {
+  constexpr int RB = 32 * EPL * (BF16 ? 2 : 4);
+  constexpr int smem = (kThreads / 32) * NST * G * RB;
+  cudaFuncSetAttribute(reduce_async_kernel<BF16, EPL, G, NST, MINB>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  reduce_async_kernel<BF16, EPL, G, NST, MINB><<<unsigned(sm_count()) * MINB, kThreads, smem, st>>>(
+      k, v, n_dev, grads, u, ch, ct, hc, tf);
+}
+
 template <bool BF16, int EPL>
 void launch_reduce(const uint32_t* k, const uint32_t* v, const int64_t* n_dev, const void* grads, UpdateArgs u,
                    float* ch, float* ct, uint8_t* hc, uint8_t* tf, int32_t* err, bool staged, cudaStream_t st) {
@@ -499,7 +809,24 @@ void launch_reduce(const uint32_t* k, const uint32_t* v, const int64_t* n_dev, c
     reduce_staged_kernel<BF16, EPL><<<unsigned(sm_count()), P::WPB * 32, P::SMEM, st>>>(
         k, v, n_dev, grads, u, ch, ct, hc, tf, err, spin_limit());
   } else {
-    reduce_kernel<BF16, EPL><<<unsigned(sm_count()) * 4, kThreads, 0, st>>>(k, v, n_dev, grads, u, ch, ct, hc, tf);
+    // (rows in flight per warp, blocks per SM): 8 x 4 fits 64 registers for any row width
+    constexpr int G8 = (16 / EPL) > 8 ? 8 : (16 / EPL);
+    constexpr int G16 = (32 / EPL) > 16 ? 16 : (32 / EPL);
+    constexpr int G4 = (8 / EPL) > 4 ? 4 : ((8 / EPL) < 1 ? 1 : (8 / EPL));
+    const unsigned sms = unsigned(sm_count());
+    switch (g_reduce_variant) {
+      case 1: reduce_kernel<BF16, EPL, G16, 3><<<sms * 3, kThreads, 0, st>>>(k, v, n_dev, grads, u, ch, ct, hc, tf); break;
+      case 2: reduce_kernel<BF16, EPL, G16, 2><<<sms * 2, kThreads, 0, st>>>(k, v, n_dev, grads, u, ch, ct, hc, tf); break;
+      case 3: reduce_kernel<BF16, EPL, G8, 6><<<sms * 6, kThreads, 0, st>>>(k, v, n_dev, grads, u, ch, ct, hc, tf); break;
+      case 4: launch_async<BF16, EPL, 8, 4, 3>(k, v, n_dev, grads, u, ch, ct, hc, tf, st); break;
+      case 7: reduce_batched_kernel<BF16, EPL, G8, 3><<<sms * 3, kThreads, 0, st>>>(k, v, n_dev, grads, u, ch, ct, hc, tf); break;
+      case 8: reduce_batched_kernel<BF16, EPL, G8, 4><<<sms * 4, kThreads, 0, st>>>(k, v, n_dev, grads, u, ch, ct, hc, tf); break;
+      case 10: reduce_batched_kernel<BF16, EPL, G8, 2><<<sms * 2, kThreads, 0, st>>>(k, v, n_dev, grads, u, ch, ct, hc, tf); break;
+      case 11: reduce_batched_kernel<BF16, EPL, G4, 4><<<sms * 4, kThreads, 0, st>>>(k, v, n_dev, grads, u, ch, ct, hc, tf); break;
+      case 5: launch_async<BF16, EPL, 8, 5, 2>(k, v, n_dev, grads, u, ch, ct, hc, tf, st); break;
+      case 6: launch_async<BF16, EPL, 4, 8, 3>(k, v, n_dev, grads, u, ch, ct, hc, tf, st); break;
+      default: reduce_kernel<BF16, EPL, G8, 4><<<sms * 4, kThreads, 0, st>>>(k, v, n_dev, grads, u, ch, ct, hc, tf); break;
+    }
   }
   fixup_kernel<BF16, EPL><<<grid, kThreads, 0, st>>>(k, n_dev, u, ch, ct, hc, tf);
 }
@@ -519,8 +846,6 @@ BwdLayout bwd_layout(int64_t T, int64_t R, int32_t dim) {
   return L;
 }
 
-bool g_force_unstaged = true;  // measured: the register path beats bulk-copy staging for 256-byte rows
-
 int epl_for(int32_t dim, fs_dtype dtype) {
   if (dim % 32 != 0) return 0;
   int e = dim / 32;
@@ -534,7 +859,10 @@ int epl_for(int32_t dim, fs_dtype dtype) {
 
 using namespace fs;
 
-extern "C" void fs_debug_reduce_variant(int32_t staged) { fs::g_force_unstaged = staged == 0; }
+extern "C" void fs_debug_reduce_variant(int32_t v) {
+  fs::g_force_unstaged = v != 9;
+  fs::g_reduce_variant = v;
+}
 
 extern "C" size_t fs_emb_backward_adagrad_workspace_size(int64_t T, int64_t num_rows, int32_t dim, fs_dtype dtype) {
   (void)dtype;

@@ -16,13 +16,16 @@ namespace {
 
 using radix::kThreads;
 
+// shard(x) = x / block.  GB300's FP64 rate is a small fraction of its FP32
+// rate, so the quotient is estimated in FP32 (exact to within one for any
+// x < 2^32 and quotient < 2^12) and corrected with integer products.
 struct SrcShard {
   using Key = int64_t;
   static constexpr bool kIndexValue = true;  // value = item index
   const int64_t* ids;
   int64_t R;
   int64_t block;
-  double inv_block;
+  float inv_block;
   int32_t n;
   __device__ __forceinline__ bool load(int64_t i, Key& key, uint32_t& val, int32_t* err) const {
     key = __ldcs(ids + i);
@@ -33,9 +36,9 @@ struct SrcShard {
   __device__ __forceinline__ uint32_t digit(Key key, int, int) const {
     if (key <= 0) return 0;
     if (key >= R) return uint32_t(n - 1);
-    int64_t q = static_cast<int64_t>(static_cast<double>(key) * inv_block);
+    int64_t q = static_cast<int64_t>(__float2uint_rz(__fmul_rz(__ull2float_rz(uint64_t(key)), inv_block)));
     if (q * block > key) --q;
-    else if ((q + 1) * block <= key) ++q;
+    if ((q + 1) * block <= key) ++q;
     return q >= n ? uint32_t(n - 1) : uint32_t(q);
   }
 };
@@ -108,7 +111,7 @@ extern "C" fs_status fs_bucketize_rowwise(const int64_t* ids, int64_t T, const i
   radix::PassWs P;
   if (!radix::carve_pass_ws(T, n, cur, P)) return FS_ERR_WORKSPACE;
   const int64_t block = (num_rows + n - 1) / n;
-  SrcShard src{ids, num_rows, block, 1.0 / static_cast<double>(block), n};
+  SrcShard src{ids, num_rows, block, 1.0f / static_cast<float>(block), n};
   int launches = 0;
   if (T > 0) {
     radix::run_pass(src, DstShardMajor{sm_ids, pos}, 0, 0, n, nullptr, T, P, err, st, &launches);

@@ -168,6 +168,36 @@ unsigned grid_for(int64_t items) {
   return unsigned(g < 1 ? 1 : g);
 }
 
+// compact + masks from two finished bitmaps; `status` ([tiles][3] words) and
+// `counter` must be zero.  Returns the number of kernels launched.
+int split_from_bitmaps(const int64_t* ids_t, int64_t T_t, const uint32_t* bm_t, const int64_t* ids_next,
+                       int64_t T_next, const uint32_t* bm_next, int64_t num_rows, int32_t n, int64_t* co,
+                       int64_t* ex_t, int64_t* ex_next, int64_t cap_rows, int64_t* counts, int64_t* co_shard_off,
+                       int64_t* ex_t_shard_off, int64_t* ex_next_shard_off, uint8_t* is_co_t, uint8_t* is_co_next,
+                       int32_t* err, uint64_t* status, int* counter, cudaStream_t st) {
+  CollLayout L = coll_layout(num_rows);
+  const int64_t block = (num_rows + n - 1) / n;
+  int launches = 0;
+  compact_kernel<<<unsigned(L.tiles), kThreads, 0, st>>>(bm_t, bm_next, L.nwords, num_rows, n, block, co, ex_t,
+                                                         ex_next, cap_rows, counts, co_shard_off, ex_t_shard_off,
+                                                         ex_next_shard_off, status, counter, err, spin_limit(),
+                                                         debug_skip_tile());
+  ++launches;
+  // masks: either may be NULL (not wanted); then that pass over its IDs is skipped
+  if (is_co_t && is_co_next && T_t + T_next > 0) {
+    mask_kernel<<<grid_for(T_t + T_next), kThreads, 0, st>>>(ids_t, T_t, ids_next, T_next, num_rows, bm_t, bm_next,
+                                                             is_co_t, is_co_next);
+    ++launches;
+  } else if (is_co_t && T_t > 0) {
+    mask_one_kernel<<<grid_for(T_t), kThreads, 0, st>>>(ids_t, T_t, num_rows, bm_next, is_co_t);
+    ++launches;
+  } else if (is_co_next && T_next > 0) {
+    mask_one_kernel<<<grid_for(T_next), kThreads, 0, st>>>(ids_next, T_next, num_rows, bm_t, is_co_next);
+    ++launches;
+  }
+  return launches;
+}
+
 }  // namespace
 }  // namespace fs
 
@@ -210,30 +240,71 @@ extern "C" fs_status fs_collision_split(const int64_t* ids_t, int64_t T_t, const
   uint64_t* status = reinterpret_cast<uint64_t*>(tail + 256);
   if (cudaMemsetAsync(zero, 0, L.zero_bytes(), st) != cudaSuccess) return FS_ERR_CUDA;
 
-  const int64_t block = (num_rows + n - 1) / n;
   int launches = 0;
   if (T_t + T_next > 0) {
     mark_kernel<<<grid_for(T_t + T_next), kThreads, 0, st>>>(ids_t, T_t, ids_next, T_next, num_rows, bm_t, bm_next,
                                                              err);
     ++launches;
   }
-  compact_kernel<<<unsigned(L.tiles), kThreads, 0, st>>>(bm_t, bm_next, L.nwords, num_rows, n, block, co, ex_t,
-                                                         ex_next, cap_rows, counts, co_shard_off, ex_t_shard_off,
-                                                         ex_next_shard_off, status, counter, err, spin_limit(),
-                                                         debug_skip_tile());
-  ++launches;
-  // masks: either may be NULL (not wanted); then that pass over its IDs is skipped
-  if (is_co_t && is_co_next && T_t + T_next > 0) {
-    mask_kernel<<<grid_for(T_t + T_next), kThreads, 0, st>>>(ids_t, T_t, ids_next, T_next, num_rows, bm_t, bm_next,
-                                                             is_co_t, is_co_next);
-    ++launches;
-  } else if (is_co_t && T_t > 0) {
-    mask_one_kernel<<<grid_for(T_t), kThreads, 0, st>>>(ids_t, T_t, num_rows, bm_next, is_co_t);
-    ++launches;
-  } else if (is_co_next && T_next > 0) {
-    mask_one_kernel<<<grid_for(T_next), kThreads, 0, st>>>(ids_next, T_next, num_rows, bm_t, is_co_next);
-    ++launches;
+  launches += split_from_bitmaps(ids_t, T_t, bm_t, ids_next, T_next, bm_next, num_rows, n, co, ex_t, ex_next, cap_rows,
+                                 counts, co_shard_off, ex_t_shard_off, ex_next_shard_off, is_co_t, is_co_next, err,
+                                 status, counter, st);
+  count_launch(launches);
+  return launch_status();
+}
+
+extern "C" size_t fs_row_bitmap_words(int64_t num_rows) { return num_rows < 1 ? 0 : size_t((num_rows + 31) / 32); }
+
+extern "C" fs_status fs_row_bitmap(const int64_t* ids, int64_t T, int64_t num_rows, uint32_t* bitmap, int32_t* err,
+                                   fs_stream_t stream) {
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (T < 0 || T > INT32_MAX || num_rows < 1 || num_rows > (int64_t(1) << 32) || !bitmap || !err)
+    return FS_ERR_INVALID_ARG;
+  if (T > 0 && !ids) return FS_ERR_INVALID_ARG;
+  if ((ids && !aligned(ids, 8)) || !aligned(bitmap, 4)) return FS_ERR_ALIGNMENT;
+  if (cudaMemsetAsync(bitmap, 0, fs_row_bitmap_words(num_rows) * sizeof(uint32_t), st) != cudaSuccess)
+    return FS_ERR_CUDA;
+  if (T > 0) {
+    mark_kernel<<<grid_for(T), kThreads, 0, st>>>(ids, T, nullptr, 0, num_rows, bitmap, nullptr, err);
+    count_launch(1);
   }
+  return launch_status();
+}
+
+extern "C" size_t fs_collision_split_bitmaps_workspace_size(int64_t num_rows) {
+  if (num_rows < 1) return 0;
+  CollLayout L = coll_layout(num_rows);
+  return align_up(size_t(L.tiles) * 3 * sizeof(uint64_t) + 256) + 256;
+}
+
+extern "C" fs_status fs_collision_split_bitmaps(const int64_t* ids_t, int64_t T_t, const uint32_t* bm_t,
+                                                const int64_t* ids_next, int64_t T_next, const uint32_t* bm_next,
+                                                int64_t num_rows, int32_t n, int64_t* co, int64_t* ex_t,
+                                                int64_t* ex_next, int64_t cap_rows, int64_t* counts,
+                                                int64_t* co_shard_off, int64_t* ex_t_shard_off,
+                                                int64_t* ex_next_shard_off, uint8_t* is_co_t, uint8_t* is_co_next,
+                                                int32_t* err, void* ws, size_t ws_bytes, fs_stream_t stream) {
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (T_t < 0 || T_next < 0 || T_t > INT32_MAX || T_next > INT32_MAX || num_rows < 1 ||
+      num_rows > (int64_t(1) << 32) || n < 1 || cap_rows < 0 || !counts || !co_shard_off || !ex_t_shard_off ||
+      !ex_next_shard_off || !err || !bm_t || !bm_next)
+    return FS_ERR_INVALID_ARG;
+  if ((is_co_t && T_t > 0 && !ids_t) || (is_co_next && T_next > 0 && !ids_next)) return FS_ERR_INVALID_ARG;
+  if (cap_rows > 0 && (!co || !ex_t || !ex_next)) return FS_ERR_INVALID_ARG;
+  if ((ids_t && !aligned(ids_t, 8)) || (ids_next && !aligned(ids_next, 8)) || !aligned(counts, 8) ||
+      !aligned(bm_t, 4) || !aligned(bm_next, 4) || (co && !aligned(co, 8)) || (ex_t && !aligned(ex_t, 8)) ||
+      (ex_next && !aligned(ex_next, 8)))
+    return FS_ERR_ALIGNMENT;
+  if (ws_bytes < fs_collision_split_bitmaps_workspace_size(num_rows) || !ws) return FS_ERR_WORKSPACE;
+  CollLayout L = coll_layout(num_rows);
+  const size_t zb = align_up(size_t(L.tiles) * 3 * sizeof(uint64_t) + 256);
+  unsigned char* zero = static_cast<unsigned char*>(ws);
+  if (cudaMemsetAsync(zero, 0, zb, st) != cudaSuccess) return FS_ERR_CUDA;
+  int* counter = reinterpret_cast<int*>(zero);
+  uint64_t* status = reinterpret_cast<uint64_t*>(zero + 256);
+  int launches = split_from_bitmaps(ids_t, T_t, bm_t, ids_next, T_next, bm_next, num_rows, n, co, ex_t, ex_next,
+                                    cap_rows, counts, co_shard_off, ex_t_shard_off, ex_next_shard_off, is_co_t,
+                                    is_co_next, err, status, counter, st);
   count_launch(launches);
   return launch_status();
 }

@@ -20,19 +20,31 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kUnroll = 8;
 bool g_gather_staged = false;  // 256-byte rows: bulk-copy staged kernel instead of the register path
+int g_gather_variant = 0;      // 256-byte rows: unroll / L2 hint of the register path
 
 // Row bytes = 16 * VPR with VPR in {4, 8, 16, 32}: a warp instruction moves
 // RPI = 32 / VPR whole rows (lanes [k*VPR, (k+1)*VPR) own row k), and a warp
 // iteration moves RPI * U consecutive rows whose IDs (and mask bytes) one
 // coalesced load brings in and shuffles out; no per-element division, U
 // independent 16-byte loads in flight per lane.
-template <int VPR>
+__device__ __forceinline__ int4 ld_row_vec(const int4* p, uint64_t pol, bool hint) {
+  if (!hint) return __ldg(p);
+  int4 v;
+  asm volatile("ld.global.nc.L2::cache_hint.v4.s32 {%0, %1, %2, %3}, [%4], %5;"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p), "l"(pol));
+  return v;
+}
+
+template <int VPR, int UNROLL = kUnroll, bool HINT = false>
 __global__ void __launch_bounds__(kThreads) gather_rows_kernel(const int4* __restrict__ table, int64_t R,
                                                                const int64_t* __restrict__ ids, int64_t T,
                                                                const uint8_t* __restrict__ mask, uint8_t sel,
                                                                int4* __restrict__ out, int32_t* err) {
   constexpr int RPI = 32 / VPR;                              // rows per warp instruction
-  constexpr int U = (32 / RPI) < kUnroll ? (32 / RPI) : kUnroll;
+  constexpr int U = (32 / RPI) < UNROLL ? (32 / RPI) : UNROLL;
+  uint64_t pol = 0;
+  if constexpr (HINT) asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
   constexpr int RPW = RPI * U;                               // rows per warp iteration, one ID per lane
   static_assert(RPW <= 32, "one lane per row ID");
   const int lane = threadIdx.x & 31;
@@ -55,7 +67,7 @@ __global__ void __launch_bounds__(kThreads) gather_rows_kernel(const int4* __res
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       id[u] = __shfl_sync(0xffffffffu, my_id, u * RPI + sub);
-      if (id[u] >= 0) v[u] = __ldg(table + id[u] * VPR + c);
+      if (id[u] >= 0) v[u] = ld_row_vec(table + id[u] * VPR + c, pol, HINT);
     }
 #pragma unroll
     for (int u = 0; u < U; ++u)
@@ -196,7 +208,10 @@ __global__ void __launch_bounds__(kThreads) gather_word_kernel(const uint32_t* _
 
 using namespace fs;
 
-extern "C" void fs_debug_gather_variant(int32_t staged) { fs::g_gather_staged = staged != 0; }
+extern "C" void fs_debug_gather_variant(int32_t v) {
+  fs::g_gather_staged = v == 9;
+  fs::g_gather_variant = v;
+}
 
 extern "C" fs_status fs_emb_gather(const void* table, int64_t num_rows, int32_t dim, fs_dtype dtype, const int64_t* ids,
                                    int64_t T, const uint8_t* mask, uint8_t sel, void* out, int32_t* err,
@@ -225,6 +240,12 @@ extern "C" fs_status fs_emb_gather(const void* table, int64_t num_rows, int32_t 
           gather_staged_kernel<256><<<unsigned(sms), P::WPB * 32, P::SMEM, st>>>(
               static_cast<const unsigned char*>(table), num_rows, ids, T, mask, sel, static_cast<unsigned char*>(out),
               err, spin_limit());
+        } else if (g_gather_variant == 1) {
+          gather_rows_kernel<16, 16, false><<<grid, kThreads, 0, st>>>(tb, num_rows, ids, T, mask, sel, ob, err);
+        } else if (g_gather_variant == 2) {
+          gather_rows_kernel<16, 8, true><<<grid, kThreads, 0, st>>>(tb, num_rows, ids, T, mask, sel, ob, err);
+        } else if (g_gather_variant == 3) {
+          gather_rows_kernel<16, 16, true><<<grid, kThreads, 0, st>>>(tb, num_rows, ids, T, mask, sel, ob, err);
         } else {
           gather_rows_kernel<16><<<grid, kThreads, 0, st>>>(tb, num_rows, ids, T, mask, sel, ob, err);
         }

@@ -37,6 +37,9 @@ class Slot:
         self.pos = torch.empty(max_T, dtype=torch.int32, device=device)
         self.splits = torch.empty(n, n, dtype=torch.int64, device=device)
         self.shard_offsets = torch.empty(n + 1, dtype=torch.int64, device=device)
+        # presence bitmap of the batch's rows: built once, used by both collision
+        # pairs the batch belongs to
+        self.bitmap = torch.empty((w.R + 31) // 32, dtype=torch.int32, device=device)
         self.T = 0
 
 
@@ -72,7 +75,7 @@ class Pipeline:
             L.fs_balance_fbs_workspace_size(self.max_S, w.n),
             L.fs_permute_jagged_workspace_size(self.max_S),
             L.fs_bucketize_rowwise_workspace_size(self.max_T, w.n),
-            L.fs_collision_split_workspace_size(self.max_T, self.max_T, w.R, w.n),
+            L.fs_collision_split_bitmaps_workspace_size(w.R),
             B.backward_workspace_size(self.max_T, w.R, w.D, B.dtype_code(table)) if w.has_update else 0,
         )
         # one workspace, reused by every call (calls on one stream run in order)
@@ -93,6 +96,7 @@ class Pipeline:
                             out_values=s.ids, rank_id_offsets=s.rank_id_offsets, err=self.err, ws=self.ws)
         B.fs_bucketize_rowwise(s.ids, s.rank_id_offsets, w.R, sm_ids=s.sm_ids, pos=s.pos, splits=s.splits,
                                shard_offsets=s.shard_offsets, err=self.err, ws=self.ws, T=T)
+        B.fs_row_bitmap(s.ids, w.R, bitmap=s.bitmap, err=self.err, T=T)
         s.T = T
 
     def collision(self, slot_t, slot_next, want_next_mask=True):
@@ -105,8 +109,8 @@ class Pipeline:
         out = dict(self.coll)
         out["is_co_t"] = self.masks[slot_t]
         out["is_co_next"] = self.masks[slot_next]
-        B.fs_collision_split(a.ids, b.ids, self.w.R, self.w.n, cap_rows=self.cap_rows, out=out, err=self.err,
-                             ws=self.ws, T_t=a.T, T_next=b.T, want_next_mask=want_next_mask)
+        B.fs_collision_split_bitmaps(a.ids, a.bitmap, b.ids, b.bitmap, self.w.R, self.w.n, out, self.cap_rows,
+                                     err=self.err, ws=self.ws, T_t=a.T, T_next=b.T, want_next_mask=want_next_mask)
 
     def gather(self, slot, out_idx=0, mask=None, sel=1):
         s = self.slots[slot]

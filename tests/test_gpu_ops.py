@@ -220,6 +220,41 @@ def test_collision_matches_oracle(R, n, Tt, Tn):
     assert np.array_equal(to_np(out["is_co_next"]), ref["is_co_next"])
 
 
+@pytest.mark.parametrize("R,n,Tt,Tn", [(100_000, 8, 70_000, 80_000), (50_000_000, 512, 300_000, 0),
+                                       (1_000_003, 7, 123_457, 98_765)])
+def test_collision_from_bitmaps_matches_oracle(R, n, Tt, Tn):
+    rng = np.random.default_rng(R + Tn)
+    a = rng.integers(0, R, Tt).astype(np.int64)
+    b = rng.integers(0, R, Tn).astype(np.int64)
+    if Tt and Tn:
+        b[: Tn // 2] = a[rng.integers(0, Tt, Tn // 2)]
+    ad, bd = torch.from_numpy(a).to(DEV), torch.from_numpy(b).to(DEV)
+    bm_a, err = B.fs_row_bitmap(ad, R)
+    bm_b, _ = B.fs_row_bitmap(bd, R, err=err)
+    _check(err)
+    # bitmap = the set of rows, bit r % 32 of word r / 32
+    words = to_np(bm_a).view(np.uint32)
+    bits = np.unpackbits(words.view(np.uint8), bitorder="little")[:R]
+    assert np.array_equal(np.flatnonzero(bits), np.unique(a))
+    cap = Tt + Tn
+    out = {k: torch.empty(cap, dtype=torch.int64, device=DEV) for k in ("co", "ex_t", "ex_next")}
+    out.update({"counts": torch.empty(3, dtype=torch.int64, device=DEV),
+                "co_off": torch.empty(n + 1, dtype=torch.int64, device=DEV),
+                "ex_t_off": torch.empty(n + 1, dtype=torch.int64, device=DEV),
+                "ex_next_off": torch.empty(n + 1, dtype=torch.int64, device=DEV),
+                "is_co_t": torch.empty(Tt, dtype=torch.uint8, device=DEV),
+                "is_co_next": torch.empty(Tn, dtype=torch.uint8, device=DEV)})
+    B.fs_collision_split_bitmaps(ad, bm_a, bd, bm_b, R, n, out, cap, err=err)
+    _check(err)
+    ref = oracle.collision_split(a, b, R, n)
+    counts = to_np(out["counts"])
+    for k, c in (("co", 0), ("ex_t", 1), ("ex_next", 2)):
+        assert np.array_equal(to_np(out[k])[: counts[c]], ref[k]), k
+        assert np.array_equal(to_np(out[k + "_off"]), ref[k + "_off"]), k
+    assert np.array_equal(to_np(out["is_co_t"]), ref["is_co_t"])
+    assert np.array_equal(to_np(out["is_co_next"]), ref["is_co_next"])
+
+
 def test_collision_single_mask():
     """Either mask may be omitted; the other one is unchanged."""
     rng = np.random.default_rng(77)
