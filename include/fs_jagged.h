@@ -58,7 +58,12 @@ typedef enum {
 
 typedef enum { FS_F32 = 0, FS_BF16 = 1 } fs_dtype;
 typedef enum { FS_SGD = 0, FS_ROWWISE_ADAGRAD = 1 } fs_optim;
-typedef enum { FS_PHASE_ALL = 0, FS_PHASE_COLLISION = 1, FS_PHASE_EXCLUSIVE = 2 } fs_phase;
+typedef enum {
+  FS_PHASE_ALL = 0,
+  FS_PHASE_COLLISION = 1,
+  FS_PHASE_EXCLUSIVE = 2,
+  FS_PHASE_COLLISION_THEN_EXCLUSIVE = 3
+} fs_phase;
 
 /* ------------------------------------------------------------------------
  * FBS partition -- FreeScale §4.1 (Partitioning Algorithms), FBS paragraph.
@@ -153,7 +158,7 @@ fs_status fs_permute_jagged(const int64_t* offsets, const int64_t* values, int64
  *   splits          [n*n] int64 out: splits[r*n + s] = IDs of source rank r in shard s
  *                         (the AllToAll send splits)
  *   shard_offsets   [n+1] int64 out
- * n in [1, 512].
+ * n in [1, 1024].
  * ---------------------------------------------------------------------- */
 size_t fs_bucketize_rowwise_workspace_size(int64_t T, int32_t n);
 fs_status fs_bucketize_rowwise(const int64_t* ids, int64_t T, const int64_t* rank_id_offsets, int32_t n,
@@ -237,7 +242,9 @@ fs_status fs_emb_gather(const void* table, int64_t num_rows, int32_t dim, fs_dty
  * even.  phase selects positions: ALL every position, COLLISION those with
  * is_co[p] == 1, EXCLUSIVE those with is_co[p] == 0.  Collision is a property
  * of the row, so COLLISION then EXCLUSIVE updates every row of the batch once,
- * collision rows first.
+ * collision rows first.  COLLISION_THEN_EXCLUSIVE does exactly that in one
+ * call: one sort of all positions (the phase is the key's top bit), then the
+ * collision rows' updates, then the exclusive rows' updates, in stream order.
  *   table [num_rows, dim] in place;  state [num_rows] fp32 in place (NULL for SGD)
  *   ids [T] int64;  grads [T, dim] of dtype (batch-major);  is_co [T] (NULL for ALL)
  * Supported: dim in {32, 64, 128} (fp32) or {32, 64, 128, 256} (bf16);

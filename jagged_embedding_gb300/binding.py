@@ -23,7 +23,7 @@ LIB_PATH = os.path.join(HERE, "libfsjagged.so")
 
 F32, BF16 = 0, 1
 SGD, ROWWISE_ADAGRAD = 0, 1
-PHASE_ALL, PHASE_COLLISION, PHASE_EXCLUSIVE = 0, 1, 2
+PHASE_ALL, PHASE_COLLISION, PHASE_EXCLUSIVE, PHASE_COLLISION_THEN_EXCLUSIVE = 0, 1, 2, 3
 
 STATUS = {0: "ok", 1: "invalid argument", 2: "ID outside [0, num_rows)", 3: "malformed offsets or permutation",
           4: "output capacity exceeded", 5: "workspace too small", 6: "bounded inter-block wait gave up",

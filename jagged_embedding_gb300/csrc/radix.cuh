@@ -30,7 +30,7 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kItems = 16;
 constexpr int kTile = kThreads * kItems;  // 4096 items per tile
-constexpr int kMaxBins = 512;
+constexpr int kMaxBins = 1024;
 
 inline int64_t num_tiles(int64_t count) { return (count + kTile - 1) / kTile; }
 
@@ -112,12 +112,21 @@ static __global__ void __launch_bounds__(kThreads) tile_scan_kernel(uint32_t* co
 static __global__ void __launch_bounds__(kThreads) digit_base_kernel(const uint32_t* totals, int nb, uint32_t* digit_base,
                                                               int64_t* n_valid) {
   __shared__ uint32_t tmp[32];
-  const int d0 = threadIdx.x * 2;  // kThreads * 2 >= kMaxBins
-  const uint32_t a = d0 < nb ? totals[d0] : 0u, b = d0 + 1 < nb ? totals[d0 + 1] : 0u;
+  constexpr int kPer = kMaxBins / kThreads;  // digits per thread
+  const int d0 = threadIdx.x * kPer;
+  uint32_t v[kPer], sum = 0;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    v[i] = d0 + i < nb ? totals[d0 + i] : 0u;
+    sum += v[i];
+  }
   uint32_t tot;
-  const uint32_t ex = block_exclusive_scan<uint32_t>(a + b, tmp, &tot);
-  if (d0 < nb) digit_base[d0] = ex;
-  if (d0 + 1 < nb) digit_base[d0 + 1] = ex + a;
+  uint32_t run = block_exclusive_scan<uint32_t>(sum, tmp, &tot);
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    if (d0 + i < nb) digit_base[d0 + i] = run;
+    run += v[i];
+  }
   if (threadIdx.x == 0 && n_valid) *n_valid = int64_t(tot);
 }
 
@@ -193,12 +202,21 @@ __global__ void __launch_bounds__(kThreads, 3) downsweep_kernel(Src src, Dst dst
   }
   __syncthreads();
   {
-    const int d0 = threadIdx.x * 2;
-    const uint32_t a = d0 < nb ? tile_count[d0] : 0, b = d0 + 1 < nb ? tile_count[d0 + 1] : 0;
+    constexpr int kPer = kMaxBins / kThreads;  // digits per thread
+    const int d0 = threadIdx.x * kPer;
+    uint32_t v[kPer], sum = 0;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      v[i] = d0 + i < nb ? tile_count[d0 + i] : 0u;
+      sum += v[i];
+    }
     uint32_t tot;
-    const uint32_t ex = block_exclusive_scan<uint32_t>(a + b, scratch, &tot);
-    if (d0 < nb) local_start[d0] = ex;
-    if (d0 + 1 < nb) local_start[d0 + 1] = ex + a;
+    uint32_t run = block_exclusive_scan<uint32_t>(sum, scratch, &tot);
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      if (d0 + i < nb) local_start[d0 + i] = run;
+      run += v[i];
+    }
     if (threadIdx.x == 0) scratch[40] = tot;
   }
   __syncthreads();
@@ -313,14 +331,14 @@ void run_pass(const Src& src, const Dst& dst, int shift, int bits, int nb, const
 
 // LSD sort of (uint32 key, uint32 value) pairs drawn from Src0 (the items of
 // [0, count) that Src0::load accepts), by the low key_bits bits of the key,
-// in passes of at most 9 bits.  Result: *out_k / *out_v, *n_valid entries
+// in passes of at most 10 bits.  Result: *out_k / *out_v, *n_valid entries
 // (n_valid stays on the device).
 struct SortPlan {
   int64_t count = 0;
   int key_bits = 1, passes = 1, bits = 1, nb = 2;
   SortPlan() = default;
   SortPlan(int64_t c, int kb) : count(c), key_bits(kb < 1 ? 1 : kb) {
-    passes = (key_bits + 8) / 9;
+    passes = (key_bits + 9) / 10;  // digits of at most 10 bits (kMaxBins)
     bits = (key_bits + passes - 1) / passes;
     nb = 1 << bits;
   }

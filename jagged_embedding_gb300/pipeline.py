@@ -135,8 +135,8 @@ class Pipeline:
         self.gather(cur)
         if self.w.has_update:
             if has_next:
-                self.backward(cur, grads, B.PHASE_COLLISION)
-                self.backward(cur, grads, B.PHASE_EXCLUSIVE)
+                # one sort, collision rows updated first, then exclusive rows
+                self.backward(cur, grads, B.PHASE_COLLISION_THEN_EXCLUSIVE)
             else:
                 self.backward(cur, grads, B.PHASE_ALL)
         return nxt

@@ -64,7 +64,7 @@ def test_host_argument_errors_return_without_launching():
     assert L.fs_balance_fbs(C.c_void_p(0x10), 10, 4, C.c_void_p(0x20), C.c_void_p(0x3000), err, ws, 16, NULL) == 5
     assert L.fs_balance_vbs(C.c_void_p(0x10), 10, 4, -1.0, 0, C.c_void_p(0x20), C.c_void_p(0x3000),
                             C.c_void_p(0x4000), err, ws, 1 << 30, NULL) == 1                   # alpha < 0
-    assert L.fs_bucketize_rowwise(C.c_void_p(0x10), 10, C.c_void_p(0x100), 513, 100, C.c_void_p(0x20),
+    assert L.fs_bucketize_rowwise(C.c_void_p(0x10), 10, C.c_void_p(0x100), 1025, 100, C.c_void_p(0x20),
                                   C.c_void_p(0x30), C.c_void_p(0x40), C.c_void_p(0x50), err, ws, 1 << 30, NULL) == 1
     assert L.fs_bucketize_rowwise(C.c_void_p(0x13), 10, C.c_void_p(0x100), 4, 100, C.c_void_p(0x20),
                                   C.c_void_p(0x30), C.c_void_p(0x40), C.c_void_p(0x50), err, ws, 1 << 30, NULL) == 8

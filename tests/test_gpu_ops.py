@@ -377,6 +377,37 @@ def test_backward_phases_and_determinism(dtype):
     assert_state_close(results[0][1], s_ref)
 
 
+@pytest.mark.parametrize("dtype,R", [("f32", 200_000), ("bf16", 3_000_000), ("f32", 100_000_000)])
+def test_backward_both_phases_in_one_call_equals_two_calls(dtype, R):
+    """COLLISION_THEN_EXCLUSIVE (one sort, phase in the key's top bit) gives the same
+    bits as a COLLISION call followed by an EXCLUSIVE call."""
+    D, T = (64 if dtype == "f32" else 128), 300_000
+    g = torch.Generator().manual_seed(31)
+    ids = synthetic.zipf_rows(R, 1.05, T, g, "cpu")
+    tt = torch.float32 if dtype == "f32" else torch.bfloat16
+    rows = torch.unique(ids)
+    W0 = (torch.randn(R, D, generator=g) * 0.01).to(tt)
+    G = torch.randn(T, D, generator=g).to(tt)
+    is_co = (torch.rand(rows.numel(), generator=g) < 0.5).to(torch.uint8)
+    mask = is_co[torch.searchsorted(rows, ids)].contiguous()
+    outs = []
+    for mode in ("one", "two"):
+        Wd, sd = W0.to(DEV), torch.zeros(R, device=DEV)
+        idd, Gd, md = ids.to(DEV), G.to(DEV), mask.to(DEV)
+        if mode == "one":
+            err = B.fs_emb_backward_adagrad(Wd, sd, idd, Gd, "adagrad", 0.01, 1e-8, is_co=md,
+                                            phase=B.PHASE_COLLISION_THEN_EXCLUSIVE)
+        else:
+            err = B.fs_emb_backward_adagrad(Wd, sd, idd, Gd, "adagrad", 0.01, 1e-8, is_co=md, phase=B.PHASE_COLLISION)
+            B.fs_emb_backward_adagrad(Wd, sd, idd, Gd, "adagrad", 0.01, 1e-8, is_co=md, phase=B.PHASE_EXCLUSIVE,
+                                      err=err)
+        _check(err)
+        outs.append((Wd[rows.to(DEV)].cpu(), sd[rows.to(DEV)].cpu()))
+    assert torch.equal(outs[0][0].view(torch.int16) if dtype == "bf16" else outs[0][0],
+                       outs[1][0].view(torch.int16) if dtype == "bf16" else outs[1][0])
+    assert torch.equal(outs[0][1], outs[1][1])
+
+
 def test_backward_single_hot_row_spans_many_tiles():
     """One row owns most positions: its sum crosses hundreds of reduce tiles (carry chain)."""
     R, D, T = 1000, 64, 1_000_000
