@@ -138,12 +138,12 @@ struct UpdateArgs {
   float eps;
 };
 
-// Apply the optimizer to one row with its reduced gradient (whole warp).
+// Optimizer step for one row (whole warp): w holds the lane's slice of the
+// row's current weights, s_old its Adagrad state, g the reduced gradient.
 template <bool BF16, int EPL>
-__device__ __forceinline__ void update_row(const UpdateArgs& u, uint32_t row, const float (&g)[EPL], int lane) {
+__device__ __forceinline__ void apply_update(const UpdateArgs& u, uint32_t row, float (&w)[EPL], float s_old,
+                                             const float (&g)[EPL], int lane) {
   constexpr int D = 32 * EPL;
-  float w[EPL];
-  load_slice<BF16, EPL, false>(u.table, row, lane, w);
   if (u.optim == FS_ROWWISE_ADAGRAD) {
     float ss = 0.f;
 #pragma unroll
@@ -151,16 +151,25 @@ __device__ __forceinline__ void update_row(const UpdateArgs& u, uint32_t row, co
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
     ss = __shfl_sync(0xffffffffu, ss, 0);  // one value for the whole row
-    const float s = u.state[row] + ss / float(D);
-    const float denom = sqrtf(s) + u.eps;
+    const float s = s_old + ss / float(D);
+    const float step = u.lr / (sqrtf(s) + u.eps);  // one division per row
     if (lane == 0) u.state[row] = s;
 #pragma unroll
-    for (int i = 0; i < EPL; ++i) w[i] = w[i] - u.lr * g[i] / denom;
+    for (int i = 0; i < EPL; ++i) w[i] = __fmaf_rn(-step, g[i], w[i]);
   } else {
 #pragma unroll
-    for (int i = 0; i < EPL; ++i) w[i] = w[i] - u.lr * g[i];
+    for (int i = 0; i < EPL; ++i) w[i] = __fmaf_rn(-u.lr, g[i], w[i]);
   }
   store_slice<BF16, EPL>(u.table, row, lane, w);
+}
+
+// Load, update and store one row (whole warp).
+template <bool BF16, int EPL>
+__device__ __forceinline__ void update_row(const UpdateArgs& u, uint32_t row, const float (&g)[EPL], int lane) {
+  float w[EPL];
+  load_slice<BF16, EPL, false>(u.table, row, lane, w);
+  const float s_old = u.optim == FS_ROWWISE_ADAGRAD ? u.state[row] : 0.f;
+  apply_update<BF16, EPL>(u, row, w, s_old, g, lane);
 }
 
 __device__ __forceinline__ void prefetch_l2(const void* p) {
@@ -168,7 +177,12 @@ __device__ __forceinline__ void prefetch_l2(const void* p) {
 }
 
 // Sorted entries [*begin_dev, *end_dev) (begin 0 when begin_dev is null);
-// row = key & row_mask.
+// row = key & row_mask.  One warp per tile of kChunk sorted entries; the
+// gradient rows of a tile are summed in entry order, GROWS rows in flight.
+// For each batch of 32 entries one ballot marks the entries that end a row
+// (the next key differs), so the per-entry work is a load and an add.  A row
+// that starts and ends in this tile is updated here; a row that crosses a
+// tile edge leaves partial sums for fixup_kernel.
 template <bool BF16, int EPL, int GROWS, int MINB>
 __global__ void __launch_bounds__(kThreads, MINB) reduce_kernel(const uint32_t* __restrict__ keys,
                                                              const uint32_t* __restrict__ vals,
@@ -192,8 +206,8 @@ __global__ void __launch_bounds__(kThreads, MINB) reduce_kernel(const uint32_t* 
     const int64_t s1 = (s0 + kChunk < n) ? s0 + kChunk : n;
     const uint32_t prev_key = s0 > 0 ? keys[s0 - 1] : kNoKey;
     const uint32_t next_key = s1 < n ? keys[s1] : kNoKey;
-    uint32_t cur = keys[s0];
-    bool from_prev = (cur == prev_key);
+    bool from_prev = (keys[s0] == prev_key);  // the tile's first row began in an earlier tile
+    bool open = false;                        // acc holds entries of a row not yet finished
     float acc[EPL];
 #pragma unroll
     for (int i = 0; i < EPL; ++i) acc[i] = 0.f;
@@ -210,7 +224,9 @@ __global__ void __launch_bounds__(kThreads, MINB) reduce_kernel(const uint32_t* 
       uint32_t nk = __shfl_down_sync(0xffffffffu, my_k, 1);
       const uint32_t first_next = __shfl_sync(0xffffffffu, pre_k, 0);
       if (lane == cnt - 1) nk = (j + cnt < s1) ? first_next : next_key;
-      if (lane < cnt && nk != my_k) {  // a row ends at this entry: bring its table row and state to L2
+      const bool ends = lane < cnt && nk != my_k;
+      const uint32_t end_mask = __ballot_sync(0xffffffffu, ends);
+      if (ends) {  // bring the finished row's table row and state to L2
         const char* rp = static_cast<const char*>(u.table) + int64_t(my_k & row_mask) * RB;
 #pragma unroll
         for (int b = 0; b < RB; b += 128) prefetch_l2(rp + b);
@@ -224,32 +240,33 @@ __global__ void __launch_bounds__(kThreads, MINB) reduce_kernel(const uint32_t* 
           const uint32_t p = __shfl_sync(0xffffffffu, my_p, e & 31);
           if (e < cnt) load_slice<BF16, EPL, true>(grads, p, lane, g[q]);
         }
+        const uint32_t m = end_mask >> e0;
 #pragma unroll
         for (int q = 0; q < G; ++q) {
-          const int e = e0 + q;
-          const uint32_t k = __shfl_sync(0xffffffffu, my_k, e & 31);
-          if (e < cnt) {
-            if (k != cur) {
-              if (from_prev) {  // the row began in an earlier tile and ends here
+          if (e0 + q < cnt) {
+#pragma unroll
+            for (int i = 0; i < EPL; ++i) acc[i] += g[q][i];
+            open = true;
+            if ((m >> q) & 1u) {  // entry e0 + q is its row's last
+              if (from_prev) {    // the row began in an earlier tile and ends here
 #pragma unroll
                 for (int i = 0; i < EPL; ++i) carry_head[t * D + lane * EPL + i] = acc[i];
                 if (lane == 0) head_cont[t] = 0;
+                from_prev = false;
               } else {
-                update_row<BF16, EPL>(u, cur & row_mask, acc, lane);
+                const uint32_t row = __shfl_sync(0xffffffffu, my_k, (e0 + q) & 31) & row_mask;
+                update_row<BF16, EPL>(u, row, acc, lane);
               }
-              cur = k;
-              from_prev = false;
+              open = false;
 #pragma unroll
               for (int i = 0; i < EPL; ++i) acc[i] = 0.f;
             }
-#pragma unroll
-            for (int i = 0; i < EPL; ++i) acc[i] += g[q][i];
           }
         }
       }
     }
-    // the tile's last row
-    if (cur == next_key) {
+    // a row still open continues into the next tile
+    if (open) {
       if (from_prev) {  // spans the whole tile
 #pragma unroll
         for (int i = 0; i < EPL; ++i) carry_head[t * D + lane * EPL + i] = acc[i];
@@ -257,20 +274,13 @@ __global__ void __launch_bounds__(kThreads, MINB) reduce_kernel(const uint32_t* 
           head_cont[t] = 1;
           tail_flag[t] = 0;
         }
-      } else {  // starts here, continues in the next tile
+      } else {  // starts here
 #pragma unroll
         for (int i = 0; i < EPL; ++i) carry_tail[t * D + lane * EPL + i] = acc[i];
         if (lane == 0) tail_flag[t] = 1;
       }
-    } else {
-      if (from_prev) {
-#pragma unroll
-        for (int i = 0; i < EPL; ++i) carry_head[t * D + lane * EPL + i] = acc[i];
-        if (lane == 0) head_cont[t] = 0;
-      } else {
-        update_row<BF16, EPL>(u, cur & row_mask, acc, lane);
-      }
-      if (lane == 0) tail_flag[t] = 0;
+    } else if (lane == 0) {
+      tail_flag[t] = 0;
     }
   }
 }

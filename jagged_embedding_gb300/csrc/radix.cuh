@@ -154,6 +154,16 @@ __global__ void __launch_bounds__(kThreads, 3) downsweep_kernel(Src src, Dst dst
   const int64_t count = count_dev ? *count_dev : count_host;
   if (tile * kTile >= count) return;
 
+  // this tile's offset inside every digit run: loaded first, so that the
+  // scattered reads overlap the item loads and the ranking below
+  constexpr int kPerT = kMaxBins / kThreads;
+  uint32_t my_off[kPerT];
+#pragma unroll
+  for (int i = 0; i < kPerT; ++i) {
+    const int d = threadIdx.x + i * kThreads;
+    my_off[i] = d < nb ? __ldg(counts + int64_t(d) * ntiles + tile) + __ldg(digit_base + d) : 0u;
+  }
+
   // per item: the key, one packed word (digit in bits 20..31, rank / local
   // position in bits 0..19) and, only for sources whose value is not the item
   // index, the value
@@ -189,16 +199,20 @@ __global__ void __launch_bounds__(kThreads, 3) downsweep_kernel(Src src, Dst dst
   __syncthreads();
 
   // exclusive over warps per digit, tile totals, global base of each digit run
-  for (int d = threadIdx.x; d < nb; d += kThreads) {
-    uint32_t run = 0;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-      const uint32_t c = warp_hist[w * nb + d];
-      warp_hist[w * nb + d] = run;
-      run += c;
+  for (int i = 0; i < kPerT; ++i) {
+    const int d = threadIdx.x + i * kThreads;
+    if (d < nb) {
+      uint32_t run = 0;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        const uint32_t c = warp_hist[w * nb + d];
+        warp_hist[w * nb + d] = run;
+        run += c;
+      }
+      tile_count[d] = run;
+      gbase[d] = int64_t(my_off[i]);
     }
-    tile_count[d] = run;
-    gbase[d] = int64_t(digit_base[d]) + int64_t(counts[int64_t(d) * ntiles + tile]);
   }
   __syncthreads();
   {

@@ -408,6 +408,28 @@ def test_backward_both_phases_in_one_call_equals_two_calls(dtype, R):
     assert torch.equal(outs[0][1], outs[1][1])
 
 
+@pytest.mark.parametrize("dtype,D", [("f32", 32), ("bf16", 64)])
+def test_backward_rows_not_16_byte_aligned(dtype, D):
+    """Gradient rows that start 4 bytes past a 16-byte boundary take the
+    narrow-load reduce (the wide one needs 16-byte rows); same result bar."""
+    R, T = 40_000, 120_000
+    ids, W, G = _bwd_case(5, R, D, T, dtype)
+    state = torch.rand(R, generator=torch.Generator().manual_seed(8))
+    Wd, sd = W.to(DEV), state.to(DEV)
+    shift = 4 // G.element_size()
+    flat = torch.empty(T * D + shift, dtype=G.dtype, device=DEV)
+    Gd = flat[shift:].view(T, D)
+    Gd.copy_(G.to(DEV))
+    assert Gd.data_ptr() % 16 == 4
+    err = B.fs_emb_backward_adagrad(Wd, sd, ids.to(DEV), Gd, "adagrad", 0.01, 1e-8)
+    _check(err)
+    W_ref, s_ref = to_np(W), state.numpy().copy()
+    oracle.emb_backward(W_ref, s_ref, ids.numpy(), to_np(G), "adagrad", 0.01, 1e-8)
+    scale = update_scale(ids.numpy(), to_np(G), R, "adagrad", 0.01, 1e-8, s_ref)
+    assert_table_close(to_np(Wd), W_ref, dtype, 0.01, scale=scale)
+    assert_state_close(to_np(sd), s_ref)
+
+
 def test_backward_single_hot_row_spans_many_tiles():
     """One row owns most positions: its sum crosses hundreds of reduce tiles (carry chain)."""
     R, D, T = 1000, 64, 1_000_000
