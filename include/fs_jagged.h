@@ -262,12 +262,15 @@ fs_status fs_emb_backward_adagrad(void* table, float* state, int64_t num_rows, i
  *   or FS_ERR_CUDA if the stream reports an error.  Host-synchronous: meant for
  *   tests and benchmarks, not for the hot loop.
  * fs_set_spin_limit: polls before a bounded inter-block wait gives up with
- *   FS_ERR_TIMEOUT (default 1<<22, roughly a second).  Applies to later calls.
+ *   FS_ERR_TIMEOUT (default 1<<22, roughly a second); a wait for a bulk copy
+ *   of gradient rows gives up after polls * 256 ns.  Applies to later calls.
  * fs_launch_count: kernels this library has launched in this process.
  * fs_debug_skip_publish: test hook for the bounded waits.  Tile `tile` of the
  *   single-pass scans (VBS weights, permute offsets, collision compaction)
  *   skips publishing its look-back status, so every later tile's wait runs out
- *   and the call reports FS_ERR_TIMEOUT instead of hanging.  -1 (the default)
+ *   and the call reports FS_ERR_TIMEOUT instead of hanging; in the embedding
+ *   update, the first bulk copy of gradient rows for sorted tile `tile` is
+ *   never issued, so the wait for it runs out the same way.  -1 (the default)
  *   turns it off.  Never used outside tests.
  * ---------------------------------------------------------------------- */
 fs_status fs_check(const int32_t* err, fs_stream_t stream);

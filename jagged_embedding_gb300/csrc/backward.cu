@@ -25,6 +25,7 @@
 
 #include <algorithm>
 
+#include "bulk.cuh"
 #include "radix.cuh"
 
 namespace fs {
@@ -150,9 +151,10 @@ __device__ __forceinline__ void apply_update(const UpdateArgs& u, uint32_t row, 
     for (int i = 0; i < EPL; ++i) ss = __fmaf_rn(g[i], g[i], ss);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    ss = __shfl_sync(0xffffffffu, ss, 0);  // one value for the whole row
+    // (the xor butterfly leaves the same bits in every lane: each level adds
+    // the same two values, a + b == b + a)
     const float s = s_old + ss / float(D);
-    const float step = u.lr / (sqrtf(s) + u.eps);  // one division per row
+    const float step = __fdividef(u.lr, sqrtf(s) + u.eps);  // one division per row, within 2 ulp
     if (lane == 0) u.state[row] = s;
 #pragma unroll
     for (int i = 0; i < EPL; ++i) w[i] = __fmaf_rn(-step, g[i], w[i]);
@@ -207,6 +209,7 @@ __global__ void __launch_bounds__(kThreads, MINB) reduce_kernel(const uint32_t* 
     const uint32_t prev_key = s0 > 0 ? keys[s0 - 1] : kNoKey;
     const uint32_t next_key = s1 < n ? keys[s1] : kNoKey;
     bool from_prev = (keys[s0] == prev_key);  // the tile's first row began in an earlier tile
+    if (lane == 0 && !from_prev) head_cont[t] = 0;  // every tile's flag is defined
     bool open = false;                        // acc holds entries of a row not yet finished
     float acc[EPL];
 #pragma unroll
@@ -285,35 +288,301 @@ __global__ void __launch_bounds__(kThreads, MINB) reduce_kernel(const uint32_t* 
   }
 }
 
-// Rows that cross tile boundaries: carry of the starting tile, then the head
-// carries of the following tiles in order.
+// Shared-memory ring of the bulk-copy reduce: per warp kRingStages stages of
+// BR gradient rows each (BR * RB <= 2 KB), the mbarriers in front.
+constexpr int kRingStages = 4;
+template <int RB>
+struct Ring {
+  static constexpr int BR = (2048 / RB) < 8 ? (2048 / RB) : 8;  // rows per stage
+  static constexpr int SPC = 32 / BR;                            // stages per 32-entry batch of keys
+  static constexpr int kStageBytes = BR * RB;
+  static constexpr int kWarpBytes = 128 + kRingStages * kStageBytes;
+  static constexpr int kBlockBytes = (kThreads / 32) * kWarpBytes;
+  static constexpr int kFit = (227 * 1024) / (kBlockBytes + 1024);
+  static constexpr int kMinBlocks = kFit > 4 ? 4 : kFit;
+  static_assert(SPC >= kRingStages - 1, "a copy issued ahead must fall in the current or the next key batch");
+  static_assert(kMinBlocks >= 1, "ring too large");
+};
+
+// Reduce with the gradient rows brought in by bulk copies.  Same tiles,
+// entry order, row ends and carries as reduce_kernel; what differs is how
+// the rows arrive: each warp keeps kRingStages - 1 stages of BR rows in
+// flight (one bulk copy per row into shared memory, completion counted in
+// bytes on the stage's mbarrier) while it sums the stage that has landed,
+// so no registers are tied up waiting for gradient rows and several KB per
+// warp stay in flight.  Keys and positions are read two batches of 32
+// ahead; table rows that a batch of 32 finishes are prefetched to L2 one
+// batch ahead, and the table slices and Adagrad states of the rows a stage
+// finishes are loaded before waiting for that stage.  A wait that exceeds
+// wait_ns nanoseconds sets FS_ERR_TIMEOUT, waits (bounded) for the warp's copies
+// still in flight and ends the warp.  skip_tile >= 0 is a test hook: the
+// first stage of that tile is never copied, so its wait runs out.
+template <bool BF16, int EPL, int MINB>
+__global__ void __launch_bounds__(kThreads, MINB) reduce_ring_kernel(
+    const uint32_t* __restrict__ keys, const uint32_t* __restrict__ vals, const int64_t* begin_dev,
+    const int64_t* end_dev, uint32_t row_mask, const void* __restrict__ grads, UpdateArgs u, float* carry_head,
+    float* carry_tail, uint8_t* head_cont, uint8_t* tail_flag, int32_t* err, uint64_t wait_ns, int64_t skip_tile) {
+  constexpr int ESZ = BF16 ? 2 : 4;
+  constexpr int D = 32 * EPL;
+  constexpr int RB = D * ESZ;
+  using RG = Ring<RB>;
+  constexpr int BR = RG::BR, SPC = RG::SPC, NS = kRingStages;
+  static_assert((NS & (NS - 1)) == 0 && (SPC & (SPC - 1)) == 0, "powers of two");
+  extern __shared__ __align__(128) unsigned char ring_smem[];
+  const int lane = threadIdx.x & 31;
+  unsigned char* wbase = ring_smem + (threadIdx.x >> 5) * RG::kWarpBytes;
+  const uint32_t bar0 = bulk::smem_addr(wbase);
+  const uint32_t data0 = bar0 + 128;
+  const unsigned char* data = wbase + 128;
+  if (lane == 0)
+    for (int s = 0; s < NS; ++s) bulk::mbar_init(bar0 + 8 * s, 1);
+  bulk::fence_init();
+  __syncwarp();
+  const uint64_t pol = bulk::evict_first_policy();
+  const char* gbytes = static_cast<const char*>(grads);
+  const bool adagrad = u.optim == FS_ROWWISE_ADAGRAD;
+
+  const int64_t b0 = begin_dev ? *begin_dev : 0;
+  keys += b0;
+  vals += b0;
+  const int64_t n = *end_dev - b0;
+  const int64_t ntiles = (n + kChunk - 1) / kChunk;
+  const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
+  uint32_t gb = 0;  // stages this warp has consumed (all tiles): stage gb % NS, phase gb / NS
+  bool failed = false;
+
+  for (int64_t t = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; t < ntiles && !failed; t += nwarps) {
+    const int64_t s0 = t * kChunk;
+    const int m = int((s0 + kChunk < n) ? kChunk : n - s0);  // entries in this tile
+    const uint32_t* tk = keys + s0;
+    const uint32_t* tv = vals + s0;
+    const uint32_t prev_key = s0 > 0 ? keys[s0 - 1] : kNoKey;
+    const uint32_t next_key = s0 + m < n ? keys[s0 + m] : kNoKey;
+    const uint32_t last_key = tk[m - 1];
+    const uint32_t nb = uint32_t((m + BR - 1) / BR);  // stages in this tile
+    const uint32_t gb_tile = gb;
+    auto ld_k = [&](int c) { const int i = c * 32 + lane; return i < m ? __ldcs(tk + i) : kNoKey; };
+    auto ld_p = [&](int c) { const int i = c * 32 + lane; return i < m ? __ldcs(tv + i) : 0u; };
+    // bits of the entries of batch c (keys kc) that end a row; kn0 = first key of batch c + 1
+    auto end_bits = [&](int c, uint32_t kc, uint32_t kn0) {
+      const int cnt = m - c * 32;  // may be <= 0 or > 32
+      uint32_t nk = __shfl_down_sync(0xffffffffu, kc, 1);
+      if (lane == 31) nk = kn0;
+      if (lane == cnt - 1) nk = next_key;  // the tile's last entry
+      const bool e = lane < cnt && nk != kc;
+      if (e) {  // bring the finished row's table row and state to L2
+        const char* rp = static_cast<const char*>(u.table) + int64_t(kc & row_mask) * RB;
+#pragma unroll
+        for (int b = 0; b < RB; b += 128) prefetch_l2(rp + b);
+        if (adagrad) prefetch_l2(u.state + (kc & row_mask));
+      }
+      return __ballot_sync(0xffffffffu, e);
+    };
+    uint32_t kc = ld_k(0), pc = ld_p(0), kn = ld_k(1), pn = ld_p(1), kn2 = ld_k(2), pn2 = ld_p(2);
+    // copy stage tb of this tile (its rows belong to batch tb / SPC, which is c or c + 1)
+    auto issue = [&](uint32_t tb, int c) {
+      if (tb >= nb || (t == skip_tile && tb == 0)) return;  // (test hook: a stage that never arrives)
+      const uint32_t p = (int(tb / SPC) == c) ? pc : pn;
+      const int first = int(tb % SPC) * BR;
+      const int left = m - int(tb) * BR;
+      const int rows = left < BR ? left : BR;
+      const uint32_t st = (gb_tile + tb) & (NS - 1);
+      const uint32_t bar = bar0 + 8 * st;
+      if (lane == first) bulk::arrive_expect_tx(bar, uint32_t(rows * RB));
+      __syncwarp();
+      const uint32_t r = uint32_t(lane - first);
+      if (r < uint32_t(rows)) bulk::copy_g2s(data0 + st * RG::kStageBytes + r * RB, gbytes + uint64_t(p) * RB, RB, bar, pol);
+    };
+    for (int k = 0; k < NS - 1; ++k) issue(uint32_t(k), 0);
+
+    bool from_prev = (__shfl_sync(0xffffffffu, kc, 0) == prev_key);
+    if (lane == 0 && !from_prev) head_cont[t] = 0;  // every tile's flag is defined
+    float acc[EPL];
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) acc[i] = 0.f;
+    uint32_t em = end_bits(0, kc, __shfl_sync(0xffffffffu, kn, 0));
+
+    // the entries of stage st (eb = its first entry in batch c); FULL: all BR present
+    // (inlined at two call sites with a constant `full`: the bounds test folds away)
+    auto consume = [&](bool full, int eb, int cnt, uint32_t st, uint32_t bm, float (&w)[BR][EPL], float my_s) {
+      const unsigned char* sp = data + st * RG::kStageBytes;
+#pragma unroll
+      for (int r = 0; r < BR; ++r) {
+        if (full || eb + r < cnt) {
+          float g[EPL];
+          load_slice<BF16, EPL, false>(sp, r, lane, g);
+#pragma unroll
+          for (int q = 0; q < EPL; ++q) acc[q] += g[q];
+          if ((bm >> r) & 1u) {  // entry eb + r is its row's last
+            if (from_prev) {     // the row began in an earlier tile and ends here
+#pragma unroll
+              for (int q = 0; q < EPL; ++q) carry_head[t * D + lane * EPL + q] = acc[q];
+              if (lane == 0) head_cont[t] = 0;
+              from_prev = false;
+            } else {
+              const uint32_t row = __shfl_sync(0xffffffffu, kc, eb + r) & row_mask;
+              const float s_old = __shfl_sync(0xffffffffu, my_s, eb + r);
+              apply_update<BF16, EPL>(u, row, w[r], s_old, acc, lane);
+            }
+#pragma unroll
+            for (int q = 0; q < EPL; ++q) acc[q] = 0.f;
+          }
+        }
+      }
+    };
+
+    for (int c = 0; c * 32 < m; ++c) {
+      const int cnt = (m - c * 32 < 32) ? m - c * 32 : 32;
+      const uint32_t em_next = end_bits(c + 1, kn, __shfl_sync(0xffffffffu, kn2, 0));
+      for (int i = 0; i < SPC; ++i) {
+        const int eb = i * BR;
+        if (eb >= cnt) break;
+        const uint32_t tb = uint32_t(c * SPC + i);
+        issue(tb + NS - 1, c);
+        // table slices and states of the rows this stage finishes
+        const uint32_t bm = (em >> eb) & ((BR == 32) ? 0xffffffffu : ((1u << BR) - 1u));
+        float w[BR][EPL];
+        float my_s = 0.f;
+        if (bm) {
+#pragma unroll
+          for (int r = 0; r < BR; ++r) {
+            if ((bm >> r) & 1u) {
+              const uint32_t row = __shfl_sync(0xffffffffu, kc, eb + r) & row_mask;
+              load_slice<BF16, EPL, false>(u.table, row, lane, w[r]);
+            }
+          }
+          if (adagrad && ((em >> lane) & 1u) && uint32_t(lane - eb) < uint32_t(BR)) my_s = u.state[kc & row_mask];
+        }
+        const uint32_t st = (gb_tile + tb) & (NS - 1);
+        const uint32_t par = ((gb_tile + tb) / NS) & 1u;
+        if (!bulk::warp_wait(bar0 + 8 * st, par, wait_ns)) {
+          // give up: record it, let this warp's other copies land, stop
+          if (lane == 0) set_err(err, FS_ERR_TIMEOUT);
+          for (uint32_t k = 1; k < NS; ++k) {
+            const uint32_t g2 = gb_tile + tb + k;
+            if (tb + k < nb) bulk::warp_wait(bar0 + 8 * (g2 & (NS - 1)), (g2 / NS) & 1u, wait_ns);
+          }
+          failed = true;
+          break;
+        }
+        if (eb + BR <= cnt) consume(true, eb, cnt, st, bm, w, my_s);
+        else consume(false, eb, cnt, st, bm, w, my_s);
+        __syncwarp();  // every lane is done with the stage before it is refilled
+      }
+      if (failed) break;
+      kc = kn;
+      pc = pn;
+      kn = kn2;
+      pn = pn2;
+      kn2 = ld_k(c + 3);
+      pn2 = ld_p(c + 3);
+      em = em_next;
+    }
+    if (failed) break;
+    gb = gb_tile + nb;
+    // a row still open continues into the next tile
+    if (last_key == next_key) {
+      if (from_prev) {  // spans the whole tile
+#pragma unroll
+        for (int q = 0; q < EPL; ++q) carry_head[t * D + lane * EPL + q] = acc[q];
+        if (lane == 0) {
+          head_cont[t] = 1;
+          tail_flag[t] = 0;
+        }
+      } else {  // starts here
+#pragma unroll
+        for (int q = 0; q < EPL; ++q) carry_tail[t * D + lane * EPL + q] = acc[q];
+        if (lane == 0) tail_flag[t] = 1;
+      }
+    } else if (lane == 0) {
+      tail_flag[t] = 0;
+    }
+  }
+  __syncwarp();
+  if (lane == 0)
+    for (int s = 0; s < NS; ++s) bulk::mbar_inval(bar0 + 8 * s);
+}
+
+// Carry chains of rows that cross tile boundaries.  A chain is the tail
+// carry of its starting tile, then the head carries of the following tiles
+// up to the first whose head does not continue.  A Zipf-hot row crosses
+// thousands of tiles, so whole aligned blocks of kCarryBlock continuing
+// tiles are summed first (block_sum_kernel, one warp per block), and the
+// chain's owner adds block sums where it can and single tiles elsewhere.
+// Sums are in fp64: the error stays at the level of one tile's fp32 sum.
+// The order is fixed, so the result is identical run to run.
+constexpr int kCarryBlock = 32;
+
+template <int EPL>
+__global__ void __launch_bounds__(kThreads) block_sum_kernel(const int64_t* begin_dev, const int64_t* end_dev,
+                                                             const float* carry_head, const uint8_t* head_cont,
+                                                             double* block_sum, uint8_t* block_full) {
+  constexpr int D = 32 * EPL;
+  const int64_t b0 = begin_dev ? *begin_dev : 0;
+  const int64_t n = *end_dev - b0;
+  const int64_t ntiles = (n + kChunk - 1) / kChunk;
+  const int64_t nblocks = ntiles / kCarryBlock;  // whole blocks only
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t bk = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; bk < nblocks; bk += nwarps) {
+    const int64_t v0 = bk * kCarryBlock;
+    const bool full = __all_sync(0xffffffffu, head_cont[v0 + lane] == 1);
+    if (lane == 0) block_full[bk] = full ? 1 : 0;
+    if (!full) continue;
+    double acc[EPL];
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) acc[i] = 0.0;
+    for (int j = 0; j < kCarryBlock; j += 8) {
+      float c[8][EPL];
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) c[q][i] = carry_head[(v0 + j + q) * D + lane * EPL + i];
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) acc[i] += double(c[q][i]);
+    }
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) block_sum[bk * D + lane * EPL + i] = acc[i];
+  }
+}
+
 template <bool BF16, int EPL>
 __global__ void __launch_bounds__(kThreads) fixup_kernel(const uint32_t* __restrict__ keys, const int64_t* begin_dev,
                                                          const int64_t* end_dev, uint32_t row_mask, UpdateArgs u,
                                                          const float* carry_head, const float* carry_tail,
-                                                         const uint8_t* head_cont, const uint8_t* tail_flag) {
+                                                         const uint8_t* head_cont, const uint8_t* tail_flag,
+                                                         const double* block_sum, const uint8_t* block_full) {
   constexpr int D = 32 * EPL;
   const int64_t b0 = begin_dev ? *begin_dev : 0;
   keys += b0;
   const int64_t n = *end_dev - b0;
   const int64_t ntiles = (n + kChunk - 1) / kChunk;
+  const int64_t nblocks = ntiles / kCarryBlock;
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
   for (int64_t t = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; t < ntiles; t += nwarps) {
     if (!tail_flag[t]) continue;
     const uint32_t row = keys[(t + 1) * kChunk - 1] & row_mask;
-    // the chain of tile partials is summed in fp64: a Zipf-hot row can cross
-    // thousands of tiles, and this keeps its error at the level of one tile's
     double acc64[EPL];
 #pragma unroll
     for (int i = 0; i < EPL; ++i) acc64[i] = double(carry_tail[t * D + lane * EPL + i]);
-    // the chain ends at the first following tile whose head does not continue;
-    // read 32 continuation flags at a time, then sum that window's carries in
-    // tile order with several loads in flight
-    for (int64_t v = t + 1; v < ntiles; v += 32) {
-      const uint8_t hc = (v + lane < ntiles) ? head_cont[v + lane] : uint8_t(0);
-      const unsigned stop = __ballot_sync(0xffffffffu, hc == 0);
-      const int last = stop ? (__ffs(stop) - 1) : 31;
+    int64_t v = t + 1;
+    while (v < ntiles) {
+      if (v % kCarryBlock == 0 && v / kCarryBlock < nblocks && block_full[v / kCarryBlock]) {
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) acc64[i] += block_sum[(v / kCarryBlock) * D + lane * EPL + i];
+        v += kCarryBlock;
+        continue;
+      }
+      // single tiles up to the end of v's block: stop at the first head
+      // that does not continue
+      const int64_t vend = (v / kCarryBlock + 1) * kCarryBlock < ntiles ? (v / kCarryBlock + 1) * kCarryBlock : ntiles;
+      const int cntw = int(vend - v);
+      const uint8_t hc = lane < cntw ? head_cont[v + lane] : uint8_t(1);
+      const unsigned stop = __ballot_sync(0xffffffffu, lane < cntw && hc == 0);
+      const int last = stop ? (__ffs(stop) - 1) : (cntw - 1);
       int j = 0;
       for (; j + 8 <= last + 1; j += 8) {
         float c[8][EPL];
@@ -330,6 +599,7 @@ __global__ void __launch_bounds__(kThreads) fixup_kernel(const uint32_t* __restr
 #pragma unroll
         for (int i = 0; i < EPL; ++i) acc64[i] += double(carry_head[(v + j) * D + lane * EPL + i]);
       if (stop) break;
+      v = vend;
     }
     float acc[EPL];
 #pragma unroll
@@ -341,16 +611,26 @@ __global__ void __launch_bounds__(kThreads) fixup_kernel(const uint32_t* __restr
 template <bool BF16, int EPL>
 void launch_reduce(const uint32_t* k, const uint32_t* v, const int64_t* begin_dev, const int64_t* end_dev,
                    uint32_t row_mask, const void* grads, UpdateArgs u, float* ch, float* ct, uint8_t* hc,
-                   uint8_t* tf, cudaStream_t st) {
-  // 8 gradient rows in flight per warp (fewer for wide rows) and 4 blocks per
-  // SM fit the 64-register budget without spills; measured best among the
-  // launch shapes and staging schemes tried (see the design notes)
-  constexpr int G = (16 / EPL) > 8 ? 8 : (16 / EPL);
+                   uint8_t* tf, double* bsum, uint8_t* bfull, int32_t* err, cudaStream_t st) {
   const unsigned sms = unsigned(sm_count());
-  reduce_kernel<BF16, EPL, G, 4><<<sms * 4, kThreads, 0, st>>>(k, v, begin_dev, end_dev, row_mask, grads, u, ch, ct,
-                                                              hc, tf);
+  if (aligned(grads, 16)) {
+    // gradient rows by bulk copy (needs 16-byte aligned rows)
+    constexpr int RB = 32 * EPL * (BF16 ? 2 : 4);
+    using RG = Ring<RB>;
+    auto kern = reduce_ring_kernel<BF16, EPL, RG::kMinBlocks>;
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, RG::kBlockBytes);
+    kern<<<sms * RG::kMinBlocks, kThreads, RG::kBlockBytes, st>>>(k, v, begin_dev, end_dev, row_mask, grads, u, ch,
+                                                                   ct, hc, tf, err, uint64_t(spin_limit()) * 256u, debug_skip_tile());
+  } else {
+    // 8 gradient rows in flight per warp (fewer for wide rows) and 4 blocks
+    // per SM fit the 64-register budget without spills
+    constexpr int G = (16 / EPL) > 8 ? 8 : (16 / EPL);
+    reduce_kernel<BF16, EPL, G, 4><<<sms * 4, kThreads, 0, st>>>(k, v, begin_dev, end_dev, row_mask, grads, u, ch,
+                                                                ct, hc, tf);
+  }
+  block_sum_kernel<EPL><<<sms * (2048 / kThreads), kThreads, 0, st>>>(begin_dev, end_dev, ch, hc, bsum, bfull);
   fixup_kernel<BF16, EPL><<<sms * (2048 / kThreads), kThreads, 0, st>>>(k, begin_dev, end_dev, row_mask, u, ch, ct,
-                                                                         hc, tf);
+                                                                         hc, tf, bsum, bfull);
 }
 
 // Number of sorted keys below `bound` (one thread; keys ascending).
@@ -365,8 +645,8 @@ __global__ void count_below_kernel(const uint32_t* keys, const int64_t* n_dev, u
 
 struct BwdLayout {
   radix::SortPlan plan;
-  int64_t max_tiles = 0;
-  size_t carry_bytes = 0, flag_bytes = 0;
+  int64_t max_tiles = 0, max_blocks = 0;
+  size_t carry_bytes = 0, flag_bytes = 0, block_bytes = 0, block_flag_bytes = 0;
 };
 
 BwdLayout bwd_layout(int64_t T, int64_t R, int32_t dim) {
@@ -375,6 +655,9 @@ BwdLayout bwd_layout(int64_t T, int64_t R, int32_t dim) {
   L.max_tiles = (T + kChunk - 1) / kChunk;
   L.carry_bytes = align_up(size_t(L.max_tiles) * size_t(dim) * sizeof(float));
   L.flag_bytes = align_up(size_t(L.max_tiles));
+  L.max_blocks = L.max_tiles / kCarryBlock + 1;
+  L.block_bytes = align_up(size_t(L.max_blocks) * size_t(dim) * sizeof(double));
+  L.block_flag_bytes = align_up(size_t(L.max_blocks));
   return L;
 }
 
@@ -397,7 +680,8 @@ extern "C" size_t fs_emb_backward_adagrad_workspace_size(int64_t T, int64_t num_
   BwdLayout L = bwd_layout(T, num_rows, dim);
   // the single-call two-phase mode sorts one more key bit (the phase)
   const size_t sort_bytes = std::max(L.plan.bytes(), radix::SortPlan(T, L.plan.key_bits + 1).bytes());
-  return sort_bytes + 2 * L.carry_bytes + 2 * L.flag_bytes + align_up(sizeof(int64_t)) + 256;
+  return sort_bytes + 2 * L.carry_bytes + 2 * L.flag_bytes + L.block_bytes + L.block_flag_bytes +
+         align_up(sizeof(int64_t)) + 256;
 }
 
 extern "C" fs_status fs_emb_backward_adagrad(void* table, float* state, int64_t num_rows, int32_t dim, fs_dtype dtype,
@@ -438,6 +722,8 @@ extern "C" fs_status fs_emb_backward_adagrad(void* table, float* state, int64_t 
   float* carry_tail = cur.take<float>(size_t(L.max_tiles) * dim);
   uint8_t* head_cont = cur.take<uint8_t>(size_t(L.max_tiles));
   uint8_t* tail_flag = cur.take<uint8_t>(size_t(L.max_tiles));
+  double* block_sum = cur.take<double>(size_t(L.max_blocks) * dim);
+  uint8_t* block_full = cur.take<uint8_t>(size_t(L.max_blocks));
   int64_t* n_first = cur.take<int64_t>(1);
   if (!cur.ok) return FS_ERR_WORKSPACE;
 
@@ -452,7 +738,8 @@ extern "C" fs_status fs_emb_backward_adagrad(void* table, float* state, int64_t 
   // one update launch over a range of the sorted entries
   auto reduce_range = [&](const int64_t* begin_dev, const int64_t* end_dev, uint32_t row_mask) {
 #define FS_REDUCE(BF, E) \
-  launch_reduce<BF, E>(sk, sv, begin_dev, end_dev, row_mask, grads, u, carry_head, carry_tail, head_cont, tail_flag, st)
+  launch_reduce<BF, E>(sk, sv, begin_dev, end_dev, row_mask, grads, u, carry_head, carry_tail, head_cont, tail_flag, \
+                       block_sum, block_full, err, st)
     switch (epl) {
       case 1: if (bf) FS_REDUCE(true, 1); else FS_REDUCE(false, 1); break;
       case 2: if (bf) FS_REDUCE(true, 2); else FS_REDUCE(false, 2); break;
@@ -460,7 +747,7 @@ extern "C" fs_status fs_emb_backward_adagrad(void* table, float* state, int64_t 
       default: FS_REDUCE(true, 8); break;
     }
 #undef FS_REDUCE
-    launches += 2;
+    launches += 3;
   };
   if (phase == FS_PHASE_COLLISION_THEN_EXCLUSIVE) {
     // collision rows sort first: update them in a first launch, the exclusive

@@ -1,0 +1,98 @@
+// Bulk asynchronous copies global -> shared memory tracked by mbarriers
+// (sm_90+ `cp.async.bulk` and `mbarrier` PTX, used on sm_103a).  A copy of
+// `bytes` bytes (a multiple of 16, both addresses 16-byte aligned) lands in
+// shared memory and decrements the barrier's transaction count; a wait on the
+// barrier's phase parity returns once every byte announced for that phase
+// with arrive_expect_tx has arrived.
+#pragma once
+
+#include <stdint.h>
+
+namespace fs {
+namespace bulk {
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+// Make barrier initialisation visible to the copy engine before first use.
+__device__ __forceinline__ void fence_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_inval(uint32_t bar) {
+  asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// One arrival on the barrier that also announces `bytes` bytes to come.
+__device__ __forceinline__ void arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile(
+      "{\n .reg .b64 st;\n mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n}" ::"r"(bar), "r"(bytes)
+      : "memory");
+}
+
+// L2 policy for data read exactly once: evict it first.
+__device__ __forceinline__ uint64_t evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+__device__ __forceinline__ void copy_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
+          "r"(dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(pol)
+      : "memory");
+}
+
+__device__ __forceinline__ bool try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Like try_wait, but the thread may sleep (up to `hint_ns`) until the phase
+// completes instead of returning at once: a waiting warp takes no issue slots.
+__device__ __forceinline__ bool try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Whole warp waits for the phase of parity `parity` to complete; gives up
+// (returns false) once `limit_ns` nanoseconds have passed.  Every lane
+// observes the completion itself, so each has the acquire ordering of the
+// copied bytes.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  bool ok = try_wait(bar, parity);
+  if (__all_sync(0xffffffffu, ok)) return true;
+  const uint64_t t0 = global_ns();
+  for (;;) {
+    if (!ok) ok = try_wait_sleep(bar, parity, 100000u);
+    if (__all_sync(0xffffffffu, ok)) return true;
+    if (global_ns() - t0 > limit_ns) return false;
+  }
+}
+
+}  // namespace bulk
+}  // namespace fs

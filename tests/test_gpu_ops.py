@@ -474,3 +474,28 @@ def test_lookback_wait_gives_up_with_timeout_status():
     # the context is still usable
     _, _, _, err = B.fs_balance_vbs(torch.from_numpy(L).to(DEV), 16, 1.5, 0)
     _check(err)
+
+
+def test_gradient_copy_wait_gives_up_with_timeout_status():
+    """A gradient stage that is never copied: the update's wait for it runs out,
+    the call reports FS_ERR_TIMEOUT, and the context stays usable."""
+    R, D, T = 5000, 64, 40_000                              # 20 sorted tiles of 2048
+    ids, W, G = _bwd_case(9, R, D, T, "f32")
+    Wd, sd, idd, Gd = W.to(DEV), torch.zeros(R, device=DEV), ids.to(DEV), G.to(DEV)
+    assert Gd.data_ptr() % 16 == 0                         # the bulk-copy path
+    B.set_spin_limit(1 << 14)
+    B.debug_skip_publish(2)
+    try:
+        err = B.fs_emb_backward_adagrad(Wd, sd, idd, Gd, "adagrad", 0.01, 1e-8)
+        with pytest.raises(B.FsError) as e:
+            _check(err)
+        assert e.value.code == 6
+    finally:
+        B.debug_skip_publish(-1)
+        B.set_spin_limit(1 << 22)
+    Wd, sd = W.to(DEV), torch.zeros(R, device=DEV)
+    err = B.fs_emb_backward_adagrad(Wd, sd, idd, Gd, "adagrad", 0.01, 1e-8)
+    _check(err)
+    W_ref, s_ref = to_np(W), np.zeros(R, np.float32)
+    oracle.emb_backward(W_ref, s_ref, ids.numpy(), to_np(G), "adagrad", 0.01, 1e-8)
+    assert_table_close(to_np(Wd), W_ref, "f32", 0.01)
