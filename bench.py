@@ -378,7 +378,7 @@ def run_gpu(args):
                    "parallelism": f"replicas x{ws}"},
         "hbm_roofline_frac_step": step_bytes / secs / (hbm_gbs * 1e9),
         "algorithmic_bytes_per_step": step_bytes / K,
-        "roofline": {"kernel": "fs_emb_gather (gather_rows_kernel<16>)", "bound": "hbm", "achieved": achieved,
+        "roofline": {"kernel": GATHER_KERNEL, "bound": "hbm", "achieved": achieved,
                      "peak": hbm_gbs, "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / hbm_gbs,
                      "traffic": traffic, "algorithmic_bytes_per_launch": gbytes, "avg_launch_ms": gather_ms},
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clk,
@@ -391,11 +391,17 @@ def run_gpu(args):
     return 0
 
 
+# the dominant kernel of the step: the unmasked gather of the synchronous order
+GATHER_KERNEL = "fs_emb_gather (gather_bulk_kernel<4, 2>)"
+
+
 def kernel_hash():
+    """Hash of the sources of the gather kernel (the recorded DRAM traffic is valid for these only)."""
     import hashlib
     h = hashlib.sha256()
-    with open(os.path.join(ROOT, "jagged_embedding_gb300", "csrc", "gather.cu"), "rb") as f:
-        h.update(f.read())
+    for name in ("gather.cu", "bulk.cuh"):
+        with open(os.path.join(ROOT, "jagged_embedding_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
     return h.hexdigest()[:16]
 
 

@@ -11,6 +11,7 @@
 // stay cached in L1/L2.  A lane moves one 16-byte vector of a row; lanes of a
 // warp cover consecutive vectors, so a 256-byte row is 16 lanes and one warp
 // instruction moves two rows.  Each lane keeps 8 independent vectors in flight.
+#include "bulk.cuh"
 #include "fs_common.cuh"
 
 namespace fs {
@@ -103,6 +104,94 @@ __global__ void __launch_bounds__(kThreads) gather_word_kernel(const uint32_t* _
   }
 }
 
+// Unmasked gather through the copy engine: each warp moves stages of BR
+// consecutive output rows (BR * row bytes <= 2 KB).  The table rows of a stage
+// arrive in a shared-memory slot by one bulk copy per row (completion counted
+// in bytes on the slot's mbarrier); the whole stage then leaves by one bulk
+// store to its contiguous place in the output.  A ring of NS slots keeps LA
+// stages of loads in flight while one stage is stored.  Table rows are read
+// with an evict-last L2 policy (hot rows are read again), the output is
+// written evict-first.  A wait that exceeds wait_ns sets FS_ERR_TIMEOUT.
+constexpr int kBulkStage = 2048;
+template <int NS, int LA>
+struct BulkRing {
+  static constexpr int kWarpBytes = 128 + NS * kBulkStage;
+  static constexpr int kBlockBytes = (kThreads / 32) * kWarpBytes;
+  static_assert(LA >= 1 && LA <= NS - 2, "one slot is being stored while LA are loading");
+};
+
+template <int NS, int LA>
+__global__ void __launch_bounds__(kThreads) gather_bulk_kernel(const char* __restrict__ table, int64_t R, int rb,
+                                                               int br, const int64_t* __restrict__ ids, int64_t T,
+                                                               char* __restrict__ out, int32_t* err,
+                                                               uint64_t wait_ns) {
+  using RG = BulkRing<NS, LA>;
+  extern __shared__ __align__(128) unsigned char gsm[];
+  const int lane = threadIdx.x & 31;
+  unsigned char* wb = gsm + (threadIdx.x >> 5) * RG::kWarpBytes;
+  const uint32_t bar0 = bulk::smem_addr(wb);
+  const uint32_t data0 = bar0 + 128;
+  if (lane == 0)
+    for (int s = 0; s < NS; ++s) bulk::mbar_init(bar0 + 8 * s, 1);
+  bulk::fence_init();
+  __syncwarp();
+  const uint64_t pol_in = bulk::evict_last_policy();
+  const uint64_t pol_out = bulk::evict_first_policy();
+  const int64_t nst = (T + br - 1) / br;
+  const int64_t w = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nw = (int64_t(gridDim.x) * blockDim.x) >> 5;
+  const int64_t nmine = w < nst ? (nst - 1 - w) / nw + 1 : 0;
+  // ID of this lane's row in stage k (-1: none or out of range)
+  auto load_id = [&](int64_t k) -> int64_t {
+    if (k >= nmine) return -1;
+    const int64_t r = (w + k * nw) * br + lane;
+    if (lane >= br || r >= T) return -1;
+    const int64_t id = __ldcs(ids + r);
+    if (id < 0 || id >= R) {
+      set_err(err, FS_ERR_ID_RANGE);
+      return -1;
+    }
+    return id;
+  };
+  auto issue = [&](int64_t k, int64_t id) {
+    if (k >= nmine) return;
+    const uint32_t s = uint32_t(k % NS);
+    const uint32_t bar = bar0 + 8 * s;
+    const unsigned valid = __ballot_sync(0xffffffffu, id >= 0);
+    if (lane == 0) bulk::arrive_expect_tx(bar, uint32_t(__popc(valid) * rb));
+    __syncwarp();
+    if (id >= 0) bulk::copy_g2s(data0 + s * kBulkStage + lane * rb, table + id * rb, uint32_t(rb), bar, pol_in);
+  };
+  for (int k = 0; k < LA; ++k) issue(k, load_id(k));
+  int64_t next_id = load_id(LA);
+  for (int64_t k = 0; k < nmine; ++k) {
+    // the slot of stage k + LA last held stage k + LA - NS, stored at least
+    // two iterations ago: at most the newest store may still be reading
+    if (lane == 0) bulk::wait_group_read<NS - LA - 1>();
+    __syncwarp();
+    issue(k + LA, next_id);
+    next_id = load_id(k + LA + 1);
+    const uint32_t s = uint32_t(k % NS);
+    if (!bulk::warp_wait(bar0 + 8 * s, uint32_t((k / NS) & 1), wait_ns)) {
+      if (lane == 0) set_err(err, FS_ERR_TIMEOUT);
+      for (int64_t j = k + 1; j <= k + LA && j < nmine; ++j)
+        bulk::warp_wait(bar0 + 8 * uint32_t(j % NS), uint32_t((j / NS) & 1), wait_ns);
+      break;
+    }
+    if (lane == 0) {
+      const int64_t r0 = (w + k * nw) * br;
+      const int64_t rows = (T - r0 < br) ? T - r0 : br;
+      bulk::fence_async_shared();
+      bulk::store_s2g(out + r0 * rb, data0 + s * kBulkStage, uint32_t(rows * rb), pol_out);
+      bulk::commit_group();
+    }
+  }
+  if (lane == 0) bulk::wait_group_all();
+  __syncwarp();
+  if (lane == 0)
+    for (int s = 0; s < NS; ++s) bulk::mbar_inval(bar0 + 8 * s);
+}
+
 }  // namespace
 }  // namespace fs
 
@@ -120,7 +209,19 @@ extern "C" fs_status fs_emb_gather(const void* table, int64_t num_rows, int32_t 
   if (row_bytes % 4 != 0) return FS_ERR_INVALID_ARG;
   if (!aligned(ids, 8) || !aligned(table, 4) || !aligned(out, 4)) return FS_ERR_ALIGNMENT;
   const int sms = sm_count();
-  if (row_bytes % 16 == 0 && aligned(table, 16) && aligned(out, 16)) {
+  if (!mask && row_bytes % 16 == 0 && row_bytes <= kBulkStage && aligned(table, 16) && aligned(out, 16)) {
+    // unmasked: every output row is written, so whole stages go out by bulk store
+    constexpr int NS = 4, LA = 2;
+    using RG = BulkRing<NS, LA>;
+    const int rb = int(row_bytes);
+    const int br = (kBulkStage / rb) < 32 ? (kBulkStage / rb) : 32;
+    auto kern = gather_bulk_kernel<NS, LA>;
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, RG::kBlockBytes);
+    const int per_sm = (227 * 1024) / (RG::kBlockBytes + 1024);
+    kern<<<unsigned(sms * per_sm), kThreads, RG::kBlockBytes, st>>>(static_cast<const char*>(table), num_rows, rb, br,
+                                                                     ids, T, static_cast<char*>(out), err,
+                                                                     uint64_t(spin_limit()) * 256u);
+  } else if (row_bytes % 16 == 0 && aligned(table, 16) && aligned(out, 16)) {
     const int vpr = int(row_bytes / 16);
     const int4* tb = static_cast<const int4*>(table);
     int4* ob = static_cast<int4*>(out);

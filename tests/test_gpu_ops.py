@@ -279,7 +279,8 @@ def test_collision_capacity_error():
 
 # ------------------------------------------------------------------ gather
 
-@pytest.mark.parametrize("dtype,D", [("f32", 64), ("bf16", 128), ("f32", 128), ("f32", 3), ("bf16", 6), ("f32", 20)])
+@pytest.mark.parametrize("dtype,D", [("f32", 64), ("bf16", 128), ("f32", 128), ("f32", 3), ("bf16", 6), ("f32", 20),
+                                     ("bf16", 8), ("f32", 512), ("f32", 1024), ("bf16", 32)])
 def test_gather_bit_exact(dtype, D):
     rng = np.random.default_rng(D)
     R, T = 5000, 77_777
