@@ -49,61 +49,75 @@ __device__ __forceinline__ int64_t item_index(int64_t tile, int warp, int i, int
 }
 
 // ------------------------------------------------------------------ upsweep
+// One block-wide histogram per tile: all item loads are issued first, then
+// one shared-memory increment per item.
 template <class Src>
 __global__ void __launch_bounds__(kThreads) upsweep_kernel(Src src, int shift, int bits, int nb,
                                                            const int64_t* count_dev, int64_t count_host,
                                                            uint32_t* counts, int64_t ntiles, int32_t* err) {
-  __shared__ uint32_t wh[kWarps * kMaxBins];
+  __shared__ uint32_t hist[kMaxBins];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t tile = blockIdx.x;
   const int64_t count = count_dev ? *count_dev : count_host;
-  for (int j = threadIdx.x; j < kWarps * nb; j += kThreads) wh[j] = 0;
+  for (int j = threadIdx.x; j < nb; j += kThreads) hist[j] = 0;
   __syncthreads();
   if (tile * kTile < count) {
-    uint32_t* mine = wh + warp * nb;
-#pragma unroll 4
+    typename Src::Key k[kItems];
+    bool ok[kItems];
+#pragma unroll
     for (int i = 0; i < kItems; ++i) {
       const int64_t idx = item_index(tile, warp, i, lane);
-      typename Src::Key k;
       uint32_t v;
-      if (idx < count && src.load(idx, k, v, err)) atomicAdd(mine + src.digit(k, shift, bits), 1u);
+      ok[i] = idx < count && src.load(idx, k[i], v, err);
     }
+#pragma unroll
+    for (int i = 0; i < kItems; ++i)
+      if (ok[i]) atomicAdd(hist + src.digit(k[i], shift, bits), 1u);
   }
   __syncthreads();
-  for (int d = threadIdx.x; d < nb; d += kThreads) {
-    uint32_t c = 0;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) c += wh[w * nb + d];
-    counts[int64_t(d) * ntiles + tile] = c;
-  }
+  for (int d = threadIdx.x; d < nb; d += kThreads) counts[int64_t(d) * ntiles + tile] = hist[d];
 }
 
 // ------------------------------------------------------------------ scans
 // Block d: exclusive scan of counts[d * ntiles + 0 .. ntiles) in place; totals[d].
+// Rows are moved in slices of kThreads * kScanPer values: coalesced loads into
+// shared memory, kScanPer consecutive values per thread, coalesced stores.
+constexpr int kScanPer = 16;
 static __global__ void __launch_bounds__(kThreads) tile_scan_kernel(uint32_t* counts, int64_t ntiles, uint32_t* totals) {
   __shared__ uint32_t tmp[32];
+  __shared__ uint32_t slice[kThreads * kScanPer];
   uint32_t* row = counts + int64_t(blockIdx.x) * ntiles;
-  constexpr int kPer = 8;
   uint32_t carry = 0;
-  for (int64_t base = 0; base < ntiles; base += int64_t(kThreads) * kPer) {
-    uint32_t v[kPer];
+  for (int64_t base = 0; base < ntiles; base += int64_t(kThreads) * kScanPer) {
+    const int64_t left = ntiles - base;
+#pragma unroll
+    for (int i = 0; i < kScanPer; ++i) {
+      const int j = i * kThreads + threadIdx.x;
+      slice[j] = j < left ? row[base + j] : 0u;
+    }
+    __syncthreads();
+    uint32_t v[kScanPer];
     uint32_t sum = 0;
 #pragma unroll
-    for (int i = 0; i < kPer; ++i) {
-      const int64_t t = base + int64_t(threadIdx.x) * kPer + i;
-      v[i] = t < ntiles ? row[t] : 0u;
+    for (int i = 0; i < kScanPer; ++i) {
+      v[i] = slice[threadIdx.x * kScanPer + i];
       sum += v[i];
     }
     uint32_t tot;
-    uint32_t ex = block_exclusive_scan<uint32_t>(sum, tmp, &tot);
-    uint32_t run = carry + ex;
+    uint32_t run = carry + block_exclusive_scan<uint32_t>(sum, tmp, &tot);
 #pragma unroll
-    for (int i = 0; i < kPer; ++i) {
-      const int64_t t = base + int64_t(threadIdx.x) * kPer + i;
-      if (t < ntiles) row[t] = run;
+    for (int i = 0; i < kScanPer; ++i) {
+      slice[threadIdx.x * kScanPer + i] = run;
       run += v[i];
     }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < kScanPer; ++i) {
+      const int j = i * kThreads + threadIdx.x;
+      if (j < left) row[base + j] = slice[j];
+    }
     carry += tot;
+    __syncthreads();
   }
   if (threadIdx.x == 0) totals[blockIdx.x] = carry;
 }
