@@ -90,7 +90,7 @@ fs_status fs_balance_fbs(const int32_t* uih_len, int64_t S, int32_t n, int32_t* 
  * -- code running while a memory pool is frozen or torn down, a plugin inside
  * another framework's process whose allocator it does not own, a step with a
  * fixed memory plan.  Same result as fs_balance_fbs; the sort's scratch is a
- * fixed array inside the library (about 4.7 MB of device memory, held on every
+ * fixed array inside the library (about 4.3 MB of device memory, held on every
  * device that loads the library until the process exits), so this call
  * allocates nothing.
  *   S must be <= 262144 (FS_ERR_INVALID_ARG otherwise).

@@ -1,0 +1,62 @@
+"""One hot-path call on seeded synthetic input, for profiling a single kernel.
+
+    python -m jagged_embedding_gb300.cases <op> <T> <R> [reps]
+
+op is one of
+  gather    -- fs_emb_gather, unmasked, f32 rows of 64, T bounded-Zipf(1.0) IDs over R rows
+  backward  -- fs_emb_backward_adagrad (sort + reduce + fixup), same IDs, f32, row-wise Adagrad,
+               collision rows (half of the rows, by a hash of the row) updated before exclusive rows
+  bucketize -- fs_bucketize_rowwise of the same IDs into 256 row-range shards
+Inputs come from jagged_embedding_gb300.synthetic; every call goes through the C ABI.
+Exits non-zero if a call reports an error.
+"""
+from __future__ import annotations
+
+import sys
+
+import torch
+
+from . import binding as B
+from . import synthetic
+
+DIM = 64
+SHARDS = 256
+
+
+def main(argv) -> int:
+    if len(argv) < 3 or argv[0] not in ("gather", "backward", "bucketize"):
+        print(__doc__)
+        return 2
+    op, T, R = argv[0], int(argv[1]), int(argv[2])
+    reps = int(argv[3]) if len(argv) > 3 else 2
+    dev = torch.device("cuda")
+    g = torch.Generator(device=dev)
+    g.manual_seed(1)
+    ids = synthetic.zipf_rows(R, 1.0, T, g, dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    if op == "gather":
+        table = torch.empty(R, DIM, device=dev).normal_(0, 0.01, generator=g)
+        out = torch.empty(T, DIM, device=dev)
+        for _ in range(reps):
+            B.fs_emb_gather(table, ids, out=out, err=err)
+    elif op == "backward":
+        table = torch.empty(R, DIM, device=dev).normal_(0, 0.01, generator=g)
+        state = torch.zeros(R, device=dev)
+        grads = torch.empty(T, DIM, device=dev).normal_(generator=g)
+        ws = B.workspace(B.backward_workspace_size(T, R, DIM, B.dtype_code(table)), dev)
+        is_co = (((ids * 0x9E3779B1) >> 7) & 1).to(torch.uint8)
+        for _ in range(reps):
+            B.fs_emb_backward_adagrad(table, state, ids, grads, "adagrad", 0.01, 1e-8, is_co=is_co,
+                                      phase=B.PHASE_COLLISION_THEN_EXCLUSIVE, err=err, ws=ws)
+    else:
+        rio = torch.linspace(0, T, SHARDS + 1, device=dev).round().to(torch.int64)
+        for _ in range(reps):
+            B.fs_bucketize_rowwise(ids, rio, R, err=err)
+    torch.cuda.synchronize()
+    B.check(err, op)
+    print(f"{op} T={T} R={R} reps={reps}: ok")
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main(sys.argv[1:]))

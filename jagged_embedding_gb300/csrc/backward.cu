@@ -46,12 +46,22 @@ struct SrcRows {
   int phase;
   int64_t R;
   int kb;  // bits of the largest row index
-  __device__ __forceinline__ bool load(int64_t i, Key& key, uint32_t& val, int32_t* err) const {
-    // the ID and the mask byte are loaded independently (no load-to-load dependency)
-    const int64_t id = __ldcs(ids + i);
+  struct Raw {
+    int64_t id;
+    uint32_t m;
+  };
+  // the ID and the mask byte are loaded independently (no load-to-load dependency)
+  __device__ __forceinline__ Raw fetch(int64_t i) const {
+    Raw r;
+    r.id = __ldcs(ids + i);
+    r.m = phase != FS_PHASE_ALL ? uint32_t(__ldcs(is_co + i)) : 0u;
+    return r;
+  }
+  __device__ __forceinline__ bool make(const Raw& r, int64_t i, Key& key, uint32_t& val, int32_t* err) const {
+    const int64_t id = r.id;
     uint32_t hi = 0;
     if (phase != FS_PHASE_ALL) {
-      const uint8_t m = __ldcs(is_co + i);
+      const uint32_t m = r.m;
       if (phase == FS_PHASE_COLLISION_THEN_EXCLUSIVE) {
         if (m > 1) return false;
         hi = uint32_t(1 - m) << kb;

@@ -21,8 +21,9 @@ struct SrcLen {
   using Key = uint32_t;
   static constexpr bool kIndexValue = true;  // value = item index
   const int32_t* L;
-  __device__ __forceinline__ bool load(int64_t i, Key& key, uint32_t& val, int32_t* err) const {
-    int32_t l = L[i];
+  using Raw = int32_t;
+  __device__ __forceinline__ Raw fetch(int64_t i) const { return L[i]; }
+  __device__ __forceinline__ bool make(Raw l, int64_t i, Key& key, uint32_t& val, int32_t* err) const {
     if (l < 0) {
       if (err) set_err(err, FS_ERR_INVALID_ARG);
       l = 0;
@@ -246,7 +247,9 @@ constexpr int64_t kNoAllocMaxS = int64_t(1) << 18;  // 262144 samples
 // 31-bit keys (4 passes of 8 bits: 256 digit values), at compile time.
 constexpr size_t ce_align(size_t x) { return (x + 255) / 256 * 256; }
 constexpr size_t kNoAllocTiles = size_t((kNoAllocMaxS + radix::kTile - 1) / radix::kTile);
+constexpr size_t kNoAllocChunks = (kNoAllocTiles + radix::kChunkTiles - 1) / radix::kChunkTiles;
 constexpr size_t kNoAllocScratchBytes = ce_align(256 * kNoAllocTiles * sizeof(uint32_t)) +
+                                        ce_align(256 * kNoAllocChunks * sizeof(uint32_t)) +
                                         2 * ce_align(radix::kMaxBins * sizeof(uint32_t)) + ce_align(sizeof(int64_t)) +
                                         4 * ce_align(size_t(kNoAllocMaxS) * sizeof(uint32_t));
 
@@ -284,8 +287,8 @@ extern "C" fs_status fs_balance_fbs_noalloc(const int32_t* uih_len, int64_t S, i
   if (s != FS_OK) return s;
   const size_t need = radix::SortPlan(S, kLenKeyBits).bytes();
   if (need > kNoAllocScratchBytes) return FS_ERR_INVALID_ARG;
-  // the sort clears its counters and look-back words itself (cudaMemsetAsync
-  // on this array), so stale contents of a previous call do no harm
+  // every count the sort reads it has written earlier in the same call, so
+  // stale contents of a previous call do no harm
   return fs_balance_fbs(uih_len, S, n, perm, rank_offsets, err, scratch, sizeof(g_fbs_scratch), stream);
 }
 

@@ -27,8 +27,10 @@ struct SrcShard {
   int64_t block;
   float inv_block;
   int32_t n;
-  __device__ __forceinline__ bool load(int64_t i, Key& key, uint32_t& val, int32_t* err) const {
-    key = __ldcs(ids + i);
+  using Raw = int64_t;
+  __device__ __forceinline__ Raw fetch(int64_t i) const { return __ldcs(ids + i); }
+  __device__ __forceinline__ bool make(Raw id, int64_t i, Key& key, uint32_t& val, int32_t* err) const {
+    key = id;
     val = static_cast<uint32_t>(i);
     if (err && (key < 0 || key >= R)) set_err(err, FS_ERR_ID_RANGE);
     return true;

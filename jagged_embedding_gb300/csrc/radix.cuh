@@ -2,23 +2,28 @@
 // Merrill & Grimshaw, "High Performance and Scalable Radix Sorting", 2011).
 //
 // One pass over the items of [0, count) keyed by one digit:
-//   1. upsweep:   per 4096-item tile, the count of every digit value
-//                 (counts[d * ntiles + tile]);
-//   2. scan:      per digit, the exclusive prefix of its counts over the tiles
-//                 (one block per digit), then the exclusive prefix of the
-//                 digit totals (one block);
-//   3. downsweep: per tile, a stable rank of every item among the tile's items
-//                 with the same digit (warp __match_any_sync multisplit, warps
-//                 combined in order), staging in digit order in shared memory
-//                 and coalesced writes of every digit run to
-//                 digit_base[d] + counts[d * ntiles + tile] + rank.
-// No block waits on another block, so nothing spins.  (A single-pass
-// decoupled look-back over ~70k tiles per pass was measured on GB300 to be
-// bound by the look-back chain, about 16 tiles per microsecond.)
+//   1. upsweep:    one block per chunk of kChunkTiles tiles of kTile items;
+//                  per tile, the count of every digit value, written as the
+//                  exclusive prefix over the chunk's earlier tiles
+//                  (counts[tile][digit]); per chunk, the digit totals;
+//   2. chunk scan: per digit, the exclusive prefix of the chunk totals over
+//                  the chunks, and the digit totals; then the exclusive
+//                  prefix of the digit totals (digit_base);
+//   3. downsweep:  per tile, a stable rank of every item among the tile's items
+//                  with the same digit (warp __match_any_sync multisplit, warps
+//                  combined in order), staging in digit order in shared memory
+//                  and coalesced writes of every digit run to
+//                  digit_base[d] + chunk_base[chunk][d] + counts[tile][d] + rank.
+// All count arrays are digit-minor, so every read and write of them is
+// coalesced.  No block waits on another block, so nothing spins.  (A
+// single-pass decoupled look-back over ~70k tiles per pass was measured on
+// GB300 to be bound by the look-back chain, about 16 tiles per microsecond.)
 //
 // Sources (`Src`) decide where keys and values come from (a plain array, a
 // length array with the index as value, an ID array filtered by a mask ...)
-// and the digit function; sinks (`Dst`) decide what is written.
+// and the digit function: fetch(i) only loads (so that a tile's loads are all
+// in flight together), make(raw, i, key, val, err) checks and converts.
+// Sinks (`Dst`) decide what is written.
 #pragma once
 
 #include "fs_common.cuh"
@@ -31,8 +36,11 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kItems = 16;
 constexpr int kTile = kThreads * kItems;  // 4096 items per tile
 constexpr int kMaxBins = 1024;
+constexpr int kChunkTiles = 16;  // tiles per upsweep block
+constexpr int kPerT = kMaxBins / kThreads;  // digits per thread
 
 inline int64_t num_tiles(int64_t count) { return (count + kTile - 1) / kTile; }
+inline int64_t num_chunks(int64_t ntiles) { return (ntiles + kChunkTiles - 1) / kChunkTiles; }
 
 template <class KeyT>
 constexpr size_t downsweep_smem_bytes() {
@@ -49,77 +57,95 @@ __device__ __forceinline__ int64_t item_index(int64_t tile, int warp, int i, int
 }
 
 // ------------------------------------------------------------------ upsweep
-// One block-wide histogram per tile: all item loads are issued first, then
-// one shared-memory increment per item.
+// Block c: tiles [c * kChunkTiles, ...) one after another.  Per tile, one
+// block-wide histogram (all item loads issued first, then one shared-memory
+// increment per item); counts[tile][d] = this chunk's count of d before the
+// tile; chunk_sums[c][d] = the chunk's count of d.
 template <class Src>
 __global__ void __launch_bounds__(kThreads) upsweep_kernel(Src src, int shift, int bits, int nb,
                                                            const int64_t* count_dev, int64_t count_host,
-                                                           uint32_t* counts, int64_t ntiles, int32_t* err) {
+                                                           uint32_t* counts, uint32_t* chunk_sums, int64_t ntiles,
+                                                           int32_t* err) {
   __shared__ uint32_t hist[kMaxBins];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int64_t tile = blockIdx.x;
+  const int64_t chunk = blockIdx.x;
   const int64_t count = count_dev ? *count_dev : count_host;
-  for (int j = threadIdx.x; j < nb; j += kThreads) hist[j] = 0;
-  __syncthreads();
-  if (tile * kTile < count) {
-    typename Src::Key k[kItems];
-    bool ok[kItems];
+  uint32_t run[kPerT];
 #pragma unroll
-    for (int i = 0; i < kItems; ++i) {
-      const int64_t idx = item_index(tile, warp, i, lane);
-      uint32_t v;
-      ok[i] = idx < count && src.load(idx, k[i], v, err);
+  for (int j = 0; j < kPerT; ++j) run[j] = 0;
+  for (int c = 0; c < kChunkTiles; ++c) {
+    const int64_t tile = chunk * kChunkTiles + c;
+    if (tile >= ntiles) break;
+    for (int j = threadIdx.x; j < nb; j += kThreads) hist[j] = 0;
+    __syncthreads();
+    if (tile * kTile < count) {
+      typename Src::Raw raw[kItems];
+#pragma unroll
+      for (int i = 0; i < kItems; ++i) {
+        const int64_t idx = item_index(tile, warp, i, lane);
+        if (idx < count) raw[i] = src.fetch(idx);
+      }
+#pragma unroll
+      for (int i = 0; i < kItems; ++i) {
+        const int64_t idx = item_index(tile, warp, i, lane);
+        typename Src::Key k;
+        uint32_t v;
+        if (idx < count && src.make(raw[i], idx, k, v, err)) atomicAdd(hist + src.digit(k, shift, bits), 1u);
+      }
     }
+    __syncthreads();
 #pragma unroll
-    for (int i = 0; i < kItems; ++i)
-      if (ok[i]) atomicAdd(hist + src.digit(k[i], shift, bits), 1u);
+    for (int j = 0; j < kPerT; ++j) {
+      const int d = threadIdx.x + j * kThreads;
+      if (d < nb) {
+        counts[tile * nb + d] = run[j];
+        run[j] += hist[d];
+      }
+    }
+    __syncthreads();
   }
-  __syncthreads();
-  for (int d = threadIdx.x; d < nb; d += kThreads) counts[int64_t(d) * ntiles + tile] = hist[d];
+#pragma unroll
+  for (int j = 0; j < kPerT; ++j) {
+    const int d = threadIdx.x + j * kThreads;
+    if (d < nb) chunk_sums[chunk * nb + d] = run[j];
+  }
 }
 
 // ------------------------------------------------------------------ scans
-// Block d: exclusive scan of counts[d * ntiles + 0 .. ntiles) in place; totals[d].
-// Rows are moved in slices of kThreads * kScanPer values: coalesced loads into
-// shared memory, kScanPer consecutive values per thread, coalesced stores.
-constexpr int kScanPer = 16;
-static __global__ void __launch_bounds__(kThreads) tile_scan_kernel(uint32_t* counts, int64_t ntiles, uint32_t* totals) {
-  __shared__ uint32_t tmp[32];
-  __shared__ uint32_t slice[kThreads * kScanPer];
-  uint32_t* row = counts + int64_t(blockIdx.x) * ntiles;
-  uint32_t carry = 0;
-  for (int64_t base = 0; base < ntiles; base += int64_t(kThreads) * kScanPer) {
-    const int64_t left = ntiles - base;
-#pragma unroll
-    for (int i = 0; i < kScanPer; ++i) {
-      const int j = i * kThreads + threadIdx.x;
-      slice[j] = j < left ? row[base + j] : 0u;
+// Exclusive prefix of chunk_sums[0 .. nchunks)[d] over the chunks, in place,
+// and totals[d].  Block b: digits [32 b, 32 b + 32), one per lane; warp w of
+// the block takes a contiguous range of chunks: range sums, exclusive over the
+// warps in shared memory, then each warp rescans its range.
+constexpr int kScanThreads = 1024;
+static __global__ void __launch_bounds__(kScanThreads) chunk_scan_kernel(uint32_t* chunk_sums, int64_t nchunks, int nb,
+                                                                        uint32_t* totals) {
+  __shared__ uint32_t part[32][33];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int d = blockIdx.x * 32 + lane;
+  const int64_t per = (nchunks + 31) / 32;
+  const int64_t c0 = w * per, c1 = (c0 + per < nchunks) ? c0 + per : nchunks;
+  uint32_t s = 0;
+  if (d < nb)
+    for (int64_t c = c0; c < c1; ++c) s += chunk_sums[c * nb + d];
+  part[w][lane] = s;
+  __syncthreads();
+  if (w == 0) {
+    uint32_t run = 0;
+    for (int ww = 0; ww < 32; ++ww) {
+      const uint32_t t = part[ww][lane];
+      part[ww][lane] = run;
+      run += t;
     }
-    __syncthreads();
-    uint32_t v[kScanPer];
-    uint32_t sum = 0;
-#pragma unroll
-    for (int i = 0; i < kScanPer; ++i) {
-      v[i] = slice[threadIdx.x * kScanPer + i];
-      sum += v[i];
-    }
-    uint32_t tot;
-    uint32_t run = carry + block_exclusive_scan<uint32_t>(sum, tmp, &tot);
-#pragma unroll
-    for (int i = 0; i < kScanPer; ++i) {
-      slice[threadIdx.x * kScanPer + i] = run;
-      run += v[i];
-    }
-    __syncthreads();
-#pragma unroll
-    for (int i = 0; i < kScanPer; ++i) {
-      const int j = i * kThreads + threadIdx.x;
-      if (j < left) row[base + j] = slice[j];
-    }
-    carry += tot;
-    __syncthreads();
+    if (d < nb) totals[d] = run;
   }
-  if (threadIdx.x == 0) totals[blockIdx.x] = carry;
+  __syncthreads();
+  uint32_t run = part[w][lane];
+  if (d < nb)
+    for (int64_t c = c0; c < c1; ++c) {
+      const uint32_t v = chunk_sums[c * nb + d];
+      chunk_sums[c * nb + d] = run;
+      run += v;
+    }
 }
 
 // Exclusive scan of the digit totals; *n_valid = their sum.
@@ -148,8 +174,8 @@ static __global__ void __launch_bounds__(kThreads) digit_base_kernel(const uint3
 template <class Src, class Dst>
 __global__ void __launch_bounds__(kThreads, 3) downsweep_kernel(Src src, Dst dst, int shift, int bits, int nb,
                                                                 const uint32_t* digit_base, const uint32_t* counts,
-                                                                int64_t ntiles, const int64_t* count_dev,
-                                                                int64_t count_host) {
+                                                                const uint32_t* chunk_base, int64_t ntiles,
+                                                                const int64_t* count_dev, int64_t count_host) {
   using KeyT = typename Src::Key;
   extern __shared__ __align__(16) unsigned char smem_raw[];
   uint32_t* warp_hist = reinterpret_cast<uint32_t*>(smem_raw);  // [kWarps][nb] (phase 1)
@@ -168,14 +194,15 @@ __global__ void __launch_bounds__(kThreads, 3) downsweep_kernel(Src src, Dst dst
   const int64_t count = count_dev ? *count_dev : count_host;
   if (tile * kTile >= count) return;
 
-  // this tile's offset inside every digit run: loaded first, so that the
-  // scattered reads overlap the item loads and the ranking below
-  constexpr int kPerT = kMaxBins / kThreads;
+  // this tile's offset inside every digit run: loaded first, so that these
+  // reads overlap the item loads and the ranking below
   uint32_t my_off[kPerT];
 #pragma unroll
   for (int i = 0; i < kPerT; ++i) {
     const int d = threadIdx.x + i * kThreads;
-    my_off[i] = d < nb ? __ldg(counts + int64_t(d) * ntiles + tile) + __ldg(digit_base + d) : 0u;
+    my_off[i] = d < nb ? __ldg(counts + tile * nb + d) + __ldg(chunk_base + (tile / kChunkTiles) * nb + d) +
+                             __ldg(digit_base + d)
+                       : 0u;
   }
 
   // per item: the key, one packed word (digit in bits 20..31, rank / local
@@ -185,13 +212,21 @@ __global__ void __launch_bounds__(kThreads, 3) downsweep_kernel(Src src, Dst dst
   uint32_t val[Src::kIndexValue ? 1 : kItems];
   uint32_t pk[kItems];
   constexpr uint32_t kSkipPk = 0xFFF00000u;
+  {
+    typename Src::Raw raw[kItems];
 #pragma unroll
-  for (int i = 0; i < kItems; ++i) {
-    const int64_t idx = item_index(tile, warp, i, lane);
-    uint32_t v = 0;
-    const bool ok = idx < count && src.load(idx, key[i], v, nullptr);
-    if constexpr (!Src::kIndexValue) val[i] = v;
-    pk[i] = ok ? (src.digit(key[i], shift, bits) << 20) : kSkipPk;
+    for (int i = 0; i < kItems; ++i) {
+      const int64_t idx = item_index(tile, warp, i, lane);
+      if (idx < count) raw[i] = src.fetch(idx);
+    }
+#pragma unroll
+    for (int i = 0; i < kItems; ++i) {
+      const int64_t idx = item_index(tile, warp, i, lane);
+      uint32_t v = 0;
+      const bool ok = idx < count && src.make(raw[i], idx, key[i], v, nullptr);
+      if constexpr (!Src::kIndexValue) val[i] = v;
+      pk[i] = ok ? (src.digit(key[i], shift, bits) << 20) : kSkipPk;
+    }
   }
   for (int j = threadIdx.x; j < kWarps * nb; j += kThreads) warp_hist[j] = 0;
   __syncthreads();
@@ -281,9 +316,11 @@ struct SrcU32 {
   static constexpr bool kIndexValue = false;
   const uint32_t* k;
   const uint32_t* v;
-  __device__ __forceinline__ bool load(int64_t i, Key& key, uint32_t& val, int32_t*) const {
-    key = __ldcs(k + i);
-    val = __ldcs(v + i);
+  using Raw = uint2;
+  __device__ __forceinline__ Raw fetch(int64_t i) const { return make_uint2(__ldcs(k + i), __ldcs(v + i)); }
+  __device__ __forceinline__ bool make(const Raw& r, int64_t, Key& key, uint32_t& val, int32_t*) const {
+    key = r.x;
+    val = r.y;
     return true;
   }
   __device__ __forceinline__ uint32_t digit(Key key, int shift, int bits) const {
@@ -315,7 +352,8 @@ inline void set_smem(K kernel, size_t bytes) {
 
 // Scratch of one counting-sort pass over up to `count` items with nb digit values.
 struct PassWs {
-  uint32_t* counts = nullptr;      // [nb][ntiles]
+  uint32_t* counts = nullptr;      // [ntiles][nb]
+  uint32_t* chunk = nullptr;       // [nchunks][nb]
   uint32_t* totals = nullptr;      // [kMaxBins]
   uint32_t* digit_base = nullptr;  // [kMaxBins]
   int64_t* n_valid = nullptr;      // [1]
@@ -323,20 +361,22 @@ struct PassWs {
 };
 
 inline size_t pass_ws_bytes(int64_t count, int nb) {
-  return align_up(size_t(nb) * size_t(num_tiles(count)) * sizeof(uint32_t)) + 2 * align_up(kMaxBins * sizeof(uint32_t)) +
-         align_up(sizeof(int64_t));
+  return align_up(size_t(nb) * size_t(num_tiles(count)) * sizeof(uint32_t)) +
+         align_up(size_t(nb) * size_t(num_chunks(num_tiles(count))) * sizeof(uint32_t)) +
+         2 * align_up(kMaxBins * sizeof(uint32_t)) + align_up(sizeof(int64_t));
 }
 
 inline bool carve_pass_ws(int64_t count, int nb, WsCursor& ws, PassWs& P) {
   P.ntiles = num_tiles(count);
   P.counts = ws.take<uint32_t>(size_t(nb) * size_t(P.ntiles));
+  P.chunk = ws.take<uint32_t>(size_t(nb) * size_t(num_chunks(P.ntiles)));
   P.totals = ws.take<uint32_t>(kMaxBins);
   P.digit_base = ws.take<uint32_t>(kMaxBins);
   P.n_valid = ws.take<int64_t>(1);
   return ws.ok;
 }
 
-// One stable counting-sort pass (upsweep, scans, downsweep).  count is
+// One stable counting-sort pass (upsweep, chunk scan, digit base, downsweep).  count is
 // *count_dev if given, else count_host; the grid covers count_host items.
 // *P.n_valid receives the number of items the source accepted.
 template <class Src, class Dst>
@@ -346,19 +386,21 @@ void run_pass(const Src& src, const Dst& dst, int shift, int bits, int nb, const
     cudaMemsetAsync(P.n_valid, 0, sizeof(int64_t), st);
     return;
   }
-  upsweep_kernel<Src><<<unsigned(P.ntiles), kThreads, 0, st>>>(src, shift, bits, nb, count_dev, count_host, P.counts,
-                                                               P.ntiles, err);
-  tile_scan_kernel<<<unsigned(nb), kThreads, 0, st>>>(P.counts, P.ntiles, P.totals);
+  const int64_t nchunks = num_chunks(P.ntiles);
+  upsweep_kernel<Src><<<unsigned(nchunks), kThreads, 0, st>>>(src, shift, bits, nb, count_dev, count_host, P.counts,
+                                                              P.chunk, P.ntiles, err);
+  chunk_scan_kernel<<<unsigned((nb + 31) / 32), kScanThreads, 0, st>>>(P.chunk, nchunks, nb, P.totals);
   digit_base_kernel<<<1, kThreads, 0, st>>>(P.totals, nb, P.digit_base, P.n_valid);
   const size_t smem = downsweep_smem_bytes<typename Src::Key>();
   set_smem(downsweep_kernel<Src, Dst>, smem);
   downsweep_kernel<Src, Dst><<<unsigned(P.ntiles), kThreads, smem, st>>>(src, dst, shift, bits, nb, P.digit_base,
-                                                                         P.counts, P.ntiles, count_dev, count_host);
+                                                                         P.counts, P.chunk, P.ntiles, count_dev,
+                                                                         count_host);
   *launches += 4;
 }
 
 // LSD sort of (uint32 key, uint32 value) pairs drawn from Src0 (the items of
-// [0, count) that Src0::load accepts), by the low key_bits bits of the key,
+// [0, count) that Src0::make accepts), by the low key_bits bits of the key,
 // in passes of at most 10 bits.  Result: *out_k / *out_v, *n_valid entries
 // (n_valid stays on the device).
 struct SortPlan {

@@ -89,3 +89,9 @@ def test_binding_refuses_cpu_tensors():
     import torch
     with pytest.raises(B.FsError):
         B.fs_balance_fbs(torch.zeros(4, dtype=torch.int32), 2)
+
+
+def test_profiling_cases_print_usage_without_arguments():
+    from jagged_embedding_gb300 import cases
+    assert cases.main([]) == 2
+    assert cases.main(["nosuchop", "1", "1"]) == 2
