@@ -32,7 +32,17 @@ namespace fs {
 namespace {
 
 using radix::kThreads;
-constexpr int kChunk = 2048;                 // sorted entries per reduce tile
+// Sorted entries per reduce tile: chosen on the device from the range's size n
+// so that a small range still spreads over every warp (about `target` tiles),
+// between kMinChunk and kMaxChunk and a multiple of 32.  Every kernel of one
+// update launch computes it from the same n and target, so they agree, and the
+// result depends only on n and the launch shape: identical run to run.
+constexpr int kMinChunk = 256, kMaxChunk = 2048;
+__device__ __forceinline__ int64_t tile_entries(int64_t n, int64_t target) {
+  int64_t c = (n + target - 1) / (target > 0 ? target : 1);
+  c = (c + 31) / 32 * 32;
+  return c < kMinChunk ? kMinChunk : (c > kMaxChunk ? kMaxChunk : c);
+}
 constexpr uint32_t kNoKey = 0xFFFFFFFFu;     // rows are < num_rows < 2^32
 
 // Sort source: the selected positions of the batch, key = row, value = position.
@@ -189,7 +199,7 @@ __device__ __forceinline__ void prefetch_l2(const void* p) {
 }
 
 // Sorted entries [*begin_dev, *end_dev) (begin 0 when begin_dev is null);
-// row = key & row_mask.  One warp per tile of kChunk sorted entries; the
+// row = key & row_mask.  One warp per tile of `chunk` sorted entries; the
 // gradient rows of a tile are summed in entry order, GROWS rows in flight.
 // For each batch of 32 entries one ballot marks the entries that end a row
 // (the next key differs), so the per-entry work is a load and an add.  A row
@@ -201,7 +211,7 @@ __global__ void __launch_bounds__(kThreads, MINB) reduce_kernel(const uint32_t* 
                                                              const int64_t* begin_dev, const int64_t* end_dev,
                                                              uint32_t row_mask, const void* __restrict__ grads,
                                                              UpdateArgs u, float* carry_head, float* carry_tail,
-                                                             uint8_t* head_cont, uint8_t* tail_flag) {
+                                                             uint8_t* head_cont, uint8_t* tail_flag, int64_t target) {
   constexpr int ESZ = BF16 ? 2 : 4;
   constexpr int D = 32 * EPL;
   constexpr int RB = D * ESZ;
@@ -210,12 +220,13 @@ __global__ void __launch_bounds__(kThreads, MINB) reduce_kernel(const uint32_t* 
   keys += b0;
   vals += b0;
   const int64_t n = *end_dev - b0;
-  const int64_t ntiles = (n + kChunk - 1) / kChunk;
+  const int64_t chunk = tile_entries(n, target);
+  const int64_t ntiles = (n + chunk - 1) / chunk;
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
   for (int64_t t = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; t < ntiles; t += nwarps) {
-    const int64_t s0 = t * kChunk;
-    const int64_t s1 = (s0 + kChunk < n) ? s0 + kChunk : n;
+    const int64_t s0 = t * chunk;
+    const int64_t s1 = (s0 + chunk < n) ? s0 + chunk : n;
     const uint32_t prev_key = s0 > 0 ? keys[s0 - 1] : kNoKey;
     const uint32_t next_key = s1 < n ? keys[s1] : kNoKey;
     bool from_prev = (keys[s0] == prev_key);  // the tile's first row began in an earlier tile
@@ -331,7 +342,8 @@ template <bool BF16, int EPL, int MINB>
 __global__ void __launch_bounds__(kThreads, MINB) reduce_ring_kernel(
     const uint32_t* __restrict__ keys, const uint32_t* __restrict__ vals, const int64_t* begin_dev,
     const int64_t* end_dev, uint32_t row_mask, const void* __restrict__ grads, UpdateArgs u, float* carry_head,
-    float* carry_tail, uint8_t* head_cont, uint8_t* tail_flag, int32_t* err, uint64_t wait_ns, int64_t skip_tile) {
+    float* carry_tail, uint8_t* head_cont, uint8_t* tail_flag, int32_t* err, uint64_t wait_ns, int64_t skip_tile,
+    int64_t target) {
   constexpr int ESZ = BF16 ? 2 : 4;
   constexpr int D = 32 * EPL;
   constexpr int RB = D * ESZ;
@@ -356,14 +368,15 @@ __global__ void __launch_bounds__(kThreads, MINB) reduce_ring_kernel(
   keys += b0;
   vals += b0;
   const int64_t n = *end_dev - b0;
-  const int64_t ntiles = (n + kChunk - 1) / kChunk;
+  const int64_t chunk = tile_entries(n, target);
+  const int64_t ntiles = (n + chunk - 1) / chunk;
   const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
   uint32_t gb = 0;  // stages this warp has consumed (all tiles): stage gb % NS, phase gb / NS
   bool failed = false;
 
   for (int64_t t = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; t < ntiles && !failed; t += nwarps) {
-    const int64_t s0 = t * kChunk;
-    const int m = int((s0 + kChunk < n) ? kChunk : n - s0);  // entries in this tile
+    const int64_t s0 = t * chunk;
+    const int m = int((s0 + chunk < n) ? chunk : n - s0);  // entries in this tile
     const uint32_t* tk = keys + s0;
     const uint32_t* tv = vals + s0;
     const uint32_t prev_key = s0 > 0 ? keys[s0 - 1] : kNoKey;
@@ -526,11 +539,12 @@ constexpr int kCarryBlock = 32;
 template <int EPL>
 __global__ void __launch_bounds__(kThreads) block_sum_kernel(const int64_t* begin_dev, const int64_t* end_dev,
                                                              const float* carry_head, const uint8_t* head_cont,
-                                                             double* block_sum, uint8_t* block_full) {
+                                                             double* block_sum, uint8_t* block_full, int64_t target) {
   constexpr int D = 32 * EPL;
   const int64_t b0 = begin_dev ? *begin_dev : 0;
   const int64_t n = *end_dev - b0;
-  const int64_t ntiles = (n + kChunk - 1) / kChunk;
+  const int64_t chunk = tile_entries(n, target);
+  const int64_t ntiles = (n + chunk - 1) / chunk;
   const int64_t nblocks = ntiles / kCarryBlock;  // whole blocks only
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
@@ -563,18 +577,20 @@ __global__ void __launch_bounds__(kThreads) fixup_kernel(const uint32_t* __restr
                                                          const int64_t* end_dev, uint32_t row_mask, UpdateArgs u,
                                                          const float* carry_head, const float* carry_tail,
                                                          const uint8_t* head_cont, const uint8_t* tail_flag,
-                                                         const double* block_sum, const uint8_t* block_full) {
+                                                         const double* block_sum, const uint8_t* block_full,
+                                                         int64_t target) {
   constexpr int D = 32 * EPL;
   const int64_t b0 = begin_dev ? *begin_dev : 0;
   keys += b0;
   const int64_t n = *end_dev - b0;
-  const int64_t ntiles = (n + kChunk - 1) / kChunk;
+  const int64_t chunk = tile_entries(n, target);
+  const int64_t ntiles = (n + chunk - 1) / chunk;
   const int64_t nblocks = ntiles / kCarryBlock;
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
   for (int64_t t = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; t < ntiles; t += nwarps) {
     if (!tail_flag[t]) continue;
-    const uint32_t row = keys[(t + 1) * kChunk - 1] & row_mask;
+    const uint32_t row = keys[(t + 1) * chunk - 1] & row_mask;
     double acc64[EPL];
 #pragma unroll
     for (int i = 0; i < EPL; ++i) acc64[i] = double(carry_tail[t * D + lane * EPL + i]);
@@ -623,24 +639,29 @@ void launch_reduce(const uint32_t* k, const uint32_t* v, const int64_t* begin_de
                    uint32_t row_mask, const void* grads, UpdateArgs u, float* ch, float* ct, uint8_t* hc,
                    uint8_t* tf, double* bsum, uint8_t* bfull, int32_t* err, cudaStream_t st) {
   const unsigned sms = unsigned(sm_count());
+  int64_t target = 0;  // tiles the range is cut into: about three per reducing warp
   if (aligned(grads, 16)) {
     // gradient rows by bulk copy (needs 16-byte aligned rows)
     constexpr int RB = 32 * EPL * (BF16 ? 2 : 4);
     using RG = Ring<RB>;
     auto kern = reduce_ring_kernel<BF16, EPL, RG::kMinBlocks>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, RG::kBlockBytes);
-    kern<<<sms * RG::kMinBlocks, kThreads, RG::kBlockBytes, st>>>(k, v, begin_dev, end_dev, row_mask, grads, u, ch,
-                                                                   ct, hc, tf, err, uint64_t(spin_limit()) * 256u, debug_skip_tile());
+    const unsigned grid = sms * RG::kMinBlocks;
+    target = 3 * int64_t(grid) * (kThreads / 32);
+    kern<<<grid, kThreads, RG::kBlockBytes, st>>>(k, v, begin_dev, end_dev, row_mask, grads, u, ch, ct, hc, tf, err,
+                                                  uint64_t(spin_limit()) * 256u, debug_skip_tile(), target);
   } else {
     // 8 gradient rows in flight per warp (fewer for wide rows) and 4 blocks
     // per SM fit the 64-register budget without spills
     constexpr int G = (16 / EPL) > 8 ? 8 : (16 / EPL);
-    reduce_kernel<BF16, EPL, G, 4><<<sms * 4, kThreads, 0, st>>>(k, v, begin_dev, end_dev, row_mask, grads, u, ch,
-                                                                ct, hc, tf);
+    const unsigned grid = sms * 4;
+    target = 3 * int64_t(grid) * (kThreads / 32);
+    reduce_kernel<BF16, EPL, G, 4><<<grid, kThreads, 0, st>>>(k, v, begin_dev, end_dev, row_mask, grads, u, ch, ct,
+                                                             hc, tf, target);
   }
-  block_sum_kernel<EPL><<<sms * (2048 / kThreads), kThreads, 0, st>>>(begin_dev, end_dev, ch, hc, bsum, bfull);
+  block_sum_kernel<EPL><<<sms * (2048 / kThreads), kThreads, 0, st>>>(begin_dev, end_dev, ch, hc, bsum, bfull, target);
   fixup_kernel<BF16, EPL><<<sms * (2048 / kThreads), kThreads, 0, st>>>(k, begin_dev, end_dev, row_mask, u, ch, ct,
-                                                                         hc, tf, bsum, bfull);
+                                                                         hc, tf, bsum, bfull, target);
 }
 
 // Number of sorted keys below `bound` (one thread; keys ascending).
@@ -662,7 +683,7 @@ struct BwdLayout {
 BwdLayout bwd_layout(int64_t T, int64_t R, int32_t dim) {
   BwdLayout L;
   L.plan = radix::SortPlan(T, radix::bits_for(uint64_t(R > 0 ? R - 1 : 0)));
-  L.max_tiles = (T + kChunk - 1) / kChunk;
+  L.max_tiles = (T + kMinChunk - 1) / kMinChunk;
   L.carry_bytes = align_up(size_t(L.max_tiles) * size_t(dim) * sizeof(float));
   L.flag_bytes = align_up(size_t(L.max_tiles));
   L.max_blocks = L.max_tiles / kCarryBlock + 1;
