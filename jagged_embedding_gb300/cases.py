@@ -6,6 +6,7 @@ op is one of
   gather    -- fs_emb_gather, unmasked, f32 rows of 64, T bounded-Zipf(1.0) IDs over R rows
   backward  -- fs_emb_backward_adagrad (sort + reduce + fixup), same IDs, f32, row-wise Adagrad,
                collision rows (half of the rows, by a hash of the row) updated before exclusive rows
+  backward-bf16 -- the same with bf16 rows of 128 (the mid-size full step's table)
   bucketize -- fs_bucketize_rowwise of the same IDs into 256 row-range shards
 Inputs come from jagged_embedding_gb300.synthetic; every call goes through the C ABI.
 Exits non-zero if a call reports an error.
@@ -24,7 +25,7 @@ SHARDS = 256
 
 
 def main(argv) -> int:
-    if len(argv) < 3 or argv[0] not in ("gather", "backward", "bucketize"):
+    if len(argv) < 3 or argv[0] not in ("gather", "backward", "backward-bf16", "bucketize"):
         print(__doc__)
         return 2
     op, T, R = argv[0], int(argv[1]), int(argv[2])
@@ -39,11 +40,12 @@ def main(argv) -> int:
         out = torch.empty(T, DIM, device=dev)
         for _ in range(reps):
             B.fs_emb_gather(table, ids, out=out, err=err)
-    elif op == "backward":
-        table = torch.empty(R, DIM, device=dev).normal_(0, 0.01, generator=g)
+    elif op in ("backward", "backward-bf16"):
+        dim, dt = (DIM, torch.float32) if op == "backward" else (128, torch.bfloat16)
+        table = torch.empty(R, dim, device=dev).normal_(0, 0.01, generator=g).to(dt)
         state = torch.zeros(R, device=dev)
-        grads = torch.empty(T, DIM, device=dev).normal_(generator=g)
-        ws = B.workspace(B.backward_workspace_size(T, R, DIM, B.dtype_code(table)), dev)
+        grads = torch.empty(T, dim, device=dev).normal_(generator=g).to(dt)
+        ws = B.workspace(B.backward_workspace_size(T, R, dim, B.dtype_code(table)), dev)
         is_co = (((ids * 0x9E3779B1) >> 7) & 1).to(torch.uint8)
         for _ in range(reps):
             B.fs_emb_backward_adagrad(table, state, ids, grads, "adagrad", 0.01, 1e-8, is_co=is_co,

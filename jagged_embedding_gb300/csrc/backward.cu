@@ -194,6 +194,64 @@ __device__ __forceinline__ void update_row(const UpdateArgs& u, uint32_t row, co
   apply_update<BF16, EPL>(u, row, w, s_old, g, lane);
 }
 
+// a0 += b0, a1 += b1 in one paired fp32 add (sm_100+ add.f32x2: two
+// independent round-to-nearest adds, the same bits as two scalar adds).
+__device__ __forceinline__ void add2(float& a0, float& a1, float b0, float b1) {
+  asm("{\n .reg .b64 a, b, r;\n mov.b64 a, {%0, %1};\n mov.b64 b, {%2, %3};\n add.rn.f32x2 r, a, b;\n"
+      " mov.b64 {%0, %1}, r;\n}"
+      : "+f"(a0), "+f"(a1)
+      : "f"(b0), "f"(b1));
+}
+
+// acc += row r of a shared-memory stage, lane's slice (elements
+// [lane*EPL, lane*EPL + EPL)); bf16 pairs unpacked with one shift or mask each.
+template <bool BF16, int EPL>
+__device__ __forceinline__ void acc_slice(const unsigned char* stage, int r, int lane, float (&acc)[EPL]) {
+  constexpr int ESZ = BF16 ? 2 : 4;
+  const unsigned char* p = stage + (size_t(r) * 32 * EPL + size_t(lane) * EPL) * ESZ;
+  if constexpr (EPL == 1) {
+    acc[0] += BF16 ? __uint_as_float(uint32_t(*reinterpret_cast<const unsigned short*>(p)) << 16)
+                   : *reinterpret_cast<const float*>(p);
+  } else if constexpr (BF16) {
+    constexpr int NW = EPL / 2;  // 32-bit words of the slice
+    uint32_t w[NW];
+    if constexpr (NW == 1) {
+      w[0] = *reinterpret_cast<const uint32_t*>(p);
+    } else if constexpr (NW == 2) {
+      const uint2 v = *reinterpret_cast<const uint2*>(p);
+      w[0] = v.x;
+      w[1] = v.y;
+    } else {
+      const uint4 v = *reinterpret_cast<const uint4*>(p);
+      w[0] = v.x;
+      w[1] = v.y;
+      w[2] = v.z;
+      w[3] = v.w;
+    }
+#pragma unroll
+    for (int j = 0; j < NW; ++j)
+      add2(acc[2 * j], acc[2 * j + 1], __uint_as_float(w[j] << 16), __uint_as_float(w[j] & 0xFFFF0000u));
+  } else {
+    float x[EPL];
+    if constexpr (EPL == 2) {
+      const float2 v = *reinterpret_cast<const float2*>(p);
+      x[0] = v.x;
+      x[1] = v.y;
+    } else {
+#pragma unroll
+      for (int j = 0; j < EPL; j += 4) {
+        const float4 v = *reinterpret_cast<const float4*>(p + j * 4);
+        x[j] = v.x;
+        x[j + 1] = v.y;
+        x[j + 2] = v.z;
+        x[j + 3] = v.w;
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < EPL; j += 2) add2(acc[j], acc[j + 1], x[j], x[j + 1]);
+  }
+}
+
 __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
@@ -336,14 +394,15 @@ struct Ring {
 // batch ahead, and the table slices and Adagrad states of the rows a stage
 // finishes are loaded before waiting for that stage.  A wait that exceeds
 // wait_ns nanoseconds sets FS_ERR_TIMEOUT, waits (bounded) for the warp's copies
-// still in flight and ends the warp.  skip_tile >= 0 is a test hook: the
+// still in flight and ends the warp.  Warps take tiles from the counter
+// *tile_next (zero at launch).  skip_tile >= 0 is a test hook: the
 // first stage of that tile is never copied, so its wait runs out.
 template <bool BF16, int EPL, int MINB>
 __global__ void __launch_bounds__(kThreads, MINB) reduce_ring_kernel(
     const uint32_t* __restrict__ keys, const uint32_t* __restrict__ vals, const int64_t* begin_dev,
     const int64_t* end_dev, uint32_t row_mask, const void* __restrict__ grads, UpdateArgs u, float* carry_head,
     float* carry_tail, uint8_t* head_cont, uint8_t* tail_flag, int32_t* err, uint64_t wait_ns, int64_t skip_tile,
-    int64_t target) {
+    int64_t target, uint32_t* tile_next) {
   constexpr int ESZ = BF16 ? 2 : 4;
   constexpr int D = 32 * EPL;
   constexpr int RB = D * ESZ;
@@ -370,11 +429,17 @@ __global__ void __launch_bounds__(kThreads, MINB) reduce_ring_kernel(
   const int64_t n = *end_dev - b0;
   const int64_t chunk = tile_entries(n, target);
   const int64_t ntiles = (n + chunk - 1) / chunk;
-  const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
   uint32_t gb = 0;  // stages this warp has consumed (all tiles): stage gb % NS, phase gb / NS
   bool failed = false;
+  // tiles are taken in order from a counter (zero before the launch): a warp
+  // that drew cheap tiles takes more, so the slowest warp does not set the pace
+  auto next_tile = [&]() -> int64_t {
+    uint32_t v = 0;
+    if (lane == 0) v = atomicAdd(tile_next, 1u);
+    return int64_t(__shfl_sync(0xffffffffu, v, 0));
+  };
 
-  for (int64_t t = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; t < ntiles && !failed; t += nwarps) {
+  for (int64_t t = next_tile(); t < ntiles && !failed; t = next_tile()) {
     const int64_t s0 = t * chunk;
     const int m = int((s0 + chunk < n) ? chunk : n - s0);  // entries in this tile
     const uint32_t* tk = keys + s0;
@@ -432,10 +497,7 @@ __global__ void __launch_bounds__(kThreads, MINB) reduce_ring_kernel(
 #pragma unroll
       for (int r = 0; r < BR; ++r) {
         if (full || eb + r < cnt) {
-          float g[EPL];
-          load_slice<BF16, EPL, false>(sp, r, lane, g);
-#pragma unroll
-          for (int q = 0; q < EPL; ++q) acc[q] += g[q];
+          acc_slice<BF16, EPL>(sp, r, lane, acc);
           if ((bm >> r) & 1u) {  // entry eb + r is its row's last
             if (from_prev) {     // the row began in an earlier tile and ends here
 #pragma unroll
@@ -637,9 +699,9 @@ __global__ void __launch_bounds__(kThreads) fixup_kernel(const uint32_t* __restr
 template <bool BF16, int EPL>
 void launch_reduce(const uint32_t* k, const uint32_t* v, const int64_t* begin_dev, const int64_t* end_dev,
                    uint32_t row_mask, const void* grads, UpdateArgs u, float* ch, float* ct, uint8_t* hc,
-                   uint8_t* tf, double* bsum, uint8_t* bfull, int32_t* err, cudaStream_t st) {
+                   uint8_t* tf, double* bsum, uint8_t* bfull, uint32_t* tile_next, int32_t* err, cudaStream_t st) {
   const unsigned sms = unsigned(sm_count());
-  int64_t target = 0;  // tiles the range is cut into: about three per reducing warp
+  int64_t target = 0;  // tiles the range is cut into, per reducing warp: six (dynamic) or three (static)
   if (aligned(grads, 16)) {
     // gradient rows by bulk copy (needs 16-byte aligned rows)
     constexpr int RB = 32 * EPL * (BF16 ? 2 : 4);
@@ -647,9 +709,10 @@ void launch_reduce(const uint32_t* k, const uint32_t* v, const int64_t* begin_de
     auto kern = reduce_ring_kernel<BF16, EPL, RG::kMinBlocks>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, RG::kBlockBytes);
     const unsigned grid = sms * RG::kMinBlocks;
-    target = 3 * int64_t(grid) * (kThreads / 32);
+    target = 6 * int64_t(grid) * (kThreads / 32);
+    cudaMemsetAsync(tile_next, 0, sizeof(uint32_t), st);
     kern<<<grid, kThreads, RG::kBlockBytes, st>>>(k, v, begin_dev, end_dev, row_mask, grads, u, ch, ct, hc, tf, err,
-                                                  uint64_t(spin_limit()) * 256u, debug_skip_tile(), target);
+                                                  uint64_t(spin_limit()) * 256u, debug_skip_tile(), target, tile_next);
   } else {
     // 8 gradient rows in flight per warp (fewer for wide rows) and 4 blocks
     // per SM fit the 64-register budget without spills
@@ -712,7 +775,7 @@ extern "C" size_t fs_emb_backward_adagrad_workspace_size(int64_t T, int64_t num_
   // the single-call two-phase mode sorts one more key bit (the phase)
   const size_t sort_bytes = std::max(L.plan.bytes(), radix::SortPlan(T, L.plan.key_bits + 1).bytes());
   return sort_bytes + 2 * L.carry_bytes + 2 * L.flag_bytes + L.block_bytes + L.block_flag_bytes +
-         align_up(sizeof(int64_t)) + 256;
+         align_up(sizeof(int64_t)) + align_up(sizeof(uint32_t)) + 256;
 }
 
 extern "C" fs_status fs_emb_backward_adagrad(void* table, float* state, int64_t num_rows, int32_t dim, fs_dtype dtype,
@@ -756,6 +819,7 @@ extern "C" fs_status fs_emb_backward_adagrad(void* table, float* state, int64_t 
   double* block_sum = cur.take<double>(size_t(L.max_blocks) * dim);
   uint8_t* block_full = cur.take<uint8_t>(size_t(L.max_blocks));
   int64_t* n_first = cur.take<int64_t>(1);
+  uint32_t* tile_next = cur.take<uint32_t>(1);
   if (!cur.ok) return FS_ERR_WORKSPACE;
 
   int launches = 0;
@@ -770,7 +834,7 @@ extern "C" fs_status fs_emb_backward_adagrad(void* table, float* state, int64_t 
   auto reduce_range = [&](const int64_t* begin_dev, const int64_t* end_dev, uint32_t row_mask) {
 #define FS_REDUCE(BF, E) \
   launch_reduce<BF, E>(sk, sv, begin_dev, end_dev, row_mask, grads, u, carry_head, carry_tail, head_cont, tail_flag, \
-                       block_sum, block_full, err, st)
+                       block_sum, block_full, tile_next, err, st)
     switch (epl) {
       case 1: if (bf) FS_REDUCE(true, 1); else FS_REDUCE(false, 1); break;
       case 2: if (bf) FS_REDUCE(true, 2); else FS_REDUCE(false, 2); break;
