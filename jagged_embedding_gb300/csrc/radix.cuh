@@ -172,7 +172,7 @@ static __global__ void __launch_bounds__(kThreads) digit_base_kernel(const uint3
 
 // ------------------------------------------------------------------ downsweep
 template <class Src, class Dst>
-__global__ void __launch_bounds__(kThreads, 3) downsweep_kernel(Src src, Dst dst, int shift, int bits, int nb,
+__global__ void __launch_bounds__(kThreads, 4) downsweep_kernel(Src src, Dst dst, int shift, int bits, int nb,
                                                                 const uint32_t* digit_base, const uint32_t* counts,
                                                                 const uint32_t* chunk_base, int64_t ntiles,
                                                                 const int64_t* count_dev, int64_t count_host) {
