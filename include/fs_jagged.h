@@ -239,22 +239,30 @@ fs_status fs_emb_gather(const void* table, int64_t num_rows, int32_t dim, fs_dty
  *   FS_SGD:             W_r -= lr * g_r
  *   FS_ROWWISE_ADAGRAD: s_r += mean_d(g_{r,d}^2);  W_r -= lr * g_r / (sqrt(s_r) + eps)
  * bf16 tables read bf16 grads, accumulate in fp32 and store round-to-nearest-
- * even.  phase selects positions: ALL every position, COLLISION those with
- * is_co[p] == 1, EXCLUSIVE those with is_co[p] == 0.  Collision is a property
- * of the row, so COLLISION then EXCLUSIVE updates every row of the batch once,
- * collision rows first.  COLLISION_THEN_EXCLUSIVE does exactly that in one
- * call: one sort of all positions (the phase is the key's top bit), then the
- * collision rows' updates, then the exclusive rows' updates, in stream order.
+ * even.  phase selects positions: ALL every position, COLLISION those of
+ * collision rows, EXCLUSIVE those of the other rows.  The collision flag is
+ * given either per position (is_co[p] in {0, 1}) or per row (co_rows: bit
+ * r & 31 of word r >> 5 set iff row r is a collision row; for Algorithm 2 this
+ * is the presence bitmap of batch t+1's rows, which fs_row_bitmap writes) --
+ * exactly one of the two unless phase is ALL.  The bitmap form reads one
+ * bitmap word per position in each pass of the sort, so when the mask exists
+ * it is the faster input.
+ * Collision is a property of the row, so COLLISION then EXCLUSIVE updates
+ * every row of the batch once, collision rows first.  COLLISION_THEN_EXCLUSIVE
+ * does exactly that in one call: one sort of all positions (the phase is the
+ * key's top bit), then the collision rows' updates, then the exclusive rows'
+ * updates, in stream order.
  *   table [num_rows, dim] in place;  state [num_rows] fp32 in place (NULL for SGD)
- *   ids [T] int64;  grads [T, dim] of dtype (batch-major);  is_co [T] (NULL for ALL)
+ *   ids [T] int64;  grads [T, dim] of dtype (batch-major)
+ *   is_co [T] uint8 or NULL;  co_rows [fs_row_bitmap_words(num_rows)] or NULL
  * Supported: dim in {32, 64, 128} (fp32) or {32, 64, 128, 256} (bf16);
  * num_rows < 2^32.
  * ---------------------------------------------------------------------- */
 size_t fs_emb_backward_adagrad_workspace_size(int64_t T, int64_t num_rows, int32_t dim, fs_dtype dtype);
 fs_status fs_emb_backward_adagrad(void* table, float* state, int64_t num_rows, int32_t dim, fs_dtype dtype,
                                   fs_optim optim, const int64_t* ids, const void* grads, int64_t T,
-                                  const uint8_t* is_co, fs_phase phase, float lr, float eps, int32_t* err,
-                                  void* ws, size_t ws_bytes, fs_stream_t stream);
+                                  const uint8_t* is_co, const uint32_t* co_rows, fs_phase phase, float lr,
+                                  float eps, int32_t* err, void* ws, size_t ws_bytes, fs_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * Utilities.

@@ -77,8 +77,8 @@ def lib():
                                        C.c_int),
         "fs_emb_gather": ([P, i64, i32, C.c_int, P, i64, P, u8, P, P, P], C.c_int),
         "fs_emb_backward_adagrad_workspace_size": ([i64, i64, i32, C.c_int], sz),
-        "fs_emb_backward_adagrad": ([P, P, i64, i32, C.c_int, C.c_int, P, P, i64, P, C.c_int, f32, f32, P, P, sz, P],
-                                    C.c_int),
+        "fs_emb_backward_adagrad": ([P, P, i64, i32, C.c_int, C.c_int, P, P, i64, P, P, C.c_int, f32, f32, P, P, sz,
+                                     P], C.c_int),
         "fs_check": ([P, P], C.c_int),
         "fs_status_string": ([C.c_int], C.c_char_p),
         "fs_set_spin_limit": ([i64], None),
@@ -336,7 +336,9 @@ def backward_workspace_size(T, num_rows, dim, dtype):
 
 
 def fs_emb_backward_adagrad(table, state, ids, grads, optim, lr, eps=0.0, is_co=None, phase=PHASE_ALL, err=None,
-                            ws=None, T=None):
+                            ws=None, T=None, co_rows=None):
+    """is_co: uint8 collision flag per position; co_rows: int32 bitmap of the collision rows (one of the two
+    unless phase is PHASE_ALL)."""
     dev = table.device
     _need(ids, torch.int64, "ids")
     if table.dim() != 2 or not table.is_contiguous():
@@ -350,11 +352,14 @@ def fs_emb_backward_adagrad(table, state, ids, grads, optim, lr, eps=0.0, is_co=
         _need(state, torch.float32, "state", R)
     if is_co is not None:
         _need(is_co, torch.uint8, "is_co")
+    if co_rows is not None:
+        _need(co_rows, torch.int32, "co_rows", (R + 31) // 32)
     err = new_err(dev) if err is None else err
     need = backward_workspace_size(T, R, D, dtype_code(table))
     ws = workspace(need, dev) if ws is None else ws
     _ok(lib().fs_emb_backward_adagrad(_ptr(table), _ptr(state) if oc == ROWWISE_ADAGRAD else None, R, D,
-                                      dtype_code(table), oc, _ptr(ids), _ptr(grads), T, _ptr(is_co), int(phase),
-                                      float(lr), float(eps), _ptr(err), _ptr(ws), ws.numel(), _stream(dev)),
+                                      dtype_code(table), oc, _ptr(ids), _ptr(grads), T, _ptr(is_co), _ptr(co_rows),
+                                      int(phase), float(lr), float(eps), _ptr(err), _ptr(ws), ws.numel(),
+                                      _stream(dev)),
         "fs_emb_backward_adagrad")
     return err

@@ -52,20 +52,29 @@ struct SrcRows {
   using Key = uint32_t;
   static constexpr bool kIndexValue = true;  // value = item index
   const int64_t* ids;
-  const uint8_t* is_co;
+  const uint8_t* is_co;     // collision flag per position, or null
+  const uint32_t* co_rows;  // collision flag per row (bitmap), or null
   int phase;
   int64_t R;
   int kb;  // bits of the largest row index
+  static constexpr bool kFetch2 = true;
   struct Raw {
     int64_t id;
     uint32_t m;
   };
-  // the ID and the mask byte are loaded independently (no load-to-load dependency)
+  // loads only: the ID and the mask byte independently; with a row bitmap,
+  // fetch2 then reads the ID's row bit (L2-resident; an out-of-range ID reads
+  // bit 0 and is rejected by make) after every ID of the tile is in flight
   __device__ __forceinline__ Raw fetch(int64_t i) const {
     Raw r;
     r.id = __ldcs(ids + i);
-    r.m = phase != FS_PHASE_ALL ? uint32_t(__ldcs(is_co + i)) : 0u;
+    r.m = (phase != FS_PHASE_ALL && !co_rows) ? uint32_t(__ldcs(is_co + i)) : 0u;
     return r;
+  }
+  __device__ __forceinline__ void fetch2(Raw& r) const {
+    if (phase == FS_PHASE_ALL || !co_rows) return;
+    const uint64_t x = uint64_t(r.id) < uint64_t(R) ? uint64_t(r.id) : 0u;
+    r.m = (__ldg(co_rows + (x >> 5)) >> (x & 31u)) & 1u;
   }
   __device__ __forceinline__ bool make(const Raw& r, int64_t i, Key& key, uint32_t& val, int32_t* err) const {
     const int64_t id = r.id;
@@ -780,8 +789,9 @@ extern "C" size_t fs_emb_backward_adagrad_workspace_size(int64_t T, int64_t num_
 
 extern "C" fs_status fs_emb_backward_adagrad(void* table, float* state, int64_t num_rows, int32_t dim, fs_dtype dtype,
                                              fs_optim optim, const int64_t* ids, const void* grads, int64_t T,
-                                             const uint8_t* is_co, fs_phase phase, float lr, float eps, int32_t* err,
-                                             void* ws, size_t ws_bytes, fs_stream_t stream) {
+                                             const uint8_t* is_co, const uint32_t* co_rows, fs_phase phase,
+                                             float lr, float eps, int32_t* err, void* ws, size_t ws_bytes,
+                                             fs_stream_t stream) {
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (T < 0 || T > INT32_MAX || num_rows < 1 || num_rows >= (int64_t(1) << 32) || !err) return FS_ERR_INVALID_ARG;
   if ((dtype != FS_F32 && dtype != FS_BF16) || (optim != FS_SGD && optim != FS_ROWWISE_ADAGRAD)) return FS_ERR_INVALID_ARG;
@@ -792,7 +802,9 @@ extern "C" fs_status fs_emb_backward_adagrad(void* table, float* state, int64_t 
   if (epl == 0) return FS_ERR_INVALID_ARG;
   if (optim == FS_ROWWISE_ADAGRAD && !state) return FS_ERR_INVALID_ARG;
   if (T == 0) return FS_OK;
-  if (!table || !ids || !grads || (phase != FS_PHASE_ALL && !is_co)) return FS_ERR_INVALID_ARG;
+  if (!table || !ids || !grads) return FS_ERR_INVALID_ARG;
+  if (phase != FS_PHASE_ALL && (is_co == nullptr) == (co_rows == nullptr)) return FS_ERR_INVALID_ARG;
+  if (co_rows && !aligned(co_rows, 4)) return FS_ERR_ALIGNMENT;
   const size_t vec = size_t(epl) * (dtype == FS_F32 ? 4 : 2);
   if (!aligned(table, vec) || !aligned(grads, vec) || !aligned(ids, 8) || (state && !aligned(state, 4)))
     return FS_ERR_ALIGNMENT;
@@ -801,10 +813,10 @@ extern "C" fs_status fs_emb_backward_adagrad(void* table, float* state, int64_t 
   const int kb = radix::bits_for(uint64_t(num_rows - 1));
   if (phase == FS_PHASE_COLLISION_THEN_EXCLUSIVE && kb > 30) {
     // the phase bit does not fit beside the row bits: two calls, same result
-    fs_status s = fs_emb_backward_adagrad(table, state, num_rows, dim, dtype, optim, ids, grads, T, is_co,
+    fs_status s = fs_emb_backward_adagrad(table, state, num_rows, dim, dtype, optim, ids, grads, T, is_co, co_rows,
                                           FS_PHASE_COLLISION, lr, eps, err, ws, ws_bytes, stream);
     if (s != FS_OK) return s;
-    return fs_emb_backward_adagrad(table, state, num_rows, dim, dtype, optim, ids, grads, T, is_co,
+    return fs_emb_backward_adagrad(table, state, num_rows, dim, dtype, optim, ids, grads, T, is_co, co_rows,
                                    FS_PHASE_EXCLUSIVE, lr, eps, err, ws, ws_bytes, stream);
   }
   BwdLayout L = bwd_layout(T, num_rows, dim);
@@ -824,7 +836,7 @@ extern "C" fs_status fs_emb_backward_adagrad(void* table, float* state, int64_t 
 
   int launches = 0;
   uint32_t *sk = nullptr, *sv = nullptr;
-  SrcRows src{ids, is_co, int(phase), num_rows, kb};
+  SrcRows src{ids, is_co, co_rows, int(phase), num_rows, kb};
   fs_status s = radix::run_sort(src, L.plan, W, err, st, &sk, &sv, &launches);
   if (s != FS_OK) return s;
   UpdateArgs u{table, optim == FS_ROWWISE_ADAGRAD ? state : nullptr, int(optim), lr, eps};

@@ -21,6 +21,7 @@ struct SrcLen {
   using Key = uint32_t;
   static constexpr bool kIndexValue = true;  // value = item index
   const int32_t* L;
+  static constexpr bool kFetch2 = false;
   using Raw = int32_t;
   __device__ __forceinline__ Raw fetch(int64_t i) const { return L[i]; }
   __device__ __forceinline__ bool make(Raw l, int64_t i, Key& key, uint32_t& val, int32_t* err) const {

@@ -22,6 +22,7 @@ using radix::kThreads;
 struct SrcShard {
   using Key = int64_t;
   static constexpr bool kIndexValue = true;  // value = item index
+  static constexpr bool kFetch2 = false;
   const int64_t* ids;
   int64_t R;
   int64_t block;

@@ -22,7 +22,8 @@
 // Sources (`Src`) decide where keys and values come from (a plain array, a
 // length array with the index as value, an ID array filtered by a mask ...)
 // and the digit function: fetch(i) only loads (so that a tile's loads are all
-// in flight together), make(raw, i, key, val, err) checks and converts.
+// in flight together), fetch2(raw) (kFetch2) the loads that depend on the
+// first ones, make(raw, i, key, val, err) checks and converts.
 // Sinks (`Dst`) decide what is written.
 #pragma once
 
@@ -85,6 +86,11 @@ __global__ void __launch_bounds__(kThreads) upsweep_kernel(Src src, int shift, i
         const int64_t idx = item_index(tile, warp, i, lane);
         if (idx < count) raw[i] = src.fetch(idx);
       }
+      if constexpr (Src::kFetch2) {  // loads that depend on the first ones, all issued together
+#pragma unroll
+        for (int i = 0; i < kItems; ++i)
+          if (item_index(tile, warp, i, lane) < count) src.fetch2(raw[i]);
+      }
 #pragma unroll
       for (int i = 0; i < kItems; ++i) {
         const int64_t idx = item_index(tile, warp, i, lane);
@@ -92,6 +98,7 @@ __global__ void __launch_bounds__(kThreads) upsweep_kernel(Src src, int shift, i
         uint32_t v;
         if (idx < count && src.make(raw[i], idx, k, v, err)) atomicAdd(hist + src.digit(k, shift, bits), 1u);
       }
+
     }
     __syncthreads();
 #pragma unroll
@@ -219,6 +226,11 @@ __global__ void __launch_bounds__(kThreads, 4) downsweep_kernel(Src src, Dst dst
       const int64_t idx = item_index(tile, warp, i, lane);
       if (idx < count) raw[i] = src.fetch(idx);
     }
+    if constexpr (Src::kFetch2) {
+#pragma unroll
+      for (int i = 0; i < kItems; ++i)
+        if (item_index(tile, warp, i, lane) < count) src.fetch2(raw[i]);
+    }
 #pragma unroll
     for (int i = 0; i < kItems; ++i) {
       const int64_t idx = item_index(tile, warp, i, lane);
@@ -316,6 +328,7 @@ struct SrcU32 {
   static constexpr bool kIndexValue = false;
   const uint32_t* k;
   const uint32_t* v;
+  static constexpr bool kFetch2 = false;
   using Raw = uint2;
   __device__ __forceinline__ Raw fetch(int64_t i) const { return make_uint2(__ldcs(k + i), __ldcs(v + i)); }
   __device__ __forceinline__ bool make(const Raw& r, int64_t, Key& key, uint32_t& val, int32_t*) const {

@@ -83,7 +83,8 @@ class Pipeline:
 
     # -------------------------------------------------------------- stages
     def prepare(self, batch, slot):
-        """Balance + permute + bucketize one batch into slot (Algorithm 1; Algorithm 2 line 8)."""
+        """Balance + permute + bucketize one batch into slot, and its rows' presence bitmap
+        (Algorithm 1; Algorithm 2 line 8)."""
         w, s = self.w, self.slots[slot]
         if w.balance == "fbs":
             B.fs_balance_fbs(batch["uih_len"], w.n, perm=s.perm, rank_offsets=s.rank_offsets, err=self.err, ws=self.ws)
@@ -99,39 +100,46 @@ class Pipeline:
         B.fs_row_bitmap(s.ids, w.R, bitmap=s.bitmap, err=self.err, T=T)
         s.T = T
 
-    def collision(self, slot_t, slot_next, want_next_mask=True):
+    def collision(self, slot_t, slot_next, want_t_mask=True, want_next_mask=True):
         """Collision / exclusive split of (t, t+1) (Algorithm 2 line 10); masks are batch-major.
 
-        The mask of t+1 only serves the prioritized order's masked gathers of t+1;
-        the synchronous order skips it.
+        The mask of t gives the update its phases; the mask of t+1 only serves
+        the prioritized order's masked gathers of t+1.
         """
         a, b = self.slots[slot_t], self.slots[slot_next]
         out = dict(self.coll)
         out["is_co_t"] = self.masks[slot_t]
         out["is_co_next"] = self.masks[slot_next]
         B.fs_collision_split_bitmaps(a.ids, a.bitmap, b.ids, b.bitmap, self.w.R, self.w.n, out, self.cap_rows,
-                                     err=self.err, ws=self.ws, T_t=a.T, T_next=b.T, want_next_mask=want_next_mask)
+                                     err=self.err, ws=self.ws, T_t=a.T, T_next=b.T, want_t_mask=want_t_mask,
+                                     want_next_mask=want_next_mask)
 
     def gather(self, slot, out_idx=0, mask=None, sel=1):
         s = self.slots[slot]
         B.fs_emb_gather(self.table, s.ids, out=self.out[out_idx], mask=mask, sel=sel, err=self.err, T=s.T)
 
-    def backward(self, slot, grads, phase=B.PHASE_ALL):
+    def backward(self, slot, grads, phase=B.PHASE_ALL, co_rows=None):
+        """Update of the batch in `slot`; the phase's collision flags come from the batch's mask, or
+        from co_rows (the row bitmap of the next batch) when given."""
         w, s = self.w, self.slots[slot]
+        use_mask = phase != B.PHASE_ALL and co_rows is None
         B.fs_emb_backward_adagrad(self.table, self.state, s.ids, grads, w.optim, w.lr, w.eps,
-                                  is_co=self.masks[slot] if phase != B.PHASE_ALL else None, phase=phase,
-                                  err=self.err, ws=self.ws, T=s.T)
+                                  is_co=self.masks[slot] if use_mask else None, phase=phase,
+                                  err=self.err, ws=self.ws, T=s.T, co_rows=co_rows)
 
     # -------------------------------------------------------------- orders
-    def step_sync(self, cur, nxt_batch, grads, has_next=True):
+    def step_sync(self, cur, nxt_batch, grads, has_next=True, want_masks=False):
         """One iteration in the synchronous order; slot `cur` holds iteration t already prepared.
 
+        The update takes its collision flags from the mask of t (one pass over the
+        IDs; reading t+1's row bitmap inside the sort passes instead was measured
+        slower).  want_masks also writes the mask of t+1.
         Returns the slot that now holds t+1.
         """
         nxt = 1 - cur
         if has_next:
             self.prepare(nxt_batch, nxt)
-            self.collision(cur, nxt, want_next_mask=False)
+            self.collision(cur, nxt, want_t_mask=True, want_next_mask=want_masks)
         self.gather(cur)
         if self.w.has_update:
             if has_next:

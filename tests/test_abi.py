@@ -75,11 +75,18 @@ def test_host_argument_errors_return_without_launching():
     # backward: dim 48 unsupported, Adagrad without state, phase without mask
     args = dict(table=C.c_void_p(0x100), R=10, ids=C.c_void_p(0x200), grads=C.c_void_p(0x300), T=4)
     assert L.fs_emb_backward_adagrad(args["table"], C.c_void_p(0x400), 10, 48, 0, 1, args["ids"], args["grads"], 4,
-                                     NULL, 0, C.c_float(0.01), C.c_float(1e-8), err, ws, 1 << 30, NULL) == 1
+                                     NULL, NULL, 0, C.c_float(0.01), C.c_float(1e-8), err, ws, 1 << 30, NULL) == 1
     assert L.fs_emb_backward_adagrad(args["table"], NULL, 10, 64, 0, 1, args["ids"], args["grads"], 4,
-                                     NULL, 0, C.c_float(0.01), C.c_float(1e-8), err, ws, 1 << 30, NULL) == 1
+                                     NULL, NULL, 0, C.c_float(0.01), C.c_float(1e-8), err, ws, 1 << 30, NULL) == 1
     assert L.fs_emb_backward_adagrad(args["table"], C.c_void_p(0x400), 10, 64, 0, 1, args["ids"], args["grads"], 4,
-                                     NULL, 1, C.c_float(0.01), C.c_float(1e-8), err, ws, 1 << 30, NULL) == 1
+                                     NULL, NULL, 1, C.c_float(0.01), C.c_float(1e-8), err, ws, 1 << 30, NULL) == 1
+    # a phase needs exactly one of is_co / co_rows; co_rows 4-byte aligned
+    assert L.fs_emb_backward_adagrad(args["table"], C.c_void_p(0x400), 10, 64, 0, 1, args["ids"], args["grads"], 4,
+                                     C.c_void_p(0x500), C.c_void_p(0x600), 1, C.c_float(0.01), C.c_float(1e-8), err,
+                                     ws, 1 << 30, NULL) == 1
+    assert L.fs_emb_backward_adagrad(args["table"], C.c_void_p(0x400), 10, 64, 0, 1, args["ids"], args["grads"], 4,
+                                     NULL, C.c_void_p(0x602), 3, C.c_float(0.01), C.c_float(1e-8), err, ws, 1 << 30,
+                                     NULL) == 8
     assert L.fs_collision_split(C.c_void_p(0x10), 5, C.c_void_p(0x20), 5, (1 << 32) + 1, 4, NULL, NULL, NULL, 0,
                                 C.c_void_p(0x30), C.c_void_p(0x40), C.c_void_p(0x50), C.c_void_p(0x60),
                                 C.c_void_p(0x70), C.c_void_p(0x80), err, ws, 1 << 30, NULL) == 1

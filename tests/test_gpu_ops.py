@@ -431,6 +431,30 @@ def test_backward_rows_not_16_byte_aligned(dtype, D):
     assert_state_close(to_np(sd), s_ref)
 
 
+@pytest.mark.parametrize("dtype,phase", [("f32", 3), ("bf16", 3), ("f32", 1), ("f32", 2)])
+def test_backward_phase_from_row_bitmap_equals_mask(dtype, phase):
+    """Collision flags read per row from a bitmap give the same bits as the per-position mask."""
+    R, D, T = 500_000, (64 if dtype == "f32" else 128), 400_000
+    g = torch.Generator().manual_seed(41)
+    ids = synthetic.zipf_rows(R, 1.05, T, g, "cpu")
+    nxt = synthetic.zipf_rows(R, 1.05, 300_000, g, "cpu")
+    tt = torch.float32 if dtype == "f32" else torch.bfloat16
+    W0 = (torch.randn(R, D, generator=g) * 0.01).to(tt)
+    G = torch.randn(T, D, generator=g).to(tt)
+    bm, err = B.fs_row_bitmap(nxt.to(DEV), R)                      # rows of the next batch
+    _check(err)
+    mask = torch.from_numpy(np.isin(ids.numpy(), nxt.numpy()).astype(np.uint8))
+    outs = []
+    for kw in ({"is_co": mask.to(DEV)}, {"co_rows": bm}):
+        Wd, sd = W0.to(DEV), torch.zeros(R, device=DEV)
+        err = B.fs_emb_backward_adagrad(Wd, sd, ids.to(DEV), G.to(DEV), "adagrad", 0.01, 1e-8, phase=phase, **kw)
+        _check(err)
+        outs.append((Wd.cpu(), sd.cpu()))
+    view = (lambda x: x.view(torch.int16)) if dtype == "bf16" else (lambda x: x)
+    assert torch.equal(view(outs[0][0]), view(outs[1][0]))
+    assert torch.equal(outs[0][1], outs[1][1])
+
+
 def test_backward_single_hot_row_spans_many_tiles():
     """One row owns most positions: its sum crosses hundreds of reduce tiles (carry chain)."""
     R, D, T = 1000, 64, 1_000_000

@@ -49,7 +49,8 @@ def _gpu_sync(w, batches_cpu, table0, grads_cpu):
                 "sm_ids": to_np(s.sm_ids[:T]), "pos": to_np(s.pos[:T]), "splits": to_np(s.splits),
                 "shard_offsets": to_np(s.shard_offsets), "seg_weight": to_np(s.seg_weight)}
         has_next = t + 1 < K
-        nxt = pipe.step_sync(cur, bd[t + 1] if has_next else None, gd[t] if gd else None, has_next=has_next)
+        nxt = pipe.step_sync(cur, bd[t + 1] if has_next else None, gd[t] if gd else None, has_next=has_next,
+                             want_masks=True)
         B.check(pipe.err, f"iteration {t}")
         snap["out"] = to_np(pipe.out[0][:T])
         if has_next:
