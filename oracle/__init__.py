@@ -37,6 +37,7 @@ def lib():
             "oracle_balance_fbs": [P, i64, i32, P, P],
             "oracle_balance_vbs": [P, i64, i32, f64, i32, P, P, P],
             "oracle_permute_jagged": [P, P, i64, P, P, P],
+            "oracle_keyed_transpose": [P, P, i64, i64, P, P, P],
             "oracle_bucketize_rowwise": [P, i64, P, i32, i64, P, P, P, P],
             "oracle_collision_split": [P, i64, P, i64, i64, i32, P, P, P, i64, P, P, P, P, P, P],
             "oracle_emb_gather": [P, i64, i64, P, i64, P, u8, P],
@@ -104,6 +105,17 @@ def permute_jagged(offsets, values, perm):
     out_off = np.empty(S + 1, np.int64)
     out_val = np.empty(val.shape[0], np.int64)
     _check(lib().oracle_permute_jagged(_p(off), _p(val), S, _p(pm), _p(out_off), _p(out_val)))
+    return out_off, out_val
+
+
+def keyed_transpose(offsets, values, F, B, row_base=None):
+    off = _c(offsets, np.int64)
+    val = _c(values, np.int64)
+    rb = None if row_base is None else _c(row_base, np.int64)
+    out_off = np.empty(F * B + 1, np.int64)
+    out_val = np.empty(val.shape[0], np.int64)
+    _check(lib().oracle_keyed_transpose(_p(off), _p(val), int(F), int(B), None if rb is None else _p(rb),
+                                        _p(out_off), _p(out_val)))
     return out_off, out_val
 
 

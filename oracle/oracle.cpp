@@ -216,6 +216,31 @@ int oracle_permute_jagged(const int64_t* offsets, const int64_t* values, int64_t
 }
 
 // ---------------------------------------------------------------------------
+// Keyed transpose.  FreeScale §4.2: jagged tensors go from the feature-major
+// form (all samples of feature 0, then all samples of feature 1, ...) to the
+// batch-major form (all features of sample 0, then of sample 1, ...).  Walk
+// the samples b, and for each the features f, appending feature f's IDs of
+// sample b (input segment f*B + b); with row_base, feature f's IDs are shifted
+// by row_base[f] (rows of feature f's own table inside a stacked table).
+int oracle_keyed_transpose(const int64_t* offsets, const int64_t* values, int64_t F, int64_t B,
+                           const int64_t* row_base, int64_t* out_offsets, int64_t* out_values) {
+  if (F < 1 || B < 0) return 1;
+  for (int64_t s = 0; s < F * B; ++s)
+    if (offsets[s + 1] < offsets[s]) return 3;
+  int64_t at = 0;
+  out_offsets[0] = 0;
+  for (int64_t b = 0; b < B; ++b) {
+    for (int64_t f = 0; f < F; ++f) {
+      const int64_t seg = f * B + b;
+      const int64_t shift = row_base ? row_base[f] : 0;
+      for (int64_t i = offsets[seg]; i < offsets[seg + 1]; ++i) out_values[at++] = values[i] + shift;
+      out_offsets[b * F + f + 1] = at;
+    }
+  }
+  return 0;
+}
+
+// ---------------------------------------------------------------------------
 // Row-wise bucketize ("ranged dispatch").  FreeScale §3.2 (batch-major vs
 // shard-major forms), Algorithm 2 line 8 (IDs AllToAll to shard-major), §4.2.
 // The table is row-wise sharded into n contiguous ranges of block = ceil(R/n)

@@ -160,3 +160,55 @@ def test_collision_on_synthetic_batches_is_order_free():
     m = np.empty_like(c_sm["is_co_t"])
     m[p0["pos"]] = c_sm["is_co_t"]
     assert np.array_equal(m, c_bm["is_co_t"])
+
+
+# ------------------------------------------------------------------ keyed transpose
+
+with open(os.path.join(GOLD, "keyed_transpose_hand_examples.json")) as f:
+    KT = json.load(f)
+
+
+@pytest.mark.parametrize("case", KT["cases"], ids=lambda c: f"F{c['F']}B{c['B']}{'_base' if c['row_base'] else ''}")
+def test_keyed_transpose_hand_examples(case):
+    off, val = oracle.keyed_transpose(np.array(case["offsets"]), np.array(case["values"]), case["F"], case["B"],
+                                      None if case["row_base"] is None else np.array(case["row_base"]))
+    assert off.tolist() == case["out_offsets"] and val.tolist() == case["out_values"]
+
+
+def _nested(off, val, F, B):
+    """Feature-major arrays as nested lists: seg[f][b] = list of IDs."""
+    return [[val[off[f * B + b]:off[f * B + b + 1]].tolist() for b in range(B)] for f in range(F)]
+
+
+@pytest.mark.parametrize("F,B,seed", [(1, 7, 0), (5, 1, 1), (4, 9, 2), (13, 6, 3), (3, 0, 4)])
+def test_keyed_transpose_against_nested_lists(F, B, seed):
+    rng = np.random.default_rng(seed)
+    off, val = _rand_jagged(rng, F * B, 10 ** 6, maxlen=12)
+    base = rng.integers(0, 10 ** 9, F).astype(np.int64)
+    o2, v2 = oracle.keyed_transpose(off, val, F, B, base)
+    seg = _nested(off, val, F, B)
+    flat, lens = [], []
+    for b in range(B):                       # batch-major: sample, then feature
+        for f in range(F):
+            flat += [x + int(base[f]) for x in seg[f][b]]
+            lens.append(len(seg[f][b]))
+    assert v2.tolist() == flat
+    expected = [0] + np.cumsum(lens).tolist() if lens else [0]
+    assert o2.tolist() == expected
+
+
+@pytest.mark.parametrize("F,B", [(4, 9), (1, 5), (6, 1), (7, 3)])
+def test_keyed_transpose_twice_with_roles_swapped_is_identity(F, B):
+    """Batch-major output read as feature-major with B features of F samples transposes back."""
+    rng = np.random.default_rng(F * 10 + B)
+    off, val = _rand_jagged(rng, F * B, 1000)
+    o2, v2 = oracle.keyed_transpose(off, val, F, B)
+    o3, v3 = oracle.keyed_transpose(o2, v2, B, F)
+    assert np.array_equal(o3, off) and np.array_equal(v3, val)
+    if F == 1 or B == 1:                     # one feature or one sample: nothing moves
+        assert np.array_equal(o2, off) and np.array_equal(v2, val)
+
+
+def test_keyed_transpose_rejects_bad_offsets():
+    with pytest.raises(oracle.OracleError):
+        oracle.keyed_transpose(np.array([0, 3, 2]), np.array([1, 2, 3]), 1, 2)
