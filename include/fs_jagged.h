@@ -145,6 +145,26 @@ fs_status fs_permute_jagged(const int64_t* offsets, const int64_t* values, int64
                             void* ws, size_t ws_bytes, fs_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Keyed transpose -- FreeScale §4.2 (the jagged kernels convert jagged tensors
+ * from the feature-major form to the batch-major form).  F features, B
+ * samples; the input is feature-major (segment f*B + b holds feature f's IDs
+ * of sample b), the output batch-major (segment b*F + f):
+ *   out segment b*F + f = in segment f*B + b, element by element,
+ *   plus row_base[f] on every ID when row_base != NULL (features with their
+ *   own tables stacked in one: the IDs become rows of the stacked table).
+ *   offsets     [F*B+1] int64, offsets[0] = 0, non-decreasing
+ *   values      [offsets[F*B]] int64
+ *   row_base    [F] int64 or NULL
+ *   out_offsets [F*B+1] int64 out
+ *   out_values  [capacity] int64 out; offsets[F*B] > capacity -> FS_ERR_CAPACITY
+ * Bad offsets -> FS_ERR_BAD_OFFSETS (error word).  F >= 1, F*B < 2^31.
+ * ---------------------------------------------------------------------- */
+size_t fs_keyed_transpose_workspace_size(int64_t F, int64_t B);
+fs_status fs_keyed_transpose(const int64_t* offsets, const int64_t* values, int64_t F, int64_t B,
+                             const int64_t* row_base, int64_t* out_offsets, int64_t* out_values, int64_t capacity,
+                             int32_t* err, void* ws, size_t ws_bytes, fs_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Row-wise bucketize ("ranged dispatch") -- FreeScale §3.2 (batch-major and
  * shard-major forms), Algorithm 2 line 8, §4.2.  The table of num_rows rows is
  * row-wise sharded into n ranges of block = ceil(num_rows / n) rows; ID x

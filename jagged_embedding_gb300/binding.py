@@ -32,7 +32,8 @@ STATUS = {0: "ok", 1: "invalid argument", 2: "ID outside [0, num_rows)", 3: "mal
 EXPORTS = [
     "fs_balance_fbs_workspace_size", "fs_balance_fbs", "fs_balance_fbs_noalloc", "fs_balance_vbs_workspace_size",
     "fs_balance_vbs",
-    "fs_permute_jagged_workspace_size", "fs_permute_jagged", "fs_bucketize_rowwise_workspace_size",
+    "fs_permute_jagged_workspace_size", "fs_permute_jagged", "fs_keyed_transpose_workspace_size",
+    "fs_keyed_transpose", "fs_bucketize_rowwise_workspace_size",
     "fs_bucketize_rowwise", "fs_collision_split_workspace_size", "fs_collision_split", "fs_row_bitmap_words",
     "fs_row_bitmap", "fs_collision_split_bitmaps_workspace_size", "fs_collision_split_bitmaps", "fs_emb_gather",
     "fs_emb_backward_adagrad_workspace_size", "fs_emb_backward_adagrad", "fs_check", "fs_status_string",
@@ -66,6 +67,8 @@ def lib():
         "fs_balance_vbs": ([P, i64, i32, f64, i32, P, P, P, P, P, sz, P], C.c_int),
         "fs_permute_jagged_workspace_size": ([i64], sz),
         "fs_permute_jagged": ([P, P, i64, P, P, P, i64, P, i32, P, P, P, sz, P], C.c_int),
+        "fs_keyed_transpose_workspace_size": ([i64, i64], sz),
+        "fs_keyed_transpose": ([P, P, i64, i64, P, P, P, i64, P, P, sz, P], C.c_int),
         "fs_bucketize_rowwise_workspace_size": ([i64, i32], sz),
         "fs_bucketize_rowwise": ([P, i64, P, i32, i64, P, P, P, P, P, P, sz, P], C.c_int),
         "fs_collision_split_workspace_size": ([i64, i64, i64, i32], sz),
@@ -227,6 +230,26 @@ def fs_permute_jagged(offsets, values, perm, capacity=None, rank_offsets=None, o
                                 _ptr(rank_offsets), n, _ptr(rank_id_offsets), _ptr(err), _ptr(ws), ws.numel(),
                                 _stream(dev)), "fs_permute_jagged")
     return out_offsets, out_values, rank_id_offsets, err
+
+
+def fs_keyed_transpose(offsets, values, F, B, row_base=None, capacity=None, out_offsets=None, out_values=None,
+                       err=None, ws=None):
+    """Feature-major [F x B] jagged IDs to batch-major [B x F]; row_base (int64 [F]) shifts feature f's IDs."""
+    dev = offsets.device
+    _need(offsets, torch.int64, "offsets", F * B + 1)
+    _need(values, torch.int64, "values")
+    if row_base is not None:
+        _need(row_base, torch.int64, "row_base", F)
+    cap = values.numel() if capacity is None else int(capacity)
+    out_offsets = torch.empty(F * B + 1, dtype=torch.int64, device=dev) if out_offsets is None else out_offsets
+    out_values = torch.empty(cap, dtype=torch.int64, device=dev) if out_values is None else out_values
+    err = new_err(dev) if err is None else err
+    need = lib().fs_keyed_transpose_workspace_size(int(F), int(B))
+    ws = workspace(need, dev) if ws is None else ws
+    _ok(lib().fs_keyed_transpose(_ptr(offsets), _ptr(values), int(F), int(B), _ptr(row_base), _ptr(out_offsets),
+                                 _ptr(out_values), cap, _ptr(err), _ptr(ws), ws.numel(), _stream(dev)),
+        "fs_keyed_transpose")
+    return out_offsets, out_values, err
 
 
 def fs_bucketize_rowwise(ids, rank_id_offsets, num_rows, sm_ids=None, pos=None, splits=None, shard_offsets=None,

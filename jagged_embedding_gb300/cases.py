@@ -8,6 +8,8 @@ op is one of
                collision rows (half of the rows, by a hash of the row) updated before exclusive rows
   backward-bf16 -- the same with bf16 rows of 128 (the mid-size full step's table)
   bucketize -- fs_bucketize_rowwise of the same IDs into 256 row-range shards
+  transpose -- fs_keyed_transpose of about T IDs in R features x 65536 samples (lengths uniform, per-feature
+               row bases); prints the time per call and the bandwidth of its algorithmic bytes
 Inputs come from jagged_embedding_gb300.synthetic; every call goes through the C ABI.
 Exits non-zero if a call reports an error.
 """
@@ -25,7 +27,7 @@ SHARDS = 256
 
 
 def main(argv) -> int:
-    if len(argv) < 3 or argv[0] not in ("gather", "backward", "backward-bf16", "bucketize"):
+    if len(argv) < 3 or argv[0] not in ("gather", "backward", "backward-bf16", "bucketize", "transpose"):
         print(__doc__)
         return 2
     op, T, R = argv[0], int(argv[1]), int(argv[2])
@@ -33,8 +35,10 @@ def main(argv) -> int:
     dev = torch.device("cuda")
     g = torch.Generator(device=dev)
     g.manual_seed(1)
-    ids = synthetic.zipf_rows(R, 1.0, T, g, dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
+    if op == "transpose":
+        return _transpose(T, R, reps, dev, g, err)
+    ids = synthetic.zipf_rows(R, 1.0, T, g, dev)
     if op == "gather":
         table = torch.empty(R, DIM, device=dev).normal_(0, 0.01, generator=g)
         out = torch.empty(T, DIM, device=dev)
@@ -57,6 +61,33 @@ def main(argv) -> int:
     torch.cuda.synchronize()
     B.check(err, op)
     print(f"{op} T={T} R={R} reps={reps}: ok")
+    return 0
+
+
+def _transpose(T, F, reps, dev, g, err):
+    Bs = 65536
+    mean = max(1, T // (F * Bs))
+    lens = torch.randint(0, 2 * mean + 1, (F * Bs,), device=dev, generator=g)
+    off = torch.zeros(F * Bs + 1, dtype=torch.int64, device=dev)
+    off[1:] = torch.cumsum(lens, 0)
+    n = int(off[-1])
+    val = torch.randint(0, 1 << 30, (n,), dtype=torch.int64, device=dev, generator=g)
+    base = torch.arange(F, dtype=torch.int64, device=dev) * (1 << 30)
+    out_off = torch.empty_like(off)
+    out_val = torch.empty_like(val)
+    ws = B.workspace(B.lib().fs_keyed_transpose_workspace_size(F, Bs), dev)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    best = None
+    for _ in range(max(reps, 2)):
+        ev[0].record()
+        B.fs_keyed_transpose(off, val, F, Bs, row_base=base, out_offsets=out_off, out_values=out_val, err=err, ws=ws)
+        ev[1].record()
+        torch.cuda.synchronize()
+        ms = ev[0].elapsed_time(ev[1])
+        best = ms if best is None else min(best, ms)
+    B.check(err, "transpose")
+    byts = 16 * n + 16 * (F * Bs + 1) + 8 * F
+    print(f"transpose F={F} B={Bs} IDs={n}: {best:.3f} ms, {byts / best / 1e6:.0f} GB/s of algorithmic bytes")
     return 0
 
 

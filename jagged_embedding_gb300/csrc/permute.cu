@@ -9,6 +9,12 @@
 // Kernel 2 (one pass over the T IDs, ID-balanced): each block copies a fixed
 // 4096-ID window of the output, whatever the sample lengths (a 16K-ID sample
 // is spread over several blocks, so long samples do not straggle).
+//
+// The keyed transpose (FreeScale §4.2: feature-major jagged tensors to
+// batch-major) is the same permutation with the source segment computed
+// instead of read: output segment b*F + f is input segment f*B + b; the copy
+// may add a per-feature row base to every ID (features with their own tables
+// stacked in one).
 #include "fs_common.cuh"
 
 namespace fs {
@@ -20,7 +26,19 @@ constexpr int kScanTile = kThreads * kScanItems;
 constexpr int kCopyItems = 16;
 constexpr int kCopyTile = kThreads * kCopyItems;  // output IDs per copy tile
 
-__global__ void __launch_bounds__(kThreads) permute_scan_kernel(const int64_t* offsets, int64_t S, const int32_t* perm,
+// Source segment of output segment k: read from an array ...
+struct PermArray {
+  const int32_t* perm;
+  __device__ __forceinline__ int64_t operator()(int64_t k) const { return perm[k]; }
+};
+// ... or the keyed transpose's: k = b*F + f comes from f*B + b.
+struct PermTranspose {
+  int64_t F, B;
+  __device__ __forceinline__ int64_t operator()(int64_t k) const { return (k % F) * B + k / F; }
+};
+
+template <class Perm>
+__global__ void __launch_bounds__(kThreads) permute_scan_kernel(const int64_t* offsets, int64_t S, Perm perm,
                                                                 int64_t* out_offsets, int64_t* src_start,
                                                                 int32_t* first_sample, int64_t n_copy_tiles,
                                                                 int64_t capacity, uint64_t* status, int* tile_counter,
@@ -41,7 +59,7 @@ __global__ void __launch_bounds__(kThreads) permute_scan_kernel(const int64_t* o
     len[i] = 0;
     src[i] = 0;
     if (k < S) {
-      int64_t g = perm[k];
+      int64_t g = perm(k);
       if (g < 0 || g >= S) {
         set_err(err, FS_ERR_BAD_OFFSETS);
       } else {
@@ -87,11 +105,14 @@ __global__ void __launch_bounds__(kThreads) permute_scan_kernel(const int64_t* o
   }
 }
 
+// row_base (nullable, [F]): added to every ID of an output segment k, by its
+// feature k % F.
 __global__ void __launch_bounds__(kThreads) permute_copy_kernel(const int64_t* values, const int64_t* out_offsets,
                                                                 const int64_t* src_start, const int32_t* first_sample,
                                                                 int64_t S, int64_t capacity, int64_t* out_values,
                                                                 const int64_t* rank_offsets, int32_t n,
-                                                                int64_t* rank_id_offsets, int32_t* err) {
+                                                                int64_t* rank_id_offsets, int32_t* err,
+                                                                const int64_t* row_base, int64_t F) {
   if (rank_offsets && blockIdx.x == 0) {
     for (int r = threadIdx.x; r <= n; r += blockDim.x) {
       int64_t q = rank_offsets[r];
@@ -108,10 +129,12 @@ __global__ void __launch_bounds__(kThreads) permute_copy_kernel(const int64_t* v
     int64_t k = first_sample[t];
     int64_t k_hi = (t + 1 < ntiles) ? int64_t(first_sample[t + 1]) : S - 1;  // last sample touching this tile
     int64_t srcidx[kCopyItems];
+    int64_t base[kCopyItems];
 #pragma unroll
     for (int i = 0; i < kCopyItems; ++i) {
       const int64_t j = j0 + int64_t(i) * kThreads + threadIdx.x;
       srcidx[i] = -1;
+      base[i] = 0;
       if (j < total) {
         // largest k' in [k, k_hi] with out_offsets[k'] <= j
         int64_t lo = k, hi = k_hi;
@@ -121,11 +144,12 @@ __global__ void __launch_bounds__(kThreads) permute_copy_kernel(const int64_t* v
         }
         k = lo;
         srcidx[i] = __ldg(src_start + k) + (j - __ldg(out_offsets + k));
+        if (row_base) base[i] = __ldg(row_base + k % F);
       }
     }
     int64_t v[kCopyItems];
 #pragma unroll
-    for (int i = 0; i < kCopyItems; ++i) v[i] = srcidx[i] >= 0 ? __ldcs(values + srcidx[i]) : 0;
+    for (int i = 0; i < kCopyItems; ++i) v[i] = srcidx[i] >= 0 ? __ldcs(values + srcidx[i]) + base[i] : 0;
 #pragma unroll
     for (int i = 0; i < kCopyItems; ++i) {
       const int64_t j = j0 + int64_t(i) * kThreads + threadIdx.x;
@@ -170,20 +194,15 @@ extern "C" size_t fs_permute_jagged_workspace_size(int64_t S) {
          256;
 }
 
-extern "C" fs_status fs_permute_jagged(const int64_t* offsets, const int64_t* values, int64_t S, const int32_t* perm,
-                                       int64_t* out_offsets, int64_t* out_values, int64_t capacity,
-                                       const int64_t* rank_offsets, int32_t n, int64_t* rank_id_offsets,
-                                       int32_t* err, void* ws, size_t ws_bytes, fs_stream_t stream) {
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if (S < 0 || S > INT32_MAX || capacity < 0 || capacity > INT32_MAX || !out_offsets || !err)
-    return FS_ERR_INVALID_ARG;
-  if (S > 0 && (!offsets || !perm)) return FS_ERR_INVALID_ARG;
-  if (capacity > 0 && (!values || !out_values)) return FS_ERR_INVALID_ARG;
-  if (rank_offsets && (n < 1 || !rank_id_offsets)) return FS_ERR_INVALID_ARG;
-  if (!aligned(out_offsets, 8) || (S > 0 && !aligned(offsets, 8)) || (out_values && !aligned(out_values, 8)) ||
-      (values && !aligned(values, 8)))
-    return FS_ERR_ALIGNMENT;
-  if (ws_bytes < fs_permute_jagged_workspace_size(S) || !ws) return FS_ERR_WORKSPACE;
+namespace fs {
+namespace {
+
+// Both calls: scan (with the permutation source P) then copy.
+template <class Perm>
+fs_status permute_launch(const int64_t* offsets, const int64_t* values, int64_t S, Perm P, int64_t* out_offsets,
+                         int64_t* out_values, int64_t capacity, const int64_t* rank_offsets, int32_t n,
+                         int64_t* rank_id_offsets, const int64_t* row_base, int64_t F, int32_t* err, void* ws,
+                         size_t ws_bytes, cudaStream_t st) {
   if (S == 0) {
     permute_empty_kernel<<<1, kThreads, 0, st>>>(out_offsets, rank_offsets, n, rank_id_offsets, err);
     count_launch(1);
@@ -198,15 +217,60 @@ extern "C" fs_status fs_permute_jagged(const int64_t* offsets, const int64_t* va
   if (cudaMemsetAsync(zero, 0, L.zero_bytes(), st) != cudaSuccess) return FS_ERR_CUDA;
   int* counter = reinterpret_cast<int*>(zero);
   uint64_t* status = reinterpret_cast<uint64_t*>(zero + 256);
-  permute_scan_kernel<<<unsigned(L.scan_tiles), kThreads, 0, st>>>(offsets, S, perm, out_offsets, src_start,
-                                                                   first_sample, L.copy_tiles, capacity, status,
-                                                                   counter, err, spin_limit(), debug_skip_tile());
+  permute_scan_kernel<Perm><<<unsigned(L.scan_tiles), kThreads, 0, st>>>(offsets, S, P, out_offsets, src_start,
+                                                                         first_sample, L.copy_tiles, capacity, status,
+                                                                         counter, err, spin_limit(), debug_skip_tile());
   int64_t grid = L.copy_tiles;
   int64_t cap = int64_t(sm_count()) * 8;
   if (grid > cap) grid = cap;
   if (grid < 1) grid = 1;
   permute_copy_kernel<<<unsigned(grid), kThreads, 0, st>>>(values, out_offsets, src_start, first_sample, S, capacity,
-                                                           out_values, rank_offsets, n, rank_id_offsets, err);
+                                                           out_values, rank_offsets, n, rank_id_offsets, err,
+                                                           row_base, F);
   count_launch(2);
   return launch_status();
+}
+
+}  // namespace
+}  // namespace fs
+
+extern "C" fs_status fs_permute_jagged(const int64_t* offsets, const int64_t* values, int64_t S, const int32_t* perm,
+                                       int64_t* out_offsets, int64_t* out_values, int64_t capacity,
+                                       const int64_t* rank_offsets, int32_t n, int64_t* rank_id_offsets,
+                                       int32_t* err, void* ws, size_t ws_bytes, fs_stream_t stream) {
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (S < 0 || S > INT32_MAX || capacity < 0 || capacity > INT32_MAX || !out_offsets || !err)
+    return FS_ERR_INVALID_ARG;
+  if (S > 0 && (!offsets || !perm)) return FS_ERR_INVALID_ARG;
+  if (capacity > 0 && (!values || !out_values)) return FS_ERR_INVALID_ARG;
+  if (rank_offsets && (n < 1 || !rank_id_offsets)) return FS_ERR_INVALID_ARG;
+  if (!aligned(out_offsets, 8) || (S > 0 && !aligned(offsets, 8)) || (out_values && !aligned(out_values, 8)) ||
+      (values && !aligned(values, 8)))
+    return FS_ERR_ALIGNMENT;
+  if (ws_bytes < fs_permute_jagged_workspace_size(S) || !ws) return FS_ERR_WORKSPACE;
+  return permute_launch(offsets, values, S, PermArray{perm}, out_offsets, out_values, capacity, rank_offsets, n,
+                        rank_id_offsets, nullptr, 1, err, ws, ws_bytes, st);
+}
+
+extern "C" size_t fs_keyed_transpose_workspace_size(int64_t F, int64_t B) {
+  if (F < 1 || B < 0 || F * B > INT32_MAX) return 0;
+  return fs_permute_jagged_workspace_size(F * B);
+}
+
+extern "C" fs_status fs_keyed_transpose(const int64_t* offsets, const int64_t* values, int64_t F, int64_t B,
+                                        const int64_t* row_base, int64_t* out_offsets, int64_t* out_values,
+                                        int64_t capacity, int32_t* err, void* ws, size_t ws_bytes,
+                                        fs_stream_t stream) {
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (F < 1 || B < 0 || F * B > INT32_MAX || capacity < 0 || capacity > INT32_MAX || !out_offsets || !err)
+    return FS_ERR_INVALID_ARG;
+  const int64_t S = F * B;
+  if (S > 0 && !offsets) return FS_ERR_INVALID_ARG;
+  if (capacity > 0 && (!values || !out_values)) return FS_ERR_INVALID_ARG;
+  if (!aligned(out_offsets, 8) || (S > 0 && !aligned(offsets, 8)) || (out_values && !aligned(out_values, 8)) ||
+      (values && !aligned(values, 8)) || (row_base && !aligned(row_base, 8)))
+    return FS_ERR_ALIGNMENT;
+  if (ws_bytes < fs_keyed_transpose_workspace_size(F, B) || !ws) return FS_ERR_WORKSPACE;
+  return permute_launch(offsets, values, S, PermTranspose{F, B}, out_offsets, out_values, capacity, nullptr, 0,
+                        nullptr, row_base, F, err, ws, ws_bytes, st);
 }

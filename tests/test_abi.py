@@ -20,7 +20,8 @@ def _declared():
 
 def test_header_declares_the_hot_path_calls():
     names = _declared()
-    for n in ["fs_balance_fbs", "fs_balance_vbs", "fs_permute_jagged", "fs_bucketize_rowwise", "fs_collision_split",
+    for n in ["fs_balance_fbs", "fs_balance_vbs", "fs_permute_jagged", "fs_keyed_transpose", "fs_bucketize_rowwise",
+              "fs_collision_split",
               "fs_emb_gather", "fs_emb_backward_adagrad"]:
         assert n in names
 
@@ -68,6 +69,14 @@ def test_host_argument_errors_return_without_launching():
                                   C.c_void_p(0x30), C.c_void_p(0x40), C.c_void_p(0x50), err, ws, 1 << 30, NULL) == 1
     assert L.fs_bucketize_rowwise(C.c_void_p(0x13), 10, C.c_void_p(0x100), 4, 100, C.c_void_p(0x20),
                                   C.c_void_p(0x30), C.c_void_p(0x40), C.c_void_p(0x50), err, ws, 1 << 30, NULL) == 8
+    # keyed transpose: F >= 1, F*B < 2^31, 8-byte aligned row bases
+    assert L.fs_keyed_transpose(C.c_void_p(0x10), C.c_void_p(0x20), 0, 4, NULL, C.c_void_p(0x30), C.c_void_p(0x40),
+                                10, err, ws, 1 << 30, NULL) == 1
+    assert L.fs_keyed_transpose(C.c_void_p(0x10), C.c_void_p(0x20), 1 << 16, 1 << 16, NULL, C.c_void_p(0x30),
+                                C.c_void_p(0x40), 10, err, ws, 1 << 30, NULL) == 1
+    assert L.fs_keyed_transpose(C.c_void_p(0x10), C.c_void_p(0x20), 2, 4, C.c_void_p(0x54), C.c_void_p(0x30),
+                                C.c_void_p(0x40), 10, err, ws, 1 << 30, NULL) == 8
+    assert L.fs_keyed_transpose_workspace_size(4, 1000) >= L.fs_permute_jagged_workspace_size(4000)
     assert L.fs_emb_gather(C.c_void_p(0x100), 10, 0, 0, C.c_void_p(0x200), 5, NULL, 1, C.c_void_p(0x300), err,
                            NULL) == 1                                                           # dim < 1
     assert L.fs_emb_gather(C.c_void_p(0x100), 10, 64, 7, C.c_void_p(0x200), 5, NULL, 1, C.c_void_p(0x300), err,

@@ -157,6 +157,38 @@ def test_permute_empty_batch():
     assert to_np(o2).tolist() == [0] and to_np(rio).tolist() == [0, 0, 0, 0]
 
 
+# ------------------------------------------------------------------ keyed transpose
+
+@pytest.mark.parametrize("F,B,maxlen,base", [(3, 1000, 40, False), (26, 4096, 12, True), (1, 5000, 30, True),
+                                              (8, 1, 20000, False), (64, 700, 3, True), (5, 0, 1, False)])
+def test_keyed_transpose_matches_oracle(F, B, maxlen, base):
+    rng = np.random.default_rng(F * 7919 + B)
+    lens = rng.integers(0, maxlen + 1, F * B)
+    off = np.zeros(F * B + 1, np.int64)
+    off[1:] = np.cumsum(lens)
+    val = rng.integers(0, 1 << 40, int(off[-1])).astype(np.int64)
+    rb = rng.integers(0, 1 << 20, F).astype(np.int64) if base else None
+    o2, v2, err = B.fs_keyed_transpose(torch.from_numpy(off).to(DEV), torch.from_numpy(val).to(DEV), F, B,
+                                       row_base=None if rb is None else torch.from_numpy(rb).to(DEV))
+    _check(err)
+    o_ref, v_ref = oracle.keyed_transpose(off, val, F, B, rb)
+    assert np.array_equal(to_np(o2), o_ref) and np.array_equal(to_np(v2), v_ref)
+
+
+def test_keyed_transpose_errors():
+    off = torch.tensor([0, 2, 1, 3], dtype=torch.int64, device=DEV)          # decreasing: bad offsets
+    val = torch.arange(3, dtype=torch.int64, device=DEV)
+    _, _, err = B.fs_keyed_transpose(off, val, 3, 1)
+    with pytest.raises(B.FsError) as e:
+        _check(err)
+    assert e.value.code == 3
+    off = torch.tensor([0, 2, 5], dtype=torch.int64, device=DEV)
+    _, _, err = B.fs_keyed_transpose(off, torch.arange(5, dtype=torch.int64, device=DEV), 2, 1, capacity=4)
+    with pytest.raises(B.FsError) as e:
+        _check(err)
+    assert e.value.code == 4
+
+
 # ------------------------------------------------------------------ bucketize
 
 @pytest.mark.parametrize("n,R,T", [(8, 100_000, 150_000), (64, 10_000_000, 500_000), (512, 50_000_000, 300_001),
