@@ -159,19 +159,20 @@ def test_permute_empty_batch():
 
 # ------------------------------------------------------------------ keyed transpose
 
-@pytest.mark.parametrize("F,B,maxlen,base", [(3, 1000, 40, False), (26, 4096, 12, True), (1, 5000, 30, True),
-                                              (8, 1, 20000, False), (64, 700, 3, True), (5, 0, 1, False)])
-def test_keyed_transpose_matches_oracle(F, B, maxlen, base):
-    rng = np.random.default_rng(F * 7919 + B)
-    lens = rng.integers(0, maxlen + 1, F * B)
-    off = np.zeros(F * B + 1, np.int64)
+@pytest.mark.parametrize("F,nb,maxlen,base", [(3, 1000, 40, False), (26, 4096, 12, True), (1, 5000, 30, True),
+                                               (8, 1, 20000, False), (64, 700, 3, True), (5, 0, 1, False)])
+def test_keyed_transpose_matches_oracle(F, nb, maxlen, base):
+    """F features x nb samples."""
+    rng = np.random.default_rng(F * 7919 + nb)
+    lens = rng.integers(0, maxlen + 1, F * nb)
+    off = np.zeros(F * nb + 1, np.int64)
     off[1:] = np.cumsum(lens)
     val = rng.integers(0, 1 << 40, int(off[-1])).astype(np.int64)
     rb = rng.integers(0, 1 << 20, F).astype(np.int64) if base else None
-    o2, v2, err = B.fs_keyed_transpose(torch.from_numpy(off).to(DEV), torch.from_numpy(val).to(DEV), F, B,
+    o2, v2, err = B.fs_keyed_transpose(torch.from_numpy(off).to(DEV), torch.from_numpy(val).to(DEV), F, nb,
                                        row_base=None if rb is None else torch.from_numpy(rb).to(DEV))
     _check(err)
-    o_ref, v_ref = oracle.keyed_transpose(off, val, F, B, rb)
+    o_ref, v_ref = oracle.keyed_transpose(off, val, F, nb, rb)
     assert np.array_equal(to_np(o2), o_ref) and np.array_equal(to_np(v2), v_ref)
 
 
