@@ -105,8 +105,10 @@ __global__ void __launch_bounds__(kThreads) permute_scan_kernel(const int64_t* o
   }
 }
 
-// row_base (nullable, [F]): added to every ID of an output segment k, by its
-// feature k % F.
+// kBase: row_base[F] is added to every ID of an output segment k, by its
+// feature k % F (a separate instantiation: the plain permute keeps its
+// 64-register footprint and four resident blocks per SM).
+template <bool kBase>
 __global__ void __launch_bounds__(kThreads) permute_copy_kernel(const int64_t* values, const int64_t* out_offsets,
                                                                 const int64_t* src_start, const int32_t* first_sample,
                                                                 int64_t S, int64_t capacity, int64_t* out_values,
@@ -129,12 +131,12 @@ __global__ void __launch_bounds__(kThreads) permute_copy_kernel(const int64_t* v
     int64_t k = first_sample[t];
     int64_t k_hi = (t + 1 < ntiles) ? int64_t(first_sample[t + 1]) : S - 1;  // last sample touching this tile
     int64_t srcidx[kCopyItems];
-    int64_t base[kCopyItems];
+    int64_t base[kBase ? kCopyItems : 1];
 #pragma unroll
     for (int i = 0; i < kCopyItems; ++i) {
       const int64_t j = j0 + int64_t(i) * kThreads + threadIdx.x;
       srcidx[i] = -1;
-      base[i] = 0;
+      if constexpr (kBase) base[i] = 0;
       if (j < total) {
         // largest k' in [k, k_hi] with out_offsets[k'] <= j
         int64_t lo = k, hi = k_hi;
@@ -144,12 +146,15 @@ __global__ void __launch_bounds__(kThreads) permute_copy_kernel(const int64_t* v
         }
         k = lo;
         srcidx[i] = __ldg(src_start + k) + (j - __ldg(out_offsets + k));
-        if (row_base) base[i] = __ldg(row_base + k % F);
+        if constexpr (kBase) base[i] = __ldg(row_base + k % F);
       }
     }
     int64_t v[kCopyItems];
 #pragma unroll
-    for (int i = 0; i < kCopyItems; ++i) v[i] = srcidx[i] >= 0 ? __ldcs(values + srcidx[i]) + base[i] : 0;
+    for (int i = 0; i < kCopyItems; ++i) {
+      v[i] = srcidx[i] >= 0 ? __ldcs(values + srcidx[i]) : 0;
+      if constexpr (kBase) v[i] += base[i];
+    }
 #pragma unroll
     for (int i = 0; i < kCopyItems; ++i) {
       const int64_t j = j0 + int64_t(i) * kThreads + threadIdx.x;
@@ -224,9 +229,9 @@ fs_status permute_launch(const int64_t* offsets, const int64_t* values, int64_t 
   int64_t cap = int64_t(sm_count()) * 8;
   if (grid > cap) grid = cap;
   if (grid < 1) grid = 1;
-  permute_copy_kernel<<<unsigned(grid), kThreads, 0, st>>>(values, out_offsets, src_start, first_sample, S, capacity,
-                                                           out_values, rank_offsets, n, rank_id_offsets, err,
-                                                           row_base, F);
+  auto copy = row_base ? permute_copy_kernel<true> : permute_copy_kernel<false>;
+  copy<<<unsigned(grid), kThreads, 0, st>>>(values, out_offsets, src_start, first_sample, S, capacity, out_values,
+                                            rank_offsets, n, rank_id_offsets, err, row_base, F);
   count_launch(2);
   return launch_status();
 }
