@@ -48,33 +48,35 @@ constexpr uint32_t kNoKey = 0xFFFFFFFFu;     // rows are < num_rows < 2^32
 // Sort source: the selected positions of the batch, key = row, value = position.
 // With both phases in one call, key = row | (exclusive << kb): collision rows
 // sort first, exclusive rows after them, each group in row order.
+template <bool kRowBits>  // collision flags from the row bitmap (true) or the per-position mask
 struct SrcRows {
   using Key = uint32_t;
   static constexpr bool kIndexValue = true;  // value = item index
   const int64_t* ids;
-  const uint8_t* is_co;     // collision flag per position, or null
-  const uint32_t* co_rows;  // collision flag per row (bitmap), or null
+  const uint8_t* is_co;     // collision flag per position (kRowBits false)
+  const uint32_t* co_rows;  // collision flag per row, bitmap (kRowBits true)
   int phase;
   int64_t R;
   int kb;  // bits of the largest row index
-  static constexpr bool kFetch2 = true;
+  static constexpr bool kFetch2 = kRowBits;
   struct Raw {
     int64_t id;
     uint32_t m;
   };
-  // loads only: the ID and the mask byte independently; with a row bitmap,
+  // loads only: the ID and the mask byte independently; with the row bitmap,
   // fetch2 then reads the ID's row bit (L2-resident; an out-of-range ID reads
   // bit 0 and is rejected by make) after every ID of the tile is in flight
   __device__ __forceinline__ Raw fetch(int64_t i) const {
     Raw r;
     r.id = __ldcs(ids + i);
-    r.m = (phase != FS_PHASE_ALL && !co_rows) ? uint32_t(__ldcs(is_co + i)) : 0u;
+    r.m = (!kRowBits && phase != FS_PHASE_ALL) ? uint32_t(__ldcs(is_co + i)) : 0u;
     return r;
   }
   __device__ __forceinline__ void fetch2(Raw& r) const {
-    if (phase == FS_PHASE_ALL || !co_rows) return;
-    const uint64_t x = uint64_t(r.id) < uint64_t(R) ? uint64_t(r.id) : 0u;
-    r.m = (__ldg(co_rows + (x >> 5)) >> (x & 31u)) & 1u;
+    if constexpr (kRowBits) {
+      const uint64_t x = uint64_t(r.id) < uint64_t(R) ? uint64_t(r.id) : 0u;
+      r.m = (__ldg(co_rows + (x >> 5)) >> (x & 31u)) & 1u;
+    }
   }
   __device__ __forceinline__ bool make(const Raw& r, int64_t i, Key& key, uint32_t& val, int32_t* err) const {
     const int64_t id = r.id;
@@ -836,8 +838,11 @@ extern "C" fs_status fs_emb_backward_adagrad(void* table, float* state, int64_t 
 
   int launches = 0;
   uint32_t *sk = nullptr, *sv = nullptr;
-  SrcRows src{ids, is_co, co_rows, int(phase), num_rows, kb};
-  fs_status s = radix::run_sort(src, L.plan, W, err, st, &sk, &sv, &launches);
+  fs_status s = (phase != FS_PHASE_ALL && co_rows)
+                    ? radix::run_sort(SrcRows<true>{ids, is_co, co_rows, int(phase), num_rows, kb}, L.plan, W, err,
+                                      st, &sk, &sv, &launches)
+                    : radix::run_sort(SrcRows<false>{ids, is_co, co_rows, int(phase), num_rows, kb}, L.plan, W, err,
+                                      st, &sk, &sv, &launches);
   if (s != FS_OK) return s;
   UpdateArgs u{table, optim == FS_ROWWISE_ADAGRAD ? state : nullptr, int(optim), lr, eps};
   const bool bf = dtype == FS_BF16;
