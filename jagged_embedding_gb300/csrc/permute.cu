@@ -25,6 +25,7 @@ constexpr int kScanItems = 8;
 constexpr int kScanTile = kThreads * kScanItems;
 constexpr int kCopyItems = 16;
 constexpr int kCopyTile = kThreads * kCopyItems;  // output IDs per copy tile
+constexpr int64_t kShortSample = 512;  // average IDs per sample below which the segment-parallel copy runs
 
 // Source segment of output segment k: read from an array ...
 struct PermArray {
@@ -163,6 +164,51 @@ __global__ void __launch_bounds__(kThreads) permute_copy_kernel(const int64_t* v
   }
 }
 
+// Copy for short samples (segment-parallel): a warp takes groups of 32
+// consecutive output samples, lane l loads sample l's destination, end,
+// source and row base, then the warp copies the samples one after another,
+// four IDs per lane in flight.  Writes stop at `capacity` (the scan reports
+// the overflow).
+constexpr int kSegUnroll = 4;
+template <bool kBase>
+__global__ void __launch_bounds__(kThreads) permute_seg_copy_kernel(const int64_t* values, const int64_t* out_offsets,
+                                                                    const int64_t* src_start, int64_t S,
+                                                                    int64_t capacity, int64_t* out_values,
+                                                                    const int64_t* row_base, int64_t F) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
+  const int64_t ngroups = (S + 31) / 32;
+  for (int64_t grp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; grp < ngroups; grp += nwarps) {
+    const int64_t k = grp * 32 + lane;
+    int64_t d = 0, e = 0, sr = 0, b = 0;
+    if (k < S) {
+      d = __ldg(out_offsets + k);
+      e = __ldg(out_offsets + k + 1);
+      sr = __ldg(src_start + k);
+      if constexpr (kBase) b = __ldg(row_base + k % F);
+    }
+    if (e > capacity) e = capacity;
+    for (int q = 0; q < 32; ++q) {
+      const int64_t dq = __shfl_sync(0xffffffffu, d, q), eq = __shfl_sync(0xffffffffu, e, q);
+      const int64_t sq = __shfl_sync(0xffffffffu, sr, q);
+      const int64_t bq = kBase ? __shfl_sync(0xffffffffu, b, q) : 0;
+      for (int64_t j0 = dq; j0 < eq; j0 += 32 * kSegUnroll) {
+        int64_t v[kSegUnroll];
+#pragma unroll
+        for (int u = 0; u < kSegUnroll; ++u) {
+          const int64_t j = j0 + u * 32 + lane;
+          v[u] = j < eq ? __ldcs(values + sq + (j - dq)) : 0;
+        }
+#pragma unroll
+        for (int u = 0; u < kSegUnroll; ++u) {
+          const int64_t j = j0 + u * 32 + lane;
+          if (j < eq) __stcs(out_values + j, v[u] + bq);
+        }
+      }
+    }
+  }
+}
+
 __global__ void permute_empty_kernel(int64_t* out_offsets, const int64_t* rank_offsets, int32_t n,
                                      int64_t* rank_id_offsets, int32_t* err) {
   if (threadIdx.x == 0) out_offsets[0] = 0;
@@ -229,9 +275,15 @@ fs_status permute_launch(const int64_t* offsets, const int64_t* values, int64_t 
   int64_t cap = int64_t(sm_count()) * 8;
   if (grid > cap) grid = cap;
   if (grid < 1) grid = 1;
-  auto copy = row_base ? permute_copy_kernel<true> : permute_copy_kernel<false>;
-  copy<<<unsigned(grid), kThreads, 0, st>>>(values, out_offsets, src_start, first_sample, S, capacity, out_values,
-                                            rank_offsets, n, rank_id_offsets, err, row_base, F);
+  if (!rank_offsets && capacity <= kShortSample * S) {
+    // short samples on average: one warp per group of 32 samples, no per-ID search
+    auto copy = row_base ? permute_seg_copy_kernel<true> : permute_seg_copy_kernel<false>;
+    copy<<<unsigned(cap), kThreads, 0, st>>>(values, out_offsets, src_start, S, capacity, out_values, row_base, F);
+  } else {
+    auto copy = row_base ? permute_copy_kernel<true> : permute_copy_kernel<false>;
+    copy<<<unsigned(grid), kThreads, 0, st>>>(values, out_offsets, src_start, first_sample, S, capacity, out_values,
+                                              rank_offsets, n, rank_id_offsets, err, row_base, F);
+  }
   count_launch(2);
   return launch_status();
 }
