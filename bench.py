@@ -218,6 +218,14 @@ def oracle_sample(w, steps, max_seconds=20.0, samples_per_rank=None, table_np=No
     return ids_done / secs, desc, ids_done, secs
 
 
+def workload_config(w, n_gpus):
+    """The workload keys both arms report (the GPU arm adds its measured IDs per step and the L2 note)."""
+    return {"workload": w.name, "n_logical_ranks": w.n, "samples_per_rank": w.B, "rows": w.R, "dim": w.D,
+            "table_dtype": w.dtype, "optimizer": w.optim, "balance": w.balance, "iterations_cycled": w.iters,
+            "schedule": "sync order, collision rows updated before exclusive rows",
+            "parallelism": f"replicas x{n_gpus}"}
+
+
 def run_reference(args):
     """`--impl reference`: the CPU oracle timed on the host cores (rank 0 only)."""
     rank, ws, _ = dist_setup()
@@ -234,7 +242,7 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": rate, "unit": "IDs/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * secs / max(1, args.steps),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": f"int64/{w.dtype}",
-            "data": "synthetic", "config": {"workload": w.name, "n_logical_ranks": w.n, "rows": w.R, "dim": w.D},
+            "data": "synthetic", "config": workload_config(w, args.gpus),
             "cpu_baseline": {"value": rate, "unit": "IDs/s", "cores": 1, "kind": "oracle", "sample": desc},
             "e2e": {"value": rate, "unit": "IDs/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
@@ -369,13 +377,9 @@ def run_gpu(args):
         "metric": METRIC, "value": value, "unit": "IDs/s", "n_gpus": ws, "steps": K, "warmup": W,
         "ms_per_step": 1000.0 * secs_max / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": f"int64/{w.dtype}", "data": "synthetic",
-        "config": {"workload": w0.name, "n_logical_ranks": w.n, "samples_per_rank": w.B, "rows": w.R, "dim": w.D,
-                   "table_dtype": w.dtype, "optimizer": w.optim, "balance": w.balance,
-                   "ids_per_step": ids_timed / K, "iterations_cycled": w.iters,
-                   "l2": "no flush: inputs larger than L2 (table %.1f GB, %.1f GB of IDs per batch)"
-                         % (table.numel() * table.element_size() / 1e9, max_T * 8 / 1e9),
-                   "schedule": "sync order, collision rows updated before exclusive rows",
-                   "parallelism": f"replicas x{ws}"},
+        "config": dict(workload_config(w0, ws), ids_per_step=ids_timed / K,
+                       l2="no flush: inputs larger than L2 (table %.1f GB, %.1f GB of IDs per batch)"
+                          % (table.numel() * table.element_size() / 1e9, max_T * 8 / 1e9)),
         "hbm_roofline_frac_step": step_bytes / secs / (hbm_gbs * 1e9),
         "algorithmic_bytes_per_step": step_bytes / K,
         "roofline": {"kernel": GATHER_KERNEL, "bound": "hbm", "achieved": achieved,
