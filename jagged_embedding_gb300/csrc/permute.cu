@@ -26,6 +26,7 @@ constexpr int kScanTile = kThreads * kScanItems;
 constexpr int kCopyItems = 16;
 constexpr int kCopyTile = kThreads * kCopyItems;  // output IDs per copy tile
 constexpr int64_t kShortSample = 512;  // average IDs per sample below which the segment-parallel copy runs
+constexpr int64_t kManySamples = 32;   // samples in one copy tile above which its warps copy whole samples
 
 // Source segment of output segment k: read from an array ...
 struct PermArray {
@@ -131,6 +132,21 @@ __global__ void __launch_bounds__(kThreads) permute_copy_kernel(const int64_t* v
     const int64_t j0 = t * kCopyTile;
     int64_t k = first_sample[t];
     int64_t k_hi = (t + 1 < ntiles) ? int64_t(first_sample[t + 1]) : S - 1;  // last sample touching this tile
+    if (k_hi - k > kManySamples) {
+      // a tile of many short samples: each warp copies whole samples (clipped
+      // to the tile) instead of searching the sample of every ID
+      const int64_t j1 = (j0 + kCopyTile < total) ? j0 + kCopyTile : total;
+      const int lane = threadIdx.x & 31;
+      for (int64_t kk = k + (threadIdx.x >> 5); kk <= k_hi; kk += kThreads / 32) {
+        const int64_t d = __ldg(out_offsets + kk), e = __ldg(out_offsets + kk + 1);
+        const int64_t a = d > j0 ? d : j0, z = e < j1 ? e : j1;
+        if (a >= z) continue;
+        const int64_t src = __ldg(src_start + kk) + (a - d);
+        const int64_t add = kBase ? __ldg(row_base + kk % F) : 0;
+        for (int64_t j = a + lane; j < z; j += 32) __stcs(out_values + j, __ldcs(values + src + (j - a)) + add);
+      }
+      continue;
+    }
     int64_t srcidx[kCopyItems];
     int64_t base[kBase ? kCopyItems : 1];
 #pragma unroll

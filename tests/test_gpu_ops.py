@@ -135,6 +135,26 @@ def test_permute_with_empty_samples_and_long_samples():
     assert np.array_equal(to_np(o2), o_ref) and np.array_equal(to_np(v2), v_ref)
 
 
+def test_permute_many_short_samples_per_tile_with_rank_offsets():
+    """Tiles covering many short samples (and runs of empty ones) next to long samples, through the
+    ID-balanced copy (rank offsets requested)."""
+    rng = np.random.default_rng(17)
+    S = 60000
+    lens = rng.integers(0, 7, S).astype(np.int64)
+    lens[rng.integers(0, S, 30)] = 9000
+    off = np.zeros(S + 1, np.int64)
+    off[1:] = np.cumsum(lens)
+    ids = rng.integers(0, 1 << 40, int(off[-1])).astype(np.int64)
+    perm = np.argsort(lens, kind="stable").astype(np.int32)       # short samples first, as a sorted VBS order
+    ro = np.linspace(0, S, 9).round().astype(np.int64)
+    o2, v2, rio, err = B.fs_permute_jagged(torch.from_numpy(off).to(DEV), torch.from_numpy(ids).to(DEV),
+                                           torch.from_numpy(perm).to(DEV), rank_offsets=torch.from_numpy(ro).to(DEV))
+    _check(err)
+    o_ref, v_ref = oracle.permute_jagged(off, ids, perm)
+    assert np.array_equal(to_np(o2), o_ref) and np.array_equal(to_np(v2), v_ref)
+    assert np.array_equal(to_np(rio), o_ref[ro])
+
+
 def test_permute_errors():
     off = torch.tensor([0, 2, 5], dtype=torch.int64, device=DEV)
     val = torch.arange(5, dtype=torch.int64, device=DEV)
