@@ -45,10 +45,11 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def algorithmic_bytes(w, S, T, U, R):
+def algorithmic_bytes(w, S, T, U, R, n_cand=0):
     """Bytes the method must move for one step (one batch), by stage.
 
     prep (balance + permute + bucketize)      16 S + 16 T + 20 T
+      (+ 16 S + 16 C with composite candidates: their lengths move with the samples, C candidates)
     collision split, per pair                  8 T + 2 T + 3 R / 8 + 16 U
     gather                                     (8 + RB) T + RB U
     backward (segment-reduce + update)         (8 + RB) T + (2 RB + 8) U
@@ -56,7 +57,7 @@ def algorithmic_bytes(w, S, T, U, R):
     """
     RB = w.row_bytes
     b = {
-        "prep": 16 * S + 36 * T,
+        "prep": 16 * S + 36 * T + ((16 * S + 16 * n_cand) if w.composite else 0),
         "collision": 10 * T + 3 * R / 8 + 16 * U,
         "gather": (8 + RB) * T + RB * U,
     }
@@ -343,7 +344,8 @@ def run_gpu(args):
     step_bytes = 0.0
     gbytes = 0.0
     for t in step_batches:
-        bb = algorithmic_bytes(w, w.S, Ts[t], U[t], w.R)
+        n_cand = int(batches[t]["cand_offsets"][-1]) if w.composite else 0
+        bb = algorithmic_bytes(w, w.S, Ts[t], U[t], w.R, n_cand)
         step_bytes += sum(bb.values())
         gbytes += gather_bytes(w, Ts[t], U[t])
     gbytes /= K
@@ -429,6 +431,11 @@ def run_e2e(w, pipe, batches, grads, K, W, dev, ws):
     ring = [{"uih_len": torch.empty(max_S1 - 1, dtype=torch.int32, device=dev),
              "offsets": torch.empty(max_S1, dtype=torch.int64, device=dev),
              "ids": torch.empty(max_T, dtype=torch.int64, device=dev)} for _ in range(3)]
+    if w.composite:  # candidate lengths travel with the batch
+        max_C = max(h["cand_lens"].numel() for h in host)
+        for r in ring:
+            r["cand_offsets"] = torch.empty(max_S1, dtype=torch.int64, device=dev)
+            r["cand_lens"] = torch.empty(max(max_C, 1), dtype=torch.int64, device=dev)
     copy_stream = torch.cuda.Stream(dev)
     main = torch.cuda.current_stream(dev)
     done = [torch.cuda.Event() for _ in range(3)]
@@ -445,10 +452,19 @@ def run_e2e(w, pipe, batches, grads, K, W, dev, ws):
             slot["uih_len"][: S1 - 1].copy_(h["uih_len"], non_blocking=True)
             slot["offsets"][:S1].copy_(h["offsets"], non_blocking=True)
             slot["ids"][: h["T"]].copy_(h["ids"], non_blocking=True)
+            if w.composite:
+                nc = h["cand_lens"].numel()
+                slot["cand_offsets"][:S1].copy_(h["cand_offsets"], non_blocking=True)
+                slot["cand_lens"][:nc].copy_(h["cand_lens"], non_blocking=True)
             done[i % 3].record(copy_stream)
         nbytes = h["uih_len"].numel() * 4 + h["offsets"].numel() * 8 + h["T"] * 8
-        return {"uih_len": slot["uih_len"][: S1 - 1], "offsets": slot["offsets"][:S1],
-                "ids": slot["ids"][: h["T"]], "T": h["T"]}, nbytes
+        b = {"uih_len": slot["uih_len"][: S1 - 1], "offsets": slot["offsets"][:S1],
+             "ids": slot["ids"][: h["T"]], "T": h["T"]}
+        if w.composite:
+            nc = h["cand_lens"].numel()
+            nbytes += S1 * 8 + nc * 8
+            b["cand_offsets"], b["cand_lens"] = slot["cand_offsets"][:S1], slot["cand_lens"][:nc]
+        return b, nbytes
 
     def run(steps, measure):
         staged = {}

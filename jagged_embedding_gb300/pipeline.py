@@ -40,6 +40,9 @@ class Slot:
         # presence bitmap of the batch's rows: built once, used by both collision
         # pairs the batch belongs to
         self.bitmap = torch.empty((w.R + 31) // 32, dtype=torch.int32, device=device)
+        if w.composite:  # candidate lengths, permuted with the samples (Algorithm 1 Stage II)
+            self.cand_offsets = torch.empty(max_S + 1, dtype=torch.int64, device=device)
+            self.cand_lens = torch.empty(max_S * max(w.cmax, 1), dtype=torch.int64, device=device)
         self.T = 0
 
 
@@ -95,6 +98,10 @@ class Pipeline:
         B.fs_permute_jagged(batch["offsets"], batch["ids"], s.perm[: batch["uih_len"].numel()], capacity=self.max_T,
                             rank_offsets=s.rank_offsets, out_offsets=s.offsets[: batch["offsets"].numel()],
                             out_values=s.ids, rank_id_offsets=s.rank_id_offsets, err=self.err, ws=self.ws)
+        if w.composite:
+            B.fs_permute_jagged(batch["cand_offsets"], batch["cand_lens"], s.perm[: batch["uih_len"].numel()],
+                                capacity=s.cand_lens.numel(), out_offsets=s.cand_offsets[: batch["offsets"].numel()],
+                                out_values=s.cand_lens, err=self.err, ws=self.ws)
         B.fs_bucketize_rowwise(s.ids, s.rank_id_offsets, w.R, sm_ids=s.sm_ids, pos=s.pos, splits=s.splits,
                                shard_offsets=s.shard_offsets, err=self.err, ws=self.ws, T=T)
         B.fs_row_bitmap(s.ids, w.R, bitmap=s.bitmap, err=self.err, T=T)

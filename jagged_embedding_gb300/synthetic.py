@@ -10,7 +10,10 @@ plus candidates, §5.2 for synthetic embedding workloads):
 
 * sample g (global index, rank-major g = r*B + b) has UIH length
   L_g = clip(round_half_even(lognormal(mu, sigma)), 1, L_max) and
-  C_g ~ U{c_min..c_max} candidates, each candidate one ID;
+  C_g ~ U{c_min..c_max} candidates, each candidate one ID -- or, in a recipe
+  with composite candidates (Algorithm 1 Stage II), each candidate c carries
+  K_c ~ U{k_min..k_max} IDs, and the batch also holds the candidate lengths
+  as a jagged tensor (cand_offsets by C_g, cand_lens = K_c);
 * the jagged row of a sample is [UIH IDs | candidate IDs];
 * every ID is drawn i.i.d. from a bounded Zipf law P(k) ~ (k+1)^-s over
   k in [0, R) by inverse CDF, then scrambled row = (k * A) mod R with
@@ -57,6 +60,8 @@ class Workload:
     lr: float
     eps: float
     seed_base: int
+    kmin: int = 1     # IDs per candidate, uniform in [kmin, kmax] (composite when kmax > 1)
+    kmax: int = 1
 
     @property
     def S(self) -> int:
@@ -69,6 +74,10 @@ class Workload:
     @property
     def has_update(self) -> bool:
         return self.optim != "none"
+
+    @property
+    def composite(self) -> bool:
+        return self.kmax > 1
 
     def scaled(self, **kw) -> "Workload":
         """Same recipe with some sizes replaced (used for reduced parity cases)."""
@@ -91,6 +100,9 @@ WORKLOADS = {
     # 256 ranks x 512 samples, FBS, 100M x 64 fp32 + row-wise Adagrad state, 4 iterations.
     "large-table-full-step": Workload("large-table-full-step", 256, 512, 6.8, 1.5, 16384, 1, 64, 100_000_000, 64,
                                       "f32", 1.0, "fbs", 1.5, False, 4, "adagrad", 0.01, 1e-8, 4000),
+    # 16 ranks x 64 samples whose candidates carry 1..16 IDs each, FBS, 1M x 64 fp32, SGD over 2 iterations.
+    "composite-cand": Workload("composite-cand", 16, 64, 5.0, 1.2, 2048, 1, 8, 1_000_000, 64, "f32",
+                               1.1, "fbs", 1.5, False, 2, "sgd", 0.01, 0.0, 5000, 1, 16),
 }
 
 
@@ -148,7 +160,9 @@ def batch(w: Workload, it: int, device="cpu") -> dict:
     """One global batch (all n logical ranks, rank-major) of iteration `it`.
 
     Returns uih_len int32[S], num_cand int32[S], offsets int64[S+1] (jagged row
-    offsets, row g = [UIH | candidates]), ids int64[T] and the host int T.
+    offsets, row g = [UIH | candidates]), ids int64[T] and the host int T; with
+    composite candidates also cand_offsets int64[S+1] (candidates per sample)
+    and cand_lens int64[sum C] (IDs per candidate).
     """
     device = torch.device(device)
     g = _gen(w.seed_base + it, device)
@@ -159,12 +173,24 @@ def batch(w: Workload, it: int, device="cpu") -> dict:
         C = torch.randint(w.cmin, w.cmax + 1, (S,), dtype=torch.int32, device=device, generator=g)
     else:
         C = torch.zeros(S, dtype=torch.int32, device=device)
-    lens = (L + C).to(torch.int64)
+    extra = {}
+    if w.composite:
+        cand_offsets = torch.zeros(S + 1, dtype=torch.int64, device=device)
+        torch.cumsum(C.to(torch.int64), 0, out=cand_offsets[1:])
+        K = torch.randint(w.kmin, w.kmax + 1, (int(cand_offsets[-1].item()),), dtype=torch.int64, device=device,
+                          generator=g)
+        ck = torch.zeros(K.numel() + 1, dtype=torch.int64, device=device)
+        torch.cumsum(K, 0, out=ck[1:])
+        cand_ids = ck[cand_offsets[1:]] - ck[cand_offsets[:-1]]   # IDs of each sample's candidates
+        lens = L.to(torch.int64) + cand_ids
+        extra = {"cand_offsets": cand_offsets, "cand_lens": K}
+    else:
+        lens = (L + C).to(torch.int64)
     offsets = torch.zeros(S + 1, dtype=torch.int64, device=device)
     torch.cumsum(lens, 0, out=offsets[1:])
     T = int(offsets[-1].item())
     ids = zipf_rows(w.R, w.zipf_s, T, g, device)
-    return {"uih_len": L, "num_cand": C, "offsets": offsets, "ids": ids, "T": T}
+    return {"uih_len": L, "num_cand": C, "offsets": offsets, "ids": ids, "T": T, **extra}
 
 
 def table(w: Workload, device="cpu") -> torch.Tensor:

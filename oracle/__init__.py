@@ -215,7 +215,8 @@ def double_to_bf16(x):
 def prepare(w, b):
     """Balance, permute and bucketize one batch (FreeScale Algorithm 1, Algorithm 2 line 8).
 
-    w: a synthetic.Workload; b: a batch dict of numpy arrays (uih_len, offsets, ids).
+    w: a synthetic.Workload; b: a batch dict of numpy arrays (uih_len, offsets, ids; with composite
+    candidates also cand_offsets, cand_lens).
     """
     if w.balance == "fbs":
         perm, ro = balance_fbs(b["uih_len"], w.n)
@@ -225,8 +226,12 @@ def prepare(w, b):
     off2, ids2 = permute_jagged(b["offsets"], b["ids"], perm)
     rio = off2[ro]
     sm, pos, splits, so = bucketize_rowwise(ids2, rio, w.n, w.R)
-    return {"perm": perm, "rank_offsets": ro, "seg_weight": sw, "offsets": off2, "ids": ids2,
-            "rank_id_offsets": rio, "sm_ids": sm, "pos": pos, "splits": splits, "shard_offsets": so}
+    res = {"perm": perm, "rank_offsets": ro, "seg_weight": sw, "offsets": off2, "ids": ids2,
+           "rank_id_offsets": rio, "sm_ids": sm, "pos": pos, "splits": splits, "shard_offsets": so}
+    if "cand_lens" in b:
+        # composite candidates (Algorithm 1 Stage II): their lengths move with the samples
+        res["cand_offsets"], res["cand_lens"] = permute_jagged(b["cand_offsets"], b["cand_lens"], perm)
+    return res
 
 
 def run_sync(w, batches, table, state, grads_list):

@@ -1,4 +1,4 @@
-"""Whole-iteration parity on the five workload recipes at reduced sizes (GPU).
+"""Whole-iteration parity on the workload recipes at reduced sizes (GPU).
 
 Each case runs the GPU pipeline over consecutive iterations in the synchronous
 order and compares with the oracle's synchronous run: every index output
@@ -28,6 +28,7 @@ CASES = {
     "mid-full-step": W["mid-full-step"].scaled(B=16, R=1_000_000),
     "long-seq-index": W["long-seq-index"].scaled(B=2, R=5_000_000),
     "large-table-full-step": W["large-table-full-step"].scaled(B=4, R=2_000_000),
+    "composite-cand": W["composite-cand"],                                              # full size
 }
 
 
@@ -48,6 +49,10 @@ def _gpu_sync(w, batches_cpu, table0, grads_cpu):
                 "offsets": to_np(s.offsets[: w.S + 1]), "rank_id_offsets": to_np(s.rank_id_offsets),
                 "sm_ids": to_np(s.sm_ids[:T]), "pos": to_np(s.pos[:T]), "splits": to_np(s.splits),
                 "shard_offsets": to_np(s.shard_offsets), "seg_weight": to_np(s.seg_weight)}
+        if w.composite:
+            nc = int(bd[t]["cand_offsets"][-1])
+            snap["cand_offsets"] = to_np(s.cand_offsets[: w.S + 1])
+            snap["cand_lens"] = to_np(s.cand_lens[:nc])
         has_next = t + 1 < K
         nxt = pipe.step_sync(cur, bd[t + 1] if has_next else None, gd[t] if gd else None, has_next=has_next,
                              want_masks=True)
@@ -95,6 +100,9 @@ def test_pipeline_matches_oracle(name):
         assert np.array_equal(g["pos"], p["pos"]), t
         assert np.array_equal(g["splits"], p["splits"]), t
         assert np.array_equal(g["shard_offsets"], p["shard_offsets"]), t
+        if w.composite:
+            assert np.array_equal(g["cand_offsets"], p["cand_offsets"]), t
+            assert np.array_equal(g["cand_lens"], p["cand_lens"]), t
         if "coll" in r:
             # (the synchronous order does not ask for the mask of t+1)
             for k in ("co", "ex_t", "ex_next", "co_off", "ex_t_off", "ex_next_off", "is_co_t"):

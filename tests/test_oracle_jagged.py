@@ -212,3 +212,24 @@ def test_keyed_transpose_twice_with_roles_swapped_is_identity(F, B):
 def test_keyed_transpose_rejects_bad_offsets():
     with pytest.raises(oracle.OracleError):
         oracle.keyed_transpose(np.array([0, 3, 2]), np.array([1, 2, 3]), 1, 2)
+
+
+# ------------------------------------------------------------------ composite candidates
+
+def test_composite_candidate_lengths_move_with_their_samples():
+    """Algorithm 1 Stage II: with multi-ID candidates, each output sample's row is its UIH IDs plus
+    the IDs of its candidates, and its candidate lengths are the source sample's, in order."""
+    w = synthetic.WORKLOADS["composite-cand"]
+    b = {k: (v.numpy() if hasattr(v, "numpy") else v) for k, v in synthetic.batch(w, 0).items()}
+    # the recipe itself: row length = UIH + sum of the candidate lengths
+    co, cl = b["cand_offsets"], b["cand_lens"]
+    per = np.array([cl[co[g]:co[g + 1]].sum() for g in range(w.S)])
+    assert np.array_equal(np.diff(b["offsets"]), b["uih_len"].astype(np.int64) + per)
+    assert np.array_equal(np.diff(co), b["num_cand"])
+    p = oracle.prepare(w, b)
+    perm = p["perm"]
+    for k in range(w.S):
+        g = perm[k]
+        assert p["cand_lens"][p["cand_offsets"][k]:p["cand_offsets"][k + 1]].tolist() == cl[co[g]:co[g + 1]].tolist()
+        row = p["ids"][p["offsets"][k]:p["offsets"][k + 1]]
+        assert row.tolist() == b["ids"][b["offsets"][g]:b["offsets"][g + 1]].tolist()
