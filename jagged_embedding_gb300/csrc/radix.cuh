@@ -416,14 +416,26 @@ void run_pass(const Src& src, const Dst& dst, int shift, int bits, int nb, const
 // [0, count) that Src0::make accepts), by the low key_bits bits of the key,
 // in passes of at most 10 bits.  Result: *out_k / *out_v, *n_valid entries
 // (n_valid stays on the device).
+// Digits of at most 10 bits (kMaxBins); when the key bits do not split evenly
+// the wider digits go last: a key's high bits take fewer distinct values
+// (rows < num_rows), so a wide high digit still has long runs per tile, while
+// narrower low digits (uniformly spread) get longer runs than 10-bit ones.
 struct SortPlan {
   int64_t count = 0;
-  int key_bits = 1, passes = 1, bits = 1, nb = 2;
+  int key_bits = 1, passes = 1, nb = 2;  // nb: digit values of the widest pass
   SortPlan() = default;
   SortPlan(int64_t c, int kb) : count(c), key_bits(kb < 1 ? 1 : kb) {
-    passes = (key_bits + 9) / 10;  // digits of at most 10 bits (kMaxBins)
-    bits = (key_bits + passes - 1) / passes;
-    nb = 1 << bits;
+    passes = (key_bits + 9) / 10;
+    nb = 1 << bits(passes - 1);
+  }
+  int bits(int p) const {  // width of pass p
+    const int base = key_bits / passes, extra = key_bits % passes;
+    return base + (p >= passes - extra ? 1 : 0);
+  }
+  int shift(int p) const {
+    int s = 0;
+    for (int q = 0; q < p; ++q) s += bits(q);
+    return s;
   }
   size_t bytes() const { return pass_ws_bytes(count, nb) + 4 * align_up(size_t(count) * sizeof(uint32_t)); }
 };
@@ -454,13 +466,14 @@ fs_status run_sort(const Src0& src0, const SortPlan& P, const SortWs& W, int32_t
   }
   for (int p = 0; p < P.passes; ++p) {
     DstU32 dst{W.k[p & 1], W.v[p & 1]};
+    const int bits = P.bits(p), nb = 1 << bits;
     if (p == 0) {
-      run_pass(src0, dst, 0, P.bits, P.nb, nullptr, P.count, W.pass, err, st, launches);
+      run_pass(src0, dst, 0, bits, nb, nullptr, P.count, W.pass, err, st, launches);
     } else {
       // later passes sort the n_valid items the first pass kept; n_valid is
       // rewritten with the same value by each pass
       SrcU32 s{W.k[(p - 1) & 1], W.v[(p - 1) & 1]};
-      run_pass(s, dst, p * P.bits, P.bits, P.nb, W.pass.n_valid, P.count, W.pass, nullptr, st, launches);
+      run_pass(s, dst, P.shift(p), bits, nb, W.pass.n_valid, P.count, W.pass, nullptr, st, launches);
     }
   }
   return launch_status();
