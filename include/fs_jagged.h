@@ -242,8 +242,10 @@ fs_status fs_collision_split_bitmaps(const int64_t* ids_t, int64_t T_t, const ui
  * With mask != NULL only positions p with mask[p] == sel are written; the
  * other rows of out are left untouched.
  *   table [num_rows, dim] of dtype, row-major;  out [T, dim] of dtype.
- * Row bytes must be a multiple of 4; multiples of 16 with 16-byte aligned
- * table and out take the vector path.
+ * Row bytes must be a multiple of 4.  Unmasked calls with 16-byte aligned
+ * table and out and rows of 16 B to 2 KB (a multiple of 16) move rows through
+ * the copy engine (bulk copies into shared memory, one bulk store per stage);
+ * other multiples of 16 take 16-byte vector loads, the rest 4-byte words.
  * ---------------------------------------------------------------------- */
 fs_status fs_emb_gather(const void* table, int64_t num_rows, int32_t dim, fs_dtype dtype, const int64_t* ids,
                         int64_t T, const uint8_t* mask, uint8_t sel, void* out, int32_t* err,

@@ -6,11 +6,13 @@
 // output buffer) and §2.1 (sequence embeddings, no pooling).
 //
 // Bandwidth layout: the output (T x row bytes) is written once and never
-// re-read here, so it is written with streaming (evict-first) stores; table
-// rows are read through the non-coherent path so that hot (Zipf head) rows
-// stay cached in L1/L2.  A lane moves one 16-byte vector of a row; lanes of a
-// warp cover consecutive vectors, so a 256-byte row is 16 lanes and one warp
-// instruction moves two rows.  Each lane keeps 8 independent vectors in flight.
+// re-read here, so it is written evict-first; table rows are read so that hot
+// (Zipf head) rows stay cached.  Unmasked calls (the whole output is written)
+// go through the copy engine: gather_bulk_kernel below.  Masked calls, which
+// must leave unselected rows untouched, use register loads: a lane moves one
+// 16-byte vector of a row, lanes of a warp cover consecutive vectors (a
+// 256-byte row is 16 lanes, one warp instruction moves two rows) and each
+// lane keeps 8 independent vectors in flight.
 #include "bulk.cuh"
 #include "fs_common.cuh"
 
