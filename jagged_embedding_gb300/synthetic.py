@@ -221,3 +221,20 @@ def grads(w: Workload, T: int, it: int = 0, device="cpu") -> torch.Tensor:
         hi = min(T, lo + rows)
         out[lo:hi] = torch.empty(hi - lo, w.D, dtype=torch.float32, device=device).normal_(0.0, 1.0, generator=g)
     return out
+
+
+def rank_times(uih_len, perm, rank_offsets, speed, beta: float, ns_per_unit: float = 1.0):
+    """Simulated local execution times of the ranks, integer nanoseconds, for
+    driving the VBS AutoTune loop without a trainer: rank r takes
+    speed[r] * sum over its samples of L^beta (times ns_per_unit), rounded.
+    The per-rank speed factors stand for what the L^alpha weights cannot see
+    (slower hosts, stragglers).  A stand-in for the trainer's clock, not part of
+    the method: only its output, the times, is handed to the AutoTune update."""
+    L = torch.as_tensor(uih_len).to("cpu", torch.float64)
+    p = torch.as_tensor(perm).to("cpu", torch.int64)
+    ro = torch.as_tensor(rank_offsets).to("cpu", torch.int64)
+    cost = torch.zeros(p.numel() + 1, dtype=torch.float64)
+    torch.cumsum(L[p] ** beta, 0, out=cost[1:])
+    per_rank = cost[ro[1:]] - cost[ro[:-1]]
+    t = torch.as_tensor(speed, dtype=torch.float64) * per_rank * ns_per_unit
+    return torch.round(t).to(torch.int64).numpy()

@@ -36,6 +36,8 @@ def lib():
         sig = {
             "oracle_balance_fbs": [P, i64, i32, P, P],
             "oracle_balance_vbs": [P, i64, i32, f64, i32, P, P, P],
+            "oracle_vbs_autotune": [P, i32, i64, i32, P],
+            "oracle_balance_vbs_tuned": [P, i64, i32, f64, i32, P, P, P, P],
             "oracle_permute_jagged": [P, P, i64, P, P, P],
             "oracle_keyed_transpose": [P, P, i64, i64, P, P, P],
             "oracle_bucketize_rowwise": [P, i64, P, i32, i64, P, P, P, P],
@@ -92,6 +94,30 @@ def balance_vbs(uih_len, n, alpha, sort_by_len):
     ro = np.empty(n + 1, np.int64)
     sw = np.empty(n, np.uint64)
     _check(lib().oracle_balance_vbs(_p(L), S, n, float(alpha), int(bool(sort_by_len)), _p(perm), _p(ro), _p(sw)))
+    return perm, ro, sw
+
+
+def vbs_autotune(times, delta, step=1, tol_ppm=0):
+    """One AutoTune update: returns the new per-rank batch corrections."""
+    t = _c(times, np.int64)
+    d = _c(delta, np.int64).copy()
+    if d.shape != t.shape:
+        raise OracleError("times and delta differ in length")
+    _check(lib().oracle_vbs_autotune(_p(t), t.shape[0], int(step), int(tol_ppm), _p(d)))
+    return d
+
+
+def balance_vbs_tuned(uih_len, n, alpha, sort_by_len, delta):
+    L = _c(uih_len, np.int32)
+    d = _c(delta, np.int64)
+    if d.shape != (n,):
+        raise OracleError("delta must hold n values")
+    S = L.shape[0]
+    perm = np.empty(S, np.int32)
+    ro = np.empty(n + 1, np.int64)
+    sw = np.empty(n, np.uint64)
+    _check(lib().oracle_balance_vbs_tuned(_p(L), S, n, float(alpha), int(bool(sort_by_len)), _p(d), _p(perm),
+                                          _p(ro), _p(sw)))
     return perm, ro, sw
 
 

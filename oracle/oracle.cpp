@@ -194,6 +194,86 @@ int oracle_balance_vbs(const int32_t* L, int64_t S, int32_t n, double alpha, int
   return 0;
 }
 
+// VBS AutoTune, the update.  FreeScale §4.1, VBS paragraph (and the AutoTune
+// module of Figure 4): because L^alpha need not match the model's real
+// execution time, each rank's local batch size is raised or lowered according
+// to how its local execution time compares with the global average.
+// Readings:
+//  * the tuned quantity is a per-rank correction delta[r] (samples) to the
+//    batch size the weight cut gives; it starts at 0 and persists across
+//    iterations;
+//  * times are integers (e.g. nanoseconds, 0 <= t < 2^53), so the comparison
+//    with the average is exact: rank r is slow when t_r > avg * (1 + tol) and
+//    fast when t_r < avg * (1 - tol), tol = tol_ppm / 10^6 (0 = the plain
+//    comparison), evaluated as n * 10^6 * t_r against (10^6 +- tol_ppm) * sum t;
+//  * the global batch is fixed (the AllGather of Algorithm 1 collects n * B
+//    samples), so decrements and increments come in pairs: with k =
+//    min(#slow, #fast), the k slowest ranks (time descending, lower rank first
+//    on ties) lose `step` samples and the k fastest (time ascending, lower rank
+//    first on ties) gain `step`; the sum of delta does not change.
+int oracle_vbs_autotune(const int64_t* t, int32_t n, int64_t step, int32_t tol_ppm, int64_t* delta) {
+  if (n <= 0 || step < 0 || tol_ppm < 0 || tol_ppm > 1000000) return 1;
+  u128 sum = 0;
+  for (int32_t r = 0; r < n; ++r) {
+    if (t[r] < 0 || t[r] >= (int64_t(1) << 53)) return 1;
+    sum += static_cast<u128>(t[r]);
+  }
+  const u128 scale = static_cast<u128>(n) * 1000000u;
+  const u128 hi = sum * static_cast<u128>(1000000 + tol_ppm);
+  const u128 lo = sum * static_cast<u128>(1000000 - tol_ppm);
+  std::vector<int32_t> slow, fast;
+  for (int32_t r = 0; r < n; ++r) {
+    const u128 x = static_cast<u128>(t[r]) * scale;
+    if (x > hi) slow.push_back(r);
+    if (x < lo) fast.push_back(r);
+  }
+  std::stable_sort(slow.begin(), slow.end(), [&](int32_t a, int32_t b) { return t[a] > t[b]; });
+  std::stable_sort(fast.begin(), fast.end(), [&](int32_t a, int32_t b) { return t[a] < t[b]; });
+  const size_t k = std::min(slow.size(), fast.size());
+  for (size_t i = 0; i < k; ++i) {
+    delta[slow[i]] -= step;
+    delta[fast[i]] += step;
+  }
+  return 0;
+}
+
+// VBS with the AutoTune correction applied.  FreeScale §4.1, VBS paragraph.
+// Steps: (1) the VBS cut above gives the order and the segment ends
+// e_r = rank_offsets[r+1]; (2) rank r's batch changes by delta[r], i.e. every
+// segment end moves by D_r = delta[0] + ... + delta[r], the segments staying
+// contiguous along the same order; (3) a correction larger than a segment can
+// give cannot make a count negative: the moved ends are clamped to [0, S] and
+// then made non-decreasing (each end is the largest of the ends up to it);
+// (4) seg_weight is the weight of the adjusted segments.  Whenever no clamp
+// acts, rank r holds exactly (its cut count + delta[r]) samples.
+// delta must sum to 0 (the global batch is fixed) and |delta[r]| <= S.
+int oracle_balance_vbs_tuned(const int32_t* L, int64_t S, int32_t n, double alpha, int32_t sort_by_len,
+                             const int64_t* delta, int32_t* perm, int64_t* rank_offsets, uint64_t* seg_weight) {
+  if (n <= 0 || S < 0) return 1;
+  int64_t total = 0;
+  for (int32_t r = 0; r < n; ++r) {
+    if (delta[r] > S || delta[r] < -S) return 1;
+    total += delta[r];
+  }
+  if (total != 0) return 1;
+  int rc = oracle_balance_vbs(L, S, n, alpha, sort_by_len, perm, rank_offsets, seg_weight);
+  if (rc != 0) return rc;
+  int64_t D = 0, run_max = 0;
+  for (int32_t r = 0; r < n; ++r) {
+    D += delta[r];
+    int64_t e = rank_offsets[r + 1] + D;
+    e = std::min<int64_t>(std::max<int64_t>(e, 0), S);
+    run_max = std::max(run_max, e);
+    rank_offsets[r + 1] = run_max;
+  }
+  for (int32_t r = 0; r < n; ++r) {
+    uint64_t sw = 0;
+    for (int64_t j = rank_offsets[r]; j < rank_offsets[r + 1]; ++j) sw += oracle_vbs_weight(L[perm[j]], alpha);
+    seg_weight[r] = sw;
+  }
+  return 0;
+}
+
 // ---------------------------------------------------------------------------
 // Jagged sample permutation ("indexed permute").  FreeScale §3.1 Algorithm 1,
 // Stage III (shuffle samples to match the partition) and §4.2: output sample k

@@ -203,3 +203,126 @@ def test_vbs_degenerate_cases():
     # empty
     perm, ro, sw = oracle.balance_vbs(np.zeros(0, np.int32), 3, 1.5, 1)
     assert ro.tolist() == [0, 0, 0, 0]
+
+
+# ------------------------------------------------------------------ VBS AutoTune
+
+_AT = _load("vbs_autotune_hand_examples.json")
+
+
+@pytest.mark.parametrize("case", _AT["update_cases"])
+def test_autotune_update_hand_examples(case):
+    out = oracle.vbs_autotune(np.array(case["t"]), np.array(case["delta_in"]), case["step"], case["tol_ppm"])
+    assert out.tolist() == case["delta_out"]
+
+
+@pytest.mark.parametrize("case", _AT["tuned_cases"])
+def test_vbs_tuned_hand_examples(case):
+    perm, ro, sw = oracle.balance_vbs_tuned(np.array(case["L"]), case["n"], case["alpha"], case["sort_by_len"],
+                                            np.array(case["delta"]))
+    assert perm.tolist() == case["perm"]
+    assert ro.tolist() == case["rank_offsets"]
+    assert sw.tolist() == case["seg_weight"]
+
+
+@pytest.mark.parametrize("case", _AT["bad_tuned_cases"])
+def test_vbs_tuned_rejects_bad_corrections(case):
+    with pytest.raises(oracle.OracleError):
+        oracle.balance_vbs_tuned(np.array(case["L"]), case["n"], 1.0, 0, np.array(case["delta"]))
+
+
+def test_autotune_update_rejects_bad_arguments():
+    for t, step, tol in (([-1, 2], 1, 0), ([1 << 53, 2], 1, 0), ([1, 2], -1, 0), ([1, 2], 1, 1000001),
+                         ([1, 2], 1, -1)):
+        with pytest.raises(oracle.OracleError):
+            oracle.vbs_autotune(np.array(t), np.zeros(2, np.int64), step, tol)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_autotune_update_invariants_random(seed):
+    """What the page's rule fixes whatever the times: the global batch stays
+    put, each rank moves by 0 or one step, only ranks above the average give
+    samples and only ranks below it take them, in equal numbers, and those
+    chosen are the most extreme ones (checked with exact fractions)."""
+    from fractions import Fraction
+    rng = np.random.default_rng(300 + seed)
+    n = int(rng.integers(1, 80))
+    t = rng.integers(0, 1000 if seed % 2 else 10**12, n)
+    if seed == 3:
+        t = rng.integers(5, 8, n)                     # many ties
+    d0 = rng.integers(-50, 50, n)
+    d0[-1] -= d0.sum()
+    step = int(rng.integers(1, 5))
+    tol = [0, 0, 20000, 0, 100000, 0][seed]
+    d1 = oracle.vbs_autotune(t, d0, step, tol)
+    ch = d1 - d0
+    assert d1.sum() == d0.sum()
+    assert set(ch.tolist()) <= {-step, 0, step}
+    mean = Fraction(int(t.sum()), n)
+    slow = [r for r in range(n) if Fraction(int(t[r])) > mean * Fraction(10**6 + tol, 10**6)]
+    fast = [r for r in range(n) if Fraction(int(t[r])) < mean * Fraction(10**6 - tol, 10**6)]
+    lost = [r for r in range(n) if ch[r] < 0]
+    gained = [r for r in range(n) if ch[r] > 0]
+    assert set(lost) <= set(slow) and set(gained) <= set(fast)
+    assert len(lost) == len(gained) == min(len(slow), len(fast))
+    for r in set(slow) - set(lost):      # every slow rank left alone is no slower than those chosen
+        assert all(t[r] < t[q] or (t[r] == t[q] and r > q) for q in lost)
+    for r in set(fast) - set(gained):
+        assert all(t[r] > t[q] or (t[r] == t[q] and r > q) for q in gained)
+
+
+@pytest.mark.parametrize("seed,sort_by_len", [(s, b) for s in range(4) for b in (0, 1)])
+def test_vbs_tuned_invariants_random(seed, sort_by_len):
+    rng = np.random.default_rng(400 + seed)
+    n = int(rng.integers(1, 40))
+    S = int(rng.integers(1, 2000))
+    L = np.clip(np.round(rng.lognormal(6, 1.4, S)), 1, 4096).astype(np.int32)
+    perm0, ro0, _ = oracle.balance_vbs(L, n, 1.5, sort_by_len)
+    # a zero correction is the plain cut
+    perm, ro, sw = oracle.balance_vbs_tuned(L, n, 1.5, sort_by_len, np.zeros(n, np.int64))
+    assert np.array_equal(perm, perm0) and np.array_equal(ro, ro0)
+    # a small correction changes every count by exactly its entry
+    c = np.diff(ro0)
+    d = np.zeros(n, np.int64)
+    for _ in range(3 * n):
+        a, b = rng.integers(0, n, 2)
+        if c[a] + d[a] > 0:
+            d[a] -= 1
+            d[b] += 1
+    perm, ro, sw = oracle.balance_vbs_tuned(L, n, 1.5, sort_by_len, d)
+    assert np.array_equal(perm, perm0)
+    assert np.array_equal(np.diff(ro), c + d)
+    w = np.array([oracle.vbs_weight(int(l), 1.5) for l in L[perm]], dtype=object)
+    assert [int(x) for x in sw] == [int(sum(w[ro[r]:ro[r + 1]])) for r in range(n)]
+    # a large one: contiguous, non-negative counts, every sample once
+    d = rng.integers(-S, S + 1, n)
+    d[-1] = 0
+    d[-1] = -d.sum()
+    if abs(d[-1]) <= S:
+        perm, ro, sw = oracle.balance_vbs_tuned(L, n, 1.5, sort_by_len, d)
+        assert ro[0] == 0 and ro[-1] == S and (np.diff(ro) >= 0).all()
+        assert sum(int(x) for x in sw) == int(sum(w))
+
+
+def test_autotune_balances_heterogeneous_ranks():
+    """The point of AutoTune: when the weights miss a per-rank cost (here four
+    ranks run 1.5x slower), repeated updates move samples off the slow ranks
+    until every rank's time is close to the average."""
+    from jagged_embedding_gb300 import synthetic
+    n, B = 16, 128
+    rng = np.random.default_rng(7)
+    L = np.clip(np.round(rng.lognormal(6, 1.4, n * B)), 1, 4096).astype(np.int32)
+    speed = np.where(np.arange(n) % 4 == 0, 1.5, 1.0)
+    d = np.zeros(n, np.int64)
+
+    def spread(d):
+        perm, ro, _ = oracle.balance_vbs_tuned(L, n, 1.5, 0, d)
+        t = synthetic.rank_times(L, perm, ro, speed, 1.5)
+        return t, t.max() / t.mean()
+
+    t, first = spread(d)
+    for _ in range(120):
+        d = oracle.vbs_autotune(t, d, 1, 0)
+        t, last = spread(d)
+    assert d.sum() == 0 and (d[::4] < 0).all()
+    assert first > 1.3 and last < 1.1
