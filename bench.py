@@ -53,7 +53,9 @@ def algorithmic_bytes(w, S, T, U, R, n_cand=0):
     collision split, per pair                  8 T + 2 T + 3 R / 8 + 16 U
     gather                                     (8 + RB) T + RB U
     backward (segment-reduce + update)         (8 + RB) T + (2 RB + 8) U
-    RB = row bytes; U = unique rows of the batch.
+    VBS AutoTune (when on)                     48 n: times in, corrections read and written,
+                                               corrections read again and segment ends moved by the cut
+    RB = row bytes; U = unique rows of the batch; n = logical ranks.
     """
     RB = w.row_bytes
     b = {
@@ -61,6 +63,8 @@ def algorithmic_bytes(w, S, T, U, R, n_cand=0):
         "collision": 10 * T + 3 * R / 8 + 16 * U,
         "gather": (8 + RB) * T + RB * U,
     }
+    if w.autotune:
+        b["autotune"] = 48 * w.n
     if w.has_update:
         b["backward"] = (8 + RB) * T + (2 * RB + (8 if w.optim == "adagrad" else 0)) * U
     return b
@@ -194,11 +198,15 @@ def oracle_sample(w, steps, max_seconds=20.0, samples_per_rank=None, table_np=No
     g = synthetic.grads(ws_, maxT, 0, gen_dev).cpu()
     G = g.view(torch.int16).numpy().view(np.uint16) if w.dtype == "bf16" else g.numpy()
     ids_done, secs, n_timed = 0, 0.0, 0
-    prep_t = oracle.prepare(ws_, batches[0])
+    delta = np.zeros(w.n, np.int64)
+    times = [synthetic.step_times(ws_, t).numpy() for t in range(steps)] if w.autotune else None
+    prep_t = oracle.prepare(ws_, batches[0], delta)
     for t in range(steps):
         timed = t >= warmup
         t0 = time.perf_counter()
-        prep_n = oracle.prepare(ws_, batches[t + 1])
+        if w.autotune:
+            delta = oracle.vbs_autotune(times[t], delta, w.tune_step, w.tune_tol_ppm)
+        prep_n = oracle.prepare(ws_, batches[t + 1], delta)
         coll = oracle.collision_split(prep_t["ids"], prep_n["ids"], w.R, w.n)
         oracle.emb_gather(table_np, prep_t["ids"])
         if w.has_update:
@@ -221,10 +229,14 @@ def oracle_sample(w, steps, max_seconds=20.0, samples_per_rank=None, table_np=No
 
 def workload_config(w, n_gpus):
     """The workload keys both arms report (the GPU arm adds its measured IDs per step and the L2 note)."""
-    return {"workload": w.name, "n_logical_ranks": w.n, "samples_per_rank": w.B, "rows": w.R, "dim": w.D,
-            "table_dtype": w.dtype, "optimizer": w.optim, "balance": w.balance, "iterations_cycled": w.iters,
-            "schedule": "sync order, collision rows updated before exclusive rows",
-            "parallelism": f"replicas x{n_gpus}"}
+    cfg = {"workload": w.name, "n_logical_ranks": w.n, "samples_per_rank": w.B, "rows": w.R, "dim": w.D,
+           "table_dtype": w.dtype, "optimizer": w.optim, "balance": w.balance, "iterations_cycled": w.iters,
+           "schedule": "sync order, collision rows updated before exclusive rows",
+           "parallelism": f"replicas x{n_gpus}"}
+    if w.autotune:
+        cfg["vbs_autotune"] = {"step": w.tune_step, "tol_ppm": w.tune_tol_ppm,
+                               "times": "seeded per-rank step times, every fourth rank 1.5x slower"}
+    return cfg
 
 
 def run_reference(args):
@@ -281,12 +293,14 @@ def run_gpu(args):
     # gradient rows of the dense model's backward: one N(0,1) pool, batch t uses its first T_t rows
     grads = synthetic.grads(w, max_T, 0, dev) if w.has_update else None
     pipe = Pipeline(w, dev, max_T, table, state)
+    # VBS AutoTune: the per-rank step times each iteration reports (seeded clock readings)
+    times = [synthetic.step_times(w, t, dev) for t in range(w.iters)] if w.autotune else None
     torch.cuda.synchronize()
 
     def step(i, cur):
-        t = i % w.iters
         nb = batches[(i + 1) % w.iters]
-        return pipe.step_sync(cur, nb, grads[: pipe.slots[cur].T] if grads is not None else None)
+        return pipe.step_sync(cur, nb, grads[: pipe.slots[cur].T] if grads is not None else None,
+                              times=times[i % w.iters] if times else None)
 
     cur = 0
     pipe.prepare(batches[0], 0)
@@ -356,7 +370,7 @@ def run_gpu(args):
     # ---- end to end through the public API with host inputs (pinned), copies inside the timed region
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(w, pipe, batches, grads, K, W, dev, ws)
+        e2e = run_e2e(w, pipe, batches, grads, K, W, dev, ws, times)
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -411,13 +425,14 @@ def kernel_hash():
     return h.hexdigest()[:16]
 
 
-def run_e2e(w, pipe, batches, grads, K, W, dev, ws):
+def run_e2e(w, pipe, batches, grads, K, W, dev, ws, times=None):
     """Same steps, inputs copied from pinned host memory inside the timed region.
 
     A copy stream brings batch i+2 while batch i is processed (a ring of three
     device staging buffers); each step reads back the collision counts and the
     error word.  Gradient rows stand for the dense model's output and stay on
-    the device.
+    the device.  With AutoTune on, each step's rank times (8 n bytes) are
+    copied in on the compute stream just before the step uses them.
     """
     import torch
 
@@ -441,7 +456,8 @@ def run_e2e(w, pipe, batches, grads, K, W, dev, ws):
     done = [torch.cuda.Event() for _ in range(3)]
     used = [torch.cuda.Event() for _ in range(3)]
     readback = torch.empty(4, dtype=torch.int64).pin_memory()
-    h2d = []
+    host_times = [x.cpu().pin_memory() for x in times] if times else None
+    times_dev = torch.empty(w.n, dtype=torch.int64, device=dev) if times else None
 
     def stage(i):
         h = host[i % w.iters]
@@ -482,7 +498,10 @@ def run_e2e(w, pipe, batches, grads, K, W, dev, ws):
             main.wait_event(done[(i + 1) % 3])
             total_ids += pipe.slots[cur].T
             gsl = grads[: pipe.slots[cur].T] if grads is not None else None
-            cur = pipe.step_sync(cur, staged[i + 1], gsl)
+            if host_times is not None:
+                times_dev.copy_(host_times[i % w.iters], non_blocking=True)
+                h2d_bytes += 8 * w.n
+            cur = pipe.step_sync(cur, staged[i + 1], gsl, times=times_dev)
             used[(i + 1) % 3].record(main)
             readback[:3].copy_(pipe.coll["counts"], non_blocking=True)
             readback[3:4].copy_(pipe.err.to(torch.int64), non_blocking=True)

@@ -6,9 +6,10 @@
  * Models with Minimal Scaling Cost", arXiv 2604.24073) over n logical ranks
  * held in one GPU's memory:
  *
- *   balance (FBS or VBS, §4.1)  ->  jagged sample permutation (Algorithm 1,
- *   Stage III; §4.2 indexed permute)  ->  row-wise bucketize into shard-major
- *   form (§3.2, Algorithm 2 line 8; §4.2 ranged dispatch)  ->  collision /
+ *   balance (FBS, or VBS with optional AutoTune, §4.1)  ->  jagged sample
+ *   permutation (Algorithm 1, Stage III; §4.2 indexed permute)  ->  row-wise
+ *   bucketize into shard-major form (§3.2, Algorithm 2 line 8; §4.2 ranged
+ *   dispatch)  ->  collision /
  *   exclusive split between iterations t and t+1 (Algorithm 2 line 10)  ->
  *   embedding gather into batch-major jagged output (Algorithm 2 lines 12
  *   and 15; ranged combine)  ->  gradient segment-reduce + row update
@@ -123,6 +124,41 @@ size_t fs_balance_vbs_workspace_size(int64_t S, int32_t n);
 fs_status fs_balance_vbs(const int32_t* uih_len, int64_t S, int32_t n, double alpha, int32_t sort_by_len,
                          int32_t* perm, int64_t* rank_offsets, uint64_t* seg_weight, int32_t* err, void* ws,
                          size_t ws_bytes, fs_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * VBS AutoTune -- FreeScale §4.1, VBS paragraph, and the AutoTune module of
+ * Figure 4: since L^alpha need not match the model's execution time, each
+ * rank's local batch size is raised or lowered by how its local execution
+ * time compares with the global average.
+ *
+ * fs_vbs_autotune: one update of the per-rank batch corrections.
+ *   times       [n] int64 in: the ranks' local execution times of the last
+ *                   iteration, integer units (e.g. ns), 0 <= t < 2^53
+ *   batch_delta [n] int64 in/out: the corrections (samples), 0 at the start
+ *   step        samples one adjustment moves, 0 <= step <= 2^31 - 1
+ *   tol_ppm     dead band in parts per million of the average, [0, 10^6]
+ * Rank r is slow when n * 10^6 * t_r > (10^6 + tol_ppm) * sum(t) and fast when
+ * n * 10^6 * t_r < (10^6 - tol_ppm) * sum(t) (exact integers).  The global
+ * batch is fixed, so with k = min(#slow, #fast) the k slowest ranks (time
+ * descending, lower rank first on ties) lose `step` and the k fastest (time
+ * ascending, lower rank first) gain `step`: sum(batch_delta) is unchanged.
+ * 1 <= n <= 65536 (O(n^2) comparisons spread over the GPU).  A time outside
+ * [0, 2^53) sets FS_ERR_INVALID_ARG in *err and leaves batch_delta as it was.
+ *
+ * fs_balance_vbs_tuned: fs_balance_vbs with a correction applied.  The cut's
+ * segment ends e_r = rank_offsets[r+1] move by D_r = batch_delta[0] + ... +
+ * batch_delta[r], are clamped to [0, S] and then made non-decreasing (each
+ * end becomes the largest end up to it); perm is the cut's, seg_weight that of
+ * the moved segments.  Where no clamp acts, rank r holds its cut count plus
+ * batch_delta[r] samples.  batch_delta [n] (device) must sum to 0 with
+ * |batch_delta[r]| <= S, else FS_ERR_INVALID_ARG in *err and the cut is left
+ * unmoved.  Workspace: fs_balance_vbs_workspace_size(S, n).
+ * ---------------------------------------------------------------------- */
+fs_status fs_vbs_autotune(const int64_t* times, int32_t n, int64_t step, int32_t tol_ppm, int64_t* batch_delta,
+                          int32_t* err, fs_stream_t stream);
+fs_status fs_balance_vbs_tuned(const int32_t* uih_len, int64_t S, int32_t n, double alpha, int32_t sort_by_len,
+                               const int64_t* batch_delta, int32_t* perm, int64_t* rank_offsets,
+                               uint64_t* seg_weight, int32_t* err, void* ws, size_t ws_bytes, fs_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * Jagged sample permutation ("indexed permute") -- FreeScale Algorithm 1

@@ -31,7 +31,7 @@ STATUS = {0: "ok", 1: "invalid argument", 2: "ID outside [0, num_rows)", 3: "mal
 
 EXPORTS = [
     "fs_balance_fbs_workspace_size", "fs_balance_fbs", "fs_balance_fbs_noalloc", "fs_balance_vbs_workspace_size",
-    "fs_balance_vbs",
+    "fs_balance_vbs", "fs_balance_vbs_tuned", "fs_vbs_autotune",
     "fs_permute_jagged_workspace_size", "fs_permute_jagged", "fs_keyed_transpose_workspace_size",
     "fs_keyed_transpose", "fs_bucketize_rowwise_workspace_size",
     "fs_bucketize_rowwise", "fs_collision_split_workspace_size", "fs_collision_split", "fs_row_bitmap_words",
@@ -65,6 +65,8 @@ def lib():
         "fs_balance_fbs_noalloc": ([P, i64, i32, P, P, P, P], C.c_int),
         "fs_balance_vbs_workspace_size": ([i64, i32], sz),
         "fs_balance_vbs": ([P, i64, i32, f64, i32, P, P, P, P, P, sz, P], C.c_int),
+        "fs_balance_vbs_tuned": ([P, i64, i32, f64, i32, P, P, P, P, P, P, sz, P], C.c_int),
+        "fs_vbs_autotune": ([P, i32, i64, i32, P, P, P], C.c_int),
         "fs_permute_jagged_workspace_size": ([i64], sz),
         "fs_permute_jagged": ([P, P, i64, P, P, P, i64, P, i32, P, P, P, sz, P], C.c_int),
         "fs_keyed_transpose_workspace_size": ([i64, i64], sz),
@@ -204,6 +206,37 @@ def fs_balance_vbs(uih_len, n, alpha, sort_by_len, perm=None, rank_offsets=None,
                              _ptr(rank_offsets), _ptr(seg_weight), _ptr(err), _ptr(ws), ws.numel(), _stream(dev)),
         "fs_balance_vbs")
     return perm, rank_offsets, seg_weight, err
+
+
+def fs_balance_vbs_tuned(uih_len, n, alpha, sort_by_len, batch_delta, perm=None, rank_offsets=None, seg_weight=None,
+                         err=None, ws=None):
+    """VBS cut with the AutoTune correction batch_delta [n] (int64, device) applied to its segment ends."""
+    dev = uih_len.device
+    _need(uih_len, torch.int32, "uih_len")
+    _need(batch_delta, torch.int64, "batch_delta", n)
+    S = uih_len.numel()
+    perm = torch.empty(S, dtype=torch.int32, device=dev) if perm is None else perm
+    rank_offsets = torch.empty(n + 1, dtype=torch.int64, device=dev) if rank_offsets is None else rank_offsets
+    seg_weight = torch.empty(n, dtype=torch.int64, device=dev) if seg_weight is None else seg_weight
+    err = new_err(dev) if err is None else err
+    need = lib().fs_balance_vbs_workspace_size(S, n)
+    ws = workspace(need, dev) if ws is None else ws
+    _ok(lib().fs_balance_vbs_tuned(_ptr(uih_len), S, n, float(alpha), int(bool(sort_by_len)), _ptr(batch_delta),
+                                   _ptr(perm), _ptr(rank_offsets), _ptr(seg_weight), _ptr(err), _ptr(ws), ws.numel(),
+                                   _stream(dev)), "fs_balance_vbs_tuned")
+    return perm, rank_offsets, seg_weight, err
+
+
+def fs_vbs_autotune(times, batch_delta, step=1, tol_ppm=0, err=None):
+    """One AutoTune update of batch_delta [n] (int64, device, in place) from the ranks' times [n] (int64, device)."""
+    dev = times.device
+    n = times.numel()
+    _need(times, torch.int64, "times")
+    _need(batch_delta, torch.int64, "batch_delta", n)
+    err = new_err(dev) if err is None else err
+    _ok(lib().fs_vbs_autotune(_ptr(times), n, int(step), int(tol_ppm), _ptr(batch_delta), _ptr(err), _stream(dev)),
+        "fs_vbs_autotune")
+    return batch_delta, err
 
 
 # ------------------------------------------------------------------ jagged ids

@@ -10,6 +10,9 @@ op is one of
   bucketize -- fs_bucketize_rowwise of the same IDs into 256 row-range shards
   transpose -- fs_keyed_transpose of about T IDs in R features x 65536 samples (lengths uniform, per-feature
                row bases); prints the time per call and the bandwidth of its algorithmic bytes
+  autotune  -- VBS AutoTune with T samples over R logical ranks (lognormal(7, 1.6) lengths up to 16384,
+               alpha 1.5, length-sorted cut): fs_vbs_autotune, fs_balance_vbs_tuned and the plain
+               fs_balance_vbs, each timed alone (median of reps calls, CUDA events)
 Inputs come from jagged_embedding_gb300.synthetic; every call goes through the C ABI.
 Exits non-zero if a call reports an error.
 """
@@ -27,7 +30,8 @@ SHARDS = 256
 
 
 def main(argv) -> int:
-    if len(argv) < 3 or argv[0] not in ("gather", "backward", "backward-bf16", "bucketize", "transpose"):
+    if len(argv) < 3 or argv[0] not in ("gather", "backward", "backward-bf16", "bucketize", "transpose",
+                                        "autotune"):
         print(__doc__)
         return 2
     op, T, R = argv[0], int(argv[1]), int(argv[2])
@@ -38,6 +42,8 @@ def main(argv) -> int:
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     if op == "transpose":
         return _transpose(T, R, reps, dev, g, err)
+    if op == "autotune":
+        return _autotune(T, R, reps, dev, g, err)
     ids = synthetic.zipf_rows(R, 1.0, T, g, dev)
     if op == "gather":
         table = torch.empty(R, DIM, device=dev).normal_(0, 0.01, generator=g)
@@ -88,6 +94,43 @@ def _transpose(T, F, reps, dev, g, err):
     B.check(err, "transpose")
     byts = 16 * n + 16 * (F * Bs + 1) + 8 * F
     print(f"transpose F={F} B={Bs} IDs={n}: {best:.3f} ms, {byts / best / 1e6:.0f} GB/s of algorithmic bytes")
+    return 0
+
+
+def _median_ms(fn, reps):
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    fn()
+    for a, b in ev:
+        a.record()
+        fn()
+        b.record()
+    torch.cuda.synchronize()
+    ms = sorted(a.elapsed_time(b) for a, b in ev)
+    return ms[len(ms) // 2]
+
+
+def _autotune(S, n, reps, dev, g, err):
+    reps = max(reps, 5)
+    L = torch.empty(S, dtype=torch.float64, device=dev).log_normal_(7.0, 1.6, generator=g)
+    L = L.round().clamp_(1, 16384).to(torch.int32)
+    times = (torch.rand(n, dtype=torch.float64, device=dev, generator=g) * 1e7 + 1e7).to(torch.int64)
+    delta = torch.zeros(n, dtype=torch.int64, device=dev)
+    perm = torch.empty(S, dtype=torch.int32, device=dev)
+    ro = torch.empty(n + 1, dtype=torch.int64, device=dev)
+    sw = torch.empty(n, dtype=torch.int64, device=dev)
+    ws = B.workspace(B.lib().fs_balance_vbs_workspace_size(S, n), dev)
+    # a few updates first, so that the timed cut moves real corrections (step 0 keeps them fixed while timing)
+    for _ in range(8):
+        B.fs_vbs_autotune(times, delta, 1, 0, err=err)
+    t_upd = _median_ms(lambda: B.fs_vbs_autotune(times, delta, 0, 0, err=err), reps)
+    t_tuned = _median_ms(lambda: B.fs_balance_vbs_tuned(L, n, 1.5, 1, delta, perm=perm, rank_offsets=ro,
+                                                         seg_weight=sw, err=err, ws=ws), reps)
+    t_plain = _median_ms(lambda: B.fs_balance_vbs(L, n, 1.5, 1, perm=perm, rank_offsets=ro, seg_weight=sw,
+                                                  err=err, ws=ws), reps)
+    torch.cuda.synchronize()
+    B.check(err, "autotune")
+    print(f"autotune S={S} n={n}: update {1000 * t_upd:.1f} us, tuned VBS cut {1000 * t_tuned:.1f} us, "
+          f"plain VBS cut {1000 * t_plain:.1f} us (median of {reps})")
     return 0
 
 

@@ -175,6 +175,147 @@ __global__ void vbs_segment_weight_kernel(const uint64_t* P, const int64_t* rank
     seg_weight[r] = P[rank_offsets[r + 1]] - P[rank_offsets[r]];
 }
 
+// ------------------------------------------------------------ VBS AutoTune
+
+constexpr int kTuneThreads = 256;
+constexpr int32_t kTuneMaxRanks = 65536;
+constexpr int64_t kTimeLimit = int64_t(1) << 53;
+
+// One AutoTune update (FreeScale §4.1, VBS paragraph; Figure 4's AutoTune
+// module): ranks slower than the average by more than the dead band give
+// `step` samples, ranks faster than it take `step`, paired so that the global
+// batch stays fixed: with k = min(#slow, #fast), the k slowest and the k
+// fastest ranks move.  Every block reduces all n times itself (integer sums:
+// the same in every block), then each thread decides for one rank.  A rank's
+// place among the slow ones is the number of ranks with a larger time plus the
+// number of lower ranks with the same time (anything slower than a slow rank
+// is slow too); the fast side is the mirror image.  O(n^2 / threads) work,
+// n <= 65536.
+__global__ void __launch_bounds__(kTuneThreads) vbs_autotune_kernel(const int64_t* t, int32_t n, int64_t step,
+                                                                    int32_t tol_ppm, int64_t* delta, int32_t* err) {
+  __shared__ uint64_t part[kTuneThreads];
+  __shared__ int counts[2];
+  __shared__ unsigned __int128 sum_s;
+  if (threadIdx.x < 2) counts[threadIdx.x] = 0;
+  uint64_t acc = 0;  // < (n / threads) * 2^53 <= 2^61 per thread
+  bool bad = false;
+  for (int32_t q = threadIdx.x; q < n; q += kTuneThreads) {
+    const int64_t x = t[q];
+    bad |= (x < 0) || (x >= kTimeLimit);
+    acc += static_cast<uint64_t>(x);
+  }
+  part[threadIdx.x] = acc;
+  if (__syncthreads_or(bad)) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) set_err(err, FS_ERR_INVALID_ARG);
+    return;
+  }
+  if (threadIdx.x == 0) {
+    unsigned __int128 s = 0;
+    for (int i = 0; i < kTuneThreads; ++i) s += part[i];
+    sum_s = s;
+  }
+  __syncthreads();
+  const unsigned __int128 sum = sum_s;
+  const unsigned __int128 scale = static_cast<unsigned __int128>(n) * 1000000u;
+  const unsigned __int128 hi = sum * static_cast<unsigned __int128>(1000000 + tol_ppm);
+  const unsigned __int128 lo = sum * static_cast<unsigned __int128>(1000000 - tol_ppm);
+  int my_slow = 0, my_fast = 0;
+  for (int32_t q = threadIdx.x; q < n; q += kTuneThreads) {
+    const unsigned __int128 x = static_cast<unsigned __int128>(t[q]) * scale;
+    my_slow += x > hi;
+    my_fast += x < lo;
+  }
+  if (my_slow) atomicAdd(&counts[0], my_slow);
+  if (my_fast) atomicAdd(&counts[1], my_fast);
+  __syncthreads();
+  const int k = min(counts[0], counts[1]);
+  const int32_t r = blockIdx.x * kTuneThreads + threadIdx.x;
+  if (r >= n || k == 0) return;
+  const int64_t tr = t[r];
+  const unsigned __int128 xr = static_cast<unsigned __int128>(tr) * scale;
+  const bool slow = xr > hi, fast = xr < lo;
+  if (!slow && !fast) return;
+  int place = 0;
+  for (int32_t q = 0; q < n; ++q) {
+    const int64_t tq = t[q];
+    place += (slow ? tq > tr : tq < tr) || (tq == tr && q < r);
+  }
+  if (place < k) delta[r] += slow ? -step : step;
+}
+
+// Inclusive max-scan of one value per thread over a block (blockDim.x <= 1024,
+// a multiple of 32); `smem` needs 32 slots.
+__device__ __forceinline__ int64_t block_inclusive_max(int64_t v, int64_t* smem) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int64_t x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int64_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x = max(x, y);
+  }
+  if (lane == 31) smem[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int64_t w = (lane < nw) ? smem[lane] : INT64_MIN;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int64_t y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w = max(w, y);
+    }
+    smem[lane] = w;
+  }
+  __syncthreads();
+  const int64_t res = (warp == 0) ? x : max(x, smem[warp - 1]);
+  __syncthreads();
+  return res;
+}
+
+constexpr int kAdjustThreads = 1024;
+
+// Apply the AutoTune correction to the VBS cut, one block: segment end r
+// moves by D_r = delta[0] + ... + delta[r], is clamped to [0, S], then the ends
+// are made non-decreasing (prefix maximum).  The correction must sum to 0 with
+// |delta[r]| <= S; otherwise FS_ERR_INVALID_ARG and the cut is left as it was.
+__global__ void __launch_bounds__(kAdjustThreads) vbs_adjust_kernel(int64_t* rank_offsets, const int64_t* delta,
+                                                                    int32_t n, int64_t S, int32_t* err) {
+  __shared__ int64_t smem[32];
+  __shared__ unsigned long long total;
+  if (threadIdx.x == 0) total = 0;
+  __syncthreads();
+  bool bad = false;
+  int64_t part = 0;  // |part| <= (n / threads) * S < 2^62
+  for (int32_t r = threadIdx.x; r < n; r += kAdjustThreads) {
+    const int64_t d = delta[r];
+    if (d > S || d < -S)
+      bad = true;
+    else
+      part += d;
+  }
+  atomicAdd(&total, static_cast<unsigned long long>(part));  // two's-complement sum
+  bad = __syncthreads_or(bad);
+  if (bad || static_cast<int64_t>(total) != 0) {
+    if (threadIdx.x == 0) set_err(err, FS_ERR_INVALID_ARG);
+    return;
+  }
+  int64_t carry = 0, run_max = 0;
+  for (int32_t c0 = 0; c0 < n; c0 += kAdjustThreads) {
+    const int32_t r = c0 + threadIdx.x;
+    const int64_t d = r < n ? delta[r] : 0;
+    int64_t chunk_sum;
+    const int64_t D = carry + block_exclusive_scan<int64_t>(d, smem, &chunk_sum) + d;
+    int64_t e = 0;
+    if (r < n) e = min(max(rank_offsets[r + 1] + D, int64_t(0)), S);
+    e = max(block_inclusive_max(e, smem), run_max);
+    if (r < n) rank_offsets[r + 1] = e;
+    carry += chunk_sum;
+    // the chunk's last end is the running maximum for the next chunk
+    if (threadIdx.x == kAdjustThreads - 1) smem[0] = e;
+    __syncthreads();
+    run_max = smem[0];
+    __syncthreads();
+  }
+}
+
 __global__ void fill_i64_kernel(int64_t* p, int64_t count, int64_t v) {
   for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < count; i += int64_t(gridDim.x) * blockDim.x)
     p[i] = v;
@@ -297,19 +438,26 @@ extern "C" size_t fs_balance_vbs_workspace_size(int64_t S, int32_t n) {
   return fs_balance_fbs_workspace_size(S, n) + vbs_extra_bytes(S) + 256;
 }
 
-extern "C" fs_status fs_balance_vbs(const int32_t* uih_len, int64_t S, int32_t n, double alpha, int32_t sort_by_len,
-                                    int32_t* perm, int64_t* rank_offsets, uint64_t* seg_weight, int32_t* err,
-                                    void* ws, size_t ws_bytes, fs_stream_t stream) {
+namespace fs {
+namespace {
+
+// The VBS cut; with batch_delta != nullptr the AutoTune correction is applied
+// to the segment ends before the segment weights are taken.
+fs_status vbs_run(const int32_t* uih_len, int64_t S, int32_t n, double alpha, int32_t sort_by_len,
+                  const int64_t* batch_delta, int32_t* perm, int64_t* rank_offsets, uint64_t* seg_weight,
+                  int32_t* err, void* ws, size_t ws_bytes, fs_stream_t stream) {
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (n < 1 || S < 0 || S > INT32_MAX || !rank_offsets || !err || !seg_weight || !(alpha >= 0.0))
     return FS_ERR_INVALID_ARG;
   if (S > 0 && (!uih_len || !perm)) return FS_ERR_INVALID_ARG;
   if (!aligned(rank_offsets, 8) || !aligned(seg_weight, 8) || !aligned(err, 4)) return FS_ERR_ALIGNMENT;
   if (ws_bytes < fs_balance_vbs_workspace_size(S, n) || (S > 0 && !ws)) return FS_ERR_WORKSPACE;
+  if (batch_delta && !aligned(batch_delta, 8)) return FS_ERR_ALIGNMENT;
   if (S == 0) {
-    fill_i64_kernel<<<1, kThreads, 0, st>>>(rank_offsets, int64_t(n) + 1, 0);
-    fill_i64_kernel<<<1, kThreads, 0, st>>>(reinterpret_cast<int64_t*>(seg_weight), n, 0);
-    count_launch(2);
+    fill_i64_kernel<<<grid_for(int64_t(n) + 1), kThreads, 0, st>>>(rank_offsets, int64_t(n) + 1, 0);
+    fill_i64_kernel<<<grid_for(n), kThreads, 0, st>>>(reinterpret_cast<int64_t*>(seg_weight), n, 0);
+    if (batch_delta) vbs_adjust_kernel<<<1, kAdjustThreads, 0, st>>>(rank_offsets, batch_delta, n, S, err);
+    count_launch(batch_delta ? 3 : 2);
     return launch_status();
   }
   int launches = 0;
@@ -335,7 +483,43 @@ extern "C" fs_status fs_balance_vbs(const int32_t* uih_len, int64_t S, int32_t n
   vbs_scan_kernel<<<unsigned(vtiles), kThreads, 0, st>>>(uih_len, order, S, alpha, P, vstatus, vcounter, err,
                                                          spin_limit(), debug_skip_tile());
   vbs_assign_kernel<<<grid_for(S), kThreads, 0, st>>>(order, P, S, n, perm, rank_offsets);
+  if (batch_delta) {
+    vbs_adjust_kernel<<<1, kAdjustThreads, 0, st>>>(rank_offsets, batch_delta, n, S, err);
+    ++launches;
+  }
   vbs_segment_weight_kernel<<<grid_for(n), kThreads, 0, st>>>(P, rank_offsets, n, seg_weight);
   count_launch(launches + 3);
+  return launch_status();
+}
+
+}  // namespace
+}  // namespace fs
+
+extern "C" fs_status fs_balance_vbs(const int32_t* uih_len, int64_t S, int32_t n, double alpha, int32_t sort_by_len,
+                                    int32_t* perm, int64_t* rank_offsets, uint64_t* seg_weight, int32_t* err,
+                                    void* ws, size_t ws_bytes, fs_stream_t stream) {
+  return vbs_run(uih_len, S, n, alpha, sort_by_len, nullptr, perm, rank_offsets, seg_weight, err, ws, ws_bytes,
+                 stream);
+}
+
+extern "C" fs_status fs_balance_vbs_tuned(const int32_t* uih_len, int64_t S, int32_t n, double alpha,
+                                          int32_t sort_by_len, const int64_t* batch_delta, int32_t* perm,
+                                          int64_t* rank_offsets, uint64_t* seg_weight, int32_t* err, void* ws,
+                                          size_t ws_bytes, fs_stream_t stream) {
+  if (!batch_delta) return FS_ERR_INVALID_ARG;
+  return vbs_run(uih_len, S, n, alpha, sort_by_len, batch_delta, perm, rank_offsets, seg_weight, err, ws, ws_bytes,
+                 stream);
+}
+
+extern "C" fs_status fs_vbs_autotune(const int64_t* times, int32_t n, int64_t step, int32_t tol_ppm,
+                                     int64_t* batch_delta, int32_t* err, fs_stream_t stream) {
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (n < 1 || n > kTuneMaxRanks || step < 0 || step > INT32_MAX || tol_ppm < 0 || tol_ppm > 1000000)
+    return FS_ERR_INVALID_ARG;
+  if (!times || !batch_delta || !err) return FS_ERR_INVALID_ARG;
+  if (!aligned(times, 8) || !aligned(batch_delta, 8) || !aligned(err, 4)) return FS_ERR_ALIGNMENT;
+  const unsigned blocks = unsigned((n + kTuneThreads - 1) / kTuneThreads);
+  vbs_autotune_kernel<<<blocks, kTuneThreads, 0, st>>>(times, n, step, tol_ppm, batch_delta, err);
+  count_launch(1);
   return launch_status();
 }

@@ -72,6 +72,8 @@ class Pipeline:
         if two_outputs:
             self.out.append(torch.empty(self.max_T, w.D, dtype=table.dtype, device=dev))
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        # VBS AutoTune: per-rank batch-size corrections, carried across iterations
+        self.batch_delta = torch.zeros(w.n, dtype=torch.int64, device=dev) if w.autotune else None
         L = B.lib()
         ws_bytes = max(
             L.fs_balance_vbs_workspace_size(self.max_S, w.n),
@@ -91,6 +93,9 @@ class Pipeline:
         w, s = self.w, self.slots[slot]
         if w.balance == "fbs":
             B.fs_balance_fbs(batch["uih_len"], w.n, perm=s.perm, rank_offsets=s.rank_offsets, err=self.err, ws=self.ws)
+        elif w.autotune:
+            B.fs_balance_vbs_tuned(batch["uih_len"], w.n, w.alpha, w.sort_by_len, self.batch_delta, perm=s.perm,
+                                   rank_offsets=s.rank_offsets, seg_weight=s.seg_weight, err=self.err, ws=self.ws)
         else:
             B.fs_balance_vbs(batch["uih_len"], w.n, w.alpha, w.sort_by_len, perm=s.perm, rank_offsets=s.rank_offsets,
                              seg_weight=s.seg_weight, err=self.err, ws=self.ws)
@@ -106,6 +111,12 @@ class Pipeline:
                                shard_offsets=s.shard_offsets, err=self.err, ws=self.ws, T=T)
         B.fs_row_bitmap(s.ids, w.R, bitmap=s.bitmap, err=self.err, T=T)
         s.T = T
+
+    def autotune(self, times):
+        """VBS AutoTune (FreeScale §4.1): fold the ranks' latest step times [n] (int64 ns, device)
+        into the batch-size corrections that the next prepared batch's cut takes."""
+        w = self.w
+        B.fs_vbs_autotune(times, self.batch_delta, step=w.tune_step, tol_ppm=w.tune_tol_ppm, err=self.err)
 
     def collision(self, slot_t, slot_next, want_t_mask=True, want_next_mask=True):
         """Collision / exclusive split of (t, t+1) (Algorithm 2 line 10); masks are batch-major.
@@ -135,16 +146,20 @@ class Pipeline:
                                   err=self.err, ws=self.ws, T=s.T, co_rows=co_rows)
 
     # -------------------------------------------------------------- orders
-    def step_sync(self, cur, nxt_batch, grads, has_next=True, want_masks=False):
+    def step_sync(self, cur, nxt_batch, grads, has_next=True, want_masks=False, times=None):
         """One iteration in the synchronous order; slot `cur` holds iteration t already prepared.
 
         The update takes its collision flags from the mask of t (one pass over the
         IDs; reading t+1's row bitmap inside the sort passes instead was measured
-        slower).  want_masks also writes the mask of t+1.
+        slower).  want_masks also writes the mask of t+1.  With AutoTune on,
+        `times` (the ranks' latest step times) is folded into the corrections
+        before t+1 is prepared.
         Returns the slot that now holds t+1.
         """
         nxt = 1 - cur
         if has_next:
+            if times is not None and self.w.autotune:
+                self.autotune(times)
             self.prepare(nxt_batch, nxt)
             self.collision(cur, nxt, want_t_mask=True, want_next_mask=want_masks)
         self.gather(cur)
@@ -156,8 +171,9 @@ class Pipeline:
                 self.backward(cur, grads, B.PHASE_ALL)
         return nxt
 
-    def run_prioritized(self, batches, grads_list, on_output=None):
-        """Algorithm 2 order over len(batches) iterations.  on_output(t, out_tensor) sees each batch's output."""
+    def run_prioritized(self, batches, grads_list, on_output=None, times_list=None):
+        """Algorithm 2 order over len(batches) iterations.  on_output(t, out_tensor) sees each batch's output;
+        with AutoTune on, times_list[t] is folded in before t+1 is prepared (as in step_sync)."""
         K = len(batches)
         assert len(self.out) == 2
         self.prepare(batches[0], 0)
@@ -169,6 +185,8 @@ class Pipeline:
                 self.backward(pending_ex[0], pending_ex[1], B.PHASE_EXCLUSIVE)
                 pending_ex = None
             if t + 1 < K:                                                # lines 8-12
+                if times_list is not None and self.w.autotune:
+                    self.autotune(times_list[t])
                 self.prepare(batches[t + 1], nxt)
                 self.collision(cur, nxt)
                 self.gather(nxt, out_idx=nxt, mask=self.masks[nxt], sel=0)

@@ -20,7 +20,10 @@ plus candidates, §5.2 for synthetic embedding workloads):
   A = 0x9E3779B97F4A7C15 mod R (bumped until gcd(A, R) = 1) so that hot rows
   spread over the row-range shards instead of piling into shard 0;
 * table rows ~ N(0, 0.01^2) (std 0.01), stored fp32 or bf16 (RNE cast);
-* gradients ~ N(0, 1) in the table dtype.
+* gradients ~ N(0, 1) in the table dtype;
+* with VBS AutoTune on, the ranks' step times are simulated clock readings
+  (step_times, rank_times below): seeded integers, never computed from the
+  method's own arithmetic.
 
 Seeds: a batch of workload w at iteration i uses seed w.seed_base + i; the
 table uses w.seed_base + 500; gradients w.seed_base + 600 + i.  torch
@@ -62,6 +65,9 @@ class Workload:
     seed_base: int
     kmin: int = 1     # IDs per candidate, uniform in [kmin, kmax] (composite when kmax > 1)
     kmax: int = 1
+    autotune: bool = False  # VBS AutoTune: per-rank batch corrections from the ranks' step times
+    tune_step: int = 1      # samples one AutoTune adjustment moves
+    tune_tol_ppm: int = 0   # AutoTune dead band, parts per million of the average time
 
     @property
     def S(self) -> int:
@@ -103,6 +109,10 @@ WORKLOADS = {
     # 16 ranks x 64 samples whose candidates carry 1..16 IDs each, FBS, 1M x 64 fp32, SGD over 2 iterations.
     "composite-cand": Workload("composite-cand", 16, 64, 5.0, 1.2, 2048, 1, 8, 1_000_000, 64, "f32",
                                1.1, "fbs", 1.5, False, 2, "sgd", 0.01, 0.0, 5000, 1, 16),
+    # the long-sequence index workload with VBS AutoTune on: every step reports per-rank times
+    # (every fourth rank 1.5x slower) and the next batch's cut takes the corrected batch sizes.
+    "long-seq-autotune": Workload("long-seq-autotune", 512, 64, 7.0, 1.6, 16384, 0, 0, 50_000_000, 128, "bf16",
+                                  1.05, "vbs", 1.5, True, 3, "none", 0.0, 0.0, 6000, autotune=True),
 }
 
 
@@ -221,6 +231,22 @@ def grads(w: Workload, T: int, it: int = 0, device="cpu") -> torch.Tensor:
         hi = min(T, lo + rows)
         out[lo:hi] = torch.empty(hi - lo, w.D, dtype=torch.float32, device=device).normal_(0.0, 1.0, generator=g)
     return out
+
+
+def rank_speed(n: int):
+    """Per-rank slowdown of the simulated clocks: every fourth rank runs 1.5x slower."""
+    return [1.5 if r % 4 == 0 else 1.0 for r in range(n)]
+
+
+def step_times(w: Workload, it: int, device="cpu") -> torch.Tensor:
+    """Seeded per-rank step times [n] (int64 ns) reported after iteration `it`:
+    rank_speed(r) * 10 ms * (1 + 0.02 * N(0, 1)).  They do not depend on the
+    cut, so every benchmarked step does the same work; the feedback loop itself
+    (times that follow the cut) is what rank_times below drives."""
+    g = _gen(w.seed_base + 700 + it, "cpu")
+    jitter = torch.randn(w.n, generator=g, dtype=torch.float64)
+    t = torch.tensor(rank_speed(w.n), dtype=torch.float64) * 1.0e7 * (1.0 + 0.02 * jitter)
+    return torch.round(t).clamp_(min=0).to(torch.int64).to(device)
 
 
 def rank_times(uih_len, perm, rank_offsets, speed, beta: float, ns_per_unit: float = 1.0):

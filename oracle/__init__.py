@@ -238,15 +238,18 @@ def double_to_bf16(x):
 
 # --------------------------------------------------------------- one iteration
 
-def prepare(w, b):
+def prepare(w, b, delta=None):
     """Balance, permute and bucketize one batch (FreeScale Algorithm 1, Algorithm 2 line 8).
 
     w: a synthetic.Workload; b: a batch dict of numpy arrays (uih_len, offsets, ids; with composite
-    candidates also cand_offsets, cand_lens).
+    candidates also cand_offsets, cand_lens); delta: the VBS AutoTune corrections, when w.autotune.
     """
     if w.balance == "fbs":
         perm, ro = balance_fbs(b["uih_len"], w.n)
         sw = None
+    elif w.autotune:
+        perm, ro, sw = balance_vbs_tuned(b["uih_len"], w.n, w.alpha, w.sort_by_len,
+                                         np.zeros(w.n, np.int64) if delta is None else delta)
     else:
         perm, ro, sw = balance_vbs(b["uih_len"], w.n, w.alpha, w.sort_by_len)
     off2, ids2 = permute_jagged(b["offsets"], b["ids"], perm)
@@ -260,14 +263,26 @@ def prepare(w, b):
     return res
 
 
-def run_sync(w, batches, table, state, grads_list):
+def _prepare_all(w, batches, times_list):
+    """Prepare every batch; with AutoTune on, the times reported in iteration t
+    update the corrections before batch t+1 is cut (FreeScale §4.1)."""
+    delta = np.zeros(w.n, np.int64)
+    preps = []
+    for t, b in enumerate(batches):
+        if t > 0 and w.autotune and times_list is not None:
+            delta = vbs_autotune(times_list[t - 1], delta, w.tune_step, w.tune_tol_ppm)
+        preps.append(prepare(w, b, delta))
+    return preps
+
+
+def run_sync(w, batches, table, state, grads_list, times_list=None):
     """Synchronous schedule: for each iteration t, out_t = gather(W, I_t), then W <- update(W, G_t, I_t).
 
     Collision rows of t (rows shared with t+1) are updated before exclusive rows
     (same result: the two row sets are disjoint).  Returns per-iteration dicts
     and updates table/state in place.
     """
-    preps = [prepare(w, b) for b in batches]
+    preps = _prepare_all(w, batches, times_list)
     res = []
     for t, pr in enumerate(preps):
         out = emb_gather(table, pr["ids"])
@@ -286,7 +301,7 @@ def run_sync(w, batches, table, state, grads_list):
     return res
 
 
-def run_prioritized(w, batches, table, state, grads_list):
+def run_prioritized(w, batches, table, state, grads_list, times_list=None):
     """Prioritized schedule of FreeScale Algorithm 2.
 
     Forward of iteration t: finish the exclusive update of t-1, prepare t+1,
@@ -295,7 +310,7 @@ def run_prioritized(w, batches, table, state, grads_list):
     the collision rows of t+1.  The exclusive rows of the last iteration are
     updated at the end.
     """
-    preps = [prepare(w, b) for b in batches]
+    preps = _prepare_all(w, batches, times_list)
     K = len(preps)
     outs = [None] * K
     colls = [None] * K

@@ -65,6 +65,18 @@ def test_host_argument_errors_return_without_launching():
     assert L.fs_balance_fbs(C.c_void_p(0x10), 10, 4, C.c_void_p(0x20), C.c_void_p(0x3000), err, ws, 16, NULL) == 5
     assert L.fs_balance_vbs(C.c_void_p(0x10), 10, 4, -1.0, 0, C.c_void_p(0x20), C.c_void_p(0x3000),
                             C.c_void_p(0x4000), err, ws, 1 << 30, NULL) == 1                   # alpha < 0
+    # VBS AutoTune: a correction is required (8-byte aligned); 1 <= n <= 65536, step >= 0, tol in [0, 10^6]
+    vbs_out = (C.c_void_p(0x20), C.c_void_p(0x3000), C.c_void_p(0x4000), err, ws, 1 << 30, NULL)
+    assert L.fs_balance_vbs_tuned(C.c_void_p(0x10), 10, 4, 1.5, 0, NULL, *vbs_out) == 1
+    assert L.fs_balance_vbs_tuned(C.c_void_p(0x10), 10, 4, 1.5, 0, C.c_void_p(0x5004), *vbs_out) == 8
+    assert L.fs_balance_vbs_tuned(C.c_void_p(0x10), 10, 0, 1.5, 0, C.c_void_p(0x5000), *vbs_out) == 1
+    tune = dict(times=C.c_void_p(0x100), delta=C.c_void_p(0x200))
+    assert L.fs_vbs_autotune(tune["times"], 0, 1, 0, tune["delta"], err, NULL) == 1
+    assert L.fs_vbs_autotune(tune["times"], 65537, 1, 0, tune["delta"], err, NULL) == 1
+    assert L.fs_vbs_autotune(tune["times"], 4, -1, 0, tune["delta"], err, NULL) == 1
+    assert L.fs_vbs_autotune(tune["times"], 4, 1, 1000001, tune["delta"], err, NULL) == 1
+    assert L.fs_vbs_autotune(tune["times"], 4, 1, 0, NULL, err, NULL) == 1
+    assert L.fs_vbs_autotune(C.c_void_p(0x104), 4, 1, 0, tune["delta"], err, NULL) == 8
     assert L.fs_bucketize_rowwise(C.c_void_p(0x10), 10, C.c_void_p(0x100), 1025, 100, C.c_void_p(0x20),
                                   C.c_void_p(0x30), C.c_void_p(0x40), C.c_void_p(0x50), err, ws, 1 << 30, NULL) == 1
     assert L.fs_bucketize_rowwise(C.c_void_p(0x13), 10, C.c_void_p(0x100), 4, 100, C.c_void_p(0x20),

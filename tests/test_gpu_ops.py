@@ -92,6 +92,124 @@ def test_vbs_general_alpha_total():
     assert abs(int(to_np(sw)[0]) - ref) <= 16
 
 
+# ------------------------------------------------------------------ VBS AutoTune
+
+def _autotune_gold():
+    import json
+    import os
+    with open(os.path.join(os.path.dirname(__file__), "golden", "vbs_autotune_hand_examples.json")) as f:
+        return json.load(f)
+
+
+def test_autotune_hand_examples():
+    gold = _autotune_gold()
+    for c in gold["update_cases"]:
+        d = torch.tensor(c["delta_in"], dtype=torch.int64, device=DEV)
+        _, err = B.fs_vbs_autotune(torch.tensor(c["t"], dtype=torch.int64, device=DEV), d, c["step"], c["tol_ppm"])
+        _check(err)
+        assert d.tolist() == c["delta_out"], c["note"]
+    for c in gold["tuned_cases"]:
+        perm, ro, sw, err = B.fs_balance_vbs_tuned(torch.tensor(c["L"], dtype=torch.int32, device=DEV), c["n"],
+                                                   c["alpha"], c["sort_by_len"],
+                                                   torch.tensor(c["delta"], dtype=torch.int64, device=DEV))
+        _check(err)
+        assert to_np(perm).tolist() == c["perm"] and to_np(ro).tolist() == c["rank_offsets"], c["note"]
+        assert to_np(sw).tolist() == c["seg_weight"]
+
+
+@pytest.mark.parametrize("n,kind,step,tol", [(1, "wide", 1, 0), (4, "ties", 1, 0), (16, "wide", 3, 0),
+                                             (512, "wide", 1, 20000), (512, "ties", 2, 0), (4097, "wide", 1, 0),
+                                             (65536, "ties", 1, 5000), (65536, "wide", 7, 0)])
+def test_autotune_update_matches_oracle(n, kind, step, tol):
+    rng = np.random.default_rng(n + step)
+    t = rng.integers(0, 2 ** 53, n) if kind == "wide" else rng.integers(1000, 1004, n)
+    d0 = rng.integers(-100, 100, n)
+    d0[-1] -= d0.sum()
+    d = torch.from_numpy(d0).to(DEV)
+    _, err = B.fs_vbs_autotune(torch.from_numpy(t).to(DEV), d, step, tol)
+    _check(err)
+    assert np.array_equal(to_np(d), oracle.vbs_autotune(t, d0, step, tol))
+
+
+def test_autotune_bad_time_sets_error_and_keeps_delta():
+    d = torch.tensor([1, -1, 0], dtype=torch.int64, device=DEV)
+    for bad in (-5, 2 ** 53):
+        _, err = B.fs_vbs_autotune(torch.tensor([3, bad, 4], dtype=torch.int64, device=DEV), d)
+        with pytest.raises(B.FsError) as e:
+            _check(err)
+        assert e.value.code == 1
+        assert d.tolist() == [1, -1, 0]
+
+
+def _zero_sum(rng, n, lim):
+    """Random corrections in [-lim, lim] that sum to 0 (entries visited in random
+    order absorb the excess; their room, n * lim + |sum|, always suffices)."""
+    d = rng.integers(-lim, lim + 1, n)
+    s = int(d.sum())
+    for i in rng.permutation(n):
+        if s == 0:
+            break
+        c = int(np.clip(-s, -lim - d[i], lim - d[i]))
+        d[i] += c
+        s += c
+    return d
+
+
+@pytest.mark.parametrize("n,S,sort_by_len,lim", [(16, 2048, 0, 3), (16, 2048, 1, 500), (512, 32768, 1, 20),
+                                                 (512, 32768, 0, 32768), (3000, 20000, 0, 4),
+                                                 (3000, 20000, 1, 20000), (2048, 2048, 0, 1), (1, 50, 0, 0),
+                                                 (7, 0, 1, 0)])
+def test_vbs_tuned_matches_oracle(n, S, sort_by_len, lim):
+    """Small corrections (each count moves by its entry) and large ones (the clamp
+    and the running maximum act); n > 1024 crosses the adjustment's chunks."""
+    rng = np.random.default_rng(n + S + lim)
+    L = _lens(rng, S, 7.0, 1.6, 16384)
+    d = _zero_sum(rng, n, lim)
+    perm, ro, sw, err = B.fs_balance_vbs_tuned(torch.from_numpy(L).to(DEV), n, 1.5, sort_by_len,
+                                               torch.from_numpy(d).to(DEV))
+    _check(err)
+    p_ref, ro_ref, sw_ref = oracle.balance_vbs_tuned(L, n, 1.5, sort_by_len, d)
+    assert np.array_equal(to_np(perm), p_ref)
+    assert np.array_equal(to_np(ro), ro_ref)
+    assert np.array_equal(to_np(sw).astype(np.uint64), sw_ref)
+
+
+def test_vbs_tuned_bad_correction_sets_error_and_keeps_cut():
+    rng = np.random.default_rng(5)
+    L = _lens(rng, 100)
+    _, ro_plain, _ = oracle.balance_vbs(L, 4, 1.5, 0)
+    for d in ([1, 0, 0, 0], [101, -101, 0, 0]):
+        _, ro, _, err = B.fs_balance_vbs_tuned(torch.from_numpy(L).to(DEV), 4, 1.5, 0,
+                                               torch.tensor(d, dtype=torch.int64, device=DEV))
+        with pytest.raises(B.FsError) as e:
+            _check(err)
+        assert e.value.code == 1
+        assert np.array_equal(to_np(ro), ro_plain)
+
+
+@pytest.mark.parametrize("n,B_,sort_by_len", [(16, 128, 0), (512, 64, 1)])
+def test_autotune_loop_matches_oracle(n, B_, sort_by_len):
+    """The whole feedback loop: tuned cut -> simulated rank times -> update, on the
+    device and in the oracle, iteration by iteration, a fresh batch each time."""
+    rng = np.random.default_rng(n)
+    speed = np.where(np.arange(n) % 4 == 0, 1.5, 1.0)
+    d_dev = torch.zeros(n, dtype=torch.int64, device=DEV)
+    d_ref = np.zeros(n, np.int64)
+    for it in range(25):
+        L = _lens(rng, n * B_, 7.0, 1.6, 16384)
+        perm, ro, _, err = B.fs_balance_vbs_tuned(torch.from_numpy(L).to(DEV), n, 1.5, sort_by_len, d_dev)
+        _check(err)
+        p_ref, ro_ref, _ = oracle.balance_vbs_tuned(L, n, 1.5, sort_by_len, d_ref)
+        assert np.array_equal(to_np(perm), p_ref) and np.array_equal(to_np(ro), ro_ref), it
+        t = synthetic.rank_times(L, p_ref, ro_ref, speed, 1.5)
+        _, err = B.fs_vbs_autotune(torch.from_numpy(t).to(DEV), d_dev, 1, 0)
+        _check(err)
+        d_ref = oracle.vbs_autotune(t, d_ref, 1, 0)
+        assert np.array_equal(to_np(d_dev), d_ref), it
+    if not sort_by_len:
+        assert (d_ref[::4] < 0).all()             # the slow ranks have given samples away
+
+
 # ------------------------------------------------------------------ permute
 
 def _jagged(rng, S, R, mu=5.0, sigma=1.2, lmax=2048):

@@ -29,7 +29,13 @@ CASES = {
     "long-seq-index": W["long-seq-index"].scaled(B=2, R=5_000_000),
     "large-table-full-step": W["large-table-full-step"].scaled(B=4, R=2_000_000),
     "composite-cand": W["composite-cand"],                                              # full size
+    "long-seq-autotune": W["long-seq-autotune"].scaled(B=2, R=5_000_000),
 }
+
+
+def _times(w, device="cpu"):
+    """The ranks' step times reported after each iteration (AutoTune recipes), else None."""
+    return [synthetic.step_times(w, t, device) for t in range(w.iters)] if w.autotune else None
 
 
 def _gpu_sync(w, batches_cpu, table0, grads_cpu):
@@ -39,6 +45,7 @@ def _gpu_sync(w, batches_cpu, table0, grads_cpu):
     gd = [g.to(DEV) for g in grads_cpu] if grads_cpu else None
     pipe = Pipeline(w, DEV, max(b["T"] for b in batches_cpu), tab, state)
     K = len(bd)
+    times = _times(w, DEV)
     rec = []
     pipe.prepare(bd[0], 0)
     cur = 0
@@ -55,7 +62,7 @@ def _gpu_sync(w, batches_cpu, table0, grads_cpu):
             snap["cand_lens"] = to_np(s.cand_lens[:nc])
         has_next = t + 1 < K
         nxt = pipe.step_sync(cur, bd[t + 1] if has_next else None, gd[t] if gd else None, has_next=has_next,
-                             want_masks=True)
+                             want_masks=True, times=times[t] if times else None)
         B.check(pipe.err, f"iteration {t}")
         snap["out"] = to_np(pipe.out[0][:T])
         if has_next:
@@ -85,12 +92,16 @@ def test_pipeline_matches_oracle(name):
     tab_ref = to_np(table0)
     st_ref = np.zeros(w.R, np.float32) if w.optim == "adagrad" else None
     g_np = [to_np(g) for g in grads] if grads else None
-    ref = oracle.run_sync(w, nb, tab_ref, st_ref, g_np)
+    times = _times(w)
+    ref = oracle.run_sync(w, nb, tab_ref, st_ref, g_np, [to_np(x) for x in times] if times else None)
     for t in range(w.iters):
         g, r = rec[t], ref[t]
         p = r["prep"]
         assert np.array_equal(g["perm"], p["perm"]), t
         assert np.array_equal(g["rank_offsets"], p["rank_offsets"]), t
+        if w.autotune and t > 0:   # the corrections moved the cut away from the plain one
+            assert not np.array_equal(p["rank_offsets"], oracle.balance_vbs(nb[t]["uih_len"], w.n, w.alpha,
+                                                                            w.sort_by_len)[1]), t
         if p["seg_weight"] is not None:
             assert np.array_equal(g["seg_weight"].astype(np.uint64), p["seg_weight"]), t
         assert np.array_equal(g["offsets"], p["offsets"]), t
@@ -124,7 +135,7 @@ def test_pipeline_matches_oracle(name):
         assert np.array_equal(tab_gpu, tab_ref)
 
 
-@pytest.mark.parametrize("name", ["tiny-fbs-sgd", "mid-full-step", "large-table-full-step"])
+@pytest.mark.parametrize("name", ["tiny-fbs-sgd", "mid-full-step", "large-table-full-step", "long-seq-autotune"])
 def test_prioritized_order_equals_sync_order_on_gpu(name):
     """Algorithm 2's order gathers exactly what the synchronous order gathers (FreeScale §3.2)."""
     w = CASES[name]
@@ -134,8 +145,8 @@ def test_prioritized_order_equals_sync_order_on_gpu(name):
     state = torch.zeros(w.R, dtype=torch.float32, device=DEV) if w.optim == "adagrad" else None
     pipe = Pipeline(w, DEV, max(b["T"] for b in batches), tab, state, two_outputs=True)
     outs = {}
-    pipe.run_prioritized([batch_to(b, DEV) for b in batches], [g.to(DEV) for g in grads],
-                         on_output=lambda t, o: outs.__setitem__(t, to_np(o)))
+    pipe.run_prioritized([batch_to(b, DEV) for b in batches], [g.to(DEV) for g in grads] if grads else None,
+                         on_output=lambda t, o: outs.__setitem__(t, to_np(o)), times_list=_times(w, DEV))
     B.check(pipe.err, "prioritized")
     for t in range(w.iters):
         assert np.array_equal(outs[t], rec[t]["out"]), t
