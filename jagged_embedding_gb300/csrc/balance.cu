@@ -186,61 +186,103 @@ constexpr int64_t kTimeLimit = int64_t(1) << 53;
 // `step` samples, ranks faster than it take `step`, paired so that the global
 // batch stays fixed: with k = min(#slow, #fast), the k slowest and the k
 // fastest ranks move.  Every block reduces all n times itself (integer sums:
-// the same in every block), then each thread decides for one rank.  A rank's
+// the same in every block), then each warp decides for one rank.  A rank's
 // place among the slow ones is the number of ranks with a larger time plus the
 // number of lower ranks with the same time (anything slower than a slow rank
-// is slow too); the fast side is the mirror image.  O(n^2 / threads) work,
-// n <= 65536.
+// is slow too); the fast side is the mirror image.  The warp's lanes split
+// that count; the times come through shared memory in tiles of kTuneTile.
+// O(n^2) comparisons in all, n <= 65536.
+constexpr int kTuneTile = 2048;
+constexpr int kTuneWarps = kTuneThreads / 32;  // ranks per block
+
 __global__ void __launch_bounds__(kTuneThreads) vbs_autotune_kernel(const int64_t* t, int32_t n, int64_t step,
                                                                     int32_t tol_ppm, int64_t* delta, int32_t* err) {
-  __shared__ uint64_t part[kTuneThreads];
+  __shared__ int64_t tile[kTuneTile];
+  __shared__ uint64_t part_lo[kTuneWarps], part_hi[kTuneWarps];
   __shared__ int counts[2];
-  __shared__ unsigned __int128 sum_s;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (threadIdx.x < 2) counts[threadIdx.x] = 0;
-  uint64_t acc = 0;  // < (n / threads) * 2^53 <= 2^61 per thread
+  // sum of the times as two exact 64-bit halves: low 32 bits and high bits of
+  // each time summed apart (< 2^48 and < 2^37 for n <= 65536)
+  uint64_t lo = 0, hi = 0;
   bool bad = false;
   for (int32_t q = threadIdx.x; q < n; q += kTuneThreads) {
     const int64_t x = t[q];
     bad |= (x < 0) || (x >= kTimeLimit);
-    acc += static_cast<uint64_t>(x);
+    lo += static_cast<uint32_t>(x);
+    hi += static_cast<uint64_t>(x) >> 32;
   }
-  part[threadIdx.x] = acc;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    lo += __shfl_down_sync(0xffffffffu, lo, o);
+    hi += __shfl_down_sync(0xffffffffu, hi, o);
+  }
+  if (lane == 0) {
+    part_lo[warp] = lo;
+    part_hi[warp] = hi;
+  }
   if (__syncthreads_or(bad)) {
     if (blockIdx.x == 0 && threadIdx.x == 0) set_err(err, FS_ERR_INVALID_ARG);
     return;
   }
-  if (threadIdx.x == 0) {
-    unsigned __int128 s = 0;
-    for (int i = 0; i < kTuneThreads; ++i) s += part[i];
-    sum_s = s;
+  uint64_t LO = 0, HI = 0;
+#pragma unroll
+  for (int w = 0; w < kTuneWarps; ++w) {
+    LO += part_lo[w];
+    HI += part_hi[w];
   }
-  __syncthreads();
-  const unsigned __int128 sum = sum_s;
+  const unsigned __int128 sum = (static_cast<unsigned __int128>(HI) << 32) + LO;
   const unsigned __int128 scale = static_cast<unsigned __int128>(n) * 1000000u;
-  const unsigned __int128 hi = sum * static_cast<unsigned __int128>(1000000 + tol_ppm);
-  const unsigned __int128 lo = sum * static_cast<unsigned __int128>(1000000 - tol_ppm);
-  int my_slow = 0, my_fast = 0;
+  const unsigned __int128 hi_bar = sum * static_cast<unsigned __int128>(1000000 + tol_ppm);
+  const unsigned __int128 lo_bar = sum * static_cast<unsigned __int128>(1000000 - tol_ppm);
+  unsigned my_slow = 0, my_fast = 0;
   for (int32_t q = threadIdx.x; q < n; q += kTuneThreads) {
     const unsigned __int128 x = static_cast<unsigned __int128>(t[q]) * scale;
-    my_slow += x > hi;
-    my_fast += x < lo;
+    my_slow += x > hi_bar;
+    my_fast += x < lo_bar;
   }
-  if (my_slow) atomicAdd(&counts[0], my_slow);
-  if (my_fast) atomicAdd(&counts[1], my_fast);
+  my_slow = __reduce_add_sync(0xffffffffu, my_slow);
+  my_fast = __reduce_add_sync(0xffffffffu, my_fast);
+  if (lane == 0 && my_slow) atomicAdd(&counts[0], int(my_slow));
+  if (lane == 0 && my_fast) atomicAdd(&counts[1], int(my_fast));
   __syncthreads();
   const int k = min(counts[0], counts[1]);
-  const int32_t r = blockIdx.x * kTuneThreads + threadIdx.x;
-  if (r >= n || k == 0) return;
-  const int64_t tr = t[r];
-  const unsigned __int128 xr = static_cast<unsigned __int128>(tr) * scale;
-  const bool slow = xr > hi, fast = xr < lo;
-  if (!slow && !fast) return;
-  int place = 0;
-  for (int32_t q = 0; q < n; ++q) {
-    const int64_t tq = t[q];
-    place += (slow ? tq > tr : tq < tr) || (tq == tr && q < r);
+  // this warp's rank (every lane holds the same values: the branches below are warp-uniform)
+  const int32_t r = blockIdx.x * kTuneWarps + warp;
+  int64_t tr = 0;
+  bool slow = false, active = false;
+  if (r < n && k > 0) {
+    tr = t[r];
+    const unsigned __int128 xr = static_cast<unsigned __int128>(tr) * scale;
+    slow = xr > hi_bar;
+    active = slow || xr < lo_bar;
   }
-  if (place < k) delta[r] += slow ? -step : step;
+  if (!__syncthreads_or(active)) return;
+  unsigned place = 0;
+  for (int32_t base = 0; base < n; base += kTuneTile) {
+    const int32_t m = min(kTuneTile, n - base);
+    __syncthreads();
+    for (int i = threadIdx.x; i < m; i += kTuneThreads) tile[i] = t[base + i];
+    __syncthreads();
+    if (active) {
+      const int32_t ties_below = r - base;  // entries i < ties_below are lower ranks
+      if (slow) {
+        for (int i = lane; i < m; i += 32) {
+          const int64_t tq = tile[i];
+          place += (tq > tr) | ((tq == tr) & (i < ties_below));
+        }
+      } else {
+        for (int i = lane; i < m; i += 32) {
+          const int64_t tq = tile[i];
+          place += (tq < tr) | ((tq == tr) & (i < ties_below));
+        }
+      }
+    }
+  }
+  if (active) {
+    place = __reduce_add_sync(0xffffffffu, place);
+    if (lane == 0 && place < unsigned(k)) delta[r] += slow ? -step : step;
+  }
 }
 
 // Inclusive max-scan of one value per thread over a block (blockDim.x <= 1024,
@@ -279,9 +321,6 @@ constexpr int kAdjustThreads = 1024;
 __global__ void __launch_bounds__(kAdjustThreads) vbs_adjust_kernel(int64_t* rank_offsets, const int64_t* delta,
                                                                     int32_t n, int64_t S, int32_t* err) {
   __shared__ int64_t smem[32];
-  __shared__ unsigned long long total;
-  if (threadIdx.x == 0) total = 0;
-  __syncthreads();
   bool bad = false;
   int64_t part = 0;  // |part| <= (n / threads) * S < 2^62
   for (int32_t r = threadIdx.x; r < n; r += kAdjustThreads) {
@@ -291,9 +330,10 @@ __global__ void __launch_bounds__(kAdjustThreads) vbs_adjust_kernel(int64_t* ran
     else
       part += d;
   }
-  atomicAdd(&total, static_cast<unsigned long long>(part));  // two's-complement sum
+  int64_t total;
+  (void)block_exclusive_scan<int64_t>(part, smem, &total);
   bad = __syncthreads_or(bad);
-  if (bad || static_cast<int64_t>(total) != 0) {
+  if (bad || total != 0) {
     if (threadIdx.x == 0) set_err(err, FS_ERR_INVALID_ARG);
     return;
   }
@@ -518,7 +558,7 @@ extern "C" fs_status fs_vbs_autotune(const int64_t* times, int32_t n, int64_t st
     return FS_ERR_INVALID_ARG;
   if (!times || !batch_delta || !err) return FS_ERR_INVALID_ARG;
   if (!aligned(times, 8) || !aligned(batch_delta, 8) || !aligned(err, 4)) return FS_ERR_ALIGNMENT;
-  const unsigned blocks = unsigned((n + kTuneThreads - 1) / kTuneThreads);
+  const unsigned blocks = unsigned((n + kTuneWarps - 1) / kTuneWarps);
   vbs_autotune_kernel<<<blocks, kTuneThreads, 0, st>>>(times, n, step, tol_ppm, batch_delta, err);
   count_launch(1);
   return launch_status();
