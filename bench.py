@@ -328,9 +328,9 @@ def run_gpu(args):
         step_batches.append(i % w.iters)
         ids_timed += pipe.slots[cur].T
 
-        def timed_gather(slot, out_idx=0, mask=None, sel=1, _k=k):
+        def timed_gather(*a, _k=k, **kw):
             g0[_k].record(stream)
-            orig_gather(slot, out_idx, mask, sel)
+            orig_gather(*a, **kw)
             g1[_k].record(stream)
 
         pipe.gather = timed_gather
@@ -380,15 +380,17 @@ def run_gpu(args):
                                          table_np=tab_np, device=dev, warmup=1)
         cpu = {"value": rate, "unit": "IDs/s", "cores": 1, "kind": "oracle", "sample": desc}
 
+    sorted_gather = w.has_update and pipe.row_sorted
     traffic = None
     tpath = os.path.join(ROOT, "profiles", "gather_traffic.json")
     if os.path.exists(tpath):
         with open(tpath) as f:
             tj = json.load(f)
-        if tj.get("kernel_hash") == kernel_hash() and tj.get("workload") == w0.name:
+        if tj.get("kernel_hash") == kernel_hash(sorted_gather) and tj.get("workload") == w0.name:
             traffic = tj.get("bytes_per_launch")
 
     achieved = gbytes / (gather_ms / 1000.0) / 1e9
+    # the synchronous step of a workload with an update gathers from the update's sorted entries
     line = {
         "metric": METRIC, "value": value, "unit": "IDs/s", "n_gpus": ws, "steps": K, "warmup": W,
         "ms_per_step": 1000.0 * secs_max / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -398,7 +400,8 @@ def run_gpu(args):
                           % (table.numel() * table.element_size() / 1e9, max_T * 8 / 1e9)),
         "hbm_roofline_frac_step": step_bytes / secs / (hbm_gbs * 1e9),
         "algorithmic_bytes_per_step": step_bytes / K,
-        "roofline": {"kernel": GATHER_KERNEL, "bound": "hbm", "achieved": achieved,
+        "roofline": {"kernel": SORTED_GATHER_KERNEL if sorted_gather else GATHER_KERNEL, "bound": "hbm",
+                     "achieved": achieved,
                      "peak": hbm_gbs, "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / hbm_gbs,
                      "traffic": traffic, "algorithmic_bytes_per_launch": gbytes, "avg_launch_ms": gather_ms},
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clk,
@@ -411,15 +414,17 @@ def run_gpu(args):
     return 0
 
 
-# the dominant kernel of the step: the unmasked gather of the synchronous order
+# the dominant kernel of the step: the unmasked gather of the synchronous order (from the update's
+# sorted entries when the workload has an update)
 GATHER_KERNEL = "fs_emb_gather (gather_bulk_kernel<4, 2>)"
+SORTED_GATHER_KERNEL = "fs_emb_gather_sorted (gather_sorted_kernel)"
 
 
-def kernel_hash():
+def kernel_hash(sorted_gather=False):
     """Hash of the sources of the gather kernel (the recorded DRAM traffic is valid for these only)."""
     import hashlib
     h = hashlib.sha256()
-    for name in ("gather.cu", "bulk.cuh"):
+    for name in (("backward.cu", "radix.cuh") if sorted_gather else ("gather.cu", "bulk.cuh")):
         with open(os.path.join(ROOT, "jagged_embedding_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]

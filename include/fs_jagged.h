@@ -323,6 +323,49 @@ fs_status fs_emb_backward_adagrad(void* table, float* state, int64_t num_rows, i
                                   float eps, int32_t* err, void* ws, size_t ws_bytes, fs_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Row-sorted path: the update's sort, run before the lookup of the same batch,
+ * also serves the lookup (Algorithm 2 line 12 and lines 18-20 on one batch).
+ * fs_emb_backward_adagrad split in two around a gather that reads each
+ * distinct table row once:
+ *
+ *   fs_emb_sort_rows      sorts the batch's entries by (phase bit, row);
+ *   fs_emb_gather_sorted  out[p] = table[ids[p]] for every sorted entry p --
+ *                         the same result as fs_emb_gather, bit for bit, but
+ *                         equal rows are adjacent, so a row is read from DRAM
+ *                         once and written to each of its positions;
+ *   fs_emb_update_sorted  the segment-reduce + row update of those entries --
+ *                         the same result as fs_emb_backward_adagrad with the
+ *                         same arguments, bit for bit.
+ *
+ * The sorted entries stay in `ws` between the calls: pass the same ws (of
+ * fs_emb_backward_adagrad_workspace_size(T, num_rows, dim, dtype) bytes) and
+ * the same T, num_rows, dim, dtype and phase to the three calls, in stream
+ * order, and use ws for nothing else in between (the gather and the update
+ * read the sort's output and may run any number of times).
+ *   phase: FS_PHASE_ALL, or FS_PHASE_COLLISION_THEN_EXCLUSIVE with is_co or
+ *          co_rows as in fs_emb_backward_adagrad (num_rows <= 2^30 there, so
+ *          that the phase bit fits beside the row bits); other phases keep
+ *          only some entries and are refused (FS_ERR_INVALID_ARG).
+ *   gather: table and out 16-byte aligned (FS_ERR_ALIGNMENT); row bytes
+ *          64 to 512 as the update allows.  Positions whose ID is out of range
+ *          (FS_ERR_ID_RANGE from the sort) or whose is_co byte is above 1 are
+ *          not sorted, and their output rows are left untouched.  A sorted
+ *          entry out of range (ws not holding this batch's sort) sets
+ *          FS_ERR_BAD_OFFSETS and is skipped.
+ *   update: reads the sorted entries without checks: calling it on a ws that
+ *          fs_emb_sort_rows did not fill for the same batch is undefined.
+ * ---------------------------------------------------------------------- */
+fs_status fs_emb_sort_rows(int64_t num_rows, int32_t dim, fs_dtype dtype, const int64_t* ids, int64_t T,
+                           const uint8_t* is_co, const uint32_t* co_rows, fs_phase phase, int32_t* err, void* ws,
+                           size_t ws_bytes, fs_stream_t stream);
+fs_status fs_emb_gather_sorted(const void* table, int64_t num_rows, int32_t dim, fs_dtype dtype, int64_t T,
+                               fs_phase phase, void* out, int32_t* err, void* ws, size_t ws_bytes,
+                               fs_stream_t stream);
+fs_status fs_emb_update_sorted(void* table, float* state, int64_t num_rows, int32_t dim, fs_dtype dtype,
+                               fs_optim optim, const void* grads, int64_t T, fs_phase phase, float lr, float eps,
+                               int32_t* err, void* ws, size_t ws_bytes, fs_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Utilities.
  * fs_check: waits for `stream`, then returns the code in *err (FS_OK if 0),
  *   or FS_ERR_CUDA if the stream reports an error.  Host-synchronous: meant for

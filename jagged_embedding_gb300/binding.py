@@ -36,7 +36,8 @@ EXPORTS = [
     "fs_keyed_transpose", "fs_bucketize_rowwise_workspace_size",
     "fs_bucketize_rowwise", "fs_collision_split_workspace_size", "fs_collision_split", "fs_row_bitmap_words",
     "fs_row_bitmap", "fs_collision_split_bitmaps_workspace_size", "fs_collision_split_bitmaps", "fs_emb_gather",
-    "fs_emb_backward_adagrad_workspace_size", "fs_emb_backward_adagrad", "fs_check", "fs_status_string",
+    "fs_emb_backward_adagrad_workspace_size", "fs_emb_backward_adagrad", "fs_emb_sort_rows",
+    "fs_emb_gather_sorted", "fs_emb_update_sorted", "fs_check", "fs_status_string",
     "fs_set_spin_limit", "fs_debug_skip_publish", "fs_launch_count", "fs_version",
 ]
 
@@ -82,6 +83,10 @@ def lib():
                                        C.c_int),
         "fs_emb_gather": ([P, i64, i32, C.c_int, P, i64, P, u8, P, P, P], C.c_int),
         "fs_emb_backward_adagrad_workspace_size": ([i64, i64, i32, C.c_int], sz),
+        "fs_emb_sort_rows": ([i64, i32, C.c_int, P, i64, P, P, C.c_int, P, P, sz, P], C.c_int),
+        "fs_emb_gather_sorted": ([P, i64, i32, C.c_int, i64, C.c_int, P, P, P, sz, P], C.c_int),
+        "fs_emb_update_sorted": ([P, P, i64, i32, C.c_int, C.c_int, P, i64, C.c_int, f32, f32, P, P, sz, P],
+                                 C.c_int),
         "fs_emb_backward_adagrad": ([P, P, i64, i32, C.c_int, C.c_int, P, P, i64, P, P, C.c_int, f32, f32, P, P, sz,
                                      P], C.c_int),
         "fs_check": ([P, P], C.c_int),
@@ -418,4 +423,58 @@ def fs_emb_backward_adagrad(table, state, ids, grads, optim, lr, eps=0.0, is_co=
                                       int(phase), float(lr), float(eps), _ptr(err), _ptr(ws), ws.numel(),
                                       _stream(dev)),
         "fs_emb_backward_adagrad")
+    return err
+
+
+# ------------------------------------------------------------------ row-sorted path
+
+def _table_shape(table):
+    if table.dim() != 2 or not table.is_contiguous():
+        raise FsError(1, "table must be a contiguous [R, D] tensor")
+    return table.shape
+
+
+def fs_emb_sort_rows(table, ids, ws, phase=PHASE_ALL, is_co=None, co_rows=None, err=None, T=None):
+    """Sort the batch's entries by (phase bit, row) into ws, for fs_emb_gather_sorted / fs_emb_update_sorted.
+    `table` only gives num_rows, dim and dtype (it is not read)."""
+    dev = ids.device
+    _need(ids, torch.int64, "ids")
+    R, D = _table_shape(table)
+    T = ids.numel() if T is None else int(T)
+    if is_co is not None:
+        _need(is_co, torch.uint8, "is_co")
+    if co_rows is not None:
+        _need(co_rows, torch.int32, "co_rows", (R + 31) // 32)
+    err = new_err(dev) if err is None else err
+    _ok(lib().fs_emb_sort_rows(R, D, dtype_code(table), _ptr(ids), T, _ptr(is_co), _ptr(co_rows), int(phase),
+                               _ptr(err), _ptr(ws), ws.numel(), _stream(dev)), "fs_emb_sort_rows")
+    return err
+
+
+def fs_emb_gather_sorted(table, T, ws, out=None, phase=PHASE_ALL, err=None):
+    """out[p] = table[ids[p]] from the entries fs_emb_sort_rows left in ws."""
+    dev = table.device
+    R, D = _table_shape(table)
+    out = torch.empty(int(T), D, dtype=table.dtype, device=dev) if out is None else out
+    if out.dtype != table.dtype or not out.is_contiguous() or out.numel() < int(T) * D:
+        raise FsError(1, "out must be contiguous [>= T, D] with the table dtype")
+    err = new_err(dev) if err is None else err
+    _ok(lib().fs_emb_gather_sorted(_ptr(table), R, D, dtype_code(table), int(T), int(phase), _ptr(out), _ptr(err),
+                                   _ptr(ws), ws.numel(), _stream(dev)), "fs_emb_gather_sorted")
+    return out, err
+
+
+def fs_emb_update_sorted(table, state, grads, T, ws, optim, lr, eps=0.0, phase=PHASE_ALL, err=None):
+    """Segment-reduce + row update of the entries fs_emb_sort_rows left in ws."""
+    dev = table.device
+    R, D = _table_shape(table)
+    if grads.dtype != table.dtype or not grads.is_contiguous():
+        raise FsError(1, "grads must be contiguous with the table dtype")
+    oc = {"sgd": SGD, "adagrad": ROWWISE_ADAGRAD}[optim] if isinstance(optim, str) else int(optim)
+    if oc == ROWWISE_ADAGRAD:
+        _need(state, torch.float32, "state", R)
+    err = new_err(dev) if err is None else err
+    _ok(lib().fs_emb_update_sorted(_ptr(table), _ptr(state) if oc == ROWWISE_ADAGRAD else None, R, D,
+                                   dtype_code(table), oc, _ptr(grads), int(T), int(phase), float(lr), float(eps),
+                                   _ptr(err), _ptr(ws), ws.numel(), _stream(dev)), "fs_emb_update_sorted")
     return err

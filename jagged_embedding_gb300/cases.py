@@ -10,6 +10,9 @@ op is one of
   bucketize -- fs_bucketize_rowwise of the same IDs into 256 row-range shards
   transpose -- fs_keyed_transpose of about T IDs in R features x 65536 samples (lengths uniform, per-feature
                row bases); prints the time per call and the bandwidth of its algorithmic bytes
+  gather-sorted -- the same IDs and table as gather: fs_emb_sort_rows once, then fs_emb_gather_sorted and
+               fs_emb_gather each timed alone (median of reps calls, CUDA events), with the bandwidth of
+               the algorithmic bytes (8 + 256 per ID, 256 per distinct row)
   autotune  -- VBS AutoTune with T samples over R logical ranks (lognormal(7, 1.6) lengths up to 16384,
                alpha 1.5, length-sorted cut): fs_vbs_autotune, fs_balance_vbs_tuned and the plain
                fs_balance_vbs, each timed alone (median of reps calls, CUDA events)
@@ -31,7 +34,7 @@ SHARDS = 256
 
 def main(argv) -> int:
     if len(argv) < 3 or argv[0] not in ("gather", "backward", "backward-bf16", "bucketize", "transpose",
-                                        "autotune"):
+                                        "autotune", "gather-sorted"):
         print(__doc__)
         return 2
     op, T, R = argv[0], int(argv[1]), int(argv[2])
@@ -45,6 +48,8 @@ def main(argv) -> int:
     if op == "autotune":
         return _autotune(T, R, reps, dev, g, err)
     ids = synthetic.zipf_rows(R, 1.0, T, g, dev)
+    if op == "gather-sorted":
+        return _gather_sorted(ids, T, R, reps, dev, g, err)
     if op == "gather":
         table = torch.empty(R, DIM, device=dev).normal_(0, 0.01, generator=g)
         out = torch.empty(T, DIM, device=dev)
@@ -107,6 +112,23 @@ def _median_ms(fn, reps):
     torch.cuda.synchronize()
     ms = sorted(a.elapsed_time(b) for a, b in ev)
     return ms[len(ms) // 2]
+
+
+def _gather_sorted(ids, T, R, reps, dev, g, err):
+    reps = max(reps, 5)
+    table = torch.empty(R, DIM, device=dev).normal_(0, 0.01, generator=g)
+    out = torch.empty(T, DIM, device=dev)
+    ws = B.workspace(B.backward_workspace_size(T, R, DIM, B.dtype_code(table)), dev)
+    B.fs_emb_sort_rows(table, ids, ws, err=err)
+    t_sorted = _median_ms(lambda: B.fs_emb_gather_sorted(table, T, ws, out=out, err=err), reps)
+    t_plain = _median_ms(lambda: B.fs_emb_gather(table, ids, out=out, err=err), reps)
+    torch.cuda.synchronize()
+    B.check(err, "gather-sorted")
+    U = int(torch.unique(ids).numel())
+    byts = (8 + 4 * DIM) * T + 4 * DIM * U
+    print(f"gather-sorted T={T} R={R} U={U}: sorted {t_sorted:.3f} ms ({byts / t_sorted / 1e6:.0f} GB/s), "
+          f"position order {t_plain:.3f} ms ({byts / t_plain / 1e6:.0f} GB/s) (median of {reps})")
+    return 0
 
 
 def _autotune(S, n, reps, dev, g, err):

@@ -9,18 +9,24 @@
 //      selects (reduce-then-scan counting passes of at most 9 bits; the first
 //      pass reads the int64 IDs and the collision mask directly, so
 //      unselected positions are never copied);
-//   2. reduce: the sorted array is cut into fixed 2048-entry tiles, one warp
-//      per tile, so a Zipf-hot row with millions of positions is spread over
-//      many warps and a long tail of single-position rows costs the same per
-//      entry.  A warp walks its entries in order, summing each row's gradient
-//      rows in fp32 (lane l owns columns [l*EPL, (l+1)*EPL)), and updates every
-//      row that starts and ends inside the tile on the spot (the table row and
-//      the Adagrad state are prefetched into L2 a batch ahead).  A row that
-//      crosses a tile boundary leaves its partial sums as carries;
+//   2. reduce: the sorted array is cut into tiles of 256 to 2048 entries (the
+//      length follows from the range's size), one warp per tile at a time, so
+//      a Zipf-hot row with millions of positions is spread over many warps and
+//      a long tail of single-position rows costs the same per entry.  A warp
+//      walks its entries in order, summing each row's gradient rows in fp32
+//      (lane l owns columns [l*EPL, (l+1)*EPL)), and updates every row that
+//      starts and ends inside the tile on the spot (the table row and the
+//      Adagrad state are prefetched into L2 a batch ahead).  A row that crosses
+//      a tile boundary leaves its partial sums as carries;
 //   3. fixup: one warp per row that crosses tile boundaries adds its carries
 //      in tile order (in fp64) and updates the row.
 // The summation order is fixed by the sorted order and the tiling, so results
 // are bit-identical from run to run.
+//
+// Row-sorted path: the same sort, run as its own call before the batch's
+// lookup, leaves the sorted entries in the workspace; a gather reads them
+// (each distinct table row once, written to all of its positions) and the
+// update then reduces them without sorting again.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -774,6 +780,96 @@ int epl_for(int32_t dim, fs_dtype dtype) {
   return 0;
 }
 
+// Pointers into the backward workspace.  They follow from (T, R, dim, phase)
+// alone, so the sort, the row-sorted gather and the update of one batch find
+// the sorted entries where the sort left them.
+struct BwdWs {
+  BwdLayout L;
+  radix::SortWs W;
+  int kb = 0;                     // bits of the largest row index
+  uint32_t row_mask = 0xFFFFFFFFu;
+  uint32_t *sk = nullptr, *sv = nullptr;  // sorted (phase bit | row) keys, positions
+  float *carry_head = nullptr, *carry_tail = nullptr;
+  uint8_t *head_cont = nullptr, *tail_flag = nullptr;
+  double* block_sum = nullptr;
+  uint8_t* block_full = nullptr;
+  int64_t* n_first = nullptr;     // sorted entries of collision rows (two-phase mode)
+  uint32_t* tile_next = nullptr;
+};
+
+bool carve_bwd(int64_t T, int64_t R, int32_t dim, fs_phase phase, void* ws, size_t ws_bytes, BwdWs& B) {
+  B.kb = radix::bits_for(uint64_t(R - 1));
+  B.L = bwd_layout(T, R, dim);
+  if (phase == FS_PHASE_COLLISION_THEN_EXCLUSIVE) {
+    B.L.plan = radix::SortPlan(T, B.kb + 1);
+    B.row_mask = (1u << B.kb) - 1u;
+  }
+  WsCursor cur(ws, ws_bytes);
+  if (!radix::carve_sort_ws(B.L.plan, cur, B.W)) return false;
+  B.sk = radix::sorted_keys(B.L.plan, B.W);
+  B.sv = radix::sorted_values(B.L.plan, B.W);
+  B.carry_head = cur.take<float>(size_t(B.L.max_tiles) * dim);
+  B.carry_tail = cur.take<float>(size_t(B.L.max_tiles) * dim);
+  B.head_cont = cur.take<uint8_t>(size_t(B.L.max_tiles));
+  B.tail_flag = cur.take<uint8_t>(size_t(B.L.max_tiles));
+  B.block_sum = cur.take<double>(size_t(B.L.max_blocks) * dim);
+  B.block_full = cur.take<uint8_t>(size_t(B.L.max_blocks));
+  B.n_first = cur.take<int64_t>(1);
+  B.tile_next = cur.take<uint32_t>(1);
+  return cur.ok;
+}
+
+// Row-sorted gather: out[pos] = table[key & row_mask] over the sorted entries
+// [0, *n_dev).  Equal rows are adjacent, so a row leaves DRAM once and its
+// further reads hit L1/L2; the writes land at the entries' batch-major
+// positions (whole rows, scattered).  Rows of 16 * VPR bytes, VPR in
+// {4, 8, 16, 32}: a warp instruction moves RPI = 32 / VPR rows, each lane keeps
+// U independent 16-byte loads in flight; one coalesced load per warp
+// iteration brings the keys and positions of RPI * U entries.  An entry whose
+// row or position is out of range (the workspace does not hold this batch's
+// sort) sets FS_ERR_BAD_OFFSETS and is skipped.
+constexpr int kGatherThreads = 256;
+
+template <int VPR>
+__global__ void __launch_bounds__(kGatherThreads) gather_sorted_kernel(const int4* __restrict__ table, int64_t R,
+                                                                       const uint32_t* __restrict__ keys,
+                                                                       const uint32_t* __restrict__ pos,
+                                                                       const int64_t* __restrict__ n_dev, int64_t T,
+                                                                       uint32_t row_mask, int4* __restrict__ out,
+                                                                       int32_t* err) {
+  constexpr int RPI = 32 / VPR;
+  constexpr int U = (32 / RPI) < 8 ? (32 / RPI) : 8;
+  constexpr int RPW = RPI * U;
+  static_assert(RPW <= 32, "one lane per entry");
+  int64_t n = *n_dev;
+  n = n < 0 ? 0 : (n > T ? T : n);
+  const int lane = threadIdx.x & 31;
+  const int sub = lane / VPR, c = lane % VPR;
+  const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t e0 = ((int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5) * RPW; e0 < n; e0 += nwarps * RPW) {
+    uint32_t my_row = 0, my_pos = 0xFFFFFFFFu;  // position all ones: no entry
+    if (lane < RPW && e0 + lane < n) {
+      my_row = __ldcs(keys + e0 + lane) & row_mask;
+      my_pos = __ldcs(pos + e0 + lane);
+      if (int64_t(my_row) >= R || int64_t(my_pos) >= T) {
+        set_err(err, FS_ERR_BAD_OFFSETS);
+        my_pos = 0xFFFFFFFFu;
+      }
+    }
+    int4 v[U];
+    uint32_t p[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const uint32_t row = __shfl_sync(0xffffffffu, my_row, u * RPI + sub);
+      p[u] = __shfl_sync(0xffffffffu, my_pos, u * RPI + sub);
+      if (p[u] != 0xFFFFFFFFu) v[u] = __ldg(table + int64_t(row) * VPR + c);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (p[u] != 0xFFFFFFFFu) __stcs(out + int64_t(p[u]) * VPR + c, v[u]);
+  }
+}
+
 }  // namespace
 }  // namespace fs
 
@@ -789,69 +885,52 @@ extern "C" size_t fs_emb_backward_adagrad_workspace_size(int64_t T, int64_t num_
          align_up(sizeof(int64_t)) + align_up(sizeof(uint32_t)) + 256;
 }
 
-extern "C" fs_status fs_emb_backward_adagrad(void* table, float* state, int64_t num_rows, int32_t dim, fs_dtype dtype,
-                                             fs_optim optim, const int64_t* ids, const void* grads, int64_t T,
-                                             const uint8_t* is_co, const uint32_t* co_rows, fs_phase phase,
-                                             float lr, float eps, int32_t* err, void* ws, size_t ws_bytes,
-                                             fs_stream_t stream) {
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+namespace fs {
+namespace {
+
+// Host checks shared by the one-call update and the row-sorted calls.
+fs_status check_bwd(int64_t T, int64_t num_rows, int32_t dim, fs_dtype dtype, fs_phase phase, int32_t* err) {
   if (T < 0 || T > INT32_MAX || num_rows < 1 || num_rows >= (int64_t(1) << 32) || !err) return FS_ERR_INVALID_ARG;
-  if ((dtype != FS_F32 && dtype != FS_BF16) || (optim != FS_SGD && optim != FS_ROWWISE_ADAGRAD)) return FS_ERR_INVALID_ARG;
+  if (dtype != FS_F32 && dtype != FS_BF16) return FS_ERR_INVALID_ARG;
   if (phase != FS_PHASE_ALL && phase != FS_PHASE_COLLISION && phase != FS_PHASE_EXCLUSIVE &&
       phase != FS_PHASE_COLLISION_THEN_EXCLUSIVE)
     return FS_ERR_INVALID_ARG;
-  const int epl = epl_for(dim, dtype);
-  if (epl == 0) return FS_ERR_INVALID_ARG;
-  if (optim == FS_ROWWISE_ADAGRAD && !state) return FS_ERR_INVALID_ARG;
-  if (T == 0) return FS_OK;
-  if (!table || !ids || !grads) return FS_ERR_INVALID_ARG;
-  if (phase != FS_PHASE_ALL && (is_co == nullptr) == (co_rows == nullptr)) return FS_ERR_INVALID_ARG;
-  if (co_rows && !aligned(co_rows, 4)) return FS_ERR_ALIGNMENT;
-  const size_t vec = size_t(epl) * (dtype == FS_F32 ? 4 : 2);
-  if (!aligned(table, vec) || !aligned(grads, vec) || !aligned(ids, 8) || (state && !aligned(state, 4)))
-    return FS_ERR_ALIGNMENT;
-  if (ws_bytes < fs_emb_backward_adagrad_workspace_size(T, num_rows, dim, dtype) || !ws) return FS_ERR_WORKSPACE;
+  if (epl_for(dim, dtype) == 0) return FS_ERR_INVALID_ARG;
+  return FS_OK;
+}
 
-  const int kb = radix::bits_for(uint64_t(num_rows - 1));
-  if (phase == FS_PHASE_COLLISION_THEN_EXCLUSIVE && kb > 30) {
-    // the phase bit does not fit beside the row bits: two calls, same result
-    fs_status s = fs_emb_backward_adagrad(table, state, num_rows, dim, dtype, optim, ids, grads, T, is_co, co_rows,
-                                          FS_PHASE_COLLISION, lr, eps, err, ws, ws_bytes, stream);
-    if (s != FS_OK) return s;
-    return fs_emb_backward_adagrad(table, state, num_rows, dim, dtype, optim, ids, grads, T, is_co, co_rows,
-                                   FS_PHASE_EXCLUSIVE, lr, eps, err, ws, ws_bytes, stream);
-  }
-  BwdLayout L = bwd_layout(T, num_rows, dim);
-  if (phase == FS_PHASE_COLLISION_THEN_EXCLUSIVE) L.plan = radix::SortPlan(T, kb + 1);
-  WsCursor cur(ws, ws_bytes);
-  radix::SortWs W;
-  if (!radix::carve_sort_ws(L.plan, cur, W)) return FS_ERR_WORKSPACE;
-  float* carry_head = cur.take<float>(size_t(L.max_tiles) * dim);
-  float* carry_tail = cur.take<float>(size_t(L.max_tiles) * dim);
-  uint8_t* head_cont = cur.take<uint8_t>(size_t(L.max_tiles));
-  uint8_t* tail_flag = cur.take<uint8_t>(size_t(L.max_tiles));
-  double* block_sum = cur.take<double>(size_t(L.max_blocks) * dim);
-  uint8_t* block_full = cur.take<uint8_t>(size_t(L.max_blocks));
-  int64_t* n_first = cur.take<int64_t>(1);
-  uint32_t* tile_next = cur.take<uint32_t>(1);
-  if (!cur.ok) return FS_ERR_WORKSPACE;
-
-  int launches = 0;
+// The update's sort: (phase bit | row, position) pairs of the entries the
+// phase keeps, ascending; in the two-phase mode also the number of collision
+// entries (they sort first).
+fs_status sort_rows(const BwdWs& B, const int64_t* ids, int64_t num_rows, const uint8_t* is_co,
+                    const uint32_t* co_rows, fs_phase phase, int32_t* err, cudaStream_t st, int* launches) {
   uint32_t *sk = nullptr, *sv = nullptr;
   fs_status s = (phase != FS_PHASE_ALL && co_rows)
-                    ? radix::run_sort(SrcRows<true>{ids, is_co, co_rows, int(phase), num_rows, kb}, L.plan, W, err,
-                                      st, &sk, &sv, &launches)
-                    : radix::run_sort(SrcRows<false>{ids, is_co, co_rows, int(phase), num_rows, kb}, L.plan, W, err,
-                                      st, &sk, &sv, &launches);
+                    ? radix::run_sort(SrcRows<true>{ids, is_co, co_rows, int(phase), num_rows, B.kb}, B.L.plan,
+                                      B.W, err, st, &sk, &sv, launches)
+                    : radix::run_sort(SrcRows<false>{ids, is_co, co_rows, int(phase), num_rows, B.kb}, B.L.plan,
+                                      B.W, err, st, &sk, &sv, launches);
   if (s != FS_OK) return s;
+  if (phase == FS_PHASE_COLLISION_THEN_EXCLUSIVE) {
+    count_below_kernel<<<1, 1, 0, st>>>(B.sk, B.W.pass.n_valid, 1u << B.kb, B.n_first);
+    ++*launches;
+  }
+  return FS_OK;
+}
+
+// Segment-reduce + row update of the sorted entries: one range, or in the
+// two-phase mode the collision rows in a first launch and the exclusive rows
+// in a second, in stream order.
+void update_rows(const BwdWs& B, void* table, float* state, int32_t dim, fs_dtype dtype, fs_optim optim,
+                 const void* grads, fs_phase phase, float lr, float eps, int32_t* err, cudaStream_t st,
+                 int* launches) {
+  const int epl = epl_for(dim, dtype);
   UpdateArgs u{table, optim == FS_ROWWISE_ADAGRAD ? state : nullptr, int(optim), lr, eps};
   const bool bf = dtype == FS_BF16;
-  const int64_t* n_valid = W.pass.n_valid;
-  // one update launch over a range of the sorted entries
   auto reduce_range = [&](const int64_t* begin_dev, const int64_t* end_dev, uint32_t row_mask) {
 #define FS_REDUCE(BF, E) \
-  launch_reduce<BF, E>(sk, sv, begin_dev, end_dev, row_mask, grads, u, carry_head, carry_tail, head_cont, tail_flag, \
-                       block_sum, block_full, tile_next, err, st)
+  launch_reduce<BF, E>(B.sk, B.sv, begin_dev, end_dev, row_mask, grads, u, B.carry_head, B.carry_tail, B.head_cont, \
+                       B.tail_flag, B.block_sum, B.block_full, B.tile_next, err, st)
     switch (epl) {
       case 1: if (bf) FS_REDUCE(true, 1); else FS_REDUCE(false, 1); break;
       case 2: if (bf) FS_REDUCE(true, 2); else FS_REDUCE(false, 2); break;
@@ -859,19 +938,150 @@ extern "C" fs_status fs_emb_backward_adagrad(void* table, float* state, int64_t 
       default: FS_REDUCE(true, 8); break;
     }
 #undef FS_REDUCE
-    launches += 3;
+    *launches += 3;
   };
   if (phase == FS_PHASE_COLLISION_THEN_EXCLUSIVE) {
-    // collision rows sort first: update them in a first launch, the exclusive
-    // rows (phase bit set) in a second, in stream order
-    const uint32_t row_mask = (1u << kb) - 1u;
-    count_below_kernel<<<1, 1, 0, st>>>(sk, n_valid, 1u << kb, n_first);
-    ++launches;
-    reduce_range(nullptr, n_first, row_mask);
-    reduce_range(n_first, n_valid, row_mask);
+    reduce_range(nullptr, B.n_first, B.row_mask);
+    reduce_range(B.n_first, B.W.pass.n_valid, B.row_mask);
   } else {
-    reduce_range(nullptr, n_valid, 0xFFFFFFFFu);
+    reduce_range(nullptr, B.W.pass.n_valid, 0xFFFFFFFFu);
   }
+}
+
+fs_status check_update_args(void* table, float* state, int32_t dim, fs_dtype dtype, fs_optim optim,
+                            const void* grads) {
+  if (optim != FS_SGD && optim != FS_ROWWISE_ADAGRAD) return FS_ERR_INVALID_ARG;
+  if (optim == FS_ROWWISE_ADAGRAD && !state) return FS_ERR_INVALID_ARG;
+  if (!table || !grads) return FS_ERR_INVALID_ARG;
+  const size_t vec = size_t(epl_for(dim, dtype)) * (dtype == FS_F32 ? 4 : 2);
+  if (!aligned(table, vec) || !aligned(grads, vec) || (state && !aligned(state, 4))) return FS_ERR_ALIGNMENT;
+  return FS_OK;
+}
+
+}  // namespace
+}  // namespace fs
+
+extern "C" fs_status fs_emb_backward_adagrad(void* table, float* state, int64_t num_rows, int32_t dim, fs_dtype dtype,
+                                             fs_optim optim, const int64_t* ids, const void* grads, int64_t T,
+                                             const uint8_t* is_co, const uint32_t* co_rows, fs_phase phase,
+                                             float lr, float eps, int32_t* err, void* ws, size_t ws_bytes,
+                                             fs_stream_t stream) {
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  fs_status s = check_bwd(T, num_rows, dim, dtype, phase, err);
+  if (s != FS_OK) return s;
+  if (optim != FS_SGD && optim != FS_ROWWISE_ADAGRAD) return FS_ERR_INVALID_ARG;
+  if (optim == FS_ROWWISE_ADAGRAD && !state) return FS_ERR_INVALID_ARG;
+  if (T == 0) return FS_OK;
+  if (!ids) return FS_ERR_INVALID_ARG;
+  if ((s = check_update_args(table, state, dim, dtype, optim, grads)) != FS_OK) return s;
+  if (phase != FS_PHASE_ALL && (is_co == nullptr) == (co_rows == nullptr)) return FS_ERR_INVALID_ARG;
+  if (co_rows && !aligned(co_rows, 4)) return FS_ERR_ALIGNMENT;
+  if (!aligned(ids, 8)) return FS_ERR_ALIGNMENT;
+  if (ws_bytes < fs_emb_backward_adagrad_workspace_size(T, num_rows, dim, dtype) || !ws) return FS_ERR_WORKSPACE;
+
+  if (phase == FS_PHASE_COLLISION_THEN_EXCLUSIVE && radix::bits_for(uint64_t(num_rows - 1)) > 30) {
+    // the phase bit does not fit beside the row bits: two calls, same result
+    s = fs_emb_backward_adagrad(table, state, num_rows, dim, dtype, optim, ids, grads, T, is_co, co_rows,
+                                FS_PHASE_COLLISION, lr, eps, err, ws, ws_bytes, stream);
+    if (s != FS_OK) return s;
+    return fs_emb_backward_adagrad(table, state, num_rows, dim, dtype, optim, ids, grads, T, is_co, co_rows,
+                                   FS_PHASE_EXCLUSIVE, lr, eps, err, ws, ws_bytes, stream);
+  }
+  BwdWs B;
+  if (!carve_bwd(T, num_rows, dim, phase, ws, ws_bytes, B)) return FS_ERR_WORKSPACE;
+  int launches = 0;
+  if ((s = sort_rows(B, ids, num_rows, is_co, co_rows, phase, err, st, &launches)) != FS_OK) return s;
+  update_rows(B, table, state, dim, dtype, optim, grads, phase, lr, eps, err, st, &launches);
+  count_launch(launches);
+  return launch_status();
+}
+
+// ------------------------------------------------------------ row-sorted path
+
+namespace fs {
+namespace {
+
+// The three row-sorted calls accept the phases whose sort keeps every entry
+// with a valid ID (all of them, or collision and exclusive ones both), and the
+// two-phase mode only while the phase bit fits beside the row bits.
+fs_status check_sorted(int64_t T, int64_t num_rows, int32_t dim, fs_dtype dtype, fs_phase phase, int32_t* err,
+                       const void* ws, size_t ws_bytes) {
+  fs_status s = check_bwd(T, num_rows, dim, dtype, phase, err);
+  if (s != FS_OK) return s;
+  if (phase != FS_PHASE_ALL && phase != FS_PHASE_COLLISION_THEN_EXCLUSIVE) return FS_ERR_INVALID_ARG;
+  if (phase == FS_PHASE_COLLISION_THEN_EXCLUSIVE && radix::bits_for(uint64_t(num_rows - 1)) > 30)
+    return FS_ERR_INVALID_ARG;
+  if (T > 0 && (ws_bytes < fs_emb_backward_adagrad_workspace_size(T, num_rows, dim, dtype) || !ws))
+    return FS_ERR_WORKSPACE;
+  return FS_OK;
+}
+
+}  // namespace
+}  // namespace fs
+
+extern "C" fs_status fs_emb_sort_rows(int64_t num_rows, int32_t dim, fs_dtype dtype, const int64_t* ids, int64_t T,
+                                      const uint8_t* is_co, const uint32_t* co_rows, fs_phase phase, int32_t* err,
+                                      void* ws, size_t ws_bytes, fs_stream_t stream) {
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  fs_status s = check_sorted(T, num_rows, dim, dtype, phase, err, ws, ws_bytes);
+  if (s != FS_OK) return s;
+  if (T == 0) return FS_OK;
+  if (!ids) return FS_ERR_INVALID_ARG;
+  if (phase != FS_PHASE_ALL && (is_co == nullptr) == (co_rows == nullptr)) return FS_ERR_INVALID_ARG;
+  if (co_rows && !aligned(co_rows, 4)) return FS_ERR_ALIGNMENT;
+  if (!aligned(ids, 8)) return FS_ERR_ALIGNMENT;
+  BwdWs B;
+  if (!carve_bwd(T, num_rows, dim, phase, ws, ws_bytes, B)) return FS_ERR_WORKSPACE;
+  int launches = 0;
+  if ((s = sort_rows(B, ids, num_rows, is_co, co_rows, phase, err, st, &launches)) != FS_OK) return s;
+  count_launch(launches);
+  return launch_status();
+}
+
+extern "C" fs_status fs_emb_gather_sorted(const void* table, int64_t num_rows, int32_t dim, fs_dtype dtype, int64_t T,
+                                          fs_phase phase, void* out, int32_t* err, void* ws, size_t ws_bytes,
+                                          fs_stream_t stream) {
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  fs_status s = check_sorted(T, num_rows, dim, dtype, phase, err, ws, ws_bytes);
+  if (s != FS_OK) return s;
+  if (T == 0) return FS_OK;
+  if (!table || !out) return FS_ERR_INVALID_ARG;
+  if (!aligned(table, 16) || !aligned(out, 16)) return FS_ERR_ALIGNMENT;
+  BwdWs B;
+  if (!carve_bwd(T, num_rows, dim, phase, ws, ws_bytes, B)) return FS_ERR_WORKSPACE;
+  const int vpr = int(int64_t(dim) * (dtype == FS_F32 ? 4 : 2) / 16);
+  const unsigned grid = unsigned(sm_count()) * (2048 / kGatherThreads);
+  const int4* tb = static_cast<const int4*>(table);
+  int4* ob = static_cast<int4*>(out);
+  const int64_t* n = B.W.pass.n_valid;
+#define FS_GATHER_SORTED(V) \
+  gather_sorted_kernel<V><<<grid, kGatherThreads, 0, st>>>(tb, num_rows, B.sk, B.sv, n, T, B.row_mask, ob, err)
+  switch (vpr) {
+    case 4: FS_GATHER_SORTED(4); break;
+    case 8: FS_GATHER_SORTED(8); break;
+    case 16: FS_GATHER_SORTED(16); break;
+    case 32: FS_GATHER_SORTED(32); break;
+    default: return FS_ERR_INVALID_ARG;
+  }
+#undef FS_GATHER_SORTED
+  count_launch(1);
+  return launch_status();
+}
+
+extern "C" fs_status fs_emb_update_sorted(void* table, float* state, int64_t num_rows, int32_t dim, fs_dtype dtype,
+                                          fs_optim optim, const void* grads, int64_t T, fs_phase phase, float lr,
+                                          float eps, int32_t* err, void* ws, size_t ws_bytes, fs_stream_t stream) {
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  fs_status s = check_sorted(T, num_rows, dim, dtype, phase, err, ws, ws_bytes);
+  if (s != FS_OK) return s;
+  if (optim != FS_SGD && optim != FS_ROWWISE_ADAGRAD) return FS_ERR_INVALID_ARG;
+  if (optim == FS_ROWWISE_ADAGRAD && !state) return FS_ERR_INVALID_ARG;
+  if (T == 0) return FS_OK;
+  if ((s = check_update_args(table, state, dim, dtype, optim, grads)) != FS_OK) return s;
+  BwdWs B;
+  if (!carve_bwd(T, num_rows, dim, phase, ws, ws_bytes, B)) return FS_ERR_WORKSPACE;
+  int launches = 0;
+  update_rows(B, table, state, dim, dtype, optim, grads, phase, lr, eps, err, st, &launches);
   count_launch(launches);
   return launch_status();
 }

@@ -455,11 +455,15 @@ inline bool carve_sort_ws(const SortPlan& P, WsCursor& ws, SortWs& W) {
   return ws.ok;
 }
 
+// The ping-pong buffers that hold the result of run_sort (the last pass's output).
+inline uint32_t* sorted_keys(const SortPlan& P, const SortWs& W) { return W.k[(P.passes - 1) & 1]; }
+inline uint32_t* sorted_values(const SortPlan& P, const SortWs& W) { return W.v[(P.passes - 1) & 1]; }
+
 template <class Src0>
 fs_status run_sort(const Src0& src0, const SortPlan& P, const SortWs& W, int32_t* err, cudaStream_t st,
                    uint32_t** out_k, uint32_t** out_v, int* launches) {
-  *out_k = W.k[(P.passes - 1) & 1];
-  *out_v = W.v[(P.passes - 1) & 1];
+  *out_k = sorted_keys(P, W);
+  *out_v = sorted_values(P, W);
   if (P.count == 0) {
     if (cudaMemsetAsync(W.pass.n_valid, 0, sizeof(int64_t), st) != cudaSuccess) return FS_ERR_CUDA;
     return FS_OK;

@@ -10,6 +10,8 @@ Two orders are provided:
   * step_sync   -- gather of iteration t, then the update of t (collision rows
                    first, then exclusive rows); the IDs of t+1 are prepared
                    and split against t before the update, as Algorithm 2 does.
+                   With an update, the update's sort runs first and the
+                   gather reads its sorted entries (each distinct row once).
   * run_prioritized -- Algorithm 2's order: exclusive rows of t+1 prefetched
                    before the update of t, collision rows of t updated first,
                    then gathered for t+1; exclusive updates of t deferred to
@@ -47,8 +49,10 @@ class Slot:
 
 
 class Pipeline:
-    def __init__(self, w, device, max_T, table, state=None, max_S=None, two_outputs=False):
+    def __init__(self, w, device, max_T, table, state=None, max_S=None, two_outputs=False, row_sorted=True):
         self.w = w
+        # synchronous order with an update: sort once, gather and update from the sorted entries
+        self.row_sorted = row_sorted
         self.dev = torch.device(device)
         self.max_T = int(max_T)
         self.max_S = int(max_S or w.S)
@@ -132,9 +136,30 @@ class Pipeline:
                                      err=self.err, ws=self.ws, T_t=a.T, T_next=b.T, want_t_mask=want_t_mask,
                                      want_next_mask=want_next_mask)
 
-    def gather(self, slot, out_idx=0, mask=None, sel=1):
+    def gather(self, slot, out_idx=0, mask=None, sel=1, sorted_phase=None):
+        """Lookup of the batch in `slot` (Algorithm 2 lines 12, 15); with sorted_phase, from the entries
+        sort_rows left in the workspace (each distinct row read once)."""
         s = self.slots[slot]
-        B.fs_emb_gather(self.table, s.ids, out=self.out[out_idx], mask=mask, sel=sel, err=self.err, T=s.T)
+        if sorted_phase is not None:
+            B.fs_emb_gather_sorted(self.table, s.T, self.ws, out=self.out[out_idx], phase=sorted_phase, err=self.err)
+        else:
+            B.fs_emb_gather(self.table, s.ids, out=self.out[out_idx], mask=mask, sel=sel, err=self.err, T=s.T)
+
+    def sort_rows(self, slot, phase):
+        """The update's sort of the batch in `slot`, ahead of its gather (collision flags from its mask)."""
+        s = self.slots[slot]
+        B.fs_emb_sort_rows(self.table, s.ids, self.ws, phase=phase,
+                           is_co=self.masks[slot] if phase != B.PHASE_ALL else None, err=self.err, T=s.T)
+
+    def update_sorted(self, slot, grads, phase):
+        w, s = self.w, self.slots[slot]
+        B.fs_emb_update_sorted(self.table, self.state, grads, s.T, self.ws, w.optim, w.lr, w.eps, phase=phase,
+                               err=self.err)
+
+    def _sorted_ok(self, phase):
+        # the phase bit must fit beside the row bits; 16-byte aligned rows for the gather
+        return (self.row_sorted and (phase == B.PHASE_ALL or self.w.R <= (1 << 30))
+                and self.table.data_ptr() % 16 == 0 and self.out[0].data_ptr() % 16 == 0)
 
     def backward(self, slot, grads, phase=B.PHASE_ALL, co_rows=None):
         """Update of the batch in `slot`; the phase's collision flags come from the batch's mask, or
@@ -162,13 +187,18 @@ class Pipeline:
                 self.autotune(times)
             self.prepare(nxt_batch, nxt)
             self.collision(cur, nxt, want_t_mask=True, want_next_mask=want_masks)
-        self.gather(cur)
-        if self.w.has_update:
-            if has_next:
-                # one sort, collision rows updated first, then exclusive rows
-                self.backward(cur, grads, B.PHASE_COLLISION_THEN_EXCLUSIVE)
-            else:
-                self.backward(cur, grads, B.PHASE_ALL)
+        if not self.w.has_update:
+            self.gather(cur)
+            return nxt
+        # one sort, collision rows updated first, then exclusive rows
+        phase = B.PHASE_COLLISION_THEN_EXCLUSIVE if has_next else B.PHASE_ALL
+        if self._sorted_ok(phase):
+            self.sort_rows(cur, phase)
+            self.gather(cur, sorted_phase=phase)
+            self.update_sorted(cur, grads, phase)
+        else:
+            self.gather(cur)
+            self.backward(cur, grads, phase)
         return nxt
 
     def run_prioritized(self, batches, grads_list, on_output=None, times_list=None):

@@ -695,3 +695,121 @@ def test_gradient_copy_wait_gives_up_with_timeout_status():
     W_ref, s_ref = to_np(W), np.zeros(R, np.float32)
     oracle.emb_backward(W_ref, s_ref, ids.numpy(), to_np(G), "adagrad", 0.01, 1e-8)
     assert_table_close(to_np(Wd), W_ref, "f32", 0.01)
+
+
+# ------------------------------------------------------------------ row-sorted path
+
+def _sorted_ws(W, T):
+    R, D = W.shape
+    return B.workspace(B.backward_workspace_size(T, R, D, B.dtype_code(W)), W.device)
+
+
+@pytest.mark.parametrize("dtype,D,T,R,phase", [
+    ("f32", 64, 300_000, 1_000_000, "all"), ("f32", 64, 250_000, 200_000, "mask"),
+    ("bf16", 128, 200_000, 10_000_000, "mask"), ("bf16", 128, 70_001, 5000, "bitmap"),
+    ("f32", 32, 50_000, 3000, "all"), ("f32", 128, 40_000, 100, "mask"), ("bf16", 64, 60_000, 70_000, "all"),
+    ("bf16", 256, 20_000, 5000, "bitmap"), ("f32", 64, 5, 10, "mask"), ("bf16", 32, 1, 1, "all"),
+])
+def test_gather_sorted_matches_oracle(dtype, D, T, R, phase):
+    """out[p] = W[ids[p]] from the update's sorted entries, bit for bit, for every row size the update
+    takes, with the phase bit in the keys or not; several tiles and a ragged tail."""
+    ids, W, _ = _bwd_case(T + 7 * D, R, D, T, dtype)
+    nxt = synthetic.zipf_rows(R, 1.1, max(T // 2, 1), torch.Generator().manual_seed(T), "cpu").numpy()
+    is_co = np.isin(ids.numpy(), nxt).astype(np.uint8)
+    Wd, idd = W.to(DEV), ids.to(DEV)
+    ws = _sorted_ws(Wd, T)
+    kw = {}
+    ph = B.PHASE_ALL
+    if phase == "mask":
+        kw, ph = {"is_co": torch.from_numpy(is_co).to(DEV)}, B.PHASE_COLLISION_THEN_EXCLUSIVE
+    elif phase == "bitmap":
+        bm = np.zeros((R + 31) // 32, np.uint32)
+        np.bitwise_or.at(bm, nxt >> 5, (np.uint32(1) << (nxt & 31).astype(np.uint32)))
+        kw, ph = {"co_rows": torch.from_numpy(bm.view(np.int32)).to(DEV)}, B.PHASE_COLLISION_THEN_EXCLUSIVE
+    err = B.fs_emb_sort_rows(Wd, idd, ws, phase=ph, **kw)
+    out, _ = B.fs_emb_gather_sorted(Wd, T, ws, phase=ph, err=err)
+    _check(err)
+    assert np.array_equal(to_np(out), oracle.emb_gather(to_np(W), ids.numpy()))
+
+
+@pytest.mark.parametrize("dtype,D,optim,T,R,phase", [
+    ("f32", 64, "adagrad", 300_000, 1_000_000, "mask"), ("bf16", 128, "adagrad", 200_000, 10_000_000, "bitmap"),
+    ("f32", 32, "sgd", 50_000, 3000, "all"), ("bf16", 256, "adagrad", 20_000, 5000, "mask"),
+])
+def test_update_sorted_equals_one_call_update(dtype, D, optim, T, R, phase):
+    """sort + gather + update from the sorted entries leaves table and state bit-identical to the one-call
+    update (same sort, same reduce order), and within tolerance of the oracle."""
+    ids, W, G = _bwd_case(T + D, R, D, T, dtype, s=1.05)
+    nxt = synthetic.zipf_rows(R, 1.05, T, torch.Generator().manual_seed(D), "cpu").numpy()
+    is_co = np.isin(ids.numpy(), nxt).astype(np.uint8)
+    kw, ph = {}, B.PHASE_ALL
+    if phase == "mask":
+        kw, ph = {"is_co": torch.from_numpy(is_co).to(DEV)}, B.PHASE_COLLISION_THEN_EXCLUSIVE
+    elif phase == "bitmap":
+        bm = np.zeros((R + 31) // 32, np.uint32)
+        np.bitwise_or.at(bm, nxt >> 5, (np.uint32(1) << (nxt & 31).astype(np.uint32)))
+        kw, ph = {"co_rows": torch.from_numpy(bm.view(np.int32)).to(DEV)}, B.PHASE_COLLISION_THEN_EXCLUSIVE
+    state = torch.rand(R, generator=torch.Generator().manual_seed(3)) if optim == "adagrad" else None
+    idd, Gd = ids.to(DEV), G.to(DEV)
+    W1, s1 = W.to(DEV), (state.to(DEV) if state is not None else None)
+    W2, s2 = W.to(DEV), (state.to(DEV) if state is not None else None)
+    err = B.fs_emb_backward_adagrad(W1, s1, idd, Gd, optim, 0.01, 1e-8, phase=ph, **kw)
+    ws = _sorted_ws(W2, T)
+    B.fs_emb_sort_rows(W2, idd, ws, phase=ph, err=err, **kw)
+    out, _ = B.fs_emb_gather_sorted(W2, T, ws, phase=ph, err=err)
+    B.fs_emb_update_sorted(W2, s2, Gd, T, ws, optim, 0.01, 1e-8, phase=ph, err=err)
+    _check(err)
+    assert np.array_equal(to_np(out), to_np(W)[ids.numpy()])        # the gather saw the table before the update
+    assert np.array_equal(to_np(W1), to_np(W2))
+    if state is not None:
+        assert np.array_equal(to_np(s1), to_np(s2))
+    W_ref = to_np(W)
+    s_ref = state.numpy().copy() if state is not None else None
+    oracle.emb_backward(W_ref, s_ref, ids.numpy(), to_np(G), optim, 0.01, 1e-8)
+    scale = update_scale(ids.numpy(), to_np(G), R, optim, 0.01, 1e-8, s_ref)
+    assert_table_close(to_np(W2), W_ref, dtype, 0.01, scale=scale)
+
+
+def test_gather_sorted_skips_unsorted_positions():
+    """A position the sort drops (an ID out of range: FS_ERR_ID_RANGE; a flag byte above 1) keeps its
+    output row; every other position gets its table row."""
+    R, D, T = 1000, 64, 5000
+    ids, W, _ = _bwd_case(9, R, D, T, "f32")
+    ids = ids.clone()
+    ids[17] = R + 5
+    m = torch.zeros(T, dtype=torch.uint8)
+    m[::3] = 1
+    m[100] = 2
+    Wd = W.to(DEV)
+    ws = _sorted_ws(Wd, T)
+    out = torch.full((T, D), -7.0, device=DEV)
+    err = B.fs_emb_sort_rows(Wd, ids.to(DEV), ws, phase=B.PHASE_COLLISION_THEN_EXCLUSIVE, is_co=m.to(DEV))
+    B.fs_emb_gather_sorted(Wd, T, ws, out=out, phase=B.PHASE_COLLISION_THEN_EXCLUSIVE, err=err)
+    with pytest.raises(B.FsError) as e:
+        _check(err)
+    assert e.value.code == 2
+    o = to_np(out)
+    keep = np.ones(T, bool)
+    keep[[17, 100]] = False
+    assert (o[~keep] == -7.0).all()
+    assert np.array_equal(o[keep], to_np(W)[ids.numpy()[keep]])
+
+
+def test_sorted_calls_refuse_partial_phases_and_misalignment():
+    R, D, T = 100, 64, 10
+    ids, W, G = _bwd_case(1, R, D, T, "f32")
+    Wd, idd = W.to(DEV), ids.to(DEV)
+    ws = _sorted_ws(Wd, T)
+    m = torch.zeros(T, dtype=torch.uint8, device=DEV)
+    for ph in (B.PHASE_COLLISION, B.PHASE_EXCLUSIVE):
+        with pytest.raises(B.FsError) as e:
+            B.fs_emb_sort_rows(Wd, idd, ws, phase=ph, is_co=m)
+        assert e.value.code == 1
+    B.fs_emb_sort_rows(Wd, idd, ws)
+    out = torch.empty(T * D + 1, device=DEV)[1:].view(T, D)               # 4-byte aligned only
+    with pytest.raises(B.FsError) as e:
+        B.fs_emb_gather_sorted(Wd, T, ws, out=out)
+    assert e.value.code == 8
+    with pytest.raises(B.FsError) as e:                                    # workspace too small
+        B.fs_emb_gather_sorted(Wd, T, ws[:16])
+    assert e.value.code == 5

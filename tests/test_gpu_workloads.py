@@ -38,12 +38,12 @@ def _times(w, device="cpu"):
     return [synthetic.step_times(w, t, device) for t in range(w.iters)] if w.autotune else None
 
 
-def _gpu_sync(w, batches_cpu, table0, grads_cpu):
+def _gpu_sync(w, batches_cpu, table0, grads_cpu, row_sorted=True):
     tab = table0.to(DEV)
     state = torch.zeros(w.R, dtype=torch.float32, device=DEV) if w.optim == "adagrad" else None
     bd = [batch_to(b, DEV) for b in batches_cpu]
     gd = [g.to(DEV) for g in grads_cpu] if grads_cpu else None
-    pipe = Pipeline(w, DEV, max(b["T"] for b in batches_cpu), tab, state)
+    pipe = Pipeline(w, DEV, max(b["T"] for b in batches_cpu), tab, state, row_sorted=row_sorted)
     K = len(bd)
     times = _times(w, DEV)
     rec = []
@@ -153,6 +153,21 @@ def test_prioritized_order_equals_sync_order_on_gpu(name):
     assert np.array_equal(to_np(tab), tab_sync)
     if state is not None:
         assert np.array_equal(to_np(state), st_sync)
+
+
+@pytest.mark.parametrize("name", ["tiny-fbs-sgd", "mid-full-step", "large-table-full-step", "composite-cand"])
+def test_row_sorted_step_equals_unsorted_step(name):
+    """Gathering from the update's sorted entries changes nothing: every iteration's output, the
+    table and the state are bit-identical to the step that gathers in position order."""
+    w = CASES[name]
+    batches, table0, grads = _inputs(w)
+    a = _gpu_sync(w, batches, table0, grads, row_sorted=True)
+    b = _gpu_sync(w, batches, table0, grads, row_sorted=False)
+    for t in range(w.iters):
+        assert np.array_equal(a[0][t]["out"], b[0][t]["out"]), t
+    assert np.array_equal(a[1], b[1])
+    if a[2] is not None:
+        assert np.array_equal(a[2], b[2])
 
 
 def test_runs_are_bit_identical():
