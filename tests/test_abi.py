@@ -108,6 +108,24 @@ def test_host_argument_errors_return_without_launching():
     assert L.fs_emb_backward_adagrad(args["table"], C.c_void_p(0x400), 10, 64, 0, 1, args["ids"], args["grads"], 4,
                                      NULL, C.c_void_p(0x602), 3, C.c_float(0.01), C.c_float(1e-8), err, ws, 1 << 30,
                                      NULL) == 8
+    # row-sorted path: only the phases that keep every entry; the phase bit must fit (rows <= 2^30);
+    # the workspace of the one-call update; 16-byte aligned table and output for the gather
+    big = L.fs_emb_backward_adagrad_workspace_size(100, 1000, 64, 0)
+    assert L.fs_emb_sort_rows(1000, 64, 0, C.c_void_p(0x200), 100, C.c_void_p(0x500), NULL, 1, err, ws, big,
+                              NULL) == 1                                                    # COLLISION alone
+    assert L.fs_emb_sort_rows((1 << 31) + 5, 64, 0, C.c_void_p(0x200), 100, C.c_void_p(0x500), NULL, 3, err, ws,
+                              1 << 40, NULL) == 1                                           # phase bit does not fit
+    assert L.fs_emb_sort_rows(1000, 64, 0, C.c_void_p(0x200), 100, NULL, NULL, 0, err, ws, 16, NULL) == 5
+    assert L.fs_emb_sort_rows(1000, 48, 0, C.c_void_p(0x200), 100, NULL, NULL, 0, err, ws, big, NULL) == 1
+    assert L.fs_emb_sort_rows(1000, 64, 0, C.c_void_p(0x204), 100, NULL, NULL, 0, err, ws, big, NULL) == 8
+    assert L.fs_emb_gather_sorted(C.c_void_p(0x100), 1000, 64, 0, 100, 0, C.c_void_p(0x308), err, ws, big,
+                                  NULL) == 8                                                # out 8-byte aligned
+    assert L.fs_emb_gather_sorted(C.c_void_p(0x100), 1000, 64, 0, 100, 2, C.c_void_p(0x300), err, ws, big,
+                                  NULL) == 1                                                # EXCLUSIVE alone
+    assert L.fs_emb_update_sorted(C.c_void_p(0x100), NULL, 1000, 64, 0, 1, C.c_void_p(0x300), 100, 0,
+                                  C.c_float(0.01), C.c_float(1e-8), err, ws, big, NULL) == 1  # Adagrad, no state
+    assert L.fs_emb_update_sorted(C.c_void_p(0x100), NULL, 1000, 64, 0, 0, C.c_void_p(0x300), 0, 0,
+                                  C.c_float(0.01), C.c_float(0.0), err, NULL, 0, NULL) == 0  # T = 0: nothing to do
     assert L.fs_collision_split(C.c_void_p(0x10), 5, C.c_void_p(0x20), 5, (1 << 32) + 1, 4, NULL, NULL, NULL, 0,
                                 C.c_void_p(0x30), C.c_void_p(0x40), C.c_void_p(0x50), C.c_void_p(0x60),
                                 C.c_void_p(0x70), C.c_void_p(0x80), err, ws, 1 << 30, NULL) == 1
