@@ -313,6 +313,8 @@ def run_gpu(args):
     n_ev = K
     g0 = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
     g1 = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
+    u0 = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
+    u1 = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ids_timed = 0
     step_batches = []
@@ -322,7 +324,7 @@ def run_gpu(args):
     barrier(ws)
     torch.cuda.synchronize()
     t_start.record(stream)
-    orig_gather = pipe.gather
+    orig_gather, orig_update, orig_backward = pipe.gather, pipe.update_sorted, pipe.backward
     for k in range(K):
         i = W + k
         step_batches.append(i % w.iters)
@@ -333,9 +335,20 @@ def run_gpu(args):
             orig_gather(*a, **kw)
             g1[_k].record(stream)
 
-        pipe.gather = timed_gather
+        # the update of the step (one call: from the sorted entries, or the one-call form)
+        def timed_update(*a, _k=k, _f=orig_update, **kw):
+            u0[_k].record(stream)
+            _f(*a, **kw)
+            u1[_k].record(stream)
+
+        def timed_backward(*a, _k=k, _f=orig_backward, **kw):
+            u0[_k].record(stream)
+            _f(*a, **kw)
+            u1[_k].record(stream)
+
+        pipe.gather, pipe.update_sorted, pipe.backward = timed_gather, timed_update, timed_backward
         cur = step(i, cur)
-    pipe.gather = orig_gather
+    pipe.gather, pipe.update_sorted, pipe.backward = orig_gather, orig_update, orig_backward
     t_end.record(stream)
     torch.cuda.synchronize()
     barrier(ws)
@@ -344,6 +357,7 @@ def run_gpu(args):
     B.check(pipe.err, "timed steps")
     secs = t_start.elapsed_time(t_end) / 1000.0
     gather_ms = sum(a.elapsed_time(b) for a, b in zip(g0, g1)) / K
+    update_ms = sum(a.elapsed_time(b) for a, b in zip(u0, u1)) / K if w.has_update else None
 
     # unique rows per batch (|co| + |ex_t| of its pair with the next batch), for the byte model
     U = {}
@@ -357,12 +371,15 @@ def run_gpu(args):
     hbm_gbs, peak_kind = measured_peaks()
     step_bytes = 0.0
     gbytes = 0.0
+    ubytes = 0.0
     for t in step_batches:
         n_cand = int(batches[t]["cand_offsets"][-1]) if w.composite else 0
         bb = algorithmic_bytes(w, w.S, Ts[t], U[t], w.R, n_cand)
         step_bytes += sum(bb.values())
         gbytes += gather_bytes(w, Ts[t], U[t])
+        ubytes += bb.get("backward", 0.0)
     gbytes /= K
+    ubytes /= K
 
     ids_all, secs_max = aggregate(ids_timed, secs, ws, dev)
     value = ids_all / secs_max
@@ -406,6 +423,14 @@ def run_gpu(args):
                      "traffic": traffic, "algorithmic_bytes_per_launch": gbytes, "avg_launch_ms": gather_ms},
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clk,
     }
+    if update_ms:
+        # the update's segment-reduce + row update (both phases), timed like the gather
+        ua = ubytes / (update_ms / 1000.0) / 1e9
+        line["roofline_update"] = {
+            "kernel": "fs_emb_update_sorted (reduce_ring_kernel, block sums, fixup; two phases)" if sorted_gather
+            else "fs_emb_backward_adagrad (sort, reduce_ring_kernel, block sums, fixup)",
+            "bound": "hbm", "achieved": ua, "peak": hbm_gbs, "peak_kind": peak_kind, "unit": "GB/s",
+            "frac": ua / hbm_gbs, "algorithmic_bytes_per_call": ubytes, "avg_call_ms": update_ms}
     if rank == 0:
         print(json.dumps(line))
     if ws > 1:
