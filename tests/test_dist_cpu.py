@@ -63,3 +63,31 @@ def test_algorithmic_bytes_model():
     g = synthetic.WORKLOADS["vbs-gather"]
     b = bench.algorithmic_bytes(g, g.S, 2.0e6, 2.0e5, g.R)
     assert "backward" not in b
+
+
+def test_algorithmic_bytes_autotune_and_config():
+    import bench
+    from jagged_embedding_gb300 import synthetic
+    w = synthetic.WORKLOADS["long-seq-autotune"]
+    plain = synthetic.WORKLOADS["long-seq-index"]
+    b = bench.algorithmic_bytes(w, w.S, 9.3e7, 1.06e7, w.R)
+    b0 = bench.algorithmic_bytes(plain, plain.S, 9.3e7, 1.06e7, plain.R)
+    assert b["autotune"] == 48 * w.n and "autotune" not in b0
+    assert sum(b.values()) - sum(b0.values()) == 48 * w.n      # nothing else changes
+    cfg = bench.workload_config(w, 1)
+    assert cfg["vbs_autotune"]["step"] == 1 and "vbs_autotune" not in bench.workload_config(plain, 1)
+    # the update's bytes: (8 + RB) per ID, 2 RB + 8 per unique row with Adagrad state
+    big = synthetic.WORKLOADS["large-table-full-step"]
+    assert bench.algorithmic_bytes(big, big.S, 10, 3, big.R)["backward"] == 264 * 10 + 520 * 3
+
+
+def test_step_times_are_seeded_and_slow_every_fourth_rank():
+    import torch
+
+    from jagged_embedding_gb300 import synthetic
+    w = synthetic.WORKLOADS["long-seq-autotune"]
+    a, b = synthetic.step_times(w, 2), synthetic.step_times(w, 2)
+    assert a.dtype == torch.int64 and a.shape == (w.n,) and torch.equal(a, b)
+    assert not torch.equal(a, synthetic.step_times(w, 3))
+    slow, fast = a[::4].double().mean(), torch.cat([a[1::4], a[2::4], a[3::4]]).double().mean()
+    assert 1.4 < float(slow / fast) < 1.6
