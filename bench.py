@@ -168,14 +168,35 @@ def aggregate(ids_local, seconds_local, ws, device=None):
 
 # --------------------------------------------------------------------------- oracle arm
 
-def oracle_sample(w, steps, max_seconds=20.0, samples_per_rank=None, table_np=None, device=None, warmup=0):
+def host_cores():
+    """Host cores this process may run on."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
+
+
+def oracle_sample(w, steps, max_seconds=20.0, samples_per_rank=None, table_np=None, device=None, warmup=0,
+                  threads=1):
     """Time the CPU oracle, as it stands, on a bounded sample of workload w.
 
     The sample keeps the workload's recipe (ranks, rows, dim, dtype, Zipf law,
     optimizer) with fewer samples per rank.  One timed unit mirrors one GPU
-    step: prepare(t+1) + collision(t, t+1) + gather(t) + backward(t).
+    step: prepare(t+1) + collision(t, t+1) + gather(t) + backward(t).  With
+    threads > 1 the oracle's multi-threaded variants run (same results, the
+    work of each step split over that many host threads).
     Returns (IDs/s, description, IDs timed, seconds).
     """
+    import oracle
+
+    oracle.set_threads(threads)
+    try:
+        return _oracle_sample(w, steps, max_seconds, samples_per_rank, table_np, device, warmup, threads)
+    finally:
+        oracle.set_threads(1)
+
+
+def _oracle_sample(w, steps, max_seconds, samples_per_rank, table_np, device, warmup, threads):
     import numpy as np
     import torch
 
@@ -222,8 +243,9 @@ def oracle_sample(w, steps, max_seconds=20.0, samples_per_rank=None, table_np=No
         prep_t = prep_n
         if secs > max_seconds:
             break
+    who = "single-threaded C++ oracle" if threads == 1 else f"C++ oracle on {threads} host threads"
     desc = (f"{w.name} recipe with {spr} samples/rank (S={ws_.S}), {ids_done} IDs over "
-            f"{n_timed} timed steps after {warmup} untimed, R={w.R}, single-threaded C++ oracle")
+            f"{n_timed} timed steps after {warmup} untimed, R={w.R}, {who}")
     return ids_done / secs, desc, ids_done, secs
 
 
@@ -248,15 +270,17 @@ def run_reference(args):
         return 0
     import torch
     dev = "cuda" if torch.cuda.is_available() else "cpu"
-    # warm-up steps are run (untimed) inside the same sample
+    # warm-up steps are run (untimed) inside the same sample; the oracle runs on every host core
+    cores = host_cores()
     rate, desc, ids, secs = oracle_sample(w, args.steps + args.warmup, max_seconds=150.0,
                                           samples_per_rank=args.ref_samples_per_rank, device=dev,
-                                          warmup=args.warmup)
+                                          warmup=args.warmup, threads=cores)
     line = {"impl": "reference", "metric": METRIC, "value": rate, "unit": "IDs/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * secs / max(1, args.steps),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": f"int64/{w.dtype}",
             "data": "synthetic", "config": workload_config(w, args.gpus),
-            "cpu_baseline": {"value": rate, "unit": "IDs/s", "cores": 1, "kind": "oracle", "sample": desc},
+            "cpu_baseline": {"value": rate, "unit": "IDs/s", "cores": cores, "kind": "oracle", "sample": desc,
+                             "host_cores": cores},
             "e2e": {"value": rate, "unit": "IDs/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
     return 0
@@ -393,9 +417,14 @@ def run_gpu(args):
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         tab_host = table.cpu()
         tab_np = tab_host.view(torch.int16).numpy().view("uint16") if w.dtype == "bf16" else tab_host.numpy()
-        rate, desc, _, _ = oracle_sample(w, 4, max_seconds=25.0, samples_per_rank=args.ref_samples_per_rank,
-                                         table_np=tab_np, device=dev, warmup=1)
-        cpu = {"value": rate, "unit": "IDs/s", "cores": 1, "kind": "oracle", "sample": desc}
+        cores = host_cores()
+        # the oracle on every host core, then single-threaded, each on a bounded sample of the workload
+        rate, desc, _, _ = oracle_sample(w, 4, max_seconds=15.0, samples_per_rank=args.ref_samples_per_rank,
+                                         table_np=tab_np, device=dev, warmup=1, threads=cores)
+        rate1, desc1, _, _ = oracle_sample(w, 4, max_seconds=15.0, samples_per_rank=args.ref_samples_per_rank,
+                                           table_np=tab_np, device=dev, warmup=1, threads=1)
+        cpu = {"value": rate, "unit": "IDs/s", "cores": cores, "kind": "oracle", "sample": desc,
+               "host_cores": cores, "single_thread": {"value": rate1, "unit": "IDs/s", "cores": 1, "sample": desc1}}
 
     sorted_gather = w.has_update and pipe.row_sorted
     traffic = None

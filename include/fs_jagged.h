@@ -366,6 +366,40 @@ fs_status fs_emb_update_sorted(void* table, float* state, int64_t num_rows, int3
                                int32_t* err, void* ws, size_t ws_bytes, fs_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * The update's sort, per shard -- FreeScale §3.2 and Algorithm 2 line 8: after
+ * the IDs AllToAll each shard's rows arrive shard-major, so the shard that
+ * updates them (lines 18-20) groups its own entries by row.  Same sorted
+ * entries as fs_emb_sort_rows, bit for bit (ordered by phase bit, row,
+ * position), written to the same place in ws, so fs_emb_gather_sorted and
+ * fs_emb_update_sorted follow it unchanged; but the input is the bucketize
+ * output, whose entries are already grouped by shard, so the sort only orders
+ * each shard's entries by the row's offset inside the shard (two counting
+ * passes where the row index would need three for 100M rows).
+ *   sm_ids, pos, shard_offsets: the outputs of fs_bucketize_rowwise for the
+ *          batch (n shards of block = ceil(num_rows / n) rows; n <= 1024)
+ *   is_co  [T] uint8 per SHARD-MAJOR entry (e.g. the mask fs_collision_split
+ *          writes when given sm_ids as its IDs): 1 for a collision row, 0 for
+ *          an exclusive one; required for FS_PHASE_COLLISION_THEN_EXCLUSIVE,
+ *          ignored for FS_PHASE_ALL
+ *   phase  FS_PHASE_ALL or FS_PHASE_COLLISION_THEN_EXCLUSIVE
+ *   ws     fs_emb_sort_rows_sharded_workspace_size(T, num_rows, dim, dtype, n)
+ *          bytes; its first fs_emb_backward_adagrad_workspace_size(...) bytes
+ *          hold what the gather and the update read.
+ * ceil(num_rows / n) must stay below 2^20 (2^19 with two phases) so that the
+ * offset inside a shard (and the phase bit) fit two passes of at most 10 bits
+ * (FS_ERR_INVALID_ARG otherwise; fs_emb_sort_rows has no such limit).  An ID
+ * outside [0, num_rows) sets FS_ERR_ID_RANGE, an ID outside the shard that
+ * shard_offsets gives it, or shard_offsets that are not non-decreasing from 0
+ * to T, set FS_ERR_BAD_OFFSETS; such entries (and flags above 1) are not
+ * sorted, as in fs_emb_sort_rows.
+ * ---------------------------------------------------------------------- */
+size_t fs_emb_sort_rows_sharded_workspace_size(int64_t T, int64_t num_rows, int32_t dim, fs_dtype dtype, int32_t n);
+fs_status fs_emb_sort_rows_sharded(int64_t num_rows, int32_t dim, fs_dtype dtype, const int64_t* sm_ids,
+                                   const int32_t* pos, int64_t T, const int64_t* shard_offsets, int32_t n,
+                                   const uint8_t* is_co, fs_phase phase, int32_t* err, void* ws, size_t ws_bytes,
+                                   fs_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Utilities.
  * fs_check: waits for `stream`, then returns the code in *err (FS_OK if 0),
  *   or FS_ERR_CUDA if the stream reports an error.  Host-synchronous: meant for

@@ -37,7 +37,8 @@ EXPORTS = [
     "fs_bucketize_rowwise", "fs_collision_split_workspace_size", "fs_collision_split", "fs_row_bitmap_words",
     "fs_row_bitmap", "fs_collision_split_bitmaps_workspace_size", "fs_collision_split_bitmaps", "fs_emb_gather",
     "fs_emb_backward_adagrad_workspace_size", "fs_emb_backward_adagrad", "fs_emb_sort_rows",
-    "fs_emb_gather_sorted", "fs_emb_update_sorted", "fs_check", "fs_status_string",
+    "fs_emb_gather_sorted", "fs_emb_update_sorted", "fs_emb_sort_rows_sharded_workspace_size",
+    "fs_emb_sort_rows_sharded", "fs_check", "fs_status_string",
     "fs_set_spin_limit", "fs_debug_skip_publish", "fs_launch_count", "fs_version",
 ]
 
@@ -85,6 +86,8 @@ def lib():
         "fs_emb_backward_adagrad_workspace_size": ([i64, i64, i32, C.c_int], sz),
         "fs_emb_sort_rows": ([i64, i32, C.c_int, P, i64, P, P, C.c_int, P, P, sz, P], C.c_int),
         "fs_emb_gather_sorted": ([P, i64, i32, C.c_int, i64, C.c_int, P, P, P, sz, P], C.c_int),
+        "fs_emb_sort_rows_sharded_workspace_size": ([i64, i64, i32, C.c_int, i32], sz),
+        "fs_emb_sort_rows_sharded": ([i64, i32, C.c_int, P, P, i64, P, i32, P, C.c_int, P, P, sz, P], C.c_int),
         "fs_emb_update_sorted": ([P, P, i64, i32, C.c_int, C.c_int, P, i64, C.c_int, f32, f32, P, P, sz, P],
                                  C.c_int),
         "fs_emb_backward_adagrad": ([P, P, i64, i32, C.c_int, C.c_int, P, P, i64, P, P, C.c_int, f32, f32, P, P, sz,
@@ -448,6 +451,30 @@ def fs_emb_sort_rows(table, ids, ws, phase=PHASE_ALL, is_co=None, co_rows=None, 
     err = new_err(dev) if err is None else err
     _ok(lib().fs_emb_sort_rows(R, D, dtype_code(table), _ptr(ids), T, _ptr(is_co), _ptr(co_rows), int(phase),
                                _ptr(err), _ptr(ws), ws.numel(), _stream(dev)), "fs_emb_sort_rows")
+    return err
+
+
+def sort_rows_sharded_workspace_size(T, num_rows, dim, dtype, n):
+    return int(lib().fs_emb_sort_rows_sharded_workspace_size(int(T), int(num_rows), int(dim), int(dtype), int(n)))
+
+
+def fs_emb_sort_rows_sharded(table, sm_ids, pos, shard_offsets, ws, phase=PHASE_ALL, is_co=None, err=None, T=None):
+    """The update's sort from the bucketize output (entries grouped by shard): the same sorted entries as
+    fs_emb_sort_rows, in ws.  is_co: the collision flag of each shard-major entry.  `table` only gives
+    num_rows, dim and dtype (it is not read)."""
+    dev = sm_ids.device
+    _need(sm_ids, torch.int64, "sm_ids")
+    _need(pos, torch.int32, "pos")
+    _need(shard_offsets, torch.int64, "shard_offsets")
+    R, D = _table_shape(table)
+    T = sm_ids.numel() if T is None else int(T)
+    n = shard_offsets.numel() - 1
+    if is_co is not None:
+        _need(is_co, torch.uint8, "is_co")
+    err = new_err(dev) if err is None else err
+    _ok(lib().fs_emb_sort_rows_sharded(R, D, dtype_code(table), _ptr(sm_ids), _ptr(pos), T, _ptr(shard_offsets), n,
+                                       _ptr(is_co), int(phase), _ptr(err), _ptr(ws), ws.numel(), _stream(dev)),
+        "fs_emb_sort_rows_sharded")
     return err
 
 

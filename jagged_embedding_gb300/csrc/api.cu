@@ -33,6 +33,7 @@ void count_launch(int k) { g_launches.fetch_add(k); }
 }  // namespace fs
 
 extern "C" fs_status fs_check(const int32_t* err, fs_stream_t stream) {
+  FS_NVTX_RANGE();
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(st) != cudaSuccess) return FS_ERR_CUDA;
   if (!err) return FS_OK;

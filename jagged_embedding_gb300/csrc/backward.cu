@@ -72,6 +72,7 @@ struct SrcRows {
   // loads only: the ID and the mask byte independently; with the row bitmap,
   // fetch2 then reads the ID's row bit (L2-resident; an out-of-range ID reads
   // bit 0 and is rejected by make) after every ID of the tile is in flight
+  template <bool>
   __device__ __forceinline__ Raw fetch(int64_t i) const {
     Raw r;
     r.id = __ldcs(ids + i);
@@ -84,7 +85,7 @@ struct SrcRows {
       r.m = (__ldg(co_rows + (x >> 5)) >> (x & 31u)) & 1u;
     }
   }
-  __device__ __forceinline__ bool make(const Raw& r, int64_t i, Key& key, uint32_t& val, int32_t* err) const {
+  __device__ __forceinline__ bool make(const Raw& r, int64_t i, int, Key& key, uint32_t& val, int32_t* err) const {
     const int64_t id = r.id;
     uint32_t hi = 0;
     if (phase != FS_PHASE_ALL) {
@@ -104,8 +105,89 @@ struct SrcRows {
     val = static_cast<uint32_t>(i);
     return true;
   }
-  __device__ __forceinline__ uint32_t digit(Key key, int shift, int bits) const {
+  __device__ __forceinline__ uint32_t digit(Key key, int shift, int bits, int) const {
     return (key >> shift) & ((1u << bits) - 1u);
+  }
+};
+
+// Sources of the per-shard sort (fs_emb_sort_rows_sharded).  Pass 1 reads the
+// shard-major IDs, their batch-major positions and collision flags; the key is
+// the same (phase bit | row) as SrcRows's and the value the position; the
+// digit is the low `bits` bits of the row's offset inside its shard (the
+// tile's segment).  An ID outside [0, R), outside the tile's shard, or with a
+// flag above 1 is dropped (the first two set the error word).
+struct SrcShardRows {
+  using Key = uint32_t;
+  static constexpr bool kIndexValue = false;
+  static constexpr bool kFetch2 = false;
+  const int64_t* sm_ids;
+  const int32_t* pos;
+  const uint8_t* is_co;  // per shard-major entry; null: one phase
+  int64_t R;
+  int64_t block;         // rows per shard
+  int kb;                // bits of the largest row index
+  uint32_t row_mask;
+  struct Raw {
+    int64_t id;
+    uint32_t p;
+    uint32_t m;
+  };
+  template <bool kVal>
+  __device__ __forceinline__ Raw fetch(int64_t i) const {
+    Raw r;
+    r.id = __ldcs(sm_ids + i);
+    r.p = kVal ? uint32_t(__ldcs(pos + i)) : 0u;
+    r.m = is_co ? uint32_t(__ldcs(is_co + i)) : 0u;
+    return r;
+  }
+  __device__ __forceinline__ bool make(const Raw& r, int64_t, int seg, Key& key, uint32_t& val, int32_t* err) const {
+    if (r.m > 1) return false;
+    if (r.id < 0 || r.id >= R) {
+      if (err) set_err(err, FS_ERR_ID_RANGE);
+      return false;
+    }
+    const int64_t local = r.id - int64_t(seg) * block;
+    if (local < 0 || local >= block) {
+      if (err) set_err(err, FS_ERR_BAD_OFFSETS);
+      return false;
+    }
+    key = uint32_t(r.id) | (is_co ? (uint32_t(1 - r.m) << kb) : 0u);
+    val = r.p;
+    return true;
+  }
+  __device__ __forceinline__ uint32_t digit(Key key, int shift, int bits, int seg) const {
+    const uint32_t local = (key & row_mask) - uint32_t(int64_t(seg) * block);
+    return (local >> shift) & ((1u << bits) - 1u);
+  }
+};
+
+// Pass 2 of the per-shard sort: pass 1's (key, position) pairs; the digit is
+// (phase bit, next `lbits` bits of the offset in the shard), the phase bit
+// being the group (collision rows of every shard before exclusive ones).
+struct SrcShardRows2 {
+  using Key = uint32_t;
+  static constexpr bool kIndexValue = false;
+  static constexpr bool kFetch2 = false;
+  const uint32_t* k;
+  const uint32_t* v;
+  int64_t block;
+  int kb;
+  uint32_t row_mask;
+  int lbits;       // bits of the shard offset this pass sorts
+  bool two_phase;  // the key's bit kb is the phase
+  using Raw = uint2;
+  template <bool kVal>
+  __device__ __forceinline__ Raw fetch(int64_t i) const { return make_uint2(__ldcs(k + i), kVal ? __ldcs(v + i) : 0u); }
+  __device__ __forceinline__ bool make(const Raw& r, int64_t, int, Key& key, uint32_t& val, int32_t*) const {
+    key = r.x;
+    val = r.y;
+    return true;
+  }
+  __device__ __forceinline__ uint32_t digit(Key key, int shift, int, int seg) const {
+    const uint32_t local = (key & row_mask) - uint32_t(int64_t(seg) * block);
+    uint32_t d = (local >> shift) & ((1u << lbits) - 1u);
+    if (two_phase) d |= ((key >> kb) & 1u) << lbits;
+    return d;
   }
 };
 
@@ -966,6 +1048,7 @@ extern "C" fs_status fs_emb_backward_adagrad(void* table, float* state, int64_t 
                                              const uint8_t* is_co, const uint32_t* co_rows, fs_phase phase,
                                              float lr, float eps, int32_t* err, void* ws, size_t ws_bytes,
                                              fs_stream_t stream) {
+  FS_NVTX_RANGE();
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   fs_status s = check_bwd(T, num_rows, dim, dtype, phase, err);
   if (s != FS_OK) return s;
@@ -1022,6 +1105,7 @@ fs_status check_sorted(int64_t T, int64_t num_rows, int32_t dim, fs_dtype dtype,
 extern "C" fs_status fs_emb_sort_rows(int64_t num_rows, int32_t dim, fs_dtype dtype, const int64_t* ids, int64_t T,
                                       const uint8_t* is_co, const uint32_t* co_rows, fs_phase phase, int32_t* err,
                                       void* ws, size_t ws_bytes, fs_stream_t stream) {
+  FS_NVTX_RANGE();
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   fs_status s = check_sorted(T, num_rows, dim, dtype, phase, err, ws, ws_bytes);
   if (s != FS_OK) return s;
@@ -1038,9 +1122,90 @@ extern "C" fs_status fs_emb_sort_rows(int64_t num_rows, int32_t dim, fs_dtype dt
   return launch_status();
 }
 
+// ------------------------------------------------------------ per-shard sort
+
+namespace fs {
+namespace {
+
+// Bit split of the per-shard sort: a row's offset inside its shard has lb
+// bits (shards of block = ceil(R / n) rows); pass 1 sorts the low b1 of them,
+// pass 2 the other lb2 with the phase bit (two-phase mode) above them.
+struct ShardSortPlan {
+  int64_t block = 1;
+  int lb = 1, ph = 0, b1 = 1, lb2 = 0;
+  bool ok = false;
+};
+
+ShardSortPlan shard_sort_plan(int64_t R, int32_t n, fs_phase phase) {
+  ShardSortPlan P;
+  P.block = (R + n - 1) / n;
+  P.lb = radix::bits_for(uint64_t(P.block - 1));
+  P.ph = phase == FS_PHASE_COLLISION_THEN_EXCLUSIVE ? 1 : 0;
+  P.b1 = (P.lb + P.ph) / 2;
+  if (P.b1 < 1) P.b1 = 1;
+  if (P.b1 > P.lb) P.b1 = P.lb;
+  P.lb2 = P.lb - P.b1;
+  P.ok = P.b1 <= 10 && P.lb2 + P.ph <= 10;
+  return P;
+}
+
+size_t sharded_extra_bytes(int64_t T, int32_t n) {
+  WsCounter c;
+  radix::take_seg_ws(T, n, c, nullptr);
+  return c.used;
+}
+
+}  // namespace
+}  // namespace fs
+
+extern "C" size_t fs_emb_sort_rows_sharded_workspace_size(int64_t T, int64_t num_rows, int32_t dim, fs_dtype dtype,
+                                                          int32_t n) {
+  if (T < 0 || num_rows < 1 || dim < 1 || n < 1 || n > radix::kSegThreads) return 0;
+  return fs_emb_backward_adagrad_workspace_size(T, num_rows, dim, dtype) + sharded_extra_bytes(T, n) + 256;
+}
+
+extern "C" fs_status fs_emb_sort_rows_sharded(int64_t num_rows, int32_t dim, fs_dtype dtype, const int64_t* sm_ids,
+                                              const int32_t* pos, int64_t T, const int64_t* shard_offsets, int32_t n,
+                                              const uint8_t* is_co, fs_phase phase, int32_t* err, void* ws,
+                                              size_t ws_bytes, fs_stream_t stream) {
+  FS_NVTX_RANGE();
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  fs_status s = check_sorted(T, num_rows, dim, dtype, phase, err, ws, ws_bytes);
+  if (s != FS_OK) return s;
+  if (n < 1 || n > radix::kSegThreads || !shard_offsets) return FS_ERR_INVALID_ARG;
+  const ShardSortPlan P = shard_sort_plan(num_rows, n, phase);
+  if (!P.ok) return FS_ERR_INVALID_ARG;
+  if (T == 0) return FS_OK;
+  if (!sm_ids || !pos || (phase == FS_PHASE_COLLISION_THEN_EXCLUSIVE && !is_co)) return FS_ERR_INVALID_ARG;
+  if (!aligned(sm_ids, 8) || !aligned(pos, 4) || !aligned(shard_offsets, 8)) return FS_ERR_ALIGNMENT;
+  if (ws_bytes < fs_emb_sort_rows_sharded_workspace_size(T, num_rows, dim, dtype, n)) return FS_ERR_WORKSPACE;
+  BwdWs B;
+  if (!carve_bwd(T, num_rows, dim, phase, ws, ws_bytes, B)) return FS_ERR_WORKSPACE;
+  // the passes' own scratch lies behind the layout the gather and the update read
+  const size_t base = fs_emb_backward_adagrad_workspace_size(T, num_rows, dim, dtype);
+  WsCursor cur(static_cast<char*>(ws) + base, ws_bytes - base);
+  radix::SegWs W;
+  radix::take_seg_ws(T, n, cur, &W);
+  if (!cur.ok) return FS_ERR_WORKSPACE;
+  // pass 2 writes where fs_emb_gather_sorted / fs_emb_update_sorted look; pass 1 into the other buffers
+  uint32_t* k1 = (B.sk == B.W.k[0]) ? B.W.k[1] : B.W.k[0];
+  uint32_t* v1 = (B.sv == B.W.v[0]) ? B.W.v[1] : B.W.v[0];
+  const bool two = phase == FS_PHASE_COLLISION_THEN_EXCLUSIVE;
+  int launches = 1;
+  radix::seg_tiles_kernel<<<1, radix::kSegThreads, 0, st>>>(shard_offsets, n, T, W.seg_off[0], W.tile_base[0], err);
+  const SrcShardRows s1{sm_ids, pos, two ? is_co : nullptr, num_rows, P.block, B.kb, B.row_mask};
+  radix::run_seg_pass(s1, radix::DstU32{k1, v1}, 0, P.b1, P.b1, W, 0, B.W.pass.n_valid, nullptr, err, st, &launches);
+  const SrcShardRows2 s2{k1, v1, P.block, B.kb, B.row_mask, P.lb2, two};
+  radix::run_seg_pass(s2, radix::DstU32{B.sk, B.sv}, P.b1, P.lb2 + P.ph, P.lb2, W, 1, B.W.pass.n_valid,
+                      two ? B.n_first : nullptr, nullptr, st, &launches);
+  count_launch(launches);
+  return launch_status();
+}
+
 extern "C" fs_status fs_emb_gather_sorted(const void* table, int64_t num_rows, int32_t dim, fs_dtype dtype, int64_t T,
                                           fs_phase phase, void* out, int32_t* err, void* ws, size_t ws_bytes,
                                           fs_stream_t stream) {
+  FS_NVTX_RANGE();
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   fs_status s = check_sorted(T, num_rows, dim, dtype, phase, err, ws, ws_bytes);
   if (s != FS_OK) return s;
@@ -1071,6 +1236,7 @@ extern "C" fs_status fs_emb_gather_sorted(const void* table, int64_t num_rows, i
 extern "C" fs_status fs_emb_update_sorted(void* table, float* state, int64_t num_rows, int32_t dim, fs_dtype dtype,
                                           fs_optim optim, const void* grads, int64_t T, fs_phase phase, float lr,
                                           float eps, int32_t* err, void* ws, size_t ws_bytes, fs_stream_t stream) {
+  FS_NVTX_RANGE();
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   fs_status s = check_sorted(T, num_rows, dim, dtype, phase, err, ws, ws_bytes);
   if (s != FS_OK) return s;

@@ -23,8 +23,9 @@ struct SrcLen {
   const int32_t* L;
   static constexpr bool kFetch2 = false;
   using Raw = int32_t;
+  template <bool>
   __device__ __forceinline__ Raw fetch(int64_t i) const { return L[i]; }
-  __device__ __forceinline__ bool make(Raw l, int64_t i, Key& key, uint32_t& val, int32_t* err) const {
+  __device__ __forceinline__ bool make(Raw l, int64_t i, int, Key& key, uint32_t& val, int32_t* err) const {
     if (l < 0) {
       if (err) set_err(err, FS_ERR_INVALID_ARG);
       l = 0;
@@ -33,7 +34,7 @@ struct SrcLen {
     val = static_cast<uint32_t>(i);
     return true;
   }
-  __device__ __forceinline__ uint32_t digit(Key key, int shift, int bits) const {
+  __device__ __forceinline__ uint32_t digit(Key key, int shift, int bits, int) const {
     return (key >> shift) & ((1u << bits) - 1u);
   }
 };
@@ -389,6 +390,7 @@ extern "C" size_t fs_balance_fbs_workspace_size(int64_t S, int32_t n) {
 extern "C" fs_status fs_balance_fbs(const int32_t* uih_len, int64_t S, int32_t n, int32_t* perm,
                                     int64_t* rank_offsets, int32_t* err, void* ws, size_t ws_bytes,
                                     fs_stream_t stream) {
+  FS_NVTX_RANGE();
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (n < 1 || S < 0 || S > INT32_MAX || !rank_offsets || !err) return FS_ERR_INVALID_ARG;
   if (S > 0 && (!uih_len || !perm)) return FS_ERR_INVALID_ARG;
@@ -425,15 +427,14 @@ namespace {
 
 constexpr int64_t kNoAllocMaxS = int64_t(1) << 18;  // 262144 samples
 
-// Same layout arithmetic as radix::SortPlan::bytes() for S = kNoAllocMaxS and
-// 31-bit keys (4 passes of 8 bits: 256 digit values), at compile time.
-constexpr size_t ce_align(size_t x) { return (x + 255) / 256 * 256; }
-constexpr size_t kNoAllocTiles = size_t((kNoAllocMaxS + radix::kTile - 1) / radix::kTile);
-constexpr size_t kNoAllocChunks = (kNoAllocTiles + radix::kChunkTiles - 1) / radix::kChunkTiles;
-constexpr size_t kNoAllocScratchBytes = ce_align(256 * kNoAllocTiles * sizeof(uint32_t)) +
-                                        ce_align(256 * kNoAllocChunks * sizeof(uint32_t)) +
-                                        2 * ce_align(radix::kMaxBins * sizeof(uint32_t)) + ce_align(sizeof(int64_t)) +
-                                        4 * ce_align(size_t(kNoAllocMaxS) * sizeof(uint32_t));
+// The sort's scratch for kNoAllocMaxS samples and 31-bit keys (passes of
+// 7 + 8 + 8 + 8 bits: at most 256 digit values), computed by the same layout
+// arithmetic that carves the workspace, so the array and the carve cannot
+// drift apart; smaller S needs less.
+constexpr size_t kNoAllocScratchBytes = radix::SortPlan(kNoAllocMaxS, kLenKeyBits).bytes();
+static_assert(radix::SortPlan(kNoAllocMaxS, kLenKeyBits).nb == 256, "31-bit keys sort in 8-bit digits at most");
+static_assert(radix::SortPlan(kNoAllocMaxS - 1, kLenKeyBits).bytes() <= kNoAllocScratchBytes,
+              "the scratch need grows with S");
 
 // Lives for as long as the library is loaded, on every device that uses it.
 static __device__ __align__(256) unsigned char g_fbs_scratch[kNoAllocScratchBytes + 256];
@@ -441,8 +442,13 @@ static __device__ __align__(256) unsigned char g_fbs_scratch[kNoAllocScratchByte
 std::mutex g_scratch_mu;
 void* g_scratch_ptr[64] = {nullptr};
 
-// Device address of g_fbs_scratch on the current device, looked up once per
-// device (host code only sees a stand-in symbol, never a device address).
+// Device address of g_fbs_scratch on the current device.  Host code only sees
+// a stand-in symbol, never a device address, so the address is looked up with
+// cudaGetSymbolAddress on the first call on each device (with that device
+// current) and kept for the life of the process.  A caller that resets a
+// device (cudaDeviceReset) gets a new module instance there; the address kept
+// from before the reset no longer belongs to it, so this entry point must not
+// be called on that device after a reset.
 fs_status scratch_for_current_device(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FS_ERR_CUDA;
@@ -461,6 +467,7 @@ fs_status scratch_for_current_device(void** out) {
 
 extern "C" fs_status fs_balance_fbs_noalloc(const int32_t* uih_len, int64_t S, int32_t n, int32_t* perm,
                                             int64_t* rank_offsets, int32_t* err, fs_stream_t stream) {
+  FS_NVTX_RANGE();
   if (S > kNoAllocMaxS) return FS_ERR_INVALID_ARG;  // beyond the fixed scratch array
   if (n < 1 || S < 0 || !rank_offsets || !err) return FS_ERR_INVALID_ARG;
   if (S > 0 && (!uih_len || !perm)) return FS_ERR_INVALID_ARG;
@@ -538,6 +545,7 @@ fs_status vbs_run(const int32_t* uih_len, int64_t S, int32_t n, double alpha, in
 extern "C" fs_status fs_balance_vbs(const int32_t* uih_len, int64_t S, int32_t n, double alpha, int32_t sort_by_len,
                                     int32_t* perm, int64_t* rank_offsets, uint64_t* seg_weight, int32_t* err,
                                     void* ws, size_t ws_bytes, fs_stream_t stream) {
+  FS_NVTX_RANGE();
   return vbs_run(uih_len, S, n, alpha, sort_by_len, nullptr, perm, rank_offsets, seg_weight, err, ws, ws_bytes,
                  stream);
 }
@@ -546,6 +554,7 @@ extern "C" fs_status fs_balance_vbs_tuned(const int32_t* uih_len, int64_t S, int
                                           int32_t sort_by_len, const int64_t* batch_delta, int32_t* perm,
                                           int64_t* rank_offsets, uint64_t* seg_weight, int32_t* err, void* ws,
                                           size_t ws_bytes, fs_stream_t stream) {
+  FS_NVTX_RANGE();
   if (!batch_delta) return FS_ERR_INVALID_ARG;
   return vbs_run(uih_len, S, n, alpha, sort_by_len, batch_delta, perm, rank_offsets, seg_weight, err, ws, ws_bytes,
                  stream);
@@ -553,6 +562,7 @@ extern "C" fs_status fs_balance_vbs_tuned(const int32_t* uih_len, int64_t S, int
 
 extern "C" fs_status fs_vbs_autotune(const int64_t* times, int32_t n, int64_t step, int32_t tol_ppm,
                                      int64_t* batch_delta, int32_t* err, fs_stream_t stream) {
+  FS_NVTX_RANGE();
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (n < 1 || n > kTuneMaxRanks || step < 0 || step > INT32_MAX || tol_ppm < 0 || tol_ppm > 1000000)
     return FS_ERR_INVALID_ARG;

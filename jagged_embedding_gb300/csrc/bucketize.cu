@@ -29,14 +29,15 @@ struct SrcShard {
   float inv_block;
   int32_t n;
   using Raw = int64_t;
+  template <bool>
   __device__ __forceinline__ Raw fetch(int64_t i) const { return __ldcs(ids + i); }
-  __device__ __forceinline__ bool make(Raw id, int64_t i, Key& key, uint32_t& val, int32_t* err) const {
+  __device__ __forceinline__ bool make(Raw id, int64_t i, int, Key& key, uint32_t& val, int32_t* err) const {
     key = id;
     val = static_cast<uint32_t>(i);
     if (err && (key < 0 || key >= R)) set_err(err, FS_ERR_ID_RANGE);
     return true;
   }
-  __device__ __forceinline__ uint32_t digit(Key key, int, int) const {
+  __device__ __forceinline__ uint32_t digit(Key key, int, int, int) const {
     if (key <= 0) return 0;
     if (key >= R) return uint32_t(n - 1);
     int64_t q = static_cast<int64_t>(__float2uint_rz(__fmul_rz(__ull2float_rz(uint64_t(key)), inv_block)));
@@ -100,6 +101,7 @@ extern "C" fs_status fs_bucketize_rowwise(const int64_t* ids, int64_t T, const i
                                           int64_t num_rows, int64_t* sm_ids, int32_t* pos, int64_t* splits,
                                           int64_t* shard_offsets, int32_t* err, void* ws, size_t ws_bytes,
                                           fs_stream_t stream) {
+  FS_NVTX_RANGE();
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (T < 0 || T > INT32_MAX || n < 1 || n > radix::kMaxBins || num_rows < 1 || !rank_id_offsets || !splits ||
       !shard_offsets || !err)

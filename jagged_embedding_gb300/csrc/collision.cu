@@ -217,6 +217,7 @@ extern "C" fs_status fs_collision_split(const int64_t* ids_t, int64_t T_t, const
                                         int64_t* ex_t_shard_off, int64_t* ex_next_shard_off, uint8_t* is_co_t,
                                         uint8_t* is_co_next, int32_t* err, void* ws, size_t ws_bytes,
                                         fs_stream_t stream) {
+  FS_NVTX_RANGE();
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (T_t < 0 || T_next < 0 || T_t > INT32_MAX || T_next > INT32_MAX || num_rows < 1 ||
       num_rows > (int64_t(1) << 32) || n < 1 || cap_rows < 0 || !counts || !co_shard_off || !ex_t_shard_off ||
@@ -257,6 +258,7 @@ extern "C" size_t fs_row_bitmap_words(int64_t num_rows) { return num_rows < 1 ? 
 
 extern "C" fs_status fs_row_bitmap(const int64_t* ids, int64_t T, int64_t num_rows, uint32_t* bitmap, int32_t* err,
                                    fs_stream_t stream) {
+  FS_NVTX_RANGE();
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (T < 0 || T > INT32_MAX || num_rows < 1 || num_rows > (int64_t(1) << 32) || !bitmap || !err)
     return FS_ERR_INVALID_ARG;
@@ -284,6 +286,7 @@ extern "C" fs_status fs_collision_split_bitmaps(const int64_t* ids_t, int64_t T_
                                                 int64_t* co_shard_off, int64_t* ex_t_shard_off,
                                                 int64_t* ex_next_shard_off, uint8_t* is_co_t, uint8_t* is_co_next,
                                                 int32_t* err, void* ws, size_t ws_bytes, fs_stream_t stream) {
+  FS_NVTX_RANGE();
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (T_t < 0 || T_next < 0 || T_t > INT32_MAX || T_next > INT32_MAX || num_rows < 1 ||
       num_rows > (int64_t(1) << 32) || n < 1 || cap_rows < 0 || !counts || !co_shard_off || !ex_t_shard_off ||

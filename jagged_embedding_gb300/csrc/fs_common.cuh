@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 #include <stdint.h>
 
 #include "../../include/fs_jagged.h"
@@ -15,11 +16,22 @@ int64_t spin_limit();                  // polls before a bounded wait gives up
 int64_t debug_skip_tile();             // test hook: tile that never publishes (-1 = none)
 void count_launch(int k = 1);          // bookkeeping for fs_launch_count()
 
+// One NVTX range per C-ABI call, named after the call, so that a profiler's
+// timeline (or `ncu --nvtx --nvtx-include`) shows which call launched which
+// kernels.  With no tool attached an NVTX call is a branch on a null hook.
+struct NvtxScope {
+  explicit NvtxScope(const char* name) { nvtxRangePushA(name); }
+  ~NvtxScope() { nvtxRangePop(); }
+  NvtxScope(const NvtxScope&) = delete;
+  NvtxScope& operator=(const NvtxScope&) = delete;
+};
+#define FS_NVTX_RANGE() ::fs::NvtxScope fs_nvtx_scope_(__func__)
+
 inline fs_status launch_status() {
   return cudaGetLastError() == cudaSuccess ? FS_OK : FS_ERR_CUDA;
 }
 
-inline size_t align_up(size_t x, size_t a = 256) { return (x + a - 1) / a * a; }
+constexpr size_t align_up(size_t x, size_t a = 256) { return (x + a - 1) / a * a; }
 
 // Bump allocator over the caller's workspace (never allocates).
 struct WsCursor {
@@ -42,7 +54,10 @@ struct WsCursor {
 struct WsCounter {
   size_t used = 0;
   template <class T>
-  void take(size_t count) { used += align_up(count * sizeof(T)); }
+  T* take(size_t count) {
+    used += align_up(count * sizeof(T));
+    return nullptr;
+  }
 };
 
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }

@@ -202,6 +202,7 @@ using namespace fs;
 extern "C" fs_status fs_emb_gather(const void* table, int64_t num_rows, int32_t dim, fs_dtype dtype, const int64_t* ids,
                                    int64_t T, const uint8_t* mask, uint8_t sel, void* out, int32_t* err,
                                    fs_stream_t stream) {
+  FS_NVTX_RANGE();
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (T < 0 || T > INT32_MAX || num_rows < 0 || dim < 1 || (dtype != FS_F32 && dtype != FS_BF16) || !err)
     return FS_ERR_INVALID_ARG;

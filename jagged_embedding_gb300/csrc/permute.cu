@@ -311,6 +311,7 @@ extern "C" fs_status fs_permute_jagged(const int64_t* offsets, const int64_t* va
                                        int64_t* out_offsets, int64_t* out_values, int64_t capacity,
                                        const int64_t* rank_offsets, int32_t n, int64_t* rank_id_offsets,
                                        int32_t* err, void* ws, size_t ws_bytes, fs_stream_t stream) {
+  FS_NVTX_RANGE();
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (S < 0 || S > INT32_MAX || capacity < 0 || capacity > INT32_MAX || !out_offsets || !err)
     return FS_ERR_INVALID_ARG;
@@ -334,6 +335,7 @@ extern "C" fs_status fs_keyed_transpose(const int64_t* offsets, const int64_t* v
                                         const int64_t* row_base, int64_t* out_offsets, int64_t* out_values,
                                         int64_t capacity, int32_t* err, void* ws, size_t ws_bytes,
                                         fs_stream_t stream) {
+  FS_NVTX_RANGE();
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (F < 1 || B < 0 || F * B > INT32_MAX || capacity < 0 || capacity > INT32_MAX || !out_offsets || !err)
     return FS_ERR_INVALID_ARG;

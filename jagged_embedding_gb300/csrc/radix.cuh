@@ -21,9 +21,12 @@
 //
 // Sources (`Src`) decide where keys and values come from (a plain array, a
 // length array with the index as value, an ID array filtered by a mask ...)
-// and the digit function: fetch(i) only loads (so that a tile's loads are all
-// in flight together), fetch2(raw) (kFetch2) the loads that depend on the
-// first ones, make(raw, i, key, val, err) checks and converts.
+// and the digit function: fetch<kVal>(i) only loads (so that a tile's loads
+// are all in flight together; the upsweep passes kVal = false and needs no
+// value), fetch2(raw) (kFetch2) the loads that depend on the first ones,
+// make(raw, i, seg, key, val, err) checks and converts, digit(key, shift,
+// bits, seg) gives the digit (seg: the tile's segment under a segment-aligned
+// tiling, 0 otherwise).
 // Sinks (`Dst`) decide what is written.
 #pragma once
 
@@ -40,65 +43,120 @@ constexpr int kMaxBins = 1024;
 constexpr int kChunkTiles = 16;  // tiles per upsweep block
 constexpr int kPerT = kMaxBins / kThreads;  // digits per thread
 
-inline int64_t num_tiles(int64_t count) { return (count + kTile - 1) / kTile; }
-inline int64_t num_chunks(int64_t ntiles) { return (ntiles + kChunkTiles - 1) / kChunkTiles; }
+constexpr int64_t num_tiles(int64_t count) { return (count + kTile - 1) / kTile; }
+constexpr int64_t num_chunks(int64_t ntiles) { return (ntiles + kChunkTiles - 1) / kChunkTiles; }
 
-template <class KeyT>
-constexpr size_t downsweep_smem_bytes() {
-  size_t stage = size_t(kTile) * (sizeof(KeyT) + sizeof(uint32_t));
-  size_t hist = size_t(kWarps) * kMaxBins * sizeof(uint32_t);
-  size_t un = stage > hist ? stage : hist;
-  return un + 2 * kMaxBins * sizeof(uint32_t) + kMaxBins * sizeof(int64_t) + 64 * sizeof(uint32_t);
-}
 
-// Index of item i of lane `lane` in warp `warp` of tile `tile` (warp-striped,
+// Index, inside its tile, of item i of lane `lane` in warp `warp` (warp-striped,
 // so a warp's slot i is 32 consecutive items; slot order = item order).
-__device__ __forceinline__ int64_t item_index(int64_t tile, int warp, int i, int lane) {
-  return tile * kTile + int64_t(warp) * 32 * kItems + i * 32 + lane;
-}
+__device__ __forceinline__ int local_index(int warp, int i, int lane) { return warp * 32 * kItems + i * 32 + lane; }
+
+// ------------------------------------------------------------------ tilings
+// Which items a tile covers: [start, start + count), all in segment `seg`.
+struct TileSpan {
+  int64_t start;
+  int32_t count;
+  int32_t seg;
+};
+
+// Plain tiling: tile t covers items [t * kTile, (t + 1) * kTile) of [0, count);
+// one segment; the downsweep adds digit_base[d] (the exclusive prefix of the
+// digit totals) to every run of digit d.
+struct PlainTiles {
+  const int64_t* count_dev;  // item count on the device, or null: count_host
+  int64_t count_host;
+  const uint32_t* digit_base;
+  __device__ __forceinline__ TileSpan span(int64_t t) const {
+    const int64_t c = count_dev ? *count_dev : count_host;
+    TileSpan r{t * kTile, 0, 0};
+    if (r.start < c) r.count = int32_t(c - r.start < kTile ? c - r.start : kTile);
+    return r;
+  }
+  __device__ __forceinline__ uint32_t base(int, int d) const { return __ldg(digit_base + d); }
+};
+
+// Segment-aligned tiling: the items are already grouped into nseg segments
+// (segment s = items [seg_off[s], seg_off[s+1])), and the pass sorts each
+// segment by the digit while keeping the segments apart.  Segment s owns tiles
+// [tile_base[s], tile_base[s+1]) (ceil(size / kTile) of them), so no tile
+// spans two segments.  Digits may carry a group in their top bits
+// (d >> group_shift): the output is ordered by (group, segment, digit), which
+// lets a key bit above the segment (the update's phase) move to the top in
+// the same pass.  The downsweep adds seg_base[s][d] + group_base[g][s]:
+// seg_base = (exclusive prefix of segment s's digit counts within the
+// digit's group) - (global exclusive count of d over the tiles before the
+// segment's first tile), group_base[g][s] = items of groups below g plus
+// items of group g in segments below s (both written by seg_base_kernel and
+// seg_offsets_kernel, modulo 2^32).
+struct SegTiles {
+  const int64_t* seg_off;     // [nseg + 1]
+  const int64_t* tile_base;   // [nseg + 1]
+  const uint32_t* seg_base;   // [nseg][nb]
+  const uint32_t* group_base; // [2][nseg]
+  int32_t nseg;
+  int32_t nb;
+  int32_t group_shift;
+  __device__ __forceinline__ TileSpan span(int64_t t) const {
+    TileSpan r{0, 0, 0};
+    if (t >= tile_base[nseg]) return r;
+    int lo = 0, hi = nseg - 1;  // the last segment whose first tile is <= t (skips empty segments)
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (tile_base[mid] <= t) lo = mid; else hi = mid - 1;
+    }
+    r.seg = lo;
+    r.start = seg_off[lo] + (t - tile_base[lo]) * kTile;
+    const int64_t left = seg_off[lo + 1] - r.start;
+    r.count = int32_t(left < kTile ? (left < 0 ? 0 : left) : kTile);
+    return r;
+  }
+  __device__ __forceinline__ uint32_t base(int seg, int d) const {
+    return __ldg(seg_base + size_t(seg) * nb + d) + __ldg(group_base + size_t(d >> group_shift) * nseg + seg);
+  }
+};
 
 // ------------------------------------------------------------------ upsweep
 // Block c: tiles [c * kChunkTiles, ...) one after another.  Per tile, one
 // block-wide histogram (all item loads issued first, then one shared-memory
 // increment per item); counts[tile][d] = this chunk's count of d before the
-// tile; chunk_sums[c][d] = the chunk's count of d.
-template <class Src>
-__global__ void __launch_bounds__(kThreads) upsweep_kernel(Src src, int shift, int bits, int nb,
-                                                           const int64_t* count_dev, int64_t count_host,
+// tile; chunk_sums[c][d] = the chunk's count of d.  Empty tiles count nothing
+// but still write their counts.
+template <class Src, class Tiles>
+__global__ void __launch_bounds__(kThreads) upsweep_kernel(Src src, Tiles tiles, int shift, int bits, int nb,
                                                            uint32_t* counts, uint32_t* chunk_sums, int64_t ntiles,
                                                            int32_t* err) {
   __shared__ uint32_t hist[kMaxBins];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t chunk = blockIdx.x;
-  const int64_t count = count_dev ? *count_dev : count_host;
   uint32_t run[kPerT];
 #pragma unroll
   for (int j = 0; j < kPerT; ++j) run[j] = 0;
   for (int c = 0; c < kChunkTiles; ++c) {
     const int64_t tile = chunk * kChunkTiles + c;
     if (tile >= ntiles) break;
+    const TileSpan sp = tiles.span(tile);
     for (int j = threadIdx.x; j < nb; j += kThreads) hist[j] = 0;
     __syncthreads();
-    if (tile * kTile < count) {
+    if (sp.count > 0) {
       typename Src::Raw raw[kItems];
 #pragma unroll
       for (int i = 0; i < kItems; ++i) {
-        const int64_t idx = item_index(tile, warp, i, lane);
-        if (idx < count) raw[i] = src.fetch(idx);
+        const int l = local_index(warp, i, lane);
+        if (l < sp.count) raw[i] = src.template fetch<false>(sp.start + l);
       }
       if constexpr (Src::kFetch2) {  // loads that depend on the first ones, all issued together
 #pragma unroll
         for (int i = 0; i < kItems; ++i)
-          if (item_index(tile, warp, i, lane) < count) src.fetch2(raw[i]);
+          if (local_index(warp, i, lane) < sp.count) src.fetch2(raw[i]);
       }
 #pragma unroll
       for (int i = 0; i < kItems; ++i) {
-        const int64_t idx = item_index(tile, warp, i, lane);
+        const int l = local_index(warp, i, lane);
         typename Src::Key k;
         uint32_t v;
-        if (idx < count && src.make(raw[i], idx, k, v, err)) atomicAdd(hist + src.digit(k, shift, bits), 1u);
+        if (l < sp.count && src.make(raw[i], sp.start + l, sp.seg, k, v, err))
+          atomicAdd(hist + src.digit(k, shift, bits, sp.seg), 1u);
       }
-
     }
     __syncthreads();
 #pragma unroll
@@ -178,28 +236,38 @@ static __global__ void __launch_bounds__(kThreads) digit_base_kernel(const uint3
 }
 
 // ------------------------------------------------------------------ downsweep
-template <class Src, class Dst>
-__global__ void __launch_bounds__(kThreads, 4) downsweep_kernel(Src src, Dst dst, int shift, int bits, int nb,
-                                                                const uint32_t* digit_base, const uint32_t* counts,
-                                                                const uint32_t* chunk_base, int64_t ntiles,
-                                                                const int64_t* count_dev, int64_t count_host) {
+// Shared memory: the per-warp digit counts during ranking, then (same space)
+// the staged keys and values in tile order; behind them the tile's digit
+// counts (later each run's output offset minus its tile-local start), the
+// tile-local starts of the runs, and scan scratch.
+template <class KeyT>
+constexpr size_t downsweep_smem_bytes() {
+  size_t stage = size_t(kTile) * (sizeof(KeyT) + sizeof(uint32_t));
+  size_t hist = size_t(kWarps) * kMaxBins * sizeof(uint32_t);
+  size_t un = stage > hist ? stage : hist;
+  return un + 2 * kMaxBins * sizeof(uint32_t) + 64 * sizeof(uint32_t);
+}
+
+template <class Src, class Dst, class Tiles>
+__global__ void __launch_bounds__(kThreads, 4) downsweep_kernel(Src src, Dst dst, Tiles tiles, int shift, int bits,
+                                                                int nb, const uint32_t* counts,
+                                                                const uint32_t* chunk_base) {
   using KeyT = typename Src::Key;
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  uint32_t* warp_hist = reinterpret_cast<uint32_t*>(smem_raw);  // [kWarps][nb] (phase 1)
-  KeyT* stage_k = reinterpret_cast<KeyT*>(smem_raw);            // [kTile]      (phase 2)
+  uint32_t* warp_hist = reinterpret_cast<uint32_t*>(smem_raw);  // [kWarps][nb] (ranking)
+  KeyT* stage_k = reinterpret_cast<KeyT*>(smem_raw);            // [kTile]      (staging)
   constexpr size_t stage_bytes = size_t(kTile) * (sizeof(KeyT) + sizeof(uint32_t));
   constexpr size_t hist_bytes = size_t(kWarps) * kMaxBins * sizeof(uint32_t);
   constexpr size_t un = stage_bytes > hist_bytes ? stage_bytes : hist_bytes;
   uint32_t* stage_v = reinterpret_cast<uint32_t*>(smem_raw + size_t(kTile) * sizeof(KeyT));
-  uint32_t* tile_count = reinterpret_cast<uint32_t*>(smem_raw + un);
-  uint32_t* local_start = tile_count + kMaxBins;
-  int64_t* gbase = reinterpret_cast<int64_t*>(local_start + kMaxBins);
-  uint32_t* scratch = reinterpret_cast<uint32_t*>(gbase + kMaxBins);
+  uint32_t* run_off = reinterpret_cast<uint32_t*>(smem_raw + un);  // tile counts, then output offset - local start
+  uint32_t* local_start = run_off + kMaxBins;
+  uint32_t* scratch = local_start + kMaxBins;
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t tile = blockIdx.x;
-  const int64_t count = count_dev ? *count_dev : count_host;
-  if (tile * kTile >= count) return;
+  const TileSpan sp = tiles.span(tile);
+  if (sp.count <= 0) return;
 
   // this tile's offset inside every digit run: loaded first, so that these
   // reads overlap the item loads and the ranking below
@@ -208,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 4) downsweep_kernel(Src src, Dst dst
   for (int i = 0; i < kPerT; ++i) {
     const int d = threadIdx.x + i * kThreads;
     my_off[i] = d < nb ? __ldg(counts + tile * nb + d) + __ldg(chunk_base + (tile / kChunkTiles) * nb + d) +
-                             __ldg(digit_base + d)
+                             tiles.base(sp.seg, d)
                        : 0u;
   }
 
@@ -223,21 +291,21 @@ __global__ void __launch_bounds__(kThreads, 4) downsweep_kernel(Src src, Dst dst
     typename Src::Raw raw[kItems];
 #pragma unroll
     for (int i = 0; i < kItems; ++i) {
-      const int64_t idx = item_index(tile, warp, i, lane);
-      if (idx < count) raw[i] = src.fetch(idx);
+      const int l = local_index(warp, i, lane);
+      if (l < sp.count) raw[i] = src.template fetch<true>(sp.start + l);
     }
     if constexpr (Src::kFetch2) {
 #pragma unroll
       for (int i = 0; i < kItems; ++i)
-        if (item_index(tile, warp, i, lane) < count) src.fetch2(raw[i]);
+        if (local_index(warp, i, lane) < sp.count) src.fetch2(raw[i]);
     }
 #pragma unroll
     for (int i = 0; i < kItems; ++i) {
-      const int64_t idx = item_index(tile, warp, i, lane);
+      const int l = local_index(warp, i, lane);
       uint32_t v = 0;
-      const bool ok = idx < count && src.make(raw[i], idx, key[i], v, nullptr);
+      const bool ok = l < sp.count && src.make(raw[i], sp.start + l, sp.seg, key[i], v, nullptr);
       if constexpr (!Src::kIndexValue) val[i] = v;
-      pk[i] = ok ? (src.digit(key[i], shift, bits) << 20) : kSkipPk;
+      pk[i] = ok ? (src.digit(key[i], shift, bits, sp.seg) << 20) : kSkipPk;
     }
   }
   for (int j = threadIdx.x; j < kWarps * nb; j += kThreads) warp_hist[j] = 0;
@@ -259,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, 4) downsweep_kernel(Src src, Dst dst
   }
   __syncthreads();
 
-  // exclusive over warps per digit, tile totals, global base of each digit run
+  // exclusive over warps per digit, tile totals
 #pragma unroll
   for (int i = 0; i < kPerT; ++i) {
     const int d = threadIdx.x + i * kThreads;
@@ -271,8 +339,7 @@ __global__ void __launch_bounds__(kThreads, 4) downsweep_kernel(Src src, Dst dst
         warp_hist[w * nb + d] = run;
         run += c;
       }
-      tile_count[d] = run;
-      gbase[d] = int64_t(my_off[i]);
+      run_off[d] = run;
     }
   }
   __syncthreads();
@@ -282,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, 4) downsweep_kernel(Src src, Dst dst
     uint32_t v[kPer], sum = 0;
 #pragma unroll
     for (int i = 0; i < kPer; ++i) {
-      v[i] = d0 + i < nb ? tile_count[d0 + i] : 0u;
+      v[i] = d0 + i < nb ? run_off[d0 + i] : 0u;
       sum += v[i];
     }
     uint32_t tot;
@@ -295,28 +362,40 @@ __global__ void __launch_bounds__(kThreads, 4) downsweep_kernel(Src src, Dst dst
     if (threadIdx.x == 0) scratch[40] = tot;
   }
   __syncthreads();
+  // each run's output position minus its tile-local start: staged item j of
+  // digit d goes to run_off[d] + j (positions < 2^31, exact modulo 2^32)
+#pragma unroll
+  for (int i = 0; i < kPerT; ++i) {
+    const int d = threadIdx.x + i * kThreads;
+    if (d < nb) run_off[d] = my_off[i] - local_start[d];
+  }
 #pragma unroll
   for (int i = 0; i < kItems; ++i)
     if (pk[i] != kSkipPk) {
       const uint32_t d = pk[i] >> 20;
-      pk[i] = local_start[d] + warp_hist[warp * nb + d] + (pk[i] & 0xFFFFFu);  // tile-local position
+      pk[i] = (d << 20) | (local_start[d] + warp_hist[warp * nb + d] + (pk[i] & 0xFFFFFu));  // tile-local position
     }
   const uint32_t nvalid = scratch[40];
   __syncthreads();  // warp_hist is dead; its space becomes the staging area
 #pragma unroll
   for (int i = 0; i < kItems; ++i)
     if (pk[i] != kSkipPk) {
-      stage_k[pk[i]] = key[i];
-      if constexpr (Src::kIndexValue)
-        stage_v[pk[i]] = uint32_t(item_index(tile, warp, i, lane));
+      const uint32_t at = pk[i] & 0xFFFFFu;
+      stage_k[at] = key[i];
+      if constexpr (Src::kIndexValue)  // digit and tile-local index: no digit to recompute below
+        stage_v[at] = ((pk[i] >> 20) << 12) | uint32_t(local_index(warp, i, lane));
       else
-        stage_v[pk[i]] = val[i];
+        stage_v[at] = val[i];
     }
   __syncthreads();
   for (uint32_t j = threadIdx.x; j < nvalid; j += kThreads) {
     const KeyT k = stage_k[j];
-    const uint32_t d = src.digit(k, shift, bits);
-    dst.store(gbase[d] + int64_t(j - local_start[d]), k, stage_v[j]);
+    const uint32_t sv = stage_v[j];
+    if constexpr (Src::kIndexValue) {
+      dst.store(int64_t(run_off[sv >> 12] + j), k, uint32_t(sp.start + (sv & 0xFFFu)));
+    } else {
+      dst.store(int64_t(run_off[src.digit(k, shift, bits, sp.seg)] + j), k, sv);
+    }
   }
 }
 
@@ -330,13 +409,15 @@ struct SrcU32 {
   const uint32_t* v;
   static constexpr bool kFetch2 = false;
   using Raw = uint2;
-  __device__ __forceinline__ Raw fetch(int64_t i) const { return make_uint2(__ldcs(k + i), __ldcs(v + i)); }
-  __device__ __forceinline__ bool make(const Raw& r, int64_t, Key& key, uint32_t& val, int32_t*) const {
+  // the upsweep needs only the key (kVal false): the value is not loaded
+  template <bool kVal>
+  __device__ __forceinline__ Raw fetch(int64_t i) const { return make_uint2(__ldcs(k + i), kVal ? __ldcs(v + i) : 0u); }
+  __device__ __forceinline__ bool make(const Raw& r, int64_t, int, Key& key, uint32_t& val, int32_t*) const {
     key = r.x;
     val = r.y;
     return true;
   }
-  __device__ __forceinline__ uint32_t digit(Key key, int shift, int bits) const {
+  __device__ __forceinline__ uint32_t digit(Key key, int shift, int bits, int) const {
     return (key >> shift) & ((1u << bits) - 1u);
   }
 };
@@ -373,7 +454,7 @@ struct PassWs {
   int64_t ntiles = 0;
 };
 
-inline size_t pass_ws_bytes(int64_t count, int nb) {
+constexpr size_t pass_ws_bytes(int64_t count, int nb) {
   return align_up(size_t(nb) * size_t(num_tiles(count)) * sizeof(uint32_t)) +
          align_up(size_t(nb) * size_t(num_chunks(num_tiles(count))) * sizeof(uint32_t)) +
          2 * align_up(kMaxBins * sizeof(uint32_t)) + align_up(sizeof(int64_t));
@@ -400,16 +481,211 @@ void run_pass(const Src& src, const Dst& dst, int shift, int bits, int nb, const
     return;
   }
   const int64_t nchunks = num_chunks(P.ntiles);
-  upsweep_kernel<Src><<<unsigned(nchunks), kThreads, 0, st>>>(src, shift, bits, nb, count_dev, count_host, P.counts,
-                                                              P.chunk, P.ntiles, err);
+  const PlainTiles tiles{count_dev, count_host, P.digit_base};
+  upsweep_kernel<Src, PlainTiles><<<unsigned(nchunks), kThreads, 0, st>>>(src, tiles, shift, bits, nb, P.counts,
+                                                                          P.chunk, P.ntiles, err);
   chunk_scan_kernel<<<unsigned((nb + 31) / 32), kScanThreads, 0, st>>>(P.chunk, nchunks, nb, P.totals);
   digit_base_kernel<<<1, kThreads, 0, st>>>(P.totals, nb, P.digit_base, P.n_valid);
   const size_t smem = downsweep_smem_bytes<typename Src::Key>();
-  set_smem(downsweep_kernel<Src, Dst>, smem);
-  downsweep_kernel<Src, Dst><<<unsigned(P.ntiles), kThreads, smem, st>>>(src, dst, shift, bits, nb, P.digit_base,
-                                                                         P.counts, P.chunk, P.ntiles, count_dev,
-                                                                         count_host);
+  set_smem(downsweep_kernel<Src, Dst, PlainTiles>, smem);
+  downsweep_kernel<Src, Dst, PlainTiles><<<unsigned(P.ntiles), kThreads, smem, st>>>(src, dst, tiles, shift, bits, nb,
+                                                                                     P.counts, P.chunk);
   *launches += 4;
+}
+
+// ------------------------------------------------------------------ segment-aligned passes
+// Passes that sort every segment of an array already grouped into segments
+// (the update's sort of shard-major IDs: one segment per shard), under
+// SegTiles.  One pass = upsweep, chunk scan, seg_base_kernel (the digit
+// bases of every segment), seg_offsets_kernel (the group bases, and the
+// segments and tiles of the pass's output for the next pass), downsweep.
+constexpr int kSegThreads = 1024;  // segments handled by one block: nseg <= kSegThreads
+
+// Segment offsets of the input, made safe to tile: seg_off[s] = the running
+// maximum of in[0..s] clamped to [0, count], seg_off[0] = 0, seg_off[nseg] =
+// count (an input that breaks these rules sets FS_ERR_BAD_OFFSETS);
+// tile_base[s] = tiles of the segments before s (ceil(size / kTile) each).
+static __global__ void __launch_bounds__(kSegThreads) seg_tiles_kernel(const int64_t* in, int32_t nseg, int64_t count,
+                                                                      int64_t* seg_off, int64_t* tile_base,
+                                                                      int32_t* err) {
+  __shared__ int64_t off[kSegThreads + 1];
+  __shared__ int64_t tmp[32];
+  for (int s = threadIdx.x; s <= nseg; s += blockDim.x) off[s] = in[s];
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    bool bad = off[0] != 0 || off[nseg] != count;
+    int64_t run = 0;
+    for (int s = 0; s <= nseg; ++s) {
+      int64_t v = off[s] < 0 ? 0 : (off[s] > count ? count : off[s]);
+      if (off[s] < run) bad = true;
+      run = v > run ? v : run;
+      off[s] = (s == 0) ? 0 : (s == nseg ? count : run);
+    }
+    if (bad) set_err(err, FS_ERR_BAD_OFFSETS);
+  }
+  __syncthreads();
+  const int s = threadIdx.x;
+  const int64_t n = s < nseg ? (off[s + 1] - off[s] + kTile - 1) / kTile : 0;
+  int64_t total;
+  const int64_t before = block_exclusive_scan<int64_t>(n, tmp, &total);
+  if (s < nseg) {
+    seg_off[s] = off[s];
+    tile_base[s] = before;
+  }
+  if (s == 0) {
+    seg_off[nseg] = count;
+    tile_base[nseg] = total;
+  }
+}
+
+// Per segment s (one block each): H[d] = global exclusive count of digit d
+// over the tiles before the segment's first tile (the totals when it has
+// none), the segment's digit counts c[d] = H_{s+1}[d] - H_s[d], their
+// exclusive prefix within each group (groups: d >> group_shift, at most two),
+// seg_base[s][d] = that prefix - H_s[d] (mod 2^32) and gtot[s][g] = the
+// segment's items in group g.
+static __global__ void __launch_bounds__(kThreads) seg_base_kernel(const uint32_t* counts, const uint32_t* chunk_base,
+                                                              const uint32_t* totals, const int64_t* tile_base,
+                                                              int32_t nseg, int nb, int group_shift,
+                                                              uint32_t* seg_base, uint32_t* gtot) {
+  __shared__ uint32_t tmp[32];
+  __shared__ uint32_t g0;
+  const int s = blockIdx.x;
+  const int64_t tiles = tile_base[nseg];
+  const int64_t f0 = tile_base[s], f1 = tile_base[s + 1];
+  auto G = [&](int64_t f, int d) -> uint32_t {
+    return f < tiles ? counts[f * nb + d] + chunk_base[(f / kChunkTiles) * nb + d] : totals[d];
+  };
+  constexpr int kPer = kMaxBins / kThreads;
+  const int d0 = threadIdx.x * kPer;  // contiguous digits per thread: the scan runs in digit order
+  const int gsize = 1 << group_shift;
+  uint32_t h[kPer], c[kPer], sum = 0;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int d = d0 + i;
+    h[i] = d < nb ? G(f0, d) : 0u;
+    c[i] = d < nb ? G(f1, d) - h[i] : 0u;
+    sum += c[i];
+  }
+  if (threadIdx.x == 0) g0 = 0;
+  uint32_t tot;
+  uint32_t run = block_exclusive_scan<uint32_t>(sum, tmp, &tot);  // (ends with a barrier)
+  uint32_t ex[kPer];
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    ex[i] = run;
+    if (d0 + i == gsize) g0 = run;  // items of group 0 (digits below gsize)
+    run += c[i];
+  }
+  __syncthreads();
+  const uint32_t g0tot = gsize < nb ? g0 : tot;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int d = d0 + i;
+    if (d < nb) seg_base[size_t(s) * nb + d] = ex[i] - (d >= gsize ? g0tot : 0u) - h[i];
+  }
+  if (threadIdx.x == 0) {
+    gtot[2 * s] = g0tot;
+    gtot[2 * s + 1] = tot - g0tot;
+  }
+}
+
+// One block of kSegThreads threads: group_base[g][s] = items of the groups
+// below g plus items of group g in the segments below s; the output's
+// segments (next_seg_off: the segments' valid items, in segment order) and
+// their first tiles (next_tile_base) for the next pass; *n_valid = all valid
+// items, *n_first = items of group 0 (when n_first is not null).
+static __global__ void __launch_bounds__(kSegThreads) seg_offsets_kernel(const uint32_t* gtot, int32_t nseg,
+                                                                        uint32_t* group_base, int64_t* next_seg_off,
+                                                                        int64_t* next_tile_base, int64_t* n_valid,
+                                                                        int64_t* n_first) {
+  __shared__ int64_t tmp[32];
+  const int s = threadIdx.x;
+  const int64_t a = s < nseg ? int64_t(gtot[2 * s]) : 0, b = s < nseg ? int64_t(gtot[2 * s + 1]) : 0;
+  int64_t ta, tb, tt;
+  const int64_t ea = block_exclusive_scan<int64_t>(a, tmp, &ta);
+  const int64_t eb = block_exclusive_scan<int64_t>(b, tmp, &tb);
+  const int64_t et = block_exclusive_scan<int64_t>((a + b + kTile - 1) / kTile, tmp, &tt);
+  if (s < nseg) {
+    group_base[s] = uint32_t(ea);
+    group_base[nseg + s] = uint32_t(ta + eb);
+    next_seg_off[s] = ea + eb;
+    next_tile_base[s] = et;
+  }
+  if (s == 0) {
+    next_seg_off[nseg] = ta + tb;
+    next_tile_base[nseg] = tt;
+    *n_valid = ta + tb;
+    if (n_first) *n_first = ta;
+  }
+}
+
+// Scratch of the segment-aligned passes over up to `count` items in nseg segments.
+struct SegWs {
+  int32_t nseg = 0;
+  int64_t max_tiles = 0;
+  uint32_t* counts = nullptr;      // [max_tiles][kMaxBins]
+  uint32_t* chunk = nullptr;       // [chunks][kMaxBins]
+  uint32_t* totals = nullptr;      // [kMaxBins]
+  uint32_t* seg_base = nullptr;    // [nseg][kMaxBins]
+  uint32_t* gtot = nullptr;        // [nseg][2]
+  uint32_t* group_base = nullptr;  // [2][nseg]
+  int64_t* seg_off[2] = {nullptr, nullptr};    // [nseg + 1] each: a pass's input segments
+  int64_t* tile_base[2] = {nullptr, nullptr};  // [nseg + 1] each
+};
+
+constexpr int64_t seg_max_tiles(int64_t count, int32_t nseg) { return num_tiles(count) + nseg; }
+
+template <class Ws>
+inline void take_seg_ws(int64_t count, int32_t nseg, Ws& ws, SegWs* W) {
+  const int64_t mt = seg_max_tiles(count, nseg);
+  uint32_t* c = ws.template take<uint32_t>(size_t(mt) * kMaxBins);
+  uint32_t* ch = ws.template take<uint32_t>(size_t(num_chunks(mt)) * kMaxBins);
+  uint32_t* tot = ws.template take<uint32_t>(kMaxBins);
+  uint32_t* sb = ws.template take<uint32_t>(size_t(nseg) * kMaxBins);
+  uint32_t* gt = ws.template take<uint32_t>(size_t(nseg) * 2);
+  uint32_t* gb = ws.template take<uint32_t>(size_t(nseg) * 2);
+  int64_t* so0 = ws.template take<int64_t>(size_t(nseg) + 1);
+  int64_t* so1 = ws.template take<int64_t>(size_t(nseg) + 1);
+  int64_t* tb0 = ws.template take<int64_t>(size_t(nseg) + 1);
+  int64_t* tb1 = ws.template take<int64_t>(size_t(nseg) + 1);
+  if (W) {
+    W->nseg = nseg;
+    W->max_tiles = mt;
+    W->counts = c;
+    W->chunk = ch;
+    W->totals = tot;
+    W->seg_base = sb;
+    W->gtot = gt;
+    W->group_base = gb;
+    W->seg_off[0] = so0;
+    W->seg_off[1] = so1;
+    W->tile_base[0] = tb0;
+    W->tile_base[1] = tb1;
+  }
+}
+
+// One segment-aligned pass reading the segments in slot `in` (seg_off[in],
+// tile_base[in]) and writing the next pass's segments to the other slot.
+// Digit of `bits` bits, of which the bits from group_shift up are the group.
+template <class Src, class Dst>
+void run_seg_pass(const Src& src, const Dst& dst, int shift, int bits, int group_shift, const SegWs& W, int in,
+                  int64_t* n_valid, int64_t* n_first, int32_t* err, cudaStream_t st, int* launches) {
+  const int nb = 1 << bits;
+  const SegTiles tiles{W.seg_off[in], W.tile_base[in], W.seg_base, W.group_base, W.nseg, nb, group_shift};
+  const int64_t nchunks = num_chunks(W.max_tiles);
+  upsweep_kernel<Src, SegTiles><<<unsigned(nchunks), kThreads, 0, st>>>(src, tiles, shift, bits, nb, W.counts,
+                                                                        W.chunk, W.max_tiles, err);
+  chunk_scan_kernel<<<unsigned((nb + 31) / 32), kScanThreads, 0, st>>>(W.chunk, nchunks, nb, W.totals);
+  seg_base_kernel<<<unsigned(W.nseg), kThreads, 0, st>>>(W.counts, W.chunk, W.totals, W.tile_base[in], W.nseg, nb,
+                                                          group_shift, W.seg_base, W.gtot);
+  seg_offsets_kernel<<<1, kSegThreads, 0, st>>>(W.gtot, W.nseg, W.group_base, W.seg_off[1 - in],
+                                                W.tile_base[1 - in], n_valid, n_first);
+  const size_t smem = downsweep_smem_bytes<typename Src::Key>();
+  set_smem(downsweep_kernel<Src, Dst, SegTiles>, smem);
+  downsweep_kernel<Src, Dst, SegTiles><<<unsigned(W.max_tiles), kThreads, smem, st>>>(src, dst, tiles, shift, bits, nb,
+                                                                                      W.counts, W.chunk);
+  *launches += 5;
 }
 
 // LSD sort of (uint32 key, uint32 value) pairs drawn from Src0 (the items of
@@ -423,21 +699,23 @@ void run_pass(const Src& src, const Dst& dst, int shift, int bits, int nb, const
 struct SortPlan {
   int64_t count = 0;
   int key_bits = 1, passes = 1, nb = 2;  // nb: digit values of the widest pass
-  SortPlan() = default;
-  SortPlan(int64_t c, int kb) : count(c), key_bits(kb < 1 ? 1 : kb) {
-    passes = (key_bits + 9) / 10;
+  constexpr SortPlan() = default;
+  constexpr SortPlan(int64_t c, int kb)
+      : count(c), key_bits(kb < 1 ? 1 : kb), passes(((kb < 1 ? 1 : kb) + 9) / 10), nb(0) {
     nb = 1 << bits(passes - 1);
   }
-  int bits(int p) const {  // width of pass p
+  constexpr int bits(int p) const {  // width of pass p
     const int base = key_bits / passes, extra = key_bits % passes;
     return base + (p >= passes - extra ? 1 : 0);
   }
-  int shift(int p) const {
+  constexpr int shift(int p) const {
     int s = 0;
     for (int q = 0; q < p; ++q) s += bits(q);
     return s;
   }
-  size_t bytes() const { return pass_ws_bytes(count, nb) + 4 * align_up(size_t(count) * sizeof(uint32_t)); }
+  constexpr size_t bytes() const {
+    return pass_ws_bytes(count, nb) + 4 * align_up(size_t(count) * sizeof(uint32_t));
+  }
 };
 
 struct SortWs {

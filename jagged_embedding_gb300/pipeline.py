@@ -72,6 +72,8 @@ class Pipeline:
             "ex_next_off": torch.empty(w.n + 1, dtype=torch.int64, device=dev),
         }
         self.masks = [torch.zeros(self.max_T, dtype=torch.uint8, device=dev) for _ in range(2)]
+        # order of each slot's mask: "batch" (aligned with ids) or "shard" (aligned with sm_ids)
+        self.mask_layout = ["batch", "batch"]
         self.out = [torch.empty(self.max_T, w.D, dtype=table.dtype, device=dev)]
         if two_outputs:
             self.out.append(torch.empty(self.max_T, w.D, dtype=table.dtype, device=dev))
@@ -86,6 +88,8 @@ class Pipeline:
             L.fs_bucketize_rowwise_workspace_size(self.max_T, w.n),
             L.fs_collision_split_bitmaps_workspace_size(w.R),
             B.backward_workspace_size(self.max_T, w.R, w.D, B.dtype_code(table)) if w.has_update else 0,
+            B.sort_rows_sharded_workspace_size(self.max_T, w.R, w.D, B.dtype_code(table), w.n)
+            if w.has_update and w.n <= 1024 else 0,
         )
         # one workspace, reused by every call (calls on one stream run in order)
         self.ws = B.workspace(ws_bytes, dev)
@@ -113,7 +117,9 @@ class Pipeline:
                                 out_values=s.cand_lens, err=self.err, ws=self.ws)
         B.fs_bucketize_rowwise(s.ids, s.rank_id_offsets, w.R, sm_ids=s.sm_ids, pos=s.pos, splits=s.splits,
                                shard_offsets=s.shard_offsets, err=self.err, ws=self.ws, T=T)
-        B.fs_row_bitmap(s.ids, w.R, bitmap=s.bitmap, err=self.err, T=T)
+        # the row set does not depend on the order; in shard-major order the IDs a warp marks
+        # fall in one shard's stretch of the bitmap
+        B.fs_row_bitmap(s.sm_ids, w.R, bitmap=s.bitmap, err=self.err, T=T)
         s.T = T
 
     def autotune(self, times):
@@ -122,19 +128,28 @@ class Pipeline:
         w = self.w
         B.fs_vbs_autotune(times, self.batch_delta, step=w.tune_step, tol_ppm=w.tune_tol_ppm, err=self.err)
 
-    def collision(self, slot_t, slot_next, want_t_mask=True, want_next_mask=True):
-        """Collision / exclusive split of (t, t+1) (Algorithm 2 line 10); masks are batch-major.
+    def collision(self, slot_t, slot_next, want_t_mask=True, want_next_mask=True, shard_major=False):
+        """Collision / exclusive split of (t, t+1) (Algorithm 2 line 10).
 
         The mask of t gives the update its phases; the mask of t+1 only serves
-        the prioritized order's masked gathers of t+1.
+        the prioritized order's masked gathers of t+1.  The masks are aligned
+        with the batch-major IDs, or with the shard-major IDs when shard_major
+        (Algorithm 2 computes the split on the shard-major form; the sets are
+        the same either way).
         """
         a, b = self.slots[slot_t], self.slots[slot_next]
         out = dict(self.coll)
         out["is_co_t"] = self.masks[slot_t]
         out["is_co_next"] = self.masks[slot_next]
-        B.fs_collision_split_bitmaps(a.ids, a.bitmap, b.ids, b.bitmap, self.w.R, self.w.n, out, self.cap_rows,
+        ids_t, ids_n = (a.sm_ids, b.sm_ids) if shard_major else (a.ids, b.ids)
+        B.fs_collision_split_bitmaps(ids_t, a.bitmap, ids_n, b.bitmap, self.w.R, self.w.n, out, self.cap_rows,
                                      err=self.err, ws=self.ws, T_t=a.T, T_next=b.T, want_t_mask=want_t_mask,
                                      want_next_mask=want_next_mask)
+        layout = "shard" if shard_major else "batch"
+        if want_t_mask:
+            self.mask_layout[slot_t] = layout
+        if want_next_mask:
+            self.mask_layout[slot_next] = layout
 
     def gather(self, slot, out_idx=0, mask=None, sel=1, sorted_phase=None):
         """Lookup of the batch in `slot` (Algorithm 2 lines 12, 15); with sorted_phase, from the entries
@@ -146,15 +161,29 @@ class Pipeline:
             B.fs_emb_gather(self.table, s.ids, out=self.out[out_idx], mask=mask, sel=sel, err=self.err, T=s.T)
 
     def sort_rows(self, slot, phase):
-        """The update's sort of the batch in `slot`, ahead of its gather (collision flags from its mask)."""
+        """The update's sort of the batch in `slot`, ahead of its gather (collision flags from its mask):
+        per shard from the shard-major IDs when the shards allow it, else over the batch-major IDs."""
         s = self.slots[slot]
-        B.fs_emb_sort_rows(self.table, s.ids, self.ws, phase=phase,
-                           is_co=self.masks[slot] if phase != B.PHASE_ALL else None, err=self.err, T=s.T)
+        two = phase != B.PHASE_ALL
+        if self._sharded_ok(phase):
+            assert not two or self.mask_layout[slot] == "shard"
+            B.fs_emb_sort_rows_sharded(self.table, s.sm_ids, s.pos, s.shard_offsets, self.ws, phase=phase,
+                                       is_co=self.masks[slot] if two else None, err=self.err, T=s.T)
+        else:
+            assert not two or self.mask_layout[slot] == "batch"
+            B.fs_emb_sort_rows(self.table, s.ids, self.ws, phase=phase, is_co=self.masks[slot] if two else None,
+                               err=self.err, T=s.T)
 
     def update_sorted(self, slot, grads, phase):
         w, s = self.w, self.slots[slot]
         B.fs_emb_update_sorted(self.table, self.state, grads, s.T, self.ws, w.optim, w.lr, w.eps, phase=phase,
                                err=self.err)
+
+    def _sharded_ok(self, phase):
+        # the per-shard sort: at most 1024 shards; a shard's row offsets (and the phase bit) in 20 bits
+        block = -(-self.w.R // self.w.n)
+        limit = 1 << (19 if phase != B.PHASE_ALL else 20)
+        return self.row_sorted and self.w.n <= 1024 and block <= limit
 
     def _sorted_ok(self, phase):
         # the phase bit must fit beside the row bits; 16-byte aligned rows for the gather
@@ -176,22 +205,26 @@ class Pipeline:
 
         The update takes its collision flags from the mask of t (one pass over the
         IDs; reading t+1's row bitmap inside the sort passes instead was measured
-        slower).  want_masks also writes the mask of t+1.  With AutoTune on,
+        slower), computed in shard-major order when the update sorts per shard
+        (or has nothing to sort): self.mask_layout says which.  want_masks also
+        writes the mask of t+1.  With AutoTune on,
         `times` (the ranks' latest step times) is folded into the corrections
         before t+1 is prepared.
         Returns the slot that now holds t+1.
         """
         nxt = 1 - cur
+        # one sort, collision rows updated first, then exclusive rows
+        phase = B.PHASE_COLLISION_THEN_EXCLUSIVE if has_next else B.PHASE_ALL
+        # masks in shard-major order unless the update reads them batch-major
+        shard_major = not self.w.has_update or (self._sorted_ok(phase) and self._sharded_ok(phase))
         if has_next:
             if times is not None and self.w.autotune:
                 self.autotune(times)
             self.prepare(nxt_batch, nxt)
-            self.collision(cur, nxt, want_t_mask=True, want_next_mask=want_masks)
+            self.collision(cur, nxt, want_t_mask=True, want_next_mask=want_masks, shard_major=shard_major)
         if not self.w.has_update:
             self.gather(cur)
             return nxt
-        # one sort, collision rows updated first, then exclusive rows
-        phase = B.PHASE_COLLISION_THEN_EXCLUSIVE if has_next else B.PHASE_ALL
         if self._sorted_ok(phase):
             self.sort_rows(cur, phase)
             self.gather(cur, sorted_phase=phase)

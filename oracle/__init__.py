@@ -44,6 +44,11 @@ def lib():
             "oracle_collision_split": [P, i64, P, i64, i64, i32, P, P, P, i64, P, P, P, P, P, P],
             "oracle_emb_gather": [P, i64, i64, P, i64, P, u8, P],
             "oracle_emb_backward": [P, P, i64, i32, i32, i32, P, P, i64, P, i32, f64, f64, P, P, P],
+            "oracle_permute_jagged_mt": [P, P, i64, P, P, P, i32],
+            "oracle_bucketize_rowwise_mt": [P, i64, P, i32, i64, P, P, P, P, i32],
+            "oracle_collision_split_mt": [P, i64, P, i64, i64, i32, P, P, P, i64, P, P, P, P, P, P, i32],
+            "oracle_emb_gather_mt": [P, i64, i64, P, i64, P, u8, P, i32],
+            "oracle_emb_backward_mt": [P, P, i64, i32, i32, i32, P, P, i64, P, i32, f64, f64, i32],
         }
         for name, args in sig.items():
             fn = getattr(L, name)
@@ -57,6 +62,21 @@ def lib():
         L.oracle_double_to_bf16.restype = C.c_uint16
         _lib = L
     return _lib
+
+
+_threads = 1
+
+
+def set_threads(k):
+    """Host threads the oracle's steps use from now on (1 = the single-threaded functions).  With k > 1 the
+    permute, bucketize, collision split, gather and update run their *_mt variants, which give the same
+    results; the balance stays single-threaded (a sort of the S sample lengths)."""
+    global _threads
+    _threads = max(1, int(k))
+
+
+def threads():
+    return _threads
 
 
 def _p(a):
@@ -130,7 +150,10 @@ def permute_jagged(offsets, values, perm):
     S = off.shape[0] - 1
     out_off = np.empty(S + 1, np.int64)
     out_val = np.empty(val.shape[0], np.int64)
-    _check(lib().oracle_permute_jagged(_p(off), _p(val), S, _p(pm), _p(out_off), _p(out_val)))
+    if _threads > 1:
+        _check(lib().oracle_permute_jagged_mt(_p(off), _p(val), S, _p(pm), _p(out_off), _p(out_val), _threads))
+    else:
+        _check(lib().oracle_permute_jagged(_p(off), _p(val), S, _p(pm), _p(out_off), _p(out_val)))
     return out_off, out_val
 
 
@@ -153,7 +176,11 @@ def bucketize_rowwise(ids, rank_id_offsets, n, R):
     pos = np.empty(T, np.int32)
     splits = np.empty(n * n, np.int64)
     so = np.empty(n + 1, np.int64)
-    _check(lib().oracle_bucketize_rowwise(_p(x), T, _p(rio), n, R, _p(sm), _p(pos), _p(splits), _p(so)))
+    if _threads > 1:
+        _check(lib().oracle_bucketize_rowwise_mt(_p(x), T, _p(rio), n, R, _p(sm), _p(pos), _p(splits), _p(so),
+                                                 _threads))
+    else:
+        _check(lib().oracle_bucketize_rowwise(_p(x), T, _p(rio), n, R, _p(sm), _p(pos), _p(splits), _p(so)))
     return sm, pos, splits.reshape(n, n), so
 
 
@@ -168,8 +195,12 @@ def collision_split(ids_t, ids_next, R, n):
     offs = [np.empty(n + 1, np.int64) for _ in range(3)]
     m_t = np.empty(a.shape[0], np.uint8)
     m_n = np.empty(b.shape[0], np.uint8)
-    _check(lib().oracle_collision_split(_p(a), a.shape[0], _p(b), b.shape[0], R, n, _p(co), _p(ext), _p(exn), cap,
-                                        _p(counts), _p(offs[0]), _p(offs[1]), _p(offs[2]), _p(m_t), _p(m_n)))
+    args = (_p(a), a.shape[0], _p(b), b.shape[0], R, n, _p(co), _p(ext), _p(exn), cap, _p(counts), _p(offs[0]),
+            _p(offs[1]), _p(offs[2]), _p(m_t), _p(m_n))
+    if _threads > 1:
+        _check(lib().oracle_collision_split_mt(*args, _threads))
+    else:
+        _check(lib().oracle_collision_split(*args))
     c0, c1, c2 = (int(v) for v in counts)
     return {"co": co[:c0].copy(), "ex_t": ext[:c1].copy(), "ex_next": exn[:c2].copy(),
             "co_off": offs[0], "ex_t_off": offs[1], "ex_next_off": offs[2],
@@ -195,7 +226,10 @@ def emb_gather(table, ids, mask=None, sel=1, out=None):
         out = np.zeros((T,) + tb.shape[1:], tb.dtype)
     m = None if mask is None else _c(mask, np.uint8)
     rb = tb.dtype.itemsize * (tb.shape[1] if tb.ndim > 1 else 1)
-    _check(lib().oracle_emb_gather(_p(tb), tb.shape[0], rb, _p(x), T, _p(m), int(sel), _p(out)))
+    if _threads > 1:
+        _check(lib().oracle_emb_gather_mt(_p(tb), tb.shape[0], rb, _p(x), T, _p(m), int(sel), _p(out), _threads))
+    else:
+        _check(lib().oracle_emb_gather(_p(tb), tb.shape[0], rb, _p(x), T, _p(m), int(sel), _p(out)))
     return out
 
 
@@ -220,6 +254,10 @@ def emb_backward(table, state, ids, grads, optim, lr, eps=0.0, is_co=None, phase
     if want_sums:
         g_out = np.empty((T, D), np.float64)
         rows = np.empty(T, np.int64)
+    if _threads > 1 and not want_sums:
+        _check(lib().oracle_emb_backward_mt(_p(table), _p(state) if oc == 1 else None, R, D, dt, oc, _p(x),
+                                            _p(grads), T, _p(m), int(phase), float(lr), float(eps), _threads))
+        return None
     _check(lib().oracle_emb_backward(_p(table), _p(state) if oc == 1 else None, R, D, dt, oc, _p(x), _p(grads), T,
                                      _p(m), int(phase), float(lr), float(eps), _p(g_out), _p(rows), _p(nrows)))
     if want_sums:
@@ -275,18 +313,23 @@ def _prepare_all(w, batches, times_list):
     return preps
 
 
-def run_sync(w, batches, table, state, grads_list, times_list=None):
+def run_sync(w, batches, table, state, grads_list, times_list=None, keep_tables=False):
     """Synchronous schedule: for each iteration t, out_t = gather(W, I_t), then W <- update(W, G_t, I_t).
 
     Collision rows of t (rows shared with t+1) are updated before exclusive rows
     (same result: the two row sets are disjoint).  Returns per-iteration dicts
-    and updates table/state in place.
+    and updates table/state in place.  keep_tables also records copies of the
+    table (and state) before the gather of t and of the table after its update.
     """
     preps = _prepare_all(w, batches, times_list)
     res = []
     for t, pr in enumerate(preps):
+        r = {"prep": pr}
+        if keep_tables:
+            r["table_before"] = table.copy()
+            r["state_before"] = None if state is None else state.copy()
         out = emb_gather(table, pr["ids"])
-        r = {"prep": pr, "out": out}
+        r["out"] = out
         if t + 1 < len(preps):
             r["coll"] = collision_split(pr["ids"], preps[t + 1]["ids"], w.R, w.n)
         if w.has_update:
@@ -297,6 +340,8 @@ def run_sync(w, batches, table, state, grads_list, times_list=None):
                 emb_backward(table, state, pr["ids"], G, w.optim, w.lr, w.eps, is_co=m, phase=2)
             else:
                 emb_backward(table, state, pr["ids"], G, w.optim, w.lr, w.eps)
+        if keep_tables:
+            r["table_after"] = table.copy()
         res.append(r)
     return res
 

@@ -3,7 +3,7 @@
 // TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
 // benchmark's CPU-baseline / reference arm may load this library.  It shares
 // no code, header, table or constant with the CUDA library; it is plain,
-// single-threaded C++17 written from the definitions on the pages:
+// C++17 written from the definitions on the pages:
 //
 //   FreeScale: Distributed Training for Sequence Recommendation Models with
 //   Minimal Scaling Cost (arXiv 2604.24073), referred to below as "FreeScale".
@@ -11,17 +11,24 @@
 // Every function states the passage it follows.  Accumulations are in fp64.
 // Each step is the plain definition of its result (sorts are std:: library
 // sorts, sets are std:: set algorithms) except FBS and VBS, which are
-// heuristics and are written out step by step.
+// heuristics and are written out step by step.  These functions are
+// single-threaded.  At the end of the file, *_mt variants of the steps whose
+// work splits into independent pieces (samples, positions, rows) compute the
+// same results on several host threads; they exist only to time the oracle
+// on every core of the host, and the CPU tests prove them identical to the
+// single-threaded functions.
 //
 // Return value of every entry point: 0 = ok, 1 = invalid argument,
 // 2 = an ID outside [0, R), 3 = malformed offsets / permutation.
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
 #include <map>
 #include <numeric>
+#include <thread>
 #include <vector>
 
 namespace {
@@ -516,5 +523,268 @@ int oracle_emb_backward(void* table, float* state, int64_t R, int32_t D, int32_t
 // Helpers the tests use to read and write single bf16 values.
 double oracle_bf16_to_double(uint16_t h) { return bf16_to_double(h); }
 uint16_t oracle_double_to_bf16(double x) { return double_to_bf16(x); }
+
+}  // extern "C"
+
+// ===========================================================================
+// Multi-threaded variants (for timing the oracle on all host cores).  Each
+// computes exactly what the single-threaded function of the same name
+// computes, with the work split into independent pieces: samples for the
+// permute, positions for the gather and the masks, rows for the collision
+// sets and the update.  Invalid inputs give the same return code; the outputs
+// are then unspecified (the single-threaded functions may have written part
+// of them, these check everything before writing).
+// ===========================================================================
+namespace {
+
+// Run f(k, lo, hi) on `threads` threads over contiguous pieces of [0, n).
+template <class F>
+void parallel_ranges(int64_t n, int threads, F f) {
+  if (threads < 1) threads = 1;
+  if (n < 1) return;
+  if (threads > n) threads = static_cast<int>(n);
+  std::vector<std::thread> pool;
+  for (int k = 0; k < threads; ++k) {
+    int64_t lo = n * k / threads, hi = n * (k + 1) / threads;
+    pool.emplace_back([=]() { f(k, lo, hi); });
+  }
+  for (auto& t : pool) t.join();
+}
+
+// Sort v on `threads` threads: each sorts one piece, then neighbouring pieces
+// are merged pairwise, round after round.
+template <class T>
+void parallel_sort(std::vector<T>& v, int threads) {
+  const int64_t n = static_cast<int64_t>(v.size());
+  if (threads < 2 || n < 2) {
+    std::sort(v.begin(), v.end());
+    return;
+  }
+  if (threads > n) threads = static_cast<int>(n);
+  std::vector<int64_t> cut(threads + 1);
+  for (int k = 0; k <= threads; ++k) cut[k] = n * k / threads;
+  parallel_ranges(threads, threads, [&](int, int64_t lo, int64_t hi) {
+    for (int64_t k = lo; k < hi; ++k) std::sort(v.begin() + cut[k], v.begin() + cut[k + 1]);
+  });
+  for (int width = 1; width < threads; width *= 2) {
+    std::vector<std::thread> pool;
+    for (int k = 0; k + width < threads; k += 2 * width) {
+      const int64_t a = cut[k], m = cut[k + width], b = cut[std::min(k + 2 * width, threads)];
+      pool.emplace_back([&v, a, m, b]() { std::inplace_merge(v.begin() + a, v.begin() + m, v.begin() + b); });
+    }
+    for (auto& t : pool) t.join();
+  }
+}
+
+}  // namespace
+
+extern "C" {
+
+// oracle_permute_jagged on several threads: the output offsets are the same
+// prefix of the permuted lengths; the samples are then copied in pieces.
+int oracle_permute_jagged_mt(const int64_t* offsets, const int64_t* values, int64_t S, const int32_t* perm,
+                             int64_t* out_offsets, int64_t* out_values, int32_t threads) {
+  if (S < 0) return 1;
+  for (int64_t g = 0; g < S; ++g)
+    if (offsets[g + 1] < offsets[g]) return 3;
+  for (int64_t k = 0; k < S; ++k)
+    if (perm[k] < 0 || perm[k] >= S) return 3;
+  out_offsets[0] = 0;
+  for (int64_t k = 0; k < S; ++k) out_offsets[k + 1] = out_offsets[k] + (offsets[perm[k] + 1] - offsets[perm[k]]);
+  parallel_ranges(S, threads, [&](int, int64_t lo, int64_t hi) {
+    for (int64_t k = lo; k < hi; ++k) {
+      const int64_t g = perm[k];
+      std::copy(values + offsets[g], values + offsets[g + 1], out_values + out_offsets[k]);
+    }
+  });
+  return 0;
+}
+
+// oracle_bucketize_rowwise on several threads.  A stable sort by shard is a
+// counting sort: each thread counts the shards of one contiguous range of
+// positions; the start of (shard s, thread k) is the number of positions in
+// shards below s plus those of shard s in the ranges of threads below k; each
+// thread then writes its range in position order.
+int oracle_bucketize_rowwise_mt(const int64_t* ids, int64_t T, const int64_t* rank_id_offsets, int32_t n, int64_t R,
+                                int64_t* sm_ids, int32_t* pos, int64_t* splits, int64_t* shard_offsets,
+                                int32_t threads) {
+  if (n <= 0 || R <= 0 || T < 0) return 1;
+  if (rank_id_offsets[0] != 0 || rank_id_offsets[n] != T) return 3;
+  for (int32_t r = 0; r < n; ++r)
+    if (rank_id_offsets[r + 1] < rank_id_offsets[r]) return 3;
+  for (int64_t p = 0; p < T; ++p)
+    if (ids[p] < 0 || ids[p] >= R) return 2;
+  const int64_t block = (R + n - 1) / n;
+  if (threads < 1) threads = 1;
+  if (T > 0 && threads > T) threads = static_cast<int>(T);
+  std::vector<std::vector<int64_t>> cnt(threads, std::vector<int64_t>(n, 0));
+  parallel_ranges(T, threads, [&](int k, int64_t lo, int64_t hi) {
+    for (int64_t p = lo; p < hi; ++p) cnt[k][ids[p] / block] += 1;
+  });
+  std::vector<std::vector<int64_t>> start(threads, std::vector<int64_t>(n, 0));
+  int64_t at = 0;
+  for (int32_t s = 0; s < n; ++s) {
+    shard_offsets[s] = at;
+    for (int k = 0; k < threads; ++k) {
+      start[k][s] = at;
+      at += cnt[k][s];
+    }
+  }
+  shard_offsets[n] = at;
+  parallel_ranges(T, threads, [&](int k, int64_t lo, int64_t hi) {
+    std::vector<int64_t>& next = start[k];
+    for (int64_t p = lo; p < hi; ++p) {
+      const int64_t j = next[ids[p] / block]++;
+      sm_ids[j] = ids[p];
+      pos[j] = static_cast<int32_t>(p);
+    }
+  });
+  for (int64_t i = 0; i < static_cast<int64_t>(n) * n; ++i) splits[i] = 0;
+  parallel_ranges(n, threads, [&](int, int64_t lo, int64_t hi) {
+    for (int64_t r = lo; r < hi; ++r)
+      for (int64_t p = rank_id_offsets[r]; p < rank_id_offsets[r + 1]; ++p) splits[r * n + ids[p] / block] += 1;
+  });
+  return 0;
+}
+
+// oracle_collision_split on several threads, through presence arrays over the
+// rows instead of sorted unique lists: rows of t and of t+1 are marked (one
+// byte per row), the three lists are the rows present in both, in t only and
+// in t+1 only, in ascending order (each thread takes a range of rows, counts,
+// then writes at the prefix of the counts), and the masks look rows up.
+int oracle_collision_split_mt(const int64_t* ids_t, int64_t T_t, const int64_t* ids_next, int64_t T_next, int64_t R,
+                              int32_t n, int64_t* co, int64_t* ex_t, int64_t* ex_next, int64_t cap_rows,
+                              int64_t* counts, int64_t* co_off, int64_t* ex_t_off, int64_t* ex_next_off,
+                              uint8_t* is_co_t, uint8_t* is_co_next, int32_t threads) {
+  if (n <= 0 || R <= 0 || T_t < 0 || T_next < 0) return 1;
+  for (int64_t j = 0; j < T_t; ++j)
+    if (ids_t[j] < 0 || ids_t[j] >= R) return 2;
+  for (int64_t j = 0; j < T_next; ++j)
+    if (ids_next[j] < 0 || ids_next[j] >= R) return 2;
+  if (threads < 1) threads = 1;
+  // marks: every writer stores the same value 1, through relaxed atomics
+  std::vector<std::atomic<uint8_t>> in_t(R), in_n(R);
+  parallel_ranges(R, threads, [&](int, int64_t lo, int64_t hi) {
+    for (int64_t r = lo; r < hi; ++r) {
+      in_t[r].store(0, std::memory_order_relaxed);
+      in_n[r].store(0, std::memory_order_relaxed);
+    }
+  });
+  parallel_ranges(T_t, threads, [&](int, int64_t lo, int64_t hi) {
+    for (int64_t j = lo; j < hi; ++j) in_t[ids_t[j]].store(1, std::memory_order_relaxed);
+  });
+  parallel_ranges(T_next, threads, [&](int, int64_t lo, int64_t hi) {
+    for (int64_t j = lo; j < hi; ++j) in_n[ids_next[j]].store(1, std::memory_order_relaxed);
+  });
+  const int pieces = static_cast<int>(std::min<int64_t>(threads, R));
+  std::vector<int64_t> c[3];
+  for (int l = 0; l < 3; ++l) c[l].assign(pieces + 1, 0);
+  auto kind = [&](int64_t r) -> int {
+    const bool a = in_t[r].load(std::memory_order_relaxed), b = in_n[r].load(std::memory_order_relaxed);
+    return a && b ? 0 : (a ? 1 : (b ? 2 : -1));
+  };
+  parallel_ranges(R, pieces, [&](int k, int64_t lo, int64_t hi) {
+    for (int64_t r = lo; r < hi; ++r) {
+      const int l = kind(r);
+      if (l >= 0) c[l][k + 1] += 1;
+    }
+  });
+  for (int l = 0; l < 3; ++l)
+    for (int k = 0; k < pieces; ++k) c[l][k + 1] += c[l][k];
+  for (int l = 0; l < 3; ++l) {
+    counts[l] = c[l][pieces];
+    if (counts[l] > cap_rows) return 1;
+  }
+  int64_t* lists[3] = {co, ex_t, ex_next};
+  parallel_ranges(R, pieces, [&](int k, int64_t lo, int64_t hi) {
+    int64_t at[3] = {c[0][k], c[1][k], c[2][k]};
+    for (int64_t r = lo; r < hi; ++r) {
+      const int l = kind(r);
+      if (l >= 0) lists[l][at[l]++] = r;
+    }
+  });
+  const int64_t block = (R + n - 1) / n;
+  int64_t* offs[3] = {co_off, ex_t_off, ex_next_off};
+  for (int l = 0; l < 3; ++l)
+    for (int32_t k = 0; k <= n; ++k)
+      offs[l][k] = std::lower_bound(lists[l], lists[l] + counts[l], static_cast<int64_t>(k) * block) - lists[l];
+  parallel_ranges(T_t, threads, [&](int, int64_t lo, int64_t hi) {
+    for (int64_t j = lo; j < hi; ++j) is_co_t[j] = in_n[ids_t[j]].load(std::memory_order_relaxed);
+  });
+  parallel_ranges(T_next, threads, [&](int, int64_t lo, int64_t hi) {
+    for (int64_t j = lo; j < hi; ++j) is_co_next[j] = in_t[ids_next[j]].load(std::memory_order_relaxed);
+  });
+  return 0;
+}
+
+// oracle_emb_gather on several threads: positions in pieces.
+int oracle_emb_gather_mt(const void* table, int64_t R, int64_t row_bytes, const int64_t* ids, int64_t T,
+                         const uint8_t* mask, uint8_t sel, void* out, int32_t threads) {
+  if (R < 0 || row_bytes <= 0 || T < 0) return 1;
+  for (int64_t p = 0; p < T; ++p)
+    if ((!mask || mask[p] == sel) && (ids[p] < 0 || ids[p] >= R)) return 2;
+  const unsigned char* tb = static_cast<const unsigned char*>(table);
+  unsigned char* ob = static_cast<unsigned char*>(out);
+  parallel_ranges(T, threads, [&](int, int64_t lo, int64_t hi) {
+    for (int64_t p = lo; p < hi; ++p) {
+      if (mask && mask[p] != sel) continue;
+      std::memcpy(ob + p * row_bytes, tb + ids[p] * row_bytes, static_cast<size_t>(row_bytes));
+    }
+  });
+  return 0;
+}
+
+// oracle_emb_backward on several threads.  The selected (row, position)
+// pairs are sorted (on all threads), so each row's positions are adjacent and
+// ascending; the rows are then cut into pieces, and each thread sums and
+// updates whole rows exactly as the single-threaded function does: fp64 sums
+// in position order, one rounding per stored value.
+int oracle_emb_backward_mt(void* table, float* state, int64_t R, int32_t D, int32_t dtype, int32_t optim,
+                           const int64_t* ids, const void* grads, int64_t T, const uint8_t* is_co, int32_t phase,
+                           double lr, double eps, int32_t threads) {
+  if (R < 0 || D <= 0 || T < 0 || (dtype != 0 && dtype != 1) || (optim != 0 && optim != 1)) return 1;
+  if (phase < 0 || phase > 2 || (phase != 0 && is_co == nullptr) || (optim == 1 && state == nullptr)) return 1;
+  std::vector<std::pair<int64_t, int64_t>> e;  // (row, position)
+  e.reserve(static_cast<size_t>(T));
+  for (int64_t p = 0; p < T; ++p) {
+    if (phase == 1 && is_co[p] != 1) continue;
+    if (phase == 2 && is_co[p] != 0) continue;
+    if (ids[p] < 0 || ids[p] >= R) return 2;
+    e.emplace_back(ids[p], p);
+  }
+  parallel_sort(e, threads);
+  // row starts, then pieces of whole rows
+  std::vector<int64_t> starts;
+  for (int64_t i = 0; i < static_cast<int64_t>(e.size()); ++i)
+    if (i == 0 || e[i].first != e[i - 1].first) starts.push_back(i);
+  const int64_t U = static_cast<int64_t>(starts.size());
+  starts.push_back(static_cast<int64_t>(e.size()));
+  parallel_ranges(U, threads, [&](int, int64_t lo, int64_t hi) {
+    std::vector<double> g(D);
+    for (int64_t u = lo; u < hi; ++u) {
+      const int64_t r = e[starts[u]].first;
+      std::fill(g.begin(), g.end(), 0.0);
+      for (int64_t i = starts[u]; i < starts[u + 1]; ++i)
+        for (int32_t d = 0; d < D; ++d) g[d] += read_elem(grads, e[i].second * D + d, dtype);
+      if (optim == 0) {
+        for (int32_t d = 0; d < D; ++d) {
+          double w = read_elem(table, r * D + d, dtype);
+          write_elem(table, r * D + d, dtype, w - lr * g[d]);
+        }
+      } else {
+        double sq = 0.0;
+        for (int32_t d = 0; d < D; ++d) sq += g[d] * g[d];
+        double s = static_cast<double>(state[r]) + sq / static_cast<double>(D);
+        state[r] = static_cast<float>(s);
+        double denom = std::sqrt(s) + eps;
+        for (int32_t d = 0; d < D; ++d) {
+          double w = read_elem(table, r * D + d, dtype);
+          write_elem(table, r * D + d, dtype, w - lr * g[d] / denom);
+        }
+      }
+    }
+  });
+  return 0;
+}
 
 }  // extern "C"

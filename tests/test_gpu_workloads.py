@@ -52,7 +52,9 @@ def _gpu_sync(w, batches_cpu, table0, grads_cpu, row_sorted=True):
     for t in range(K):
         s = pipe.slots[cur]
         T = s.T
-        snap = {"perm": to_np(s.perm[: w.S]), "rank_offsets": to_np(s.rank_offsets), "ids": to_np(s.ids[:T]),
+        # the table as the gather of t reads it (the update of t-1 has landed)
+        snap = {"table_before": to_np(tab), "state_before": to_np(state) if state is not None else None,
+                "perm": to_np(s.perm[: w.S]), "rank_offsets": to_np(s.rank_offsets), "ids": to_np(s.ids[:T]),
                 "offsets": to_np(s.offsets[: w.S + 1]), "rank_id_offsets": to_np(s.rank_id_offsets),
                 "sm_ids": to_np(s.sm_ids[:T]), "pos": to_np(s.pos[:T]), "splits": to_np(s.splits),
                 "shard_offsets": to_np(s.shard_offsets), "seg_weight": to_np(s.seg_weight)}
@@ -68,9 +70,14 @@ def _gpu_sync(w, batches_cpu, table0, grads_cpu, row_sorted=True):
         if has_next:
             c = {k: to_np(v) for k, v in pipe.coll.items()}
             counts = c["counts"]
+            m = to_np(pipe.masks[cur][:T])
+            if pipe.mask_layout[cur] == "shard":        # aligned with sm_ids: back to batch-major order
+                bm = np.empty_like(m)
+                bm[snap["pos"]] = m
+                m = bm
             snap["coll"] = {"co": c["co"][: counts[0]], "ex_t": c["ex_t"][: counts[1]],
                             "ex_next": c["ex_next"][: counts[2]], "co_off": c["co_off"], "ex_t_off": c["ex_t_off"],
-                            "ex_next_off": c["ex_next_off"], "is_co_t": to_np(pipe.masks[cur][:T])}
+                            "ex_next_off": c["ex_next_off"], "is_co_t": m}
         rec.append(snap)
         cur = nxt
     return rec, to_np(tab), (to_np(state) if state is not None else None)
@@ -93,7 +100,8 @@ def test_pipeline_matches_oracle(name):
     st_ref = np.zeros(w.R, np.float32) if w.optim == "adagrad" else None
     g_np = [to_np(g) for g in grads] if grads else None
     times = _times(w)
-    ref = oracle.run_sync(w, nb, tab_ref, st_ref, g_np, [to_np(x) for x in times] if times else None)
+    ref = oracle.run_sync(w, nb, tab_ref, st_ref, g_np, [to_np(x) for x in times] if times else None,
+                          keep_tables=True)
     for t in range(w.iters):
         g, r = rec[t], ref[t]
         p = r["prep"]
@@ -118,12 +126,28 @@ def test_pipeline_matches_oracle(name):
             # (the synchronous order does not ask for the mask of t+1)
             for k in ("co", "ex_t", "ex_next", "co_off", "ex_t_off", "ex_next_off", "is_co_t"):
                 assert np.array_equal(g["coll"][k], r["coll"][k]), (t, k)
-        # gathered rows: exact only for the first iteration or gather-only workloads
-        # (later ones read rows the GPU updated, which are compared within tolerance)
+        # gathered rows: a byte copy, so bit-exact against the oracle's gather of the table the GPU
+        # gather read (the table before step t); that table is the oracle's within the update tolerance
+        assert np.array_equal(g["out"], oracle.emb_gather(g["table_before"], p["ids"])), t
         if t == 0 or not w.has_update:
             assert np.array_equal(g["out"], r["out"]), t
+            assert np.array_equal(g["table_before"], r["table_before"]), t
         else:
-            assert_table_close(g["out"], r["out"], w.dtype, w.lr, scale=1.0)
+            ids_prev = np.concatenate([ref[k]["prep"]["ids"] for k in range(t)])
+            g_prev = np.concatenate(g_np[:t])
+            sc = update_scale(ids_prev, g_prev, w.R, w.optim, w.lr, w.eps, r["state_before"])
+            assert_table_close(g["table_before"], r["table_before"], w.dtype, w.lr, scale=sc, ulps=t)
+            if st_ref is not None:
+                assert_state_close(g["state_before"], r["state_before"])
+        if w.has_update:
+            # the update of t writes the rows of uniq(I^t) and no other row (FreeScale Algorithm 2,
+            # lines 7 and 20: each row of the batch is updated once, by its phase)
+            after = rec[t + 1]["table_before"] if t + 1 < w.iters else tab_gpu
+            changed = np.flatnonzero((after != g["table_before"]).any(axis=1))
+            uniq = np.unique(p["ids"])
+            assert np.isin(changed, uniq).all(), t
+            moved = np.flatnonzero((r["table_after"] != r["table_before"]).any(axis=1))
+            assert np.isin(moved, changed).all(), t
     if w.has_update:
         ids_all = np.concatenate([r["prep"]["ids"] for r in ref])
         g_all = np.concatenate(g_np)

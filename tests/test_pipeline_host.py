@@ -15,7 +15,8 @@ from jagged_embedding_gb300 import synthetic
 
 CALLS = ["fs_balance_fbs", "fs_balance_vbs", "fs_balance_vbs_tuned", "fs_vbs_autotune", "fs_permute_jagged",
          "fs_bucketize_rowwise", "fs_row_bitmap", "fs_collision_split_bitmaps", "fs_emb_gather",
-         "fs_emb_gather_sorted", "fs_emb_sort_rows", "fs_emb_update_sorted", "fs_emb_backward_adagrad"]
+         "fs_emb_gather_sorted", "fs_emb_sort_rows", "fs_emb_sort_rows_sharded", "fs_emb_update_sorted",
+         "fs_emb_backward_adagrad"]
 
 
 @pytest.fixture
@@ -54,18 +55,34 @@ def test_sync_step_sorts_before_the_lookup(calls):
     nxt = pipe.step_sync(0, _batch(TINY), torch.zeros(1, TINY.D))
     CT = B.PHASE_COLLISION_THEN_EXCLUSIVE
     assert nxt == 1
-    assert _names(calls) == [("fs_collision_split_bitmaps", None), ("fs_emb_sort_rows", CT),
+    # the update sorts each shard's entries of the bucketize output (shards of 125 rows)
+    assert _names(calls) == [("fs_collision_split_bitmaps", None), ("fs_emb_sort_rows_sharded", CT),
                              ("fs_emb_gather_sorted", CT), ("fs_emb_update_sorted", CT)]
+    assert pipe.mask_layout[0] == "shard"           # its collision flags follow the shard-major IDs
     # the batch is prepared (balanced, permuted, bucketized, marked) before the split
     assert [n for n, _ in calls[:4]] == ["fs_balance_fbs", "fs_permute_jagged", "fs_bucketize_rowwise",
                                         "fs_row_bitmap"]
+
+
+def test_sync_step_sorts_batch_major_ids_when_shards_are_too_large(calls):
+    w = TINY.scaled(n=1, B=TINY.S, R=(1 << 19) + 1)  # one shard: 2^19 + 1 rows and the phase bit
+    pipe = _pipe(w)
+    pipe.step_sync(0, _batch(w), torch.zeros(1, w.D))
+    CT = B.PHASE_COLLISION_THEN_EXCLUSIVE
+    assert _names(calls)[-3:] == [("fs_emb_sort_rows", CT), ("fs_emb_gather_sorted", CT),
+                                  ("fs_emb_update_sorted", CT)]
+    assert pipe.mask_layout[0] == "batch"
+    calls.clear()
+    pipe.step_sync(0, None, torch.zeros(1, w.D), has_next=False)   # one phase: 20 bits fit
+    assert _names(calls)[0] == ("fs_emb_sort_rows_sharded", B.PHASE_ALL)
 
 
 def test_last_iteration_sorts_every_row_in_one_phase(calls):
     pipe = _pipe(TINY)
     pipe.step_sync(0, None, torch.zeros(1, TINY.D), has_next=False)
     A = B.PHASE_ALL
-    assert _names(calls) == [("fs_emb_sort_rows", A), ("fs_emb_gather_sorted", A), ("fs_emb_update_sorted", A)]
+    assert _names(calls) == [("fs_emb_sort_rows_sharded", A), ("fs_emb_gather_sorted", A),
+                             ("fs_emb_update_sorted", A)]
 
 
 def test_position_order_step_when_asked_or_when_the_phase_bit_does_not_fit(calls):
@@ -86,7 +103,8 @@ def test_gather_only_workload_keeps_the_position_order_gather(calls):
     pipe.step_sync(0, _batch(w), None)
     names = [n for n, _ in calls]
     assert "fs_balance_vbs" in names and names[-1] == "fs_emb_gather"
-    assert not {"fs_emb_sort_rows", "fs_emb_update_sorted", "fs_vbs_autotune"} & set(names)
+    assert not {"fs_emb_sort_rows", "fs_emb_sort_rows_sharded", "fs_emb_update_sorted", "fs_vbs_autotune"} & set(names)
+    assert pipe.mask_layout[0] == "shard"
 
 
 def test_autotune_folds_the_times_in_before_the_next_cut(calls):
@@ -119,3 +137,4 @@ def test_prioritized_order_follows_algorithm_2(calls):
         else:
             expect.append(("fs_emb_backward_adagrad", A))
     assert seq == expect
+    assert pipe.mask_layout == ["batch", "batch"]   # the masked lookups and updates read batch-major masks

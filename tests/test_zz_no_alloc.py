@@ -5,14 +5,17 @@ Callers that cannot allocate device memory at the time they partition a batch
 allocator it does not own, a fixed memory plan) use fs_balance_fbs_noalloc: it
 keeps the sort's scratch in a fixed array inside the library.  These checks
 call it through the C ABI, twice in a row with different batches, and compare
-with fs_balance_fbs, which takes a caller workspace.  This file is collected
-last on purpose and must pass both alone and after every other test.
+with the CPU oracle's FBS partition and with fs_balance_fbs, which takes a
+caller workspace.  This file is collected last on purpose and must pass both
+alone and after every other test.
 """
 import numpy as np
 import pytest
 import torch
 
+import oracle
 from jagged_embedding_gb300 import binding as B
+from tests.helpers import to_np
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -38,6 +41,9 @@ def test_noalloc_matches_workspace_entry_point_twice(n, S):
     for call in range(2):                          # two calls in a row share the fixed scratch array
         L = _lens(1000 * call + S, S)
         perm, ro = _noalloc(L, n)
+        p_ora, ro_ora = oracle.balance_fbs(to_np(L), n)
+        assert np.array_equal(to_np(perm), p_ora), call
+        assert np.array_equal(to_np(ro), ro_ora), call
         p_ref, ro_ref, err = B.fs_balance_fbs(L, n)
         B.check(err, "fs_balance_fbs")
         assert torch.equal(perm, p_ref), call
@@ -48,6 +54,8 @@ def test_noalloc_at_the_size_limit_and_beyond():
     S = 1 << 18
     L = _lens(7, S)
     perm, ro = _noalloc(L, 512)
+    p_ora, ro_ora = oracle.balance_fbs(to_np(L), 512)
+    assert np.array_equal(to_np(perm), p_ora) and np.array_equal(to_np(ro), ro_ora)
     p_ref, ro_ref, err = B.fs_balance_fbs(L, 512)
     B.check(err)
     assert torch.equal(perm, p_ref) and torch.equal(ro, ro_ref)
