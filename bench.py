@@ -9,6 +9,7 @@ batches / device time; the roofline fraction uses the algorithmic bytes of
 the step (see algorithmic_bytes()).
 
 python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl gpu|reference]
+                [--schedule sync|prioritized]
 
 Under torchrun (N > 1) every rank runs an independent replica of the workload
 on its own GPU (weak scaling, no data-path collective); the timing is the
@@ -306,6 +307,7 @@ def run_gpu(args):
     w0 = synthetic.WORKLOADS[args.workload]
     w = w0.scaled(seed_base=w0.seed_base + 100 * rank)
     K, W = args.steps, args.warmup
+    prio = args.schedule == "prioritized"
 
     # ---- resident inputs (all iterations' batches, table, state, gradients)
     batches = [synthetic.batch(w, t, dev) for t in range(w.iters)]
@@ -316,29 +318,42 @@ def run_gpu(args):
     state = torch.zeros(w.R, dtype=torch.float32, device=dev) if w.optim == "adagrad" else None
     # gradient rows of the dense model's backward: one N(0,1) pool, batch t uses its first T_t rows
     grads = synthetic.grads(w, max_T, 0, dev) if w.has_update else None
-    pipe = Pipeline(w, dev, max_T, table, state)
+    if prio:
+        # Algorithm 2 needs the output of t+1 beside that of t and a third batch slot
+        need = max_T * (w.row_bytes + 8 * 3 + 5) + w.R // 4
+        free, _ = torch.cuda.mem_get_info(dev)
+        if need > 0.9 * free:
+            raise SystemExit(f"the prioritized order of {w.name} needs about {need / 1e9:.0f} GB more device "
+                             f"memory than the {free / 1e9:.0f} GB free")
+    pipe = Pipeline(w, dev, max_T, table, state, two_outputs=prio, streams=prio)
     # VBS AutoTune: the per-rank step times each iteration reports (seeded clock readings)
     times = [synthetic.step_times(w, t, dev) for t in range(w.iters)] if w.autotune else None
     torch.cuda.synchronize()
 
     def step(i, cur):
         nb = batches[(i + 1) % w.iters]
-        return pipe.step_sync(cur, nb, grads[: pipe.slots[cur].T] if grads is not None else None,
-                              times=times[i % w.iters] if times else None)
+        tm = times[i % w.iters] if times else None
+        if prio:   # one iteration of Algorithm 2: batch i % iters is slot i % 3
+            T = Ts[i % w.iters]
+            pipe.prio_step(nb, grads[:T] if grads is not None else None, times=tm)
+            return (i + 1) % 3
+        return pipe.step_sync(cur, nb, grads[: pipe.slots[cur].T] if grads is not None else None, times=tm)
 
     cur = 0
-    pipe.prepare(batches[0], 0)
+    if prio:
+        pipe.prio_begin(batches[0])
+    else:
+        pipe.prepare(batches[0], 0)
     for i in range(W):
         cur = step(i, cur)
     torch.cuda.synchronize()
     B.check(pipe.err, "warm-up")
 
     stream = torch.cuda.current_stream(dev)
-    n_ev = K
-    g0 = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
-    g1 = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
-    u0 = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
-    u1 = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
+    g0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    g1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    u0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    u1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ids_timed = 0
     step_batches = []
@@ -352,36 +367,42 @@ def run_gpu(args):
     for k in range(K):
         i = W + k
         step_batches.append(i % w.iters)
-        ids_timed += pipe.slots[cur].T
+        ids_timed += Ts[i % w.iters]
+        if not prio:
+            # the gather and the update of the synchronous step, timed with events on the stream
+            # they run on (the prioritized order splits both into masked parts on two streams)
+            def timed_gather(*a, _k=k, **kw):
+                g0[_k].record(stream)
+                orig_gather(*a, **kw)
+                g1[_k].record(stream)
 
-        def timed_gather(*a, _k=k, **kw):
-            g0[_k].record(stream)
-            orig_gather(*a, **kw)
-            g1[_k].record(stream)
+            def timed_update(*a, _k=k, _f=orig_update, **kw):
+                u0[_k].record(stream)
+                _f(*a, **kw)
+                u1[_k].record(stream)
 
-        # the update of the step (one call: from the sorted entries, or the one-call form)
-        def timed_update(*a, _k=k, _f=orig_update, **kw):
-            u0[_k].record(stream)
-            _f(*a, **kw)
-            u1[_k].record(stream)
+            def timed_backward(*a, _k=k, _f=orig_backward, **kw):
+                u0[_k].record(stream)
+                _f(*a, **kw)
+                u1[_k].record(stream)
 
-        def timed_backward(*a, _k=k, _f=orig_backward, **kw):
-            u0[_k].record(stream)
-            _f(*a, **kw)
-            u1[_k].record(stream)
-
-        pipe.gather, pipe.update_sorted, pipe.backward = timed_gather, timed_update, timed_backward
+            pipe.gather, pipe.update_sorted, pipe.backward = timed_gather, timed_update, timed_backward
         cur = step(i, cur)
     pipe.gather, pipe.update_sorted, pipe.backward = orig_gather, orig_update, orig_backward
-    t_end.record(stream)
+    t_end.record(stream)          # (the prioritized step leaves the side stream joined to this one)
     torch.cuda.synchronize()
     barrier(ws)
     launches = B.launch_count() - launches0
     clk = clocks.stop()
     B.check(pipe.err, "timed steps")
     secs = t_start.elapsed_time(t_end) / 1000.0
-    gather_ms = sum(a.elapsed_time(b) for a, b in zip(g0, g1)) / K
-    update_ms = sum(a.elapsed_time(b) for a, b in zip(u0, u1)) / K if w.has_update else None
+    gather_ms = update_ms = None
+    if not prio:
+        gather_ms = sum(a.elapsed_time(b) for a, b in zip(g0, g1)) / K
+        update_ms = sum(a.elapsed_time(b) for a, b in zip(u0, u1)) / K if w.has_update else None
+    if prio:
+        pipe.prio_finish()
+        torch.cuda.synchronize()
 
     # unique rows per batch (|co| + |ex_t| of its pair with the next batch), for the byte model
     U = {}
@@ -410,7 +431,7 @@ def run_gpu(args):
 
     # ---- end to end through the public API with host inputs (pinned), copies inside the timed region
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not prio:
         e2e = run_e2e(w, pipe, batches, grads, K, W, dev, ws, times)
 
     cpu = None
@@ -426,40 +447,41 @@ def run_gpu(args):
         cpu = {"value": rate, "unit": "IDs/s", "cores": cores, "kind": "oracle", "sample": desc,
                "host_cores": cores, "single_thread": {"value": rate1, "unit": "IDs/s", "cores": 1, "sample": desc1}}
 
-    sorted_gather = w.has_update and pipe.row_sorted
-    traffic = None
-    tpath = os.path.join(ROOT, "profiles", "gather_traffic.json")
-    if os.path.exists(tpath):
-        with open(tpath) as f:
-            tj = json.load(f)
-        if tj.get("kernel_hash") == kernel_hash(sorted_gather) and tj.get("workload") == w0.name:
-            traffic = tj.get("bytes_per_launch")
-
-    achieved = gbytes / (gather_ms / 1000.0) / 1e9
-    # the synchronous step of a workload with an update gathers from the update's sorted entries
+    cfg = dict(workload_config(w0, ws), ids_per_step=ids_timed / K,
+               l2="no flush: inputs larger than L2 (table %.1f GB, %.1f GB of IDs per batch)"
+                  % (table.numel() * table.element_size() / 1e9, max_T * 8 / 1e9))
+    if prio:
+        cfg["schedule"] = ("FreeScale Algorithm 2: exclusive rows of t+1 prefetched and exclusive updates of t "
+                           "deferred on a side stream; collision rows of t updated, then gathered for t+1")
     line = {
         "metric": METRIC, "value": value, "unit": "IDs/s", "n_gpus": ws, "steps": K, "warmup": W,
         "ms_per_step": 1000.0 * secs_max / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": f"int64/{w.dtype}", "data": "synthetic",
-        "config": dict(workload_config(w0, ws), ids_per_step=ids_timed / K,
-                       l2="no flush: inputs larger than L2 (table %.1f GB, %.1f GB of IDs per batch)"
-                          % (table.numel() * table.element_size() / 1e9, max_T * 8 / 1e9)),
+        "dtype": f"int64/{w.dtype}", "data": "synthetic", "config": cfg,
         "hbm_roofline_frac_step": step_bytes / secs / (hbm_gbs * 1e9),
         "algorithmic_bytes_per_step": step_bytes / K,
-        "roofline": {"kernel": SORTED_GATHER_KERNEL if sorted_gather else GATHER_KERNEL, "bound": "hbm",
-                     "achieved": achieved,
-                     "peak": hbm_gbs, "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / hbm_gbs,
-                     "traffic": traffic, "algorithmic_bytes_per_launch": gbytes, "avg_launch_ms": gather_ms},
-        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clk,
+        "roofline": None, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clk,
     }
-    if update_ms:
-        # the update's segment-reduce + row update (both phases), timed like the gather
-        ua = ubytes / (update_ms / 1000.0) / 1e9
-        line["roofline_update"] = {
-            "kernel": "fs_emb_update_sorted (reduce_ring_kernel, block sums, fixup; two phases)" if sorted_gather
-            else "fs_emb_backward_adagrad (sort, reduce_ring_kernel, block sums, fixup)",
-            "bound": "hbm", "achieved": ua, "peak": hbm_gbs, "peak_kind": peak_kind, "unit": "GB/s",
-            "frac": ua / hbm_gbs, "algorithmic_bytes_per_call": ubytes, "avg_call_ms": update_ms}
+    if not prio:
+        sorted_gather = w.has_update and pipe.row_sorted
+        ga = gbytes / (gather_ms / 1000.0) / 1e9
+        calls = {"gather": {"kernel": SORTED_GATHER_KERNEL if sorted_gather else GATHER_KERNEL, "bound": "hbm",
+                            "achieved": ga, "peak": hbm_gbs, "peak_kind": peak_kind, "unit": "GB/s",
+                            "frac": ga / hbm_gbs, "traffic": recorded_traffic("gather", w0.name, sorted_gather),
+                            "algorithmic_bytes_per_launch": gbytes, "avg_launch_ms": gather_ms}}
+        if update_ms:
+            # the update's segment-reduce + row update (both phases), timed like the gather
+            ua = ubytes / (update_ms / 1000.0) / 1e9
+            calls["update"] = {
+                "kernel": "fs_emb_update_sorted (reduce_ring_kernel x2, block sums, fixup)" if sorted_gather
+                else "fs_emb_backward_adagrad (sort, reduce_ring_kernel, block sums, fixup)",
+                "bound": "hbm", "achieved": ua, "peak": hbm_gbs, "peak_kind": peak_kind, "unit": "GB/s",
+                "frac": ua / hbm_gbs, "traffic": recorded_traffic("update", w0.name, sorted_gather),
+                "algorithmic_bytes_per_launch": ubytes, "avg_launch_ms": update_ms}
+        # the dominant call of the step: the one that takes longer
+        dom = max(calls, key=lambda c: calls[c]["avg_launch_ms"])
+        line["roofline"] = dict(calls[dom], call=dom)
+        for c, v in calls.items():
+            line[f"roofline_{c}"] = v
     if rank == 0:
         print(json.dumps(line))
     if ws > 1:
@@ -468,17 +490,33 @@ def run_gpu(args):
     return 0
 
 
+def recorded_traffic(call, workload, sorted_gather):
+    """DRAM bytes per launch of `call` on `workload` from profiles/traffic.json (scaled from a small-case ncu
+    capture), or None when there is no record or the kernel's sources changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f).get(f"{call}/{workload}")
+    if not rec or rec.get("kernel_hash") != kernel_hash(call, sorted_gather):
+        return None
+    return rec.get("bytes_per_launch")
+
+
 # the dominant kernel of the step: the unmasked gather of the synchronous order (from the update's
 # sorted entries when the workload has an update)
 GATHER_KERNEL = "fs_emb_gather (gather_bulk_kernel<4, 2>)"
 SORTED_GATHER_KERNEL = "fs_emb_gather_sorted (gather_sorted_kernel)"
 
 
-def kernel_hash(sorted_gather=False):
-    """Hash of the sources of the gather kernel (the recorded DRAM traffic is valid for these only)."""
+def kernel_hash(call="gather", sorted_gather=False):
+    """Hash of the sources of a call's kernels (a recorded DRAM traffic is valid for these only)."""
     import hashlib
+    names = {("gather", False): ("gather.cu", "bulk.cuh"), ("gather", True): ("backward.cu", "radix.cuh"),
+             ("update", False): ("backward.cu", "radix.cuh", "bulk.cuh"),
+             ("update", True): ("backward.cu", "radix.cuh", "bulk.cuh")}[(call, sorted_gather)]
     h = hashlib.sha256()
-    for name in (("backward.cu", "radix.cuh") if sorted_gather else ("gather.cu", "bulk.cuh")):
+    for name in names:
         with open(os.path.join(ROOT, "jagged_embedding_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -593,6 +631,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
+    ap.add_argument("--schedule", default="sync", choices=["sync", "prioritized"],
+                    help="sync: the synchronous order (default); prioritized: FreeScale Algorithm 2 on two streams")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-samples-per-rank", type=int, default=None)

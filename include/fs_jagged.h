@@ -223,6 +223,32 @@ fs_status fs_bucketize_rowwise(const int64_t* ids, int64_t T, const int64_t* ran
                                fs_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Fused jagged permute + row-wise bucketize -- FreeScale Algorithm 1 Stage III
+ * and §4.2 (the indexed permute and the ranged dispatch that prepare the IDs
+ * AllToAll), Algorithm 2 line 8.  One call with the results of
+ *   fs_permute_jagged(offsets, values, S, perm, out_offsets, out_values,
+ *                     capacity, rank_offsets, n, rank_id_offsets, ...)
+ * followed by
+ *   fs_bucketize_rowwise(out_values, T, rank_id_offsets, n, num_rows, sm_ids,
+ *                        pos, splits, shard_offsets, ...),   T = out_offsets[S],
+ * bit for bit, but the source IDs are read once: each 4096-ID output tile is
+ * counted per shard as it is written, so the bucketize needs no counting pass
+ * of its own; T stays on the device.
+ *   rank_offsets [n+1] required (n in [1, 1024]: ranks = shards)
+ *   out_values, sm_ids [capacity] int64, pos [capacity] int32; offsets[S] >
+ *   capacity -> FS_ERR_CAPACITY (the first `capacity` IDs are still written
+ *   and bucketized)
+ * Errors as the two calls (FS_ERR_BAD_OFFSETS, FS_ERR_ID_RANGE,
+ * FS_ERR_CAPACITY in *err).
+ * ---------------------------------------------------------------------- */
+size_t fs_permute_bucketize_workspace_size(int64_t S, int64_t capacity, int32_t n);
+fs_status fs_permute_bucketize(const int64_t* offsets, const int64_t* values, int64_t S, const int32_t* perm,
+                               const int64_t* rank_offsets, int32_t n, int64_t num_rows, int64_t* out_offsets,
+                               int64_t* out_values, int64_t capacity, int64_t* rank_id_offsets, int64_t* sm_ids,
+                               int32_t* pos, int64_t* splits, int64_t* shard_offsets, int32_t* err, void* ws,
+                               size_t ws_bytes, fs_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Collision / exclusive split -- FreeScale Algorithm 2 line 10
  * (compute_collision) and the notation paragraph after Algorithm 2: a
  * collision row is used by both iteration t and t+1, an exclusive row by one

@@ -34,7 +34,8 @@ EXPORTS = [
     "fs_balance_vbs", "fs_balance_vbs_tuned", "fs_vbs_autotune",
     "fs_permute_jagged_workspace_size", "fs_permute_jagged", "fs_keyed_transpose_workspace_size",
     "fs_keyed_transpose", "fs_bucketize_rowwise_workspace_size",
-    "fs_bucketize_rowwise", "fs_collision_split_workspace_size", "fs_collision_split", "fs_row_bitmap_words",
+    "fs_bucketize_rowwise", "fs_permute_bucketize_workspace_size", "fs_permute_bucketize",
+    "fs_collision_split_workspace_size", "fs_collision_split", "fs_row_bitmap_words",
     "fs_row_bitmap", "fs_collision_split_bitmaps_workspace_size", "fs_collision_split_bitmaps", "fs_emb_gather",
     "fs_emb_backward_adagrad_workspace_size", "fs_emb_backward_adagrad", "fs_emb_sort_rows",
     "fs_emb_gather_sorted", "fs_emb_update_sorted", "fs_emb_sort_rows_sharded_workspace_size",
@@ -75,6 +76,8 @@ def lib():
         "fs_keyed_transpose": ([P, P, i64, i64, P, P, P, i64, P, P, sz, P], C.c_int),
         "fs_bucketize_rowwise_workspace_size": ([i64, i32], sz),
         "fs_bucketize_rowwise": ([P, i64, P, i32, i64, P, P, P, P, P, P, sz, P], C.c_int),
+        "fs_permute_bucketize_workspace_size": ([i64, i64, i32], sz),
+        "fs_permute_bucketize": ([P, P, i64, P, P, i32, i64, P, P, i64, P, P, P, P, P, P, P, sz, P], C.c_int),
         "fs_collision_split_workspace_size": ([i64, i64, i64, i32], sz),
         "fs_collision_split": ([P, i64, P, i64, i64, i32, P, P, P, i64, P, P, P, P, P, P, P, P, sz, P], C.c_int),
         "fs_row_bitmap_words": ([i64], sz),
@@ -311,6 +314,40 @@ def fs_bucketize_rowwise(ids, rank_id_offsets, num_rows, sm_ids=None, pos=None, 
                                    _ptr(splits), _ptr(shard_offsets), _ptr(err), _ptr(ws), ws.numel(), _stream(dev)),
         "fs_bucketize_rowwise")
     return sm_ids, pos, splits, shard_offsets, err
+
+
+def fs_permute_bucketize(offsets, values, perm, rank_offsets, num_rows, capacity=None, out_offsets=None,
+                         out_values=None, rank_id_offsets=None, sm_ids=None, pos=None, splits=None,
+                         shard_offsets=None, err=None, ws=None):
+    """fs_permute_jagged (with rank_offsets) then fs_bucketize_rowwise, in one call that reads the source IDs
+    once.  Returns (out_offsets, out_values, rank_id_offsets, sm_ids, pos, splits, shard_offsets, err)."""
+    dev = offsets.device
+    _need(offsets, torch.int64, "offsets")
+    _need(values, torch.int64, "values")
+    _need(perm, torch.int32, "perm")
+    _need(rank_offsets, torch.int64, "rank_offsets")
+    S = offsets.numel() - 1
+    n = rank_offsets.numel() - 1
+    cap = values.numel() if capacity is None else int(capacity)
+    new = lambda t, k, dt: torch.empty(k, dtype=dt, device=dev) if t is None else t  # noqa: E731
+    out_offsets = new(out_offsets, S + 1, torch.int64)
+    out_values = new(out_values, cap, torch.int64)
+    rank_id_offsets = new(rank_id_offsets, n + 1, torch.int64)
+    sm_ids = new(sm_ids, cap, torch.int64)
+    pos = new(pos, cap, torch.int32)
+    splits = torch.empty(n, n, dtype=torch.int64, device=dev) if splits is None else splits
+    shard_offsets = new(shard_offsets, n + 1, torch.int64)
+    for t, nm, dt, k in ((out_values, "out_values", torch.int64, cap), (sm_ids, "sm_ids", torch.int64, cap),
+                         (pos, "pos", torch.int32, cap), (out_offsets, "out_offsets", torch.int64, S + 1)):
+        _need(t, dt, nm, k)
+    err = new_err(dev) if err is None else err
+    need = lib().fs_permute_bucketize_workspace_size(S, cap, n)
+    ws = workspace(need, dev) if ws is None else ws
+    _ok(lib().fs_permute_bucketize(_ptr(offsets), _ptr(values), S, _ptr(perm), _ptr(rank_offsets), n, int(num_rows),
+                                   _ptr(out_offsets), _ptr(out_values), cap, _ptr(rank_id_offsets), _ptr(sm_ids),
+                                   _ptr(pos), _ptr(splits), _ptr(shard_offsets), _ptr(err), _ptr(ws), ws.numel(),
+                                   _stream(dev)), "fs_permute_bucketize")
+    return out_offsets, out_values, rank_id_offsets, sm_ids, pos, splits, shard_offsets, err
 
 
 def fs_collision_split(ids_t, ids_next, num_rows, n, cap_rows=None, out=None, err=None, ws=None, T_t=None,

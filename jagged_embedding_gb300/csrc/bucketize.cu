@@ -9,81 +9,14 @@
 // computed afterwards from the sorted positions (inside a shard they are
 // ascending, so each (source rank, shard) count is two binary searches),
 // which is the local recomputation of the AllToAll metadata.
-#include "radix.cuh"
+#include "shard.cuh"
 
 namespace fs {
 namespace {
 
 using radix::kThreads;
-
-// shard(x) = x / block.  GB300's FP64 rate is a small fraction of its FP32
-// rate, so the quotient is estimated in FP32 (exact to within one for any
-// x < 2^32 and quotient < 2^12) and corrected with integer products.
-struct SrcShard {
-  using Key = int64_t;
-  static constexpr bool kIndexValue = true;  // value = item index
-  static constexpr bool kFetch2 = false;
-  const int64_t* ids;
-  int64_t R;
-  int64_t block;
-  float inv_block;
-  int32_t n;
-  using Raw = int64_t;
-  template <bool>
-  __device__ __forceinline__ Raw fetch(int64_t i) const { return __ldcs(ids + i); }
-  __device__ __forceinline__ bool make(Raw id, int64_t i, int, Key& key, uint32_t& val, int32_t* err) const {
-    key = id;
-    val = static_cast<uint32_t>(i);
-    if (err && (key < 0 || key >= R)) set_err(err, FS_ERR_ID_RANGE);
-    return true;
-  }
-  __device__ __forceinline__ uint32_t digit(Key key, int, int, int) const {
-    if (key <= 0) return 0;
-    if (key >= R) return uint32_t(n - 1);
-    int64_t q = static_cast<int64_t>(__float2uint_rz(__fmul_rz(__ull2float_rz(uint64_t(key)), inv_block)));
-    if (q * block > key) --q;
-    if ((q + 1) * block <= key) ++q;
-    return q >= n ? uint32_t(n - 1) : uint32_t(q);
-  }
-};
-
-struct DstShardMajor {
-  int64_t* sm_ids;
-  int32_t* pos;
-  __device__ __forceinline__ void store(int64_t o, int64_t key, uint32_t val) const {
-    __stcs(sm_ids + o, key);
-    __stcs(pos + o, static_cast<int32_t>(val));
-  }
-};
-
-__global__ void shard_offsets_kernel(const uint32_t* digit_offsets, int32_t n, int64_t T, int64_t* shard_offsets) {
-  for (int s = threadIdx.x; s <= n; s += blockDim.x) shard_offsets[s] = (s == n) ? T : int64_t(digit_offsets[s]);
-}
-
-__device__ __forceinline__ int64_t lower_bound_i32(const int32_t* a, int64_t lo, int64_t hi, int64_t x) {
-  while (lo < hi) {
-    int64_t mid = (lo + hi) >> 1;
-    if (int64_t(a[mid]) < x) lo = mid + 1; else hi = mid;
-  }
-  return lo;
-}
-
-// splits[r*n + s] = #{ j in shard s : rio[r] <= pos[j] < rio[r+1] }; validates rio.
-__global__ void splits_kernel(const int32_t* pos, const int64_t* shard_offsets, const int64_t* rio, int32_t n,
-                              int64_t T, int64_t* splits, int32_t* err) {
-  const int64_t nn = int64_t(n) * n;
-  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < nn; i += int64_t(gridDim.x) * blockDim.x) {
-    const int64_t r = i / n, s = i % n;
-    int64_t a = rio[r], b = rio[r + 1];
-    if (a < 0 || b < a || b > T || (r == 0 && a != 0) || (r == n - 1 && b != T)) {
-      set_err(err, FS_ERR_BAD_OFFSETS);
-      a = a < 0 ? 0 : (a > T ? T : a);
-      b = b < a ? a : (b > T ? T : b);
-    }
-    const int64_t lo = shard_offsets[s], hi = shard_offsets[s + 1];
-    splits[i] = lower_bound_i32(pos, lo, hi, b) - lower_bound_i32(pos, lo, hi, a);
-  }
-}
+using shard::DstShardMajor;
+using shard::SrcShard;
 
 size_t bucketize_bytes(int64_t T, int32_t n) { return radix::pass_ws_bytes(T, n); }
 
@@ -123,11 +56,12 @@ extern "C" fs_status fs_bucketize_rowwise(const int64_t* ids, int64_t T, const i
   } else {
     if (cudaMemsetAsync(P.digit_base, 0, size_t(n) * sizeof(uint32_t), st) != cudaSuccess) return FS_ERR_CUDA;
   }
-  shard_offsets_kernel<<<1, kThreads, 0, st>>>(P.digit_base, n, T, shard_offsets);
+  shard::shard_offsets_kernel<<<1, kThreads, 0, st>>>(P.digit_base, n, T, nullptr, shard_offsets);
   int64_t nn = int64_t(n) * n;
   int64_t g = (nn + kThreads - 1) / kThreads;
   if (g > int64_t(sm_count()) * 8) g = int64_t(sm_count()) * 8;
-  splits_kernel<<<unsigned(g < 1 ? 1 : g), kThreads, 0, st>>>(pos, shard_offsets, rank_id_offsets, n, T, splits, err);
+  shard::splits_kernel<<<unsigned(g < 1 ? 1 : g), kThreads, 0, st>>>(pos, shard_offsets, rank_id_offsets, n, T, nullptr,
+                                                                     splits, err);
   count_launch(launches + 2);
   return launch_status();
 }

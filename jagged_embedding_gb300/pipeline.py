@@ -15,7 +15,11 @@ Two orders are provided:
   * run_prioritized -- Algorithm 2's order: exclusive rows of t+1 prefetched
                    before the update of t, collision rows of t updated first,
                    then gathered for t+1; exclusive updates of t deferred to
-                   the next forward.  It needs a second output buffer.
+                   the next forward.  It needs a second output buffer and a
+                   third batch slot.  With streams=True the exclusive-row work
+                   (the deferred updates and the prefetch, Algorithm 2's
+                   "C.stream") runs on a side stream, ordered against the main
+                   stream by events only where the two touch the same data.
 """
 from __future__ import annotations
 
@@ -49,7 +53,8 @@ class Slot:
 
 
 class Pipeline:
-    def __init__(self, w, device, max_T, table, state=None, max_S=None, two_outputs=False, row_sorted=True):
+    def __init__(self, w, device, max_T, table, state=None, max_S=None, two_outputs=False, row_sorted=True,
+                 streams=False):
         self.w = w
         # synchronous order with an update: sort once, gather and update from the sorted entries
         self.row_sorted = row_sorted
@@ -59,7 +64,8 @@ class Pipeline:
         self.table = table
         self.state = state
         dev = self.dev
-        self.slots = [Slot(w, self.max_S, self.max_T, dev), Slot(w, self.max_S, self.max_T, dev)]
+        # the prioritized order keeps three batches: t-1 (its exclusive update is deferred), t and t+1
+        self.slots = [Slot(w, self.max_S, self.max_T, dev) for _ in range(3 if two_outputs else 2)]
         cap = min(2 * self.max_T, w.R)
         self.cap_rows = cap
         self.coll = {
@@ -71,9 +77,9 @@ class Pipeline:
             "ex_t_off": torch.empty(w.n + 1, dtype=torch.int64, device=dev),
             "ex_next_off": torch.empty(w.n + 1, dtype=torch.int64, device=dev),
         }
-        self.masks = [torch.zeros(self.max_T, dtype=torch.uint8, device=dev) for _ in range(2)]
+        self.masks = [torch.zeros(self.max_T, dtype=torch.uint8, device=dev) for _ in self.slots]
         # order of each slot's mask: "batch" (aligned with ids) or "shard" (aligned with sm_ids)
-        self.mask_layout = ["batch", "batch"]
+        self.mask_layout = ["batch"] * len(self.slots)
         self.out = [torch.empty(self.max_T, w.D, dtype=table.dtype, device=dev)]
         if two_outputs:
             self.out.append(torch.empty(self.max_T, w.D, dtype=table.dtype, device=dev))
@@ -86,6 +92,7 @@ class Pipeline:
             L.fs_balance_fbs_workspace_size(self.max_S, w.n),
             L.fs_permute_jagged_workspace_size(self.max_S),
             L.fs_bucketize_rowwise_workspace_size(self.max_T, w.n),
+            L.fs_permute_bucketize_workspace_size(self.max_S, self.max_T, w.n),
             L.fs_collision_split_bitmaps_workspace_size(w.R),
             B.backward_workspace_size(self.max_T, w.R, w.D, B.dtype_code(table)) if w.has_update else 0,
             B.sort_rows_sharded_workspace_size(self.max_T, w.R, w.D, B.dtype_code(table), w.n)
@@ -93,6 +100,12 @@ class Pipeline:
         )
         # one workspace, reused by every call (calls on one stream run in order)
         self.ws = B.workspace(ws_bytes, dev)
+        # Algorithm 2's side stream: the deferred exclusive updates sort in a workspace of their own
+        self.side = None
+        if streams:
+            self.side = torch.cuda.Stream(dev)
+            self.ws_side = B.workspace(B.backward_workspace_size(self.max_T, w.R, w.D, B.dtype_code(table))
+                                       if w.has_update else 256, dev)
 
     # -------------------------------------------------------------- stages
     def prepare(self, batch, slot):
@@ -108,15 +121,15 @@ class Pipeline:
             B.fs_balance_vbs(batch["uih_len"], w.n, w.alpha, w.sort_by_len, perm=s.perm, rank_offsets=s.rank_offsets,
                              seg_weight=s.seg_weight, err=self.err, ws=self.ws)
         T = int(batch["T"])
-        B.fs_permute_jagged(batch["offsets"], batch["ids"], s.perm[: batch["uih_len"].numel()], capacity=self.max_T,
-                            rank_offsets=s.rank_offsets, out_offsets=s.offsets[: batch["offsets"].numel()],
-                            out_values=s.ids, rank_id_offsets=s.rank_id_offsets, err=self.err, ws=self.ws)
+        # the shuffle and the ranged dispatch in one call: the source IDs are read once (§4.2)
+        B.fs_permute_bucketize(batch["offsets"], batch["ids"], s.perm[: batch["uih_len"].numel()], s.rank_offsets,
+                               w.R, capacity=self.max_T, out_offsets=s.offsets[: batch["offsets"].numel()],
+                               out_values=s.ids, rank_id_offsets=s.rank_id_offsets, sm_ids=s.sm_ids, pos=s.pos,
+                               splits=s.splits, shard_offsets=s.shard_offsets, err=self.err, ws=self.ws)
         if w.composite:
             B.fs_permute_jagged(batch["cand_offsets"], batch["cand_lens"], s.perm[: batch["uih_len"].numel()],
                                 capacity=s.cand_lens.numel(), out_offsets=s.cand_offsets[: batch["offsets"].numel()],
                                 out_values=s.cand_lens, err=self.err, ws=self.ws)
-        B.fs_bucketize_rowwise(s.ids, s.rank_id_offsets, w.R, sm_ids=s.sm_ids, pos=s.pos, splits=s.splits,
-                               shard_offsets=s.shard_offsets, err=self.err, ws=self.ws, T=T)
         # the row set does not depend on the order; in shard-major order the IDs a warp marks
         # fall in one shard's stretch of the bitmap
         B.fs_row_bitmap(s.sm_ids, w.R, bitmap=s.bitmap, err=self.err, T=T)
@@ -190,14 +203,14 @@ class Pipeline:
         return (self.row_sorted and (phase == B.PHASE_ALL or self.w.R <= (1 << 30))
                 and self.table.data_ptr() % 16 == 0 and self.out[0].data_ptr() % 16 == 0)
 
-    def backward(self, slot, grads, phase=B.PHASE_ALL, co_rows=None):
+    def backward(self, slot, grads, phase=B.PHASE_ALL, co_rows=None, ws=None):
         """Update of the batch in `slot`; the phase's collision flags come from the batch's mask, or
         from co_rows (the row bitmap of the next batch) when given."""
         w, s = self.w, self.slots[slot]
         use_mask = phase != B.PHASE_ALL and co_rows is None
         B.fs_emb_backward_adagrad(self.table, self.state, s.ids, grads, w.optim, w.lr, w.eps,
                                   is_co=self.masks[slot] if use_mask else None, phase=phase,
-                                  err=self.err, ws=self.ws, T=s.T, co_rows=co_rows)
+                                  err=self.err, ws=self.ws if ws is None else ws, T=s.T, co_rows=co_rows)
 
     # -------------------------------------------------------------- orders
     def step_sync(self, cur, nxt_batch, grads, has_next=True, want_masks=False, times=None):
@@ -234,34 +247,95 @@ class Pipeline:
             self.backward(cur, grads, phase)
         return nxt
 
+    # ------------------------------------------------ Algorithm 2, one iteration at a time
+    def prio_begin(self, batch0):
+        """Prioritized order: prepare the first batch and gather it whole (slot 0, output 0)."""
+        assert len(self.out) == 2 and len(self.slots) == 3
+        self.prepare(batch0, 0)
+        self.gather(0, out_idx=0)
+        self._t = 0
+        self._pending_ex = None                # (slot, grads, event after its split) of the deferred update
+        self._slot_free = [None] * 3           # side-stream event after which a slot may be rewritten
+
+    def _exclusive_update(self, slot, grads, ev_split):
+        """Algorithm 2 line 7: the deferred update of the batch in `slot`'s exclusive rows (side stream)."""
+        if self.side is None:
+            self.backward(slot, grads, B.PHASE_EXCLUSIVE)
+            return
+        self.side.wait_event(ev_split)
+        with torch.cuda.stream(self.side):
+            self.backward(slot, grads, B.PHASE_EXCLUSIVE, ws=self.ws_side)
+        ev = torch.cuda.Event()
+        ev.record(self.side)
+        self._slot_free[slot] = ev
+
+    def prio_step(self, next_batch, grads, times=None, on_output=None):
+        """Iteration t of Algorithm 2 (t counts calls since prio_begin); next_batch is None for the last.
+
+        Batch t lives in slot t % 3 and its output in out[t % 2]; on_output(t, rows) sees it whole.
+        Main stream: prepare t+1, the split of (t, t+1), the collision rows of t (line 20), then
+        their lookup for t+1 (line 21).  Side stream (or the main one): the deferred exclusive update
+        of t-1 (line 7), then the prefetch of t+1's exclusive rows (line 12), which may read rows
+        that update wrote.  The two streams touch disjoint rows: the exclusive rows of t-1 are not
+        rows of t, and those of t+1 are not rows of t either.
+        """
+        t = self._t
+        cur, nxt = t % 3, (t + 1) % 3
+        side = self.side
+        main = torch.cuda.current_stream(self.dev) if side is not None else None
+        if self._pending_ex is not None:                                 # line 7
+            self._exclusive_update(*self._pending_ex)
+            self._pending_ex = None
+        ev_split = ev_pref = None
+        if next_batch is not None:                                       # lines 8-12
+            if self._slot_free[nxt] is not None:                         # batch t-2's deferred update read it
+                main.wait_event(self._slot_free[nxt])
+                self._slot_free[nxt] = None
+            if times is not None and self.w.autotune:
+                self.autotune(times)
+            self.prepare(next_batch, nxt)
+            self.collision(cur, nxt)
+            if side is not None:
+                ev_split = torch.cuda.Event()
+                ev_split.record(main)
+                side.wait_event(ev_split)
+                with torch.cuda.stream(side):
+                    self.gather(nxt, out_idx=(t + 1) % 2, mask=self.masks[nxt], sel=0)
+                ev_pref = torch.cuda.Event()
+                ev_pref.record(side)
+            else:
+                self.gather(nxt, out_idx=(t + 1) % 2, mask=self.masks[nxt], sel=0)
+        if on_output is not None:
+            on_output(t, self.out[t % 2][: self.slots[cur].T])
+        if self.w.has_update:                                            # lines 18-20
+            if next_batch is not None:
+                self.backward(cur, grads, B.PHASE_COLLISION)
+                self._pending_ex = (cur, grads, ev_split)
+            else:
+                self.backward(cur, grads, B.PHASE_ALL)
+        if next_batch is not None:                                       # line 21
+            self.gather(nxt, out_idx=(t + 1) % 2, mask=self.masks[nxt], sel=1)
+            if ev_pref is not None:
+                main.wait_event(ev_pref)                                 # the output of t+1 is whole
+        self._t = t + 1
+
+    def prio_finish(self):
+        """The exclusive update still deferred after the last iteration; the side stream joins the main one."""
+        if self._pending_ex is not None:
+            self._exclusive_update(*self._pending_ex)
+            self._pending_ex = None
+        if self.side is not None:
+            ev = torch.cuda.Event()
+            ev.record(self.side)
+            torch.cuda.current_stream(self.dev).wait_event(ev)
+        self._slot_free = [None] * 3
+
     def run_prioritized(self, batches, grads_list, on_output=None, times_list=None):
         """Algorithm 2 order over len(batches) iterations.  on_output(t, out_tensor) sees each batch's output;
         with AutoTune on, times_list[t] is folded in before t+1 is prepared (as in step_sync)."""
         K = len(batches)
-        assert len(self.out) == 2
-        self.prepare(batches[0], 0)
-        self.gather(0, out_idx=0)
-        pending_ex = None
+        self.prio_begin(batches[0])
         for t in range(K):
-            cur, nxt = t % 2, (t + 1) % 2
-            if pending_ex is not None:                                   # line 7
-                self.backward(pending_ex[0], pending_ex[1], B.PHASE_EXCLUSIVE)
-                pending_ex = None
-            if t + 1 < K:                                                # lines 8-12
-                if times_list is not None and self.w.autotune:
-                    self.autotune(times_list[t])
-                self.prepare(batches[t + 1], nxt)
-                self.collision(cur, nxt)
-                self.gather(nxt, out_idx=nxt, mask=self.masks[nxt], sel=0)
-            if on_output is not None:
-                on_output(t, self.out[cur][: self.slots[cur].T])
-            if self.w.has_update:                                        # lines 18-20
-                if t + 1 < K:
-                    self.backward(cur, grads_list[t], B.PHASE_COLLISION)
-                    pending_ex = (cur, grads_list[t])
-                else:
-                    self.backward(cur, grads_list[t], B.PHASE_ALL)
-            if t + 1 < K:                                                # line 21
-                self.gather(nxt, out_idx=nxt, mask=self.masks[nxt], sel=1)
-        if pending_ex is not None:
-            self.backward(pending_ex[0], pending_ex[1], B.PHASE_EXCLUSIVE)
+            self.prio_step(batches[t + 1] if t + 1 < K else None, grads_list[t] if grads_list else None,
+                           times=times_list[t] if times_list is not None else None, on_output=on_output)
+        self.prio_finish()

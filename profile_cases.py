@@ -1,6 +1,9 @@
 """One hot-path call on seeded synthetic input, for profiling a single kernel.
 
-    python -m jagged_embedding_gb300.cases <op> <T> <R> [reps]
+    python profile_cases.py <op> <T> <R> [reps]
+
+These are the small cases that the ncu summaries under profiles/ were taken
+on (a few GB on the device, one kernel at a time).
 
 op is one of
   gather    -- fs_emb_gather, unmasked, f32 rows of 64, T bounded-Zipf(1.0) IDs over R rows
@@ -8,6 +11,12 @@ op is one of
                collision rows (half of the rows, by a hash of the row) updated before exclusive rows
   backward-bf16 -- the same with bf16 rows of 128 (the mid-size full step's table)
   bucketize -- fs_bucketize_rowwise of the same IDs into 256 row-range shards
+  prep      -- fs_permute_bucketize: T IDs in samples of lognormal(6.8, 1.5) lengths up to 16384 dealt to
+               256 ranks by FBS, permuted and bucketized into 256 row-range shards over R rows
+  sorted-step -- the large-table step's update path on the same IDs (256 ranks and shards, f32 rows of 64,
+               row-wise Adagrad, half the rows collision rows): fs_bucketize_rowwise, the mask in
+               shard-major order, fs_emb_sort_rows_sharded, fs_emb_gather_sorted, fs_emb_update_sorted;
+               prints each call's median time and the bandwidth of its algorithmic bytes
   transpose -- fs_keyed_transpose of about T IDs in R features x 65536 samples (lengths uniform, per-feature
                row bases); prints the time per call and the bandwidth of its algorithmic bytes
   gather-sorted -- the same IDs and table as gather: fs_emb_sort_rows once, then fs_emb_gather_sorted and
@@ -21,12 +30,16 @@ Exits non-zero if a call reports an error.
 """
 from __future__ import annotations
 
+import os
 import sys
 
 import torch
 
-from . import binding as B
-from . import synthetic
+sys.path.insert(0, os.path.dirname(os.path.abspath(__file__)))
+
+from jagged_embedding_gb300 import binding as B  # noqa: E402
+from jagged_embedding_gb300 import build as cuda_build  # noqa: E402
+from jagged_embedding_gb300 import synthetic  # noqa: E402
 
 DIM = 64
 SHARDS = 256
@@ -34,11 +47,12 @@ SHARDS = 256
 
 def main(argv) -> int:
     if len(argv) < 3 or argv[0] not in ("gather", "backward", "backward-bf16", "bucketize", "transpose",
-                                        "autotune", "gather-sorted"):
+                                        "autotune", "gather-sorted", "prep", "sorted-step"):
         print(__doc__)
         return 2
     op, T, R = argv[0], int(argv[1]), int(argv[2])
     reps = int(argv[3]) if len(argv) > 3 else 2
+    cuda_build.build()
     dev = torch.device("cuda")
     g = torch.Generator(device=dev)
     g.manual_seed(1)
@@ -47,7 +61,11 @@ def main(argv) -> int:
         return _transpose(T, R, reps, dev, g, err)
     if op == "autotune":
         return _autotune(T, R, reps, dev, g, err)
+    if op == "prep":
+        return _prep(T, R, reps, dev, g, err)
     ids = synthetic.zipf_rows(R, 1.0, T, g, dev)
+    if op == "sorted-step":
+        return _sorted_step(ids, T, R, reps, dev, g, err)
     if op == "gather-sorted":
         return _gather_sorted(ids, T, R, reps, dev, g, err)
     if op == "gather":
@@ -128,6 +146,65 @@ def _gather_sorted(ids, T, R, reps, dev, g, err):
     byts = (8 + 4 * DIM) * T + 4 * DIM * U
     print(f"gather-sorted T={T} R={R} U={U}: sorted {t_sorted:.3f} ms ({byts / t_sorted / 1e6:.0f} GB/s), "
           f"position order {t_plain:.3f} ms ({byts / t_plain / 1e6:.0f} GB/s) (median of {reps})")
+    return 0
+
+
+def _prep(T, R, reps, dev, g, err):
+    reps = max(reps, 3)
+    n = SHARDS
+    L = torch.empty(T // 2000 + 1, dtype=torch.float64, device=dev).log_normal_(6.8, 1.5, generator=g)
+    L = L.round().clamp_(1, 16384).to(torch.int64)
+    S = (L.numel() // n) * n
+    L = L[:S]
+    off = torch.zeros(S + 1, dtype=torch.int64, device=dev)
+    off[1:] = torch.cumsum(L, 0)
+    Tn = int(off[-1])
+    ids = synthetic.zipf_rows(R, 1.0, Tn, g, dev)
+    perm, ro, e0 = B.fs_balance_fbs(L.to(torch.int32), n)
+    B.check(e0, "prep balance")
+    outs = [torch.empty(S + 1, dtype=torch.int64, device=dev), torch.empty(Tn, dtype=torch.int64, device=dev),
+            torch.empty(n + 1, dtype=torch.int64, device=dev), torch.empty(Tn, dtype=torch.int64, device=dev),
+            torch.empty(Tn, dtype=torch.int32, device=dev), torch.empty(n, n, dtype=torch.int64, device=dev),
+            torch.empty(n + 1, dtype=torch.int64, device=dev)]
+    ws = B.workspace(B.lib().fs_permute_bucketize_workspace_size(S, Tn, n), dev)
+
+    def call():
+        B.fs_permute_bucketize(off, ids, perm, ro, R, capacity=Tn, out_offsets=outs[0], out_values=outs[1],
+                               rank_id_offsets=outs[2], sm_ids=outs[3], pos=outs[4], splits=outs[5],
+                               shard_offsets=outs[6], err=err, ws=ws)
+    t = _median_ms(call, reps)
+    B.check(err, "prep")
+    byts = 16 * S + 36 * Tn
+    print(f"prep S={S} T={Tn} R={R}: {t:.3f} ms, {byts / t / 1e6:.0f} GB/s of algorithmic bytes (median of {reps})")
+    return 0
+
+
+def _sorted_step(ids, T, R, reps, dev, g, err):
+    reps = max(reps, 3)
+    n = SHARDS
+    table = torch.empty(R, DIM, device=dev).normal_(0, 0.01, generator=g)
+    state = torch.zeros(R, device=dev)
+    grads = torch.empty(T, DIM, device=dev).normal_(generator=g)
+    rio = torch.linspace(0, T, n + 1, device=dev).round().to(torch.int64)
+    sm, pos, _, so, e0 = B.fs_bucketize_rowwise(ids, rio, R)
+    B.check(e0, "sorted-step bucketize")
+    is_co = (((sm * 0x9E3779B1) >> 7) & 1).to(torch.uint8)             # half the rows, shard-major
+    out = torch.empty(T, DIM, device=dev)
+    ws = B.workspace(B.sort_rows_sharded_workspace_size(T, R, DIM, B.dtype_code(table), n), dev)
+    ph = B.PHASE_COLLISION_THEN_EXCLUSIVE
+    t_sort = _median_ms(lambda: B.fs_emb_sort_rows_sharded(table, sm, pos, so, ws, phase=ph, is_co=is_co, err=err),
+                        reps)
+    t_gather = _median_ms(lambda: B.fs_emb_gather_sorted(table, T, ws, out=out, phase=ph, err=err), reps)
+    t_update = _median_ms(lambda: B.fs_emb_update_sorted(table, state, grads, T, ws, "adagrad", 0.01, 1e-8,
+                                                         phase=ph, err=err), reps)
+    torch.cuda.synchronize()
+    B.check(err, "sorted-step")
+    U = int(torch.unique(ids).numel())
+    rb = 4 * DIM
+    gb, ub = (8 + rb) * T + rb * U, (8 + rb) * T + (2 * rb + 8) * U
+    print(f"sorted-step T={T} R={R} U={U}: sort {t_sort:.3f} ms, gather {t_gather:.3f} ms "
+          f"({gb / t_gather / 1e6:.0f} GB/s), update {t_update:.3f} ms ({ub / t_update / 1e6:.0f} GB/s) "
+          f"(median of {reps}); algorithmic bytes gather {gb}, update {ub}")
     return 0
 
 

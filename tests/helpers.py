@@ -80,3 +80,35 @@ def assert_state_close(got, ref, rtol=1e-5):
     if bad.any():
         i = int(np.argwhere(bad)[0][0])
         raise AssertionError(f"{int(bad.sum())} state entries out of tolerance; first row {i}: {g[i]} vs {r[i]}")
+
+
+class Guarded:
+    """A device tensor between two guard bands of seeded bytes (4 KB each).
+
+    `t` is the tensor a call may write (exactly `shape`, no slack); `check()`
+    asserts that neither band changed, i.e. that the call wrote nothing before
+    or after its output.  `init` fills `t` first (for in-place arguments).
+    """
+
+    BAND = 4096
+
+    def __init__(self, shape, dtype, device="cuda", init=None, seed=0):
+        shape = tuple(shape) if isinstance(shape, (tuple, list)) else (int(shape),)
+        numel = int(np.prod(shape)) if shape else 1
+        esz = torch.empty(0, dtype=dtype).element_size()
+        self.band = self.BAND // esz
+        self.nbytes = self.band * esz
+        self.buf = torch.empty(numel + 2 * self.band, dtype=dtype, device=device)
+        g = torch.Generator().manual_seed(numel * 31 + seed)
+        raw = self.buf.view(torch.uint8)
+        self.pattern = torch.randint(0, 256, (raw.numel(),), dtype=torch.uint8, generator=g)
+        raw.copy_(self.pattern.to(device))
+        self.t = self.buf[self.band: self.band + numel].view(shape)
+        if init is not None:
+            self.t.copy_(init)
+
+    def check(self, what=""):
+        raw = self.buf.view(torch.uint8).cpu()
+        nb = self.nbytes
+        assert torch.equal(raw[:nb], self.pattern[:nb]), f"{what}: guard band before the output was written"
+        assert torch.equal(raw[-nb:], self.pattern[-nb:]), f"{what}: guard band after the output was written"

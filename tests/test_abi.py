@@ -126,6 +126,25 @@ def test_host_argument_errors_return_without_launching():
                                   C.c_float(0.01), C.c_float(1e-8), err, ws, big, NULL) == 1  # Adagrad, no state
     assert L.fs_emb_update_sorted(C.c_void_p(0x100), NULL, 1000, 64, 0, 0, C.c_void_p(0x300), 0, 0,
                                   C.c_float(0.01), C.c_float(0.0), err, NULL, 0, NULL) == 0  # T = 0: nothing to do
+    # fused permute + bucketize: rank offsets required, n <= 1024, 8-byte aligned outputs, workspace
+    pb = [C.c_void_p(0x10), C.c_void_p(0x20), 10, C.c_void_p(0x30), C.c_void_p(0x40), 4, 100, C.c_void_p(0x50),
+          C.c_void_p(0x60), 64, C.c_void_p(0x70), C.c_void_p(0x80), C.c_void_p(0x90), C.c_void_p(0xa0),
+          C.c_void_p(0xb0), err, ws, 1 << 30, NULL]
+    assert L.fs_permute_bucketize(*(pb[:4] + [NULL] + pb[5:])) == 1
+    assert L.fs_permute_bucketize(*(pb[:5] + [1025] + pb[6:])) == 1
+    assert L.fs_permute_bucketize(*(pb[:11] + [C.c_void_p(0x84)] + pb[12:])) == 8
+    assert L.fs_permute_bucketize(*(pb[:17] + [16] + pb[18:])) == 5
+    assert L.fs_permute_bucketize_workspace_size(10, 64, 4) > 0 and L.fs_permute_bucketize_workspace_size(10, 64, 0) == 0
+    # per-shard update sort: n <= 1024, the phase bit beside shards of at most 2^19 rows, the flags for two phases
+    big_s = L.fs_emb_sort_rows_sharded_workspace_size(100, 1000, 64, 0, 8)
+    assert big_s > L.fs_emb_backward_adagrad_workspace_size(100, 1000, 64, 0)
+    sh = [1000, 64, 0, C.c_void_p(0x200), C.c_void_p(0x300), 100, C.c_void_p(0x400), 8, C.c_void_p(0x500), 3, err,
+          ws, big_s, NULL]
+    assert L.fs_emb_sort_rows_sharded(*(sh[:7] + [1025] + sh[8:])) == 1
+    assert L.fs_emb_sort_rows_sharded(*([(1 << 19) + 1] + sh[1:7] + [1] + sh[8:12] + [1 << 40] + sh[13:])) == 1
+    assert L.fs_emb_sort_rows_sharded(*(sh[:8] + [NULL] + sh[9:])) == 1
+    assert L.fs_emb_sort_rows_sharded(*(sh[:4] + [C.c_void_p(0x302)] + sh[5:])) == 8
+    assert L.fs_emb_sort_rows_sharded(*(sh[:12] + [big_s - 256] + sh[13:])) == 5
     assert L.fs_collision_split(C.c_void_p(0x10), 5, C.c_void_p(0x20), 5, (1 << 32) + 1, 4, NULL, NULL, NULL, 0,
                                 C.c_void_p(0x30), C.c_void_p(0x40), C.c_void_p(0x50), C.c_void_p(0x60),
                                 C.c_void_p(0x70), C.c_void_p(0x80), err, ws, 1 << 30, NULL) == 1
@@ -138,6 +157,6 @@ def test_binding_refuses_cpu_tensors():
 
 
 def test_profiling_cases_print_usage_without_arguments():
-    from jagged_embedding_gb300 import cases
-    assert cases.main([]) == 2
-    assert cases.main(["nosuchop", "1", "1"]) == 2
+    import profile_cases
+    assert profile_cases.main([]) == 2
+    assert profile_cases.main(["nosuchop", "1", "1"]) == 2

@@ -159,15 +159,17 @@ def test_pipeline_matches_oracle(name):
         assert np.array_equal(tab_gpu, tab_ref)
 
 
+@pytest.mark.parametrize("streams", [False, True])
 @pytest.mark.parametrize("name", ["tiny-fbs-sgd", "mid-full-step", "large-table-full-step", "long-seq-autotune"])
-def test_prioritized_order_equals_sync_order_on_gpu(name):
-    """Algorithm 2's order gathers exactly what the synchronous order gathers (FreeScale §3.2)."""
+def test_prioritized_order_equals_sync_order_on_gpu(name, streams):
+    """Algorithm 2's order gathers exactly what the synchronous order gathers (FreeScale §3.2), on one
+    stream and with the exclusive-row work on a side stream."""
     w = CASES[name]
     batches, table0, grads = _inputs(w)
     rec, tab_sync, st_sync = _gpu_sync(w, batches, table0, grads)
     tab = table0.to(DEV)
     state = torch.zeros(w.R, dtype=torch.float32, device=DEV) if w.optim == "adagrad" else None
-    pipe = Pipeline(w, DEV, max(b["T"] for b in batches), tab, state, two_outputs=True)
+    pipe = Pipeline(w, DEV, max(b["T"] for b in batches), tab, state, two_outputs=True, streams=streams)
     outs = {}
     pipe.run_prioritized([batch_to(b, DEV) for b in batches], [g.to(DEV) for g in grads] if grads else None,
                          on_output=lambda t, o: outs.__setitem__(t, to_np(o)), times_list=_times(w, DEV))

@@ -14,7 +14,7 @@ from jagged_embedding_gb300 import pipeline as P
 from jagged_embedding_gb300 import synthetic
 
 CALLS = ["fs_balance_fbs", "fs_balance_vbs", "fs_balance_vbs_tuned", "fs_vbs_autotune", "fs_permute_jagged",
-         "fs_bucketize_rowwise", "fs_row_bitmap", "fs_collision_split_bitmaps", "fs_emb_gather",
+         "fs_bucketize_rowwise", "fs_permute_bucketize", "fs_row_bitmap", "fs_collision_split_bitmaps", "fs_emb_gather",
          "fs_emb_gather_sorted", "fs_emb_sort_rows", "fs_emb_sort_rows_sharded", "fs_emb_update_sorted",
          "fs_emb_backward_adagrad"]
 
@@ -41,7 +41,7 @@ def _batch(w):
             "ids": torch.zeros(S, dtype=torch.int64), "T": S}
 
 
-def _names(log, skip=("fs_balance_fbs", "fs_permute_jagged", "fs_bucketize_rowwise", "fs_row_bitmap")):
+def _names(log, skip=("fs_balance_fbs", "fs_permute_bucketize", "fs_permute_jagged", "fs_row_bitmap")):
     return [(n, ph) for n, ph in log if n not in skip]
 
 
@@ -59,9 +59,8 @@ def test_sync_step_sorts_before_the_lookup(calls):
     assert _names(calls) == [("fs_collision_split_bitmaps", None), ("fs_emb_sort_rows_sharded", CT),
                              ("fs_emb_gather_sorted", CT), ("fs_emb_update_sorted", CT)]
     assert pipe.mask_layout[0] == "shard"           # its collision flags follow the shard-major IDs
-    # the batch is prepared (balanced, permuted, bucketized, marked) before the split
-    assert [n for n, _ in calls[:4]] == ["fs_balance_fbs", "fs_permute_jagged", "fs_bucketize_rowwise",
-                                        "fs_row_bitmap"]
+    # the batch is prepared (balanced, permuted and bucketized in one call, marked) before the split
+    assert [n for n, _ in calls[:3]] == ["fs_balance_fbs", "fs_permute_bucketize", "fs_row_bitmap"]
 
 
 def test_sync_step_sorts_batch_major_ids_when_shards_are_too_large(calls):
@@ -137,4 +136,5 @@ def test_prioritized_order_follows_algorithm_2(calls):
         else:
             expect.append(("fs_emb_backward_adagrad", A))
     assert seq == expect
-    assert pipe.mask_layout == ["batch", "batch"]   # the masked lookups and updates read batch-major masks
+    assert pipe.mask_layout == ["batch"] * 3        # the masked lookups and updates read batch-major masks
+    assert len(pipe.slots) == 3                     # batches t-1 (deferred update), t and t+1

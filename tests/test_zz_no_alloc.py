@@ -15,7 +15,7 @@ import torch
 
 import oracle
 from jagged_embedding_gb300 import binding as B
-from tests.helpers import to_np
+from tests.helpers import Guarded, to_np
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -28,12 +28,15 @@ def _lens(seed, S):
 
 def _noalloc(L, n):
     S = L.numel()
-    perm = torch.full((S,), -1, dtype=torch.int32, device=DEV)
-    ro = torch.full((n + 1,), -1, dtype=torch.int64, device=DEV)
+    # outputs between guard bands: the call writes nothing before or after them
+    perm = Guarded(S, torch.int32, DEV, torch.full((S,), -1, dtype=torch.int32))
+    ro = Guarded(n + 1, torch.int64, DEV, torch.full((n + 1,), -1, dtype=torch.int64))
     err = torch.zeros(1, dtype=torch.int32, device=DEV)
-    B.fs_balance_fbs_noalloc(L, n, perm, ro, err)
+    B.fs_balance_fbs_noalloc(L, n, perm.t, ro.t, err)
     B.check(err, "fs_balance_fbs_noalloc")
-    return perm, ro
+    perm.check("perm")
+    ro.check("rank_offsets")
+    return perm.t, ro.t
 
 
 @pytest.mark.parametrize("n,S", [(256, 131072), (64, 16384), (3, 7)])
