@@ -46,13 +46,17 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def algorithmic_bytes(w, S, T, U, R, n_cand=0):
+def algorithmic_bytes(w, S, T, U, R, n_cand=0, masks=False):
     """Bytes the method must move for one step (one batch), by stage.
 
     prep (balance + permute + bucketize)      16 S + 16 T + 20 T
       (+ 16 S + 16 C with composite candidates: their lengths move with the samples, C candidates)
-    collision split, per pair                  8 T + 2 T + 3 R / 8 + 16 U
+    collision split, per pair                  8 T + 3 R / 8 + 16 U
+      (+ 2 T when the per-position collision masks are written: the prioritized order's masked
+       lookups and updates read them; the synchronous step's update reads t+1's row bitmap instead)
     gather                                     (8 + RB) T + RB U
+      (+ 4 T when it gathers in shard-major order: the batch-major position of each entry; the
+       gather-only workloads do)
     backward (segment-reduce + update)         (8 + RB) T + (2 RB + 8) U
     VBS AutoTune (when on)                     48 n: times in, corrections read and written,
                                                corrections read again and segment ends moved by the cut
@@ -61,8 +65,8 @@ def algorithmic_bytes(w, S, T, U, R, n_cand=0):
     RB = w.row_bytes
     b = {
         "prep": 16 * S + 36 * T + ((16 * S + 16 * n_cand) if w.composite else 0),
-        "collision": 10 * T + 3 * R / 8 + 16 * U,
-        "gather": (8 + RB) * T + RB * U,
+        "collision": (10 if masks else 8) * T + 3 * R / 8 + 16 * U,
+        "gather": gather_bytes(w, T, U),
     }
     if w.autotune:
         b["autotune"] = 48 * w.n
@@ -72,7 +76,9 @@ def algorithmic_bytes(w, S, T, U, R, n_cand=0):
 
 
 def gather_bytes(w, T, U):
-    return (8 + w.row_bytes) * T + w.row_bytes * U
+    """The lookup: IDs in, rows out, each distinct row read once; the gather-only workloads read the
+    shard-major IDs and their batch-major positions (4 more bytes per ID)."""
+    return (8 + (0 if w.has_update else 4) + w.row_bytes) * T + w.row_bytes * U
 
 
 class ClockSampler:
@@ -419,7 +425,7 @@ def run_gpu(args):
     ubytes = 0.0
     for t in step_batches:
         n_cand = int(batches[t]["cand_offsets"][-1]) if w.composite else 0
-        bb = algorithmic_bytes(w, w.S, Ts[t], U[t], w.R, n_cand)
+        bb = algorithmic_bytes(w, w.S, Ts[t], U[t], w.R, n_cand, masks=prio)
         step_bytes += sum(bb.values())
         gbytes += gather_bytes(w, Ts[t], U[t])
         ubytes += bb.get("backward", 0.0)
@@ -464,7 +470,8 @@ def run_gpu(args):
     if not prio:
         sorted_gather = w.has_update and pipe.row_sorted
         ga = gbytes / (gather_ms / 1000.0) / 1e9
-        calls = {"gather": {"kernel": SORTED_GATHER_KERNEL if sorted_gather else GATHER_KERNEL, "bound": "hbm",
+        gk = SORTED_GATHER_KERNEL if sorted_gather else (GATHER_KERNEL if w.has_update else SHARD_GATHER_KERNEL)
+        calls = {"gather": {"kernel": gk, "bound": "hbm",
                             "achieved": ga, "peak": hbm_gbs, "peak_kind": peak_kind, "unit": "GB/s",
                             "frac": ga / hbm_gbs, "traffic": recorded_traffic("gather", w0.name, sorted_gather),
                             "algorithmic_bytes_per_launch": gbytes, "avg_launch_ms": gather_ms}}
@@ -503,16 +510,17 @@ def recorded_traffic(call, workload, sorted_gather):
     return rec.get("bytes_per_launch")
 
 
-# the dominant kernel of the step: the unmasked gather of the synchronous order (from the update's
-# sorted entries when the workload has an update)
+# the synchronous step's gather: from the update's sorted entries when the workload has an update, in
+# shard-major order from the bucketize output otherwise (the position-order gather when neither applies)
 GATHER_KERNEL = "fs_emb_gather (gather_bulk_kernel<4, 2>)"
 SORTED_GATHER_KERNEL = "fs_emb_gather_sorted (gather_sorted_kernel)"
+SHARD_GATHER_KERNEL = "fs_emb_gather_shard_major (gather_scatter_kernel)"
 
 
 def kernel_hash(call="gather", sorted_gather=False):
     """Hash of the sources of a call's kernels (a recorded DRAM traffic is valid for these only)."""
     import hashlib
-    names = {("gather", False): ("gather.cu", "bulk.cuh"), ("gather", True): ("backward.cu", "radix.cuh"),
+    names = {("gather", False): ("gather.cu",), ("gather", True): ("backward.cu", "radix.cuh"),
              ("update", False): ("backward.cu", "radix.cuh", "bulk.cuh"),
              ("update", True): ("backward.cu", "radix.cuh", "bulk.cuh")}[(call, sorted_gather)]
     h = hashlib.sha256()

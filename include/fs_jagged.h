@@ -314,6 +314,26 @@ fs_status fs_emb_gather(const void* table, int64_t num_rows, int32_t dim, fs_dty
                         fs_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Embedding gather in shard-major order -- FreeScale Algorithm 2 line 12 as
+ * the shards make it: each shard looks up the rows of its shard-major IDs,
+ * and the ranged combine puts every row back at its batch-major position:
+ *   out[pos[j], :] = table[sm_ids[j], :]   for j in [0, T)
+ * With (sm_ids, pos) from fs_bucketize_rowwise (or fs_permute_bucketize) of
+ * ids, pos is a permutation of [0, T) and the result is fs_emb_gather's
+ * unmasked result, bit for bit.  A shard's entries come together, so a
+ * shard's repeated rows are read from L2 rather than again from DRAM while it
+ * is gathered (shards of up to tens of MB of rows).
+ *   sm_ids [T] int64, pos [T] int32 (in [0, T); FS_ERR_BAD_OFFSETS and the
+ *   entry skipped otherwise; an ID outside [0, num_rows) FS_ERR_ID_RANGE)
+ *   table [num_rows, dim] of dtype, out [T, dim] of dtype.
+ * Row bytes must be a multiple of 4; rows of 64, 128, 256 or 512 bytes with
+ * 16-byte aligned table and out move as 16-byte vectors.
+ * ---------------------------------------------------------------------- */
+fs_status fs_emb_gather_shard_major(const void* table, int64_t num_rows, int32_t dim, fs_dtype dtype,
+                                    const int64_t* sm_ids, const int32_t* pos, int64_t T, void* out, int32_t* err,
+                                    fs_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Embedding backward: gradient segment-reduce per row + row update --
  * FreeScale Algorithm 2 lines 7 and 20 (update_embedding on the exclusive and
  * the collision rows) and line 18 (split of the gradients).  The pages name
@@ -405,8 +425,14 @@ fs_status fs_emb_update_sorted(void* table, float* state, int64_t num_rows, int3
  *          batch (n shards of block = ceil(num_rows / n) rows; n <= 1024)
  *   is_co  [T] uint8 per SHARD-MAJOR entry (e.g. the mask fs_collision_split
  *          writes when given sm_ids as its IDs): 1 for a collision row, 0 for
- *          an exclusive one; required for FS_PHASE_COLLISION_THEN_EXCLUSIVE,
- *          ignored for FS_PHASE_ALL
+ *          an exclusive one; or
+ *   co_rows the collision rows as a row bitmap (bit r & 31 of word r >> 5; for
+ *          Algorithm 2 the presence bitmap of batch t+1, which fs_row_bitmap
+ *          writes): the sort looks each entry's row up, so no mask pass is
+ *          needed; entries come shard-major, so a tile's lookups stay in its
+ *          shard's stretch of the bitmap.
+ *          Exactly one of the two for FS_PHASE_COLLISION_THEN_EXCLUSIVE;
+ *          both ignored for FS_PHASE_ALL.
  *   phase  FS_PHASE_ALL or FS_PHASE_COLLISION_THEN_EXCLUSIVE
  *   ws     fs_emb_sort_rows_sharded_workspace_size(T, num_rows, dim, dtype, n)
  *          bytes; its first fs_emb_backward_adagrad_workspace_size(...) bytes
@@ -422,8 +448,8 @@ fs_status fs_emb_update_sorted(void* table, float* state, int64_t num_rows, int3
 size_t fs_emb_sort_rows_sharded_workspace_size(int64_t T, int64_t num_rows, int32_t dim, fs_dtype dtype, int32_t n);
 fs_status fs_emb_sort_rows_sharded(int64_t num_rows, int32_t dim, fs_dtype dtype, const int64_t* sm_ids,
                                    const int32_t* pos, int64_t T, const int64_t* shard_offsets, int32_t n,
-                                   const uint8_t* is_co, fs_phase phase, int32_t* err, void* ws, size_t ws_bytes,
-                                   fs_stream_t stream);
+                                   const uint8_t* is_co, const uint32_t* co_rows, fs_phase phase, int32_t* err,
+                                   void* ws, size_t ws_bytes, fs_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * Utilities.

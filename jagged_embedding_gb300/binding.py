@@ -36,7 +36,7 @@ EXPORTS = [
     "fs_keyed_transpose", "fs_bucketize_rowwise_workspace_size",
     "fs_bucketize_rowwise", "fs_permute_bucketize_workspace_size", "fs_permute_bucketize",
     "fs_collision_split_workspace_size", "fs_collision_split", "fs_row_bitmap_words",
-    "fs_row_bitmap", "fs_collision_split_bitmaps_workspace_size", "fs_collision_split_bitmaps", "fs_emb_gather",
+    "fs_row_bitmap", "fs_collision_split_bitmaps_workspace_size", "fs_collision_split_bitmaps", "fs_emb_gather", "fs_emb_gather_shard_major",
     "fs_emb_backward_adagrad_workspace_size", "fs_emb_backward_adagrad", "fs_emb_sort_rows",
     "fs_emb_gather_sorted", "fs_emb_update_sorted", "fs_emb_sort_rows_sharded_workspace_size",
     "fs_emb_sort_rows_sharded", "fs_check", "fs_status_string",
@@ -86,11 +86,12 @@ def lib():
         "fs_collision_split_bitmaps": ([P, i64, P, P, i64, P, i64, i32, P, P, P, i64, P, P, P, P, P, P, P, P, sz, P],
                                        C.c_int),
         "fs_emb_gather": ([P, i64, i32, C.c_int, P, i64, P, u8, P, P, P], C.c_int),
+        "fs_emb_gather_shard_major": ([P, i64, i32, C.c_int, P, P, i64, P, P, P], C.c_int),
         "fs_emb_backward_adagrad_workspace_size": ([i64, i64, i32, C.c_int], sz),
         "fs_emb_sort_rows": ([i64, i32, C.c_int, P, i64, P, P, C.c_int, P, P, sz, P], C.c_int),
         "fs_emb_gather_sorted": ([P, i64, i32, C.c_int, i64, C.c_int, P, P, P, sz, P], C.c_int),
         "fs_emb_sort_rows_sharded_workspace_size": ([i64, i64, i32, C.c_int, i32], sz),
-        "fs_emb_sort_rows_sharded": ([i64, i32, C.c_int, P, P, i64, P, i32, P, C.c_int, P, P, sz, P], C.c_int),
+        "fs_emb_sort_rows_sharded": ([i64, i32, C.c_int, P, P, i64, P, i32, P, P, C.c_int, P, P, sz, P], C.c_int),
         "fs_emb_update_sorted": ([P, P, i64, i32, C.c_int, C.c_int, P, i64, C.c_int, f32, f32, P, P, sz, P],
                                  C.c_int),
         "fs_emb_backward_adagrad": ([P, P, i64, i32, C.c_int, C.c_int, P, P, i64, P, P, C.c_int, f32, f32, P, P, sz,
@@ -432,6 +433,22 @@ def fs_emb_gather(table, ids, out=None, mask=None, sel=1, err=None, T=None):
     return out, err
 
 
+def fs_emb_gather_shard_major(table, sm_ids, pos, out=None, err=None, T=None):
+    """out[pos[j]] = table[sm_ids[j]]: the gather from the bucketize output (the same bytes as fs_emb_gather)."""
+    dev = table.device
+    _need(sm_ids, torch.int64, "sm_ids")
+    _need(pos, torch.int32, "pos")
+    R, D = _table_shape(table)
+    T = sm_ids.numel() if T is None else int(T)
+    out = torch.empty(T, D, dtype=table.dtype, device=dev) if out is None else out
+    if out.dtype != table.dtype or not out.is_contiguous() or out.numel() < T * D:
+        raise FsError(1, "out must be contiguous [>= T, D] with the table dtype")
+    err = new_err(dev) if err is None else err
+    _ok(lib().fs_emb_gather_shard_major(_ptr(table), R, D, dtype_code(table), _ptr(sm_ids), _ptr(pos), T, _ptr(out),
+                                        _ptr(err), _stream(dev)), "fs_emb_gather_shard_major")
+    return out, err
+
+
 def backward_workspace_size(T, num_rows, dim, dtype):
     return int(lib().fs_emb_backward_adagrad_workspace_size(int(T), int(num_rows), int(dim), int(dtype)))
 
@@ -495,10 +512,11 @@ def sort_rows_sharded_workspace_size(T, num_rows, dim, dtype, n):
     return int(lib().fs_emb_sort_rows_sharded_workspace_size(int(T), int(num_rows), int(dim), int(dtype), int(n)))
 
 
-def fs_emb_sort_rows_sharded(table, sm_ids, pos, shard_offsets, ws, phase=PHASE_ALL, is_co=None, err=None, T=None):
+def fs_emb_sort_rows_sharded(table, sm_ids, pos, shard_offsets, ws, phase=PHASE_ALL, is_co=None, co_rows=None,
+                             err=None, T=None):
     """The update's sort from the bucketize output (entries grouped by shard): the same sorted entries as
-    fs_emb_sort_rows, in ws.  is_co: the collision flag of each shard-major entry.  `table` only gives
-    num_rows, dim and dtype (it is not read)."""
+    fs_emb_sort_rows, in ws.  is_co: the collision flag of each shard-major entry; co_rows: the collision
+    rows as an int32 bitmap (one of the two for two phases).  `table` only gives num_rows, dim and dtype."""
     dev = sm_ids.device
     _need(sm_ids, torch.int64, "sm_ids")
     _need(pos, torch.int32, "pos")
@@ -508,9 +526,12 @@ def fs_emb_sort_rows_sharded(table, sm_ids, pos, shard_offsets, ws, phase=PHASE_
     n = shard_offsets.numel() - 1
     if is_co is not None:
         _need(is_co, torch.uint8, "is_co")
+    if co_rows is not None:
+        _need(co_rows, torch.int32, "co_rows", (R + 31) // 32)
     err = new_err(dev) if err is None else err
     _ok(lib().fs_emb_sort_rows_sharded(R, D, dtype_code(table), _ptr(sm_ids), _ptr(pos), T, _ptr(shard_offsets), n,
-                                       _ptr(is_co), int(phase), _ptr(err), _ptr(ws), ws.numel(), _stream(dev)),
+                                       _ptr(is_co), _ptr(co_rows), int(phase), _ptr(err), _ptr(ws), ws.numel(),
+                                       _stream(dev)),
         "fs_emb_sort_rows_sharded")
     return err
 

@@ -79,6 +79,7 @@ struct SrcRows {
     r.m = (!kRowBits && phase != FS_PHASE_ALL) ? uint32_t(__ldcs(is_co + i)) : 0u;
     return r;
   }
+  template <bool>
   __device__ __forceinline__ void fetch2(Raw& r) const {
     if constexpr (kRowBits) {
       const uint64_t x = uint64_t(r.id) < uint64_t(R) ? uint64_t(r.id) : 0u;
@@ -110,22 +111,40 @@ struct SrcRows {
   }
 };
 
+#ifndef FS_SHARD_SORT_MINB
+#define FS_SHARD_SORT_MINB 3
+#endif
+#ifndef FS_SHARD_SORT2_MINB
+#define FS_SHARD_SORT2_MINB 4
+#endif
+
 // Sources of the per-shard sort (fs_emb_sort_rows_sharded).  Pass 1 reads the
 // shard-major IDs, their batch-major positions and collision flags; the key is
 // the same (phase bit | row) as SrcRows's and the value the position; the
 // digit is the low `bits` bits of the row's offset inside its shard (the
 // tile's segment).  An ID outside [0, R), outside the tile's shard, or with a
-// flag above 1 is dropped (the first two set the error word).
+// flag above 1 is dropped (the first two set the error word).  The flag comes
+// from a per-entry mask (kRowBits false) or from the row bitmap of the
+// collision rows (kRowBits true: one bitmap word per entry, read after the
+// IDs are in; in shard-major order a tile's words lie in its shard's stretch
+// of the bitmap).  The digit does not depend on the flag; a bitmap flag is
+// always 0 or 1, so the upsweep skips the bitmap (a mask byte above 1 drops
+// the entry, so the upsweep reads the mask).
+template <bool kRowBits>
 struct SrcShardRows {
   using Key = uint32_t;
   static constexpr bool kIndexValue = false;
-  static constexpr bool kFetch2 = false;
+  static constexpr bool kFetch2 = kRowBits;
+  // three loads per item in flight (ID, position, flag): the downsweep keeps
+  // them without spilling on the register budget of 3 blocks per SM
+  static constexpr int kMinBlocks = FS_SHARD_SORT_MINB;
   const int64_t* sm_ids;
   const int32_t* pos;
-  const uint8_t* is_co;  // per shard-major entry; null: one phase
+  const uint8_t* is_co;     // per shard-major entry (kRowBits false); null: one phase
+  const uint32_t* co_rows;  // collision rows (kRowBits true)
   int64_t R;
-  int64_t block;         // rows per shard
-  int kb;                // bits of the largest row index
+  int64_t block;            // rows per shard
+  int kb;                   // bits of the largest row index
   uint32_t row_mask;
   struct Raw {
     int64_t id;
@@ -137,8 +156,18 @@ struct SrcShardRows {
     Raw r;
     r.id = __ldcs(sm_ids + i);
     r.p = kVal ? uint32_t(__ldcs(pos + i)) : 0u;
-    r.m = is_co ? uint32_t(__ldcs(is_co + i)) : 0u;
+    // (the upsweep needs the mask too: a flag above 1 drops the entry there as well)
+    r.m = (!kRowBits && is_co) ? uint32_t(__ldcs(is_co + i)) : 0u;
     return r;
+  }
+  template <bool kVal>
+  __device__ __forceinline__ void fetch2(Raw& r) const {
+    if constexpr (kRowBits) {
+      if (kVal) {
+        const uint64_t x = uint64_t(r.id) < uint64_t(R) ? uint64_t(r.id) : 0u;
+        r.m = (__ldg(co_rows + (x >> 5)) >> (x & 31u)) & 1u;
+      }
+    }
   }
   __device__ __forceinline__ bool make(const Raw& r, int64_t, int seg, Key& key, uint32_t& val, int32_t* err) const {
     if (r.m > 1) return false;
@@ -151,7 +180,7 @@ struct SrcShardRows {
       if (err) set_err(err, FS_ERR_BAD_OFFSETS);
       return false;
     }
-    key = uint32_t(r.id) | (is_co ? (uint32_t(1 - r.m) << kb) : 0u);
+    key = uint32_t(r.id) | ((kRowBits || is_co) ? (uint32_t(1 - r.m) << kb) : 0u);
     val = r.p;
     return true;
   }
@@ -168,6 +197,7 @@ struct SrcShardRows2 {
   using Key = uint32_t;
   static constexpr bool kIndexValue = false;
   static constexpr bool kFetch2 = false;
+  static constexpr int kMinBlocks = FS_SHARD_SORT2_MINB;
   const uint32_t* k;
   const uint32_t* v;
   int64_t block;
@@ -1166,8 +1196,8 @@ extern "C" size_t fs_emb_sort_rows_sharded_workspace_size(int64_t T, int64_t num
 
 extern "C" fs_status fs_emb_sort_rows_sharded(int64_t num_rows, int32_t dim, fs_dtype dtype, const int64_t* sm_ids,
                                               const int32_t* pos, int64_t T, const int64_t* shard_offsets, int32_t n,
-                                              const uint8_t* is_co, fs_phase phase, int32_t* err, void* ws,
-                                              size_t ws_bytes, fs_stream_t stream) {
+                                              const uint8_t* is_co, const uint32_t* co_rows, fs_phase phase,
+                                              int32_t* err, void* ws, size_t ws_bytes, fs_stream_t stream) {
   FS_NVTX_RANGE();
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   fs_status s = check_sorted(T, num_rows, dim, dtype, phase, err, ws, ws_bytes);
@@ -1176,8 +1206,10 @@ extern "C" fs_status fs_emb_sort_rows_sharded(int64_t num_rows, int32_t dim, fs_
   const ShardSortPlan P = shard_sort_plan(num_rows, n, phase);
   if (!P.ok) return FS_ERR_INVALID_ARG;
   if (T == 0) return FS_OK;
-  if (!sm_ids || !pos || (phase == FS_PHASE_COLLISION_THEN_EXCLUSIVE && !is_co)) return FS_ERR_INVALID_ARG;
-  if (!aligned(sm_ids, 8) || !aligned(pos, 4) || !aligned(shard_offsets, 8)) return FS_ERR_ALIGNMENT;
+  const bool two = phase == FS_PHASE_COLLISION_THEN_EXCLUSIVE;
+  if (!sm_ids || !pos || (two && (is_co == nullptr) == (co_rows == nullptr))) return FS_ERR_INVALID_ARG;
+  if (!aligned(sm_ids, 8) || !aligned(pos, 4) || !aligned(shard_offsets, 8) || (co_rows && !aligned(co_rows, 4)))
+    return FS_ERR_ALIGNMENT;
   if (ws_bytes < fs_emb_sort_rows_sharded_workspace_size(T, num_rows, dim, dtype, n)) return FS_ERR_WORKSPACE;
   BwdWs B;
   if (!carve_bwd(T, num_rows, dim, phase, ws, ws_bytes, B)) return FS_ERR_WORKSPACE;
@@ -1190,11 +1222,17 @@ extern "C" fs_status fs_emb_sort_rows_sharded(int64_t num_rows, int32_t dim, fs_
   // pass 2 writes where fs_emb_gather_sorted / fs_emb_update_sorted look; pass 1 into the other buffers
   uint32_t* k1 = (B.sk == B.W.k[0]) ? B.W.k[1] : B.W.k[0];
   uint32_t* v1 = (B.sv == B.W.v[0]) ? B.W.v[1] : B.W.v[0];
-  const bool two = phase == FS_PHASE_COLLISION_THEN_EXCLUSIVE;
   int launches = 1;
   radix::seg_tiles_kernel<<<1, radix::kSegThreads, 0, st>>>(shard_offsets, n, T, W.seg_off[0], W.tile_base[0], err);
-  const SrcShardRows s1{sm_ids, pos, two ? is_co : nullptr, num_rows, P.block, B.kb, B.row_mask};
-  radix::run_seg_pass(s1, radix::DstU32{k1, v1}, 0, P.b1, P.b1, W, 0, B.W.pass.n_valid, nullptr, err, st, &launches);
+  if (two && co_rows) {
+    const SrcShardRows<true> s1{sm_ids, pos, nullptr, co_rows, num_rows, P.block, B.kb, B.row_mask};
+    radix::run_seg_pass(s1, radix::DstU32{k1, v1}, 0, P.b1, P.b1, W, 0, B.W.pass.n_valid, nullptr, err, st,
+                        &launches);
+  } else {
+    const SrcShardRows<false> s1{sm_ids, pos, two ? is_co : nullptr, nullptr, num_rows, P.block, B.kb, B.row_mask};
+    radix::run_seg_pass(s1, radix::DstU32{k1, v1}, 0, P.b1, P.b1, W, 0, B.W.pass.n_valid, nullptr, err, st,
+                        &launches);
+  }
   const SrcShardRows2 s2{k1, v1, P.block, B.kb, B.row_mask, P.lb2, two};
   radix::run_seg_pass(s2, radix::DstU32{B.sk, B.sv}, P.b1, P.lb2 + P.ph, P.lb2, W, 1, B.W.pass.n_valid,
                       two ? B.n_first : nullptr, nullptr, st, &launches);

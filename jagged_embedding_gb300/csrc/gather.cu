@@ -106,6 +106,81 @@ __global__ void __launch_bounds__(kThreads) gather_word_kernel(const uint32_t* _
   }
 }
 
+// Gather in shard-major order (the lookup of Algorithm 2 line 12 as each shard
+// owner makes it, followed by the ranged combine back to batch-major):
+// out[pos[j]] = table[sm_ids[j]] for every shard-major entry j.  Entries of
+// one shard come together, so the rows a stretch of entries reads lie in one
+// shard's row range; while it is being gathered, a shard's repeated rows are
+// served by L2 rather than read again from DRAM.  Rows of 16 * VPR bytes, VPR
+// in {4, 8, 16, 32}: lanes [k*VPR, (k+1)*VPR) move row k, U rows in flight
+// per lane; whole rows are written to their scattered positions.  An ID out of
+// range sets FS_ERR_ID_RANGE, a position out of [0, T) FS_ERR_BAD_OFFSETS;
+// either entry is skipped.
+template <int VPR>
+__global__ void __launch_bounds__(kThreads) gather_scatter_kernel(const int4* __restrict__ table, int64_t R,
+                                                                  const int64_t* __restrict__ sm_ids,
+                                                                  const int32_t* __restrict__ pos, int64_t T,
+                                                                  int4* __restrict__ out, int32_t* err) {
+  constexpr int RPI = 32 / VPR;
+  constexpr int U = (32 / RPI) < kUnroll ? (32 / RPI) : kUnroll;
+  constexpr int RPW = RPI * U;
+  static_assert(RPW <= 32, "one lane per entry");
+  const int lane = threadIdx.x & 31;
+  const int sub = lane / VPR, c = lane % VPR;
+  const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t e0 = ((int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5) * RPW; e0 < T; e0 += nwarps * RPW) {
+    int64_t my_id = -1;
+    int32_t my_pos = -1;
+    if (lane < RPW && e0 + lane < T) {
+      my_id = __ldcs(sm_ids + e0 + lane);
+      my_pos = __ldcs(pos + e0 + lane);
+      if (my_id < 0 || my_id >= R) {
+        set_err(err, FS_ERR_ID_RANGE);
+        my_id = -1;
+      } else if (my_pos < 0 || int64_t(my_pos) >= T) {
+        set_err(err, FS_ERR_BAD_OFFSETS);
+        my_id = -1;
+      }
+    }
+    int4 v[U];
+    int64_t id[U];
+    int32_t p[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      id[u] = __shfl_sync(0xffffffffu, my_id, u * RPI + sub);
+      p[u] = __shfl_sync(0xffffffffu, my_pos, u * RPI + sub);
+      if (id[u] >= 0) v[u] = __ldg(table + id[u] * VPR + c);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (id[u] >= 0) __stcs(out + int64_t(p[u]) * VPR + c, v[u]);
+  }
+}
+
+// Other row sizes, 4-byte words: thread per word of an entry's row.
+__global__ void __launch_bounds__(kThreads) gather_scatter_word_kernel(const uint32_t* __restrict__ table, int64_t R,
+                                                                       int wpr, const int64_t* __restrict__ sm_ids,
+                                                                       const int32_t* __restrict__ pos, int64_t T,
+                                                                       uint32_t* __restrict__ out, int32_t* err) {
+  const int64_t total = T * wpr;
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  for (int64_t f = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; f < total; f += stride) {
+    const int64_t j = f / wpr;
+    const int c = int(f - j * wpr);
+    const int64_t id = __ldg(sm_ids + j);
+    const int32_t p = __ldg(pos + j);
+    if (id < 0 || id >= R) {
+      set_err(err, FS_ERR_ID_RANGE);
+      continue;
+    }
+    if (p < 0 || int64_t(p) >= T) {
+      set_err(err, FS_ERR_BAD_OFFSETS);
+      continue;
+    }
+    __stcs(out + int64_t(p) * wpr + c, __ldg(table + id * wpr + c));
+  }
+}
+
 // Unmasked gather through the copy engine: each warp moves stages of BR
 // consecutive output rows (BR * row bytes <= 2 KB).  The table rows of a stage
 // arrive in a shared-memory slot by one bulk copy per row (completion counted
@@ -249,6 +324,40 @@ extern "C" fs_status fs_emb_gather(const void* table, int64_t num_rows, int32_t 
     if (grid > int64_t(sms) * 8) grid = int64_t(sms) * 8;
     gather_word_kernel<<<unsigned(grid < 1 ? 1 : grid), kThreads, 0, st>>>(
         static_cast<const uint32_t*>(table), num_rows, wpr, ids, T, mask, sel, static_cast<uint32_t*>(out), err);
+  }
+  count_launch(1);
+  return launch_status();
+}
+
+extern "C" fs_status fs_emb_gather_shard_major(const void* table, int64_t num_rows, int32_t dim, fs_dtype dtype,
+                                               const int64_t* sm_ids, const int32_t* pos, int64_t T, void* out,
+                                               int32_t* err, fs_stream_t stream) {
+  FS_NVTX_RANGE();
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (T < 0 || T > INT32_MAX || num_rows < 0 || dim < 1 || (dtype != FS_F32 && dtype != FS_BF16) || !err)
+    return FS_ERR_INVALID_ARG;
+  if (T == 0) return FS_OK;
+  if (!table || !sm_ids || !pos || !out) return FS_ERR_INVALID_ARG;
+  const int64_t row_bytes = int64_t(dim) * (dtype == FS_F32 ? 4 : 2);
+  if (row_bytes % 4 != 0) return FS_ERR_INVALID_ARG;
+  if (!aligned(sm_ids, 8) || !aligned(pos, 4) || !aligned(table, 4) || !aligned(out, 4)) return FS_ERR_ALIGNMENT;
+  const int sms = sm_count();
+  const unsigned grid = unsigned(sms) * (2048 / kThreads);
+  const int vpr = (row_bytes % 16 == 0 && aligned(table, 16) && aligned(out, 16)) ? int(row_bytes / 16) : 0;
+  const int4* tb = static_cast<const int4*>(table);
+  int4* ob = static_cast<int4*>(out);
+  switch (vpr) {
+    case 4: gather_scatter_kernel<4><<<grid, kThreads, 0, st>>>(tb, num_rows, sm_ids, pos, T, ob, err); break;
+    case 8: gather_scatter_kernel<8><<<grid, kThreads, 0, st>>>(tb, num_rows, sm_ids, pos, T, ob, err); break;
+    case 16: gather_scatter_kernel<16><<<grid, kThreads, 0, st>>>(tb, num_rows, sm_ids, pos, T, ob, err); break;
+    case 32: gather_scatter_kernel<32><<<grid, kThreads, 0, st>>>(tb, num_rows, sm_ids, pos, T, ob, err); break;
+    default: {
+      const int wpr = int(row_bytes / 4);
+      int64_t g = (T * wpr + kThreads - 1) / kThreads;
+      if (g > int64_t(sms) * 8) g = int64_t(sms) * 8;
+      gather_scatter_word_kernel<<<unsigned(g < 1 ? 1 : g), kThreads, 0, st>>>(
+          static_cast<const uint32_t*>(table), num_rows, wpr, sm_ids, pos, T, static_cast<uint32_t*>(out), err);
+    }
   }
   count_launch(1);
   return launch_status();

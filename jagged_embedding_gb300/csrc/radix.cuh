@@ -23,7 +23,7 @@
 // length array with the index as value, an ID array filtered by a mask ...)
 // and the digit function: fetch<kVal>(i) only loads (so that a tile's loads
 // are all in flight together; the upsweep passes kVal = false and needs no
-// value), fetch2(raw) (kFetch2) the loads that depend on the first ones,
+// value), fetch2<kVal>(raw) (kFetch2) the loads that depend on the first ones,
 // make(raw, i, seg, key, val, err) checks and converts, digit(key, shift,
 // bits, seg) gives the digit (seg: the tile's segment under a segment-aligned
 // tiling, 0 otherwise).
@@ -147,7 +147,7 @@ __global__ void __launch_bounds__(kThreads) upsweep_kernel(Src src, Tiles tiles,
       if constexpr (Src::kFetch2) {  // loads that depend on the first ones, all issued together
 #pragma unroll
         for (int i = 0; i < kItems; ++i)
-          if (local_index(warp, i, lane) < sp.count) src.fetch2(raw[i]);
+          if (local_index(warp, i, lane) < sp.count) src.template fetch2<false>(raw[i]);
       }
 #pragma unroll
       for (int i = 0; i < kItems; ++i) {
@@ -248,8 +248,20 @@ constexpr size_t downsweep_smem_bytes() {
   return un + 2 * kMaxBins * sizeof(uint32_t) + 64 * sizeof(uint32_t);
 }
 
+// Resident blocks per SM the downsweep is compiled for (its register budget:
+// 64 registers a thread at 4, 85 at 3): a source may set kMinBlocks; the
+// default 4 fits the 40 KB of shared memory of 32-bit keys.
+template <class Src, class = void>
+struct DownBlocks {
+  static constexpr int value = 4;
+};
+template <class Src>
+struct DownBlocks<Src, decltype(void(Src::kMinBlocks))> {
+  static constexpr int value = Src::kMinBlocks;
+};
+
 template <class Src, class Dst, class Tiles>
-__global__ void __launch_bounds__(kThreads, 4) downsweep_kernel(Src src, Dst dst, Tiles tiles, int shift, int bits,
+__global__ void __launch_bounds__(kThreads, DownBlocks<Src>::value) downsweep_kernel(Src src, Dst dst, Tiles tiles, int shift, int bits,
                                                                 int nb, const uint32_t* counts,
                                                                 const uint32_t* chunk_base) {
   using KeyT = typename Src::Key;
@@ -297,7 +309,7 @@ __global__ void __launch_bounds__(kThreads, 4) downsweep_kernel(Src src, Dst dst
     if constexpr (Src::kFetch2) {
 #pragma unroll
       for (int i = 0; i < kItems; ++i)
-        if (local_index(warp, i, lane) < sp.count) src.fetch2(raw[i]);
+        if (local_index(warp, i, lane) < sp.count) src.template fetch2<true>(raw[i]);
     }
 #pragma unroll
     for (int i = 0; i < kItems; ++i) {

@@ -15,6 +15,9 @@ namespace shard {
 struct SrcShard {
   using Key = int64_t;
   static constexpr bool kIndexValue = true;  // value = item index
+  // 56 KB of shared memory (int64 keys) leave room for 3 blocks per SM anyway:
+  // the downsweep takes their register budget and spills nothing
+  static constexpr int kMinBlocks = 3;
   static constexpr bool kFetch2 = false;
   const int64_t* ids;
   int64_t R;

@@ -164,24 +164,32 @@ class Pipeline:
         if want_next_mask:
             self.mask_layout[slot_next] = layout
 
-    def gather(self, slot, out_idx=0, mask=None, sel=1, sorted_phase=None):
+    def gather(self, slot, out_idx=0, mask=None, sel=1, sorted_phase=None, shard_major=False):
         """Lookup of the batch in `slot` (Algorithm 2 lines 12, 15); with sorted_phase, from the entries
-        sort_rows left in the workspace (each distinct row read once)."""
+        sort_rows left in the workspace (each distinct row read once); with shard_major, from the
+        bucketize output (each shard's rows looked up together, then put at their batch-major positions)."""
         s = self.slots[slot]
         if sorted_phase is not None:
             B.fs_emb_gather_sorted(self.table, s.T, self.ws, out=self.out[out_idx], phase=sorted_phase, err=self.err)
+        elif shard_major:
+            assert mask is None
+            B.fs_emb_gather_shard_major(self.table, s.sm_ids, s.pos, out=self.out[out_idx], err=self.err, T=s.T)
         else:
             B.fs_emb_gather(self.table, s.ids, out=self.out[out_idx], mask=mask, sel=sel, err=self.err, T=s.T)
 
-    def sort_rows(self, slot, phase):
-        """The update's sort of the batch in `slot`, ahead of its gather (collision flags from its mask):
-        per shard from the shard-major IDs when the shards allow it, else over the batch-major IDs."""
+    def sort_rows(self, slot, phase, co_rows=None):
+        """The update's sort of the batch in `slot`, ahead of its gather: per shard from the shard-major
+        IDs when the shards allow it (collision flags from co_rows, the next batch's row bitmap, when
+        given, else from the batch's shard-major mask), else over the batch-major IDs (flags from the
+        batch-major mask)."""
         s = self.slots[slot]
         two = phase != B.PHASE_ALL
         if self._sharded_ok(phase):
-            assert not two or self.mask_layout[slot] == "shard"
+            if two and co_rows is None:
+                assert self.mask_layout[slot] == "shard"
             B.fs_emb_sort_rows_sharded(self.table, s.sm_ids, s.pos, s.shard_offsets, self.ws, phase=phase,
-                                       is_co=self.masks[slot] if two else None, err=self.err, T=s.T)
+                                       is_co=self.masks[slot] if two and co_rows is None else None,
+                                       co_rows=co_rows if two else None, err=self.err, T=s.T)
         else:
             assert not two or self.mask_layout[slot] == "batch"
             B.fs_emb_sort_rows(self.table, s.ids, self.ws, phase=phase, is_co=self.masks[slot] if two else None,
@@ -216,11 +224,13 @@ class Pipeline:
     def step_sync(self, cur, nxt_batch, grads, has_next=True, want_masks=False, times=None):
         """One iteration in the synchronous order; slot `cur` holds iteration t already prepared.
 
-        The update takes its collision flags from the mask of t (one pass over the
-        IDs; reading t+1's row bitmap inside the sort passes instead was measured
-        slower), computed in shard-major order when the update sorts per shard
-        (or has nothing to sort): self.mask_layout says which.  want_masks also
-        writes the mask of t+1.  With AutoTune on,
+        The update's collision flags: the per-shard sort looks each entry's row up
+        in t+1's row bitmap (its entries come shard-major, so the lookups of a
+        tile stay in one shard's stretch of the bitmap); the batch-major sort and
+        the one-call update read the mask of t instead (in batch-major order a
+        bitmap lookup per entry was measured slower than the mask pass).
+        want_masks also writes the masks of t and t+1 (shard-major unless the
+        update reads them batch-major: self.mask_layout says which).  With AutoTune on,
         `times` (the ranks' latest step times) is folded into the corrections
         before t+1 is prepared.
         Returns the slot that now holds t+1.
@@ -228,18 +238,21 @@ class Pipeline:
         nxt = 1 - cur
         # one sort, collision rows updated first, then exclusive rows
         phase = B.PHASE_COLLISION_THEN_EXCLUSIVE if has_next else B.PHASE_ALL
-        # masks in shard-major order unless the update reads them batch-major
-        shard_major = not self.w.has_update or (self._sorted_ok(phase) and self._sharded_ok(phase))
+        sharded = self.w.has_update and self._sorted_ok(phase) and self._sharded_ok(phase)
+        # the per-shard sort reads the collision rows from t+1's row bitmap; only the other updates read
+        # the mask of t (batch-major).  Masks asked for (want_masks) are shard-major unless those read them.
+        batch_major_update = self.w.has_update and not sharded
         if has_next:
             if times is not None and self.w.autotune:
                 self.autotune(times)
             self.prepare(nxt_batch, nxt)
-            self.collision(cur, nxt, want_t_mask=True, want_next_mask=want_masks, shard_major=shard_major)
+            self.collision(cur, nxt, want_t_mask=want_masks or batch_major_update, want_next_mask=want_masks,
+                           shard_major=not batch_major_update)
         if not self.w.has_update:
-            self.gather(cur)
+            self.gather(cur, shard_major=True)
             return nxt
         if self._sorted_ok(phase):
-            self.sort_rows(cur, phase)
+            self.sort_rows(cur, phase, co_rows=self.slots[nxt].bitmap if (sharded and has_next) else None)
             self.gather(cur, sorted_phase=phase)
             self.update_sorted(cur, grads, phase)
         else:

@@ -138,13 +138,21 @@ def test_host_argument_errors_return_without_launching():
     # per-shard update sort: n <= 1024, the phase bit beside shards of at most 2^19 rows, the flags for two phases
     big_s = L.fs_emb_sort_rows_sharded_workspace_size(100, 1000, 64, 0, 8)
     assert big_s > L.fs_emb_backward_adagrad_workspace_size(100, 1000, 64, 0)
-    sh = [1000, 64, 0, C.c_void_p(0x200), C.c_void_p(0x300), 100, C.c_void_p(0x400), 8, C.c_void_p(0x500), 3, err,
-          ws, big_s, NULL]
+    sh = [1000, 64, 0, C.c_void_p(0x200), C.c_void_p(0x300), 100, C.c_void_p(0x400), 8, C.c_void_p(0x500), NULL, 3,
+          err, ws, big_s, NULL]
     assert L.fs_emb_sort_rows_sharded(*(sh[:7] + [1025] + sh[8:])) == 1
-    assert L.fs_emb_sort_rows_sharded(*([(1 << 19) + 1] + sh[1:7] + [1] + sh[8:12] + [1 << 40] + sh[13:])) == 1
-    assert L.fs_emb_sort_rows_sharded(*(sh[:8] + [NULL] + sh[9:])) == 1
+    assert L.fs_emb_sort_rows_sharded(*([(1 << 19) + 1] + sh[1:7] + [1] + sh[8:13] + [1 << 40] + sh[14:])) == 1
+    assert L.fs_emb_sort_rows_sharded(*(sh[:8] + [NULL] + sh[9:])) == 1                 # no flags
+    assert L.fs_emb_sort_rows_sharded(*(sh[:9] + [C.c_void_p(0x600)] + sh[10:])) == 1   # both flag forms
+    assert L.fs_emb_sort_rows_sharded(*(sh[:8] + [NULL, C.c_void_p(0x602)] + sh[10:])) == 8
     assert L.fs_emb_sort_rows_sharded(*(sh[:4] + [C.c_void_p(0x302)] + sh[5:])) == 8
-    assert L.fs_emb_sort_rows_sharded(*(sh[:12] + [big_s - 256] + sh[13:])) == 5
+    assert L.fs_emb_sort_rows_sharded(*(sh[:13] + [big_s - 256] + sh[14:])) == 5
+    # shard-major gather: positions 4-byte aligned, IDs 8-byte aligned, a known dtype
+    gs = [C.c_void_p(0x100), 10, 64, 0, C.c_void_p(0x200), C.c_void_p(0x300), 5, C.c_void_p(0x400), err, NULL]
+    assert L.fs_emb_gather_shard_major(*(gs[:4] + [C.c_void_p(0x204)] + gs[5:])) == 8
+    assert L.fs_emb_gather_shard_major(*(gs[:5] + [C.c_void_p(0x302)] + gs[6:])) == 8
+    assert L.fs_emb_gather_shard_major(*(gs[:3] + [9] + gs[4:])) == 1
+    assert L.fs_emb_gather_shard_major(*(gs[:5] + [NULL] + gs[6:])) == 1
     assert L.fs_collision_split(C.c_void_p(0x10), 5, C.c_void_p(0x20), 5, (1 << 32) + 1, 4, NULL, NULL, NULL, 0,
                                 C.c_void_p(0x30), C.c_void_p(0x40), C.c_void_p(0x50), C.c_void_p(0x60),
                                 C.c_void_p(0x70), C.c_void_p(0x80), err, ws, 1 << 30, NULL) == 1

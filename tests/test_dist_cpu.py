@@ -63,6 +63,9 @@ def test_algorithmic_bytes_model():
     g = synthetic.WORKLOADS["vbs-gather"]
     b = bench.algorithmic_bytes(g, g.S, 2.0e6, 2.0e5, g.R)
     assert "backward" not in b
+    # the collision masks (a byte written and read per position) count only where they are written
+    bm = bench.algorithmic_bytes(w, w.S, 3.0e8, 3.7e7, w.R, masks=True)
+    assert bm["collision"] - bench.algorithmic_bytes(w, w.S, 3.0e8, 3.7e7, w.R)["collision"] == 2 * 3.0e8
 
 
 def test_algorithmic_bytes_autotune_and_config():

@@ -131,8 +131,9 @@ def test_full_size_matches_oracle(name):
         tab_before = to_np(table[need_d])
         st_before = to_np(state[need_d]) if state is not None else None
 
+        # (want_masks: the masks are written for the check below; the step's calls are the benchmark's)
         nxt = pipe.step_sync(cur, batches[t + 1] if has_next else None, grads[:T] if grads is not None else None,
-                             has_next=has_next)
+                             has_next=has_next, want_masks=True)
         B.check(pipe.err, f"{name} iteration {t}")
 
         # gathered rows: bit for bit

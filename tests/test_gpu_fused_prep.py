@@ -1,4 +1,5 @@
-"""Fused jagged permute + row-wise bucketize (fs_permute_bucketize) (GPU).
+"""Fused jagged permute + row-wise bucketize (fs_permute_bucketize), and the gather
+from its output in shard-major order (fs_emb_gather_shard_major) (GPU).
 
 Its outputs must equal, bit for bit, the oracle's permute followed by its
 bucketize (FreeScale Algorithm 1 Stage III and §4.2; Algorithm 2 line 8) and
@@ -100,3 +101,49 @@ def test_fused_prep_reports_bad_ids_and_capacity():
     off2, ids2 = oracle.permute_jagged(off, ids, perm)
     assert np.array_equal(to_np(g[1]), ids2[: T - 5])
     assert to_np(g[6])[-1] == T - 5
+
+
+@pytest.mark.parametrize("dtype,D,n,R", [("bf16", 128, 512, 5_000_000), ("f32", 64, 16, 1_000_000),
+                                         ("f32", 24, 8, 100_000), ("bf16", 256, 1, 50_000)])
+def test_shard_major_gather_equals_oracle_gather(dtype, D, n, R):
+    """out[pos[j]] = table[sm_ids[j]] over the bucketize output: the oracle's gather in position order,
+    bit for bit (FreeScale Algorithm 2 line 12: lookup on the shard-major IDs, ranged combine back)."""
+    L, off, ids = _batch(D + n, 3000, 5.0, 1.2, 2048, R)
+    perm, ro = _perm(L, n, "fbs")
+    d = {k: torch.from_numpy(v).to(DEV) for k, v in dict(off=off, ids=ids, perm=perm, ro=ro).items()}
+    g = B.fs_permute_bucketize(d["off"], d["ids"], d["perm"], d["ro"], R)
+    B.check(g[-1])
+    T = int(off[-1])
+    tdt = torch.float32 if dtype == "f32" else torch.bfloat16
+    W = (torch.randn(R, D, generator=torch.Generator().manual_seed(R)) * 0.01).to(tdt)
+    Wd = W.to(DEV)
+    out, err = B.fs_emb_gather_shard_major(Wd, g[3], g[4], T=T)
+    B.check(err)
+    _, ids2 = oracle.permute_jagged(off, ids, perm)
+    assert np.array_equal(to_np(out), oracle.emb_gather(to_np(W), ids2))
+    ref, err = B.fs_emb_gather(Wd, g[1], T=T)
+    B.check(err)
+    assert torch.equal(out, ref)
+
+
+def test_shard_major_gather_reports_bad_entries():
+    R, D, T = 100, 64, 50
+    W = torch.randn(R, D, device=DEV)
+    sm = torch.arange(T, dtype=torch.int64, device=DEV)
+    pos = torch.arange(T, dtype=torch.int32, device=DEV).flip(0).contiguous()
+    sm[3] = R
+    out = torch.full((T, D), 5.0, device=DEV)
+    _, err = B.fs_emb_gather_shard_major(W, sm, pos, out=out)
+    with pytest.raises(B.FsError) as e:
+        B.check(err)
+    assert e.value.code == 2
+    o = to_np(out)
+    assert (o[T - 1 - 3] == 5.0).all()                          # the bad entry's row is left untouched
+    keep = [j for j in range(T) if j != 3]
+    assert np.array_equal(o[[T - 1 - j for j in keep]], to_np(W)[keep])
+    pos2 = pos.clone()
+    pos2[0] = T
+    _, err = B.fs_emb_gather_shard_major(W, torch.arange(T, dtype=torch.int64, device=DEV), pos2, out=out)
+    with pytest.raises(B.FsError) as e:
+        B.check(err)
+    assert e.value.code == 3

@@ -192,6 +192,15 @@ def test_gathers_write_only_their_outputs(dtype, D):
     oracle.emb_gather(to_np(W), ids.numpy(), mask=mask.numpy(), sel=1, out=exp)
     assert np.array_equal(to_np(out.t), exp)
     out.check("masked gather")
+    # shard-major order: the entries of a bucketize of the same IDs into 8 shards
+    rio = torch.tensor([T * r // 8 for r in range(9)], dtype=i64, device=DEV)
+    sm, pos, _, _, e2 = B.fs_bucketize_rowwise(idd, rio, R)
+    B.check(e2)
+    out = G((T, D), tdt)
+    B.fs_emb_gather_shard_major(Wd, sm, pos, out=out.t, err=e)
+    B.check(e)
+    assert np.array_equal(to_np(out.t), ref)
+    out.check("shard-major gather")
 
 
 @pytest.mark.parametrize("path", ["one-call", "sorted", "sharded"])

@@ -22,11 +22,18 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
+def _bitmap(rows, R):
+    bm = np.zeros((R + 31) // 32, np.uint32)
+    np.bitwise_or.at(bm, rows >> 5, (np.uint32(1) << (rows & 31).astype(np.uint32)))
+    return torch.from_numpy(bm.view(np.int32))
+
+
 def _case(seed, R, D, T, n, dtype, s=1.05):
     g = torch.Generator().manual_seed(seed)
     ids = synthetic.zipf_rows(R, s, T, g, "cpu")
     nxt = synthetic.zipf_rows(R, s, max(T // 2, 1), g, "cpu").numpy()
     is_co = np.isin(ids.numpy(), nxt).astype(np.uint8)
+    _case.next_rows = nxt
     tdt = torch.float32 if dtype == "f32" else torch.bfloat16
     W = (torch.randn(R, D, generator=g) * 0.01).to(tdt)
     G = torch.randn(T, D, generator=g).to(tdt)
@@ -57,13 +64,17 @@ def test_sharded_sort_equals_batch_major_sort(dtype, D, optim, T, R, n, two):
     sm, pos, so = _bucketize(idd, riod, R)
     m_bm = torch.from_numpy(is_co).to(DEV)
     m_sm = m_bm[pos.long()].contiguous()
+    co_rows = _bitmap(_case.next_rows, R).to(DEV)
     ph = B.PHASE_COLLISION_THEN_EXCLUSIVE if two else B.PHASE_ALL
     state = torch.rand(R, generator=torch.Generator().manual_seed(5)) if optim == "adagrad" else None
     res = []
-    for sharded in (False, True):
+    for sharded in ((False, True, "bitmap") if two else (False, True)):
         Wd = W.to(DEV)
         sd = state.to(DEV) if state is not None else None
-        if sharded:
+        if sharded == "bitmap":          # the flags from the next batch's row bitmap
+            ws = B.workspace(B.sort_rows_sharded_workspace_size(T, R, D, B.dtype_code(Wd), n), DEV)
+            err = B.fs_emb_sort_rows_sharded(Wd, sm, pos, so, ws, phase=ph, co_rows=co_rows)
+        elif sharded:
             ws = B.workspace(B.sort_rows_sharded_workspace_size(T, R, D, B.dtype_code(Wd), n), DEV)
             err = B.fs_emb_sort_rows_sharded(Wd, sm, pos, so, ws, phase=ph, is_co=m_sm if two else None)
         else:
@@ -73,7 +84,11 @@ def test_sharded_sort_equals_batch_major_sort(dtype, D, optim, T, R, n, two):
         B.fs_emb_update_sorted(Wd, sd, Gd, T, ws, optim, 0.01, 1e-8, phase=ph, err=err)
         B.check(err)
         res.append((to_np(out), to_np(Wd), to_np(sd) if sd is not None else None))
-    (o0, w0, s0), (o1, w1, s1) = res
+    for o2, w2, s2 in res[2:]:       # the bitmap form: the same bytes as the mask form
+        assert np.array_equal(o2, res[1][0]) and np.array_equal(w2, res[1][1])
+        if s2 is not None:
+            assert np.array_equal(s2, res[1][2])
+    (o0, w0, s0), (o1, w1, s1) = res[:2]
     assert np.array_equal(o1, o0)
     assert np.array_equal(o1, oracle.emb_gather(to_np(W), ids.numpy()))
     assert np.array_equal(w1, w0)

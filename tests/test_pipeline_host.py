@@ -13,18 +13,23 @@ from jagged_embedding_gb300 import binding as B
 from jagged_embedding_gb300 import pipeline as P
 from jagged_embedding_gb300 import synthetic
 
-CALLS = ["fs_balance_fbs", "fs_balance_vbs", "fs_balance_vbs_tuned", "fs_vbs_autotune", "fs_permute_jagged",
+CALLS = ["fs_emb_gather_shard_major", "fs_balance_fbs", "fs_balance_vbs", "fs_balance_vbs_tuned", "fs_vbs_autotune", "fs_permute_jagged",
          "fs_bucketize_rowwise", "fs_permute_bucketize", "fs_row_bitmap", "fs_collision_split_bitmaps", "fs_emb_gather",
          "fs_emb_gather_sorted", "fs_emb_sort_rows", "fs_emb_sort_rows_sharded", "fs_emb_update_sorted",
          "fs_emb_backward_adagrad"]
 
 
+KWARGS = {}   # keyword arguments of the last call of each name
+
+
 @pytest.fixture
 def calls(monkeypatch):
     log = []
+    KWARGS.clear()
     for name in CALLS:
         def rec(*a, _n=name, **kw):
             log.append((_n, kw.get("phase")))
+            KWARGS[_n] = kw
         monkeypatch.setattr(P.B, name, rec)
     return log
 
@@ -58,9 +63,16 @@ def test_sync_step_sorts_before_the_lookup(calls):
     # the update sorts each shard's entries of the bucketize output (shards of 125 rows)
     assert _names(calls) == [("fs_collision_split_bitmaps", None), ("fs_emb_sort_rows_sharded", CT),
                              ("fs_emb_gather_sorted", CT), ("fs_emb_update_sorted", CT)]
-    assert pipe.mask_layout[0] == "shard"           # its collision flags follow the shard-major IDs
+    # its collision flags come from the next batch's row bitmap: no mask pass
+    assert KWARGS["fs_emb_sort_rows_sharded"]["co_rows"] is pipe.slots[1].bitmap
+    assert KWARGS["fs_collision_split_bitmaps"]["want_t_mask"] is False
+    calls.clear()
+    pipe.step_sync(1, _batch(TINY), torch.zeros(1, TINY.D), want_masks=True)   # masks asked for: shard-major
+    assert pipe.mask_layout == ["shard", "shard"]
+    assert KWARGS["fs_collision_split_bitmaps"]["want_t_mask"] is True
     # the batch is prepared (balanced, permuted and bucketized in one call, marked) before the split
     assert [n for n, _ in calls[:3]] == ["fs_balance_fbs", "fs_permute_bucketize", "fs_row_bitmap"]
+    assert KWARGS["fs_row_bitmap"]["T"] == TINY.S
 
 
 def test_sync_step_sorts_batch_major_ids_when_shards_are_too_large(calls):
@@ -70,7 +82,8 @@ def test_sync_step_sorts_batch_major_ids_when_shards_are_too_large(calls):
     CT = B.PHASE_COLLISION_THEN_EXCLUSIVE
     assert _names(calls)[-3:] == [("fs_emb_sort_rows", CT), ("fs_emb_gather_sorted", CT),
                                   ("fs_emb_update_sorted", CT)]
-    assert pipe.mask_layout[0] == "batch"
+    assert pipe.mask_layout[0] == "batch"                  # the batch-major sort reads the mask of t
+    assert KWARGS["fs_collision_split_bitmaps"]["want_t_mask"] is True
     calls.clear()
     pipe.step_sync(0, None, torch.zeros(1, w.D), has_next=False)   # one phase: 20 bits fit
     assert _names(calls)[0] == ("fs_emb_sort_rows_sharded", B.PHASE_ALL)
@@ -96,14 +109,15 @@ def test_position_order_step_when_asked_or_when_the_phase_bit_does_not_fit(calls
     assert _names(calls)[-2:] == [("fs_emb_gather", None), ("fs_emb_backward_adagrad", CT)]
 
 
-def test_gather_only_workload_keeps_the_position_order_gather(calls):
+def test_gather_only_workload_gathers_in_shard_major_order(calls):
     w = synthetic.WORKLOADS["vbs-gather"].scaled(R=1000)
     pipe = _pipe(w)
     pipe.step_sync(0, _batch(w), None)
     names = [n for n, _ in calls]
-    assert "fs_balance_vbs" in names and names[-1] == "fs_emb_gather"
+    # the lookup reads the shard-major IDs (each shard's rows together) and scatters to batch-major positions
+    assert "fs_balance_vbs" in names and names[-1] == "fs_emb_gather_shard_major"
     assert not {"fs_emb_sort_rows", "fs_emb_sort_rows_sharded", "fs_emb_update_sorted", "fs_vbs_autotune"} & set(names)
-    assert pipe.mask_layout[0] == "shard"
+    assert KWARGS["fs_collision_split_bitmaps"]["want_t_mask"] is False       # nothing reads the masks
 
 
 def test_autotune_folds_the_times_in_before_the_next_cut(calls):
