@@ -558,7 +558,7 @@ def run_e2e(w, pipe, batches, grads, K, W, dev, ws, times=None):
             r["cand_lens"] = torch.empty(max(max_C, 1), dtype=torch.int64, device=dev)
     copy_stream = torch.cuda.Stream(dev)
     main = torch.cuda.current_stream(dev)
-    done = [torch.cuda.Event() for _ in range(3)]
+    done = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
     used = [torch.cuda.Event() for _ in range(3)]
     readback = torch.empty(4, dtype=torch.int64).pin_memory()
     host_times = [x.cpu().pin_memory() for x in times] if times else None
@@ -569,6 +569,10 @@ def run_e2e(w, pipe, batches, grads, K, W, dev, ws, times=None):
         slot = ring[i % 3]
         with torch.cuda.stream(copy_stream):
             copy_stream.wait_event(used[i % 3])
+            c0 = None
+            if copy_ev is not None:
+                c0 = torch.cuda.Event(enable_timing=True)
+                c0.record(copy_stream)
             S1 = h["offsets"].numel()
             slot["uih_len"][: S1 - 1].copy_(h["uih_len"], non_blocking=True)
             slot["offsets"][:S1].copy_(h["offsets"], non_blocking=True)
@@ -578,6 +582,8 @@ def run_e2e(w, pipe, batches, grads, K, W, dev, ws, times=None):
                 slot["cand_offsets"][:S1].copy_(h["cand_offsets"], non_blocking=True)
                 slot["cand_lens"][:nc].copy_(h["cand_lens"], non_blocking=True)
             done[i % 3].record(copy_stream)
+            if copy_ev is not None:
+                copy_ev.append((c0, done[i % 3]))
         nbytes = h["uih_len"].numel() * 4 + h["offsets"].numel() * 8 + h["T"] * 8
         b = {"uih_len": slot["uih_len"][: S1 - 1], "offsets": slot["offsets"][:S1],
              "ids": slot["ids"][: h["T"]], "T": h["T"]}
@@ -586,6 +592,8 @@ def run_e2e(w, pipe, batches, grads, K, W, dev, ws, times=None):
             nbytes += S1 * 8 + nc * 8
             b["cand_offsets"], b["cand_lens"] = slot["cand_offsets"][:S1], slot["cand_lens"][:nc]
         return b, nbytes
+
+    copy_ev = None  # (start, end) events of the timed steps' host-to-device copies
 
     def run(steps, measure):
         staged = {}
@@ -619,6 +627,7 @@ def run_e2e(w, pipe, batches, grads, K, W, dev, ws, times=None):
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
+    copy_ev = []
     t0.record(main)
     ids, h2d_bytes = run(K, True)
     t1.record(main)
@@ -626,10 +635,15 @@ def run_e2e(w, pipe, batches, grads, K, W, dev, ws, times=None):
     barrier(ws)
     B.check(pipe.err, "e2e")
     secs = t0.elapsed_time(t1) / 1000.0
+    # each copy's duration is read before its `done` event is recorded again (three-slot ring,
+    # synchronised above): the last three are exact, earlier ones were re-recorded, so keep those
+    copy_ms = [a.elapsed_time(b) for a, b in copy_ev[-3:]]
     ids_all, secs_max = aggregate(ids, secs, ws, dev)
     return {"value": ids_all / secs_max, "unit": "IDs/s", "h2d_bytes_per_step": h2d_bytes / K,
-            "d2h_bytes_per_step": 32, "note": "batch IDs + lengths + offsets from pinned host memory, "
-                                              "copy of batch i+2 overlapped with step i; gradients device-resident"}
+            "d2h_bytes_per_step": 32, "h2d_copy_ms_last": [round(x, 3) for x in copy_ms],
+            "note": "batch IDs + lengths + offsets from pinned host memory, "
+                    "copy of batch i+2 overlapped with step i; gradients device-resident; "
+                    "h2d_copy_ms_last: durations of the last timed copies (a step waits for its batch's copy)"}
 
 
 def main():

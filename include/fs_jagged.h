@@ -214,7 +214,10 @@ fs_status fs_keyed_transpose(const int64_t* offsets, const int64_t* values, int6
  *   splits          [n*n] int64 out: splits[r*n + s] = IDs of source rank r in shard s
  *                         (the AllToAll send splits)
  *   shard_offsets   [n+1] int64 out
- * n in [1, 1024].
+ * n in [1, 1024].  An ID outside [0, num_rows) sets FS_ERR_ID_RANGE; its
+ * entry still takes a place (shard 0 below the range, shard n-1 above it), but
+ * its shard-major copy may be the clamped value (0, or num_rows) rather than
+ * the ID itself.
  * ---------------------------------------------------------------------- */
 size_t fs_bucketize_rowwise_workspace_size(int64_t T, int32_t n);
 fs_status fs_bucketize_rowwise(const int64_t* ids, int64_t T, const int64_t* rank_id_offsets, int32_t n,

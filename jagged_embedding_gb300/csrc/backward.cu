@@ -787,11 +787,34 @@ __global__ void __launch_bounds__(kThreads) fixup_kernel(const uint32_t* __restr
     for (int i = 0; i < EPL; ++i) acc64[i] = double(carry_tail[t * D + lane * EPL + i]);
     int64_t v = t + 1;
     while (v < ntiles) {
-      if (v % kCarryBlock == 0 && v / kCarryBlock < nblocks && block_full[v / kCarryBlock]) {
+      if (v % kCarryBlock == 0 && v / kCarryBlock < nblocks) {
+        // the run of full blocks starting here (one flag per lane, up to 32 blocks at a time),
+        // their sums added in block order with Q loads in flight (a Zipf-hot row's chain
+        // crosses hundreds of blocks: one dependent load per block would set the pace)
+        const int64_t b0 = v / kCarryBlock;
+        const bool f = b0 + lane < nblocks && block_full[b0 + lane];
+        const unsigned fm = __ballot_sync(0xffffffffu, f);
+        const int run = (fm == 0xffffffffu) ? 32 : (__ffs(~fm) - 1);
+        if (run > 0) {
+          constexpr int Q = EPL >= 8 ? 2 : (EPL >= 4 ? 4 : 8);
+          int q = 0;
+          for (; q + Q <= run; q += Q) {
+            double c[Q][EPL];
 #pragma unroll
-        for (int i = 0; i < EPL; ++i) acc64[i] += block_sum[(v / kCarryBlock) * D + lane * EPL + i];
-        v += kCarryBlock;
-        continue;
+            for (int qq = 0; qq < Q; ++qq)
+#pragma unroll
+              for (int i = 0; i < EPL; ++i) c[qq][i] = block_sum[(b0 + q + qq) * D + lane * EPL + i];
+#pragma unroll
+            for (int qq = 0; qq < Q; ++qq)
+#pragma unroll
+              for (int i = 0; i < EPL; ++i) acc64[i] += c[qq][i];
+          }
+          for (; q < run; ++q)
+#pragma unroll
+            for (int i = 0; i < EPL; ++i) acc64[i] += block_sum[(b0 + q) * D + lane * EPL + i];
+          v += int64_t(run) * kCarryBlock;
+          continue;
+        }
       }
       // single tiles up to the end of v's block: stop at the first head
       // that does not continue

@@ -65,6 +65,139 @@ __global__ void fbs_assign_kernel(const uint32_t* sorted_g, int64_t S, int32_t n
     rank_offsets[r] = fbs_rank_offset(r, S, n);
 }
 
+// FBS of up to kFbsSmallMax samples in one block of 1024 threads: the (L, g)
+// keys stay in registers and shared memory, and the stable LSD passes (8-bit
+// digits, as many as the largest length needs: two for lengths below 65536)
+// run inside the block, then the snake deal.  Same sorted order as the
+// device-wide passes (a stable sort by L, ties by g), so the same perm.
+constexpr int kFbsSmallThreads = 1024;
+constexpr int kFbsSmallItems = 16;
+constexpr int kFbsSmallMax = kFbsSmallThreads * kFbsSmallItems;  // 16384
+constexpr int kFbsSmallWarps = kFbsSmallThreads / 32;
+constexpr size_t kFbsSmallSmem = (2 * size_t(kFbsSmallMax) + size_t(kFbsSmallWarps) * 256 + 256 + 64) * sizeof(uint32_t);
+
+__global__ void __launch_bounds__(kFbsSmallThreads, 1) fbs_small_kernel(const int32_t* L, int32_t S, int32_t n,
+                                                                        int32_t* perm, int64_t* rank_offsets,
+                                                                        int32_t* err) {
+  extern __shared__ uint32_t fsm[];
+  uint32_t* keys = fsm;                            // [kFbsSmallMax] one pass's output order
+  uint32_t* vals = keys + kFbsSmallMax;            // [kFbsSmallMax]
+  uint32_t* hist = vals + kFbsSmallMax;            // [kFbsSmallWarps][256]
+  uint32_t* dstart = hist + kFbsSmallWarps * 256;  // [256]
+  uint32_t* red = dstart + 256;                    // [64]
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  auto slot = [&](int i) { return warp * 32 * kFbsSmallItems + i * 32 + lane; };  // slot order = item order
+  uint32_t k[kFbsSmallItems], v[kFbsSmallItems];
+  uint32_t kmax = 0;
+#pragma unroll
+  for (int i = 0; i < kFbsSmallItems; ++i) {
+    const int g = slot(i);
+    int32_t l = g < S ? L[g] : 0;
+    if (l < 0) {
+      set_err(err, FS_ERR_INVALID_ARG);
+      l = 0;
+    }
+    k[i] = uint32_t(l);
+    v[i] = uint32_t(g);
+    kmax = k[i] > kmax ? k[i] : kmax;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const uint32_t x = __shfl_xor_sync(0xffffffffu, kmax, o);
+    kmax = x > kmax ? x : kmax;
+  }
+  if (lane == 0) red[warp] = kmax;
+  __syncthreads();
+  kmax = 0;
+  for (int w = 0; w < kFbsSmallWarps; ++w) kmax = red[w] > kmax ? red[w] : kmax;
+  const int passes = (32 - __clz(kmax) + 7) / 8;  // 0 when every length is 0: the order is g
+  for (int pass = 0; pass < passes; ++pass) {
+    const int shift = 8 * pass;
+    for (int j = threadIdx.x; j < kFbsSmallWarps * 256; j += kFbsSmallThreads) hist[j] = 0u;
+    __syncthreads();
+    // warp multisplit by ballots (8-bit digits), slot by slot
+    // (a warp's rank of an item among its equal digits, < 512, rides in the
+    // top bits of the item's value: g < 2^14)
+    uint32_t* wh = hist + warp * 256;
+#pragma unroll
+    for (int i = 0; i < kFbsSmallItems; ++i) {
+      const bool live = slot(i) < S;
+      const uint32_t d = (k[i] >> shift) & 255u;
+      const unsigned lv = __ballot_sync(0xffffffffu, live);
+      unsigned peers = live ? lv : ~lv;
+#pragma unroll
+      for (int b = 0; b < 8; ++b) {
+        const bool on = (d >> b) & 1u;
+        const unsigned m = __ballot_sync(0xffffffffu, on);
+        peers &= on ? m : ~m;
+      }
+      const unsigned lt = __popc(peers & lanemask_lt());
+      const uint32_t base = live ? wh[d] : 0u;
+      v[i] |= (base + lt) << 16;
+      __syncwarp();
+      if (live && lt == 0) wh[d] = base + __popc(peers);
+      __syncwarp();
+    }
+    __syncthreads();
+    // per digit: exclusive over the warps, then over the digits
+    uint32_t tot = 0;
+    if (threadIdx.x < 256) {
+      const int d = threadIdx.x;
+      for (int w = 0; w < kFbsSmallWarps; ++w) {
+        const uint32_t c = hist[w * 256 + d];
+        hist[w * 256 + d] = tot;
+        tot += c;
+      }
+    }
+    // exclusive scan of the 256 digit totals by the first 8 warps
+    uint32_t x = tot;
+    if (warp < 8) {
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      if (lane == 31) red[32 + warp] = x;
+    }
+    __syncthreads();
+    if (warp < 8) {
+      uint32_t before = 0;
+      for (int w = 0; w < warp; ++w) before += red[32 + w];
+      dstart[threadIdx.x] = before + x - tot;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < kFbsSmallItems; ++i)
+      if (slot(i) < S) {
+        const uint32_t d = (k[i] >> shift) & 255u;
+        const uint32_t at = dstart[d] + hist[warp * 256 + d] + (v[i] >> 16);
+        keys[at] = k[i];
+        vals[at] = v[i] & 0xFFFFu;
+      }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < kFbsSmallItems; ++i) {
+      const int p = slot(i);
+      if (p < S) {
+        k[i] = keys[p];
+        v[i] = vals[p];
+      }
+    }
+    __syncthreads();
+  }
+  // sorted position p = slot(i): the snake deal
+#pragma unroll
+  for (int i = 0; i < kFbsSmallItems; ++i) {
+    const int64_t p = slot(i);
+    if (p < S) {
+      const int64_t rho = p / n, kk = p % n;
+      const int64_t r = (rho & 1) ? (n - 1 - kk) : kk;
+      perm[fbs_rank_offset(r, S, n) + rho] = int32_t(v[i]);
+    }
+  }
+  for (int64_t r = threadIdx.x; r <= n; r += kFbsSmallThreads) rank_offsets[r] = fbs_rank_offset(r, S, n);
+}
+
 // ------------------------------------------------------------------- VBS
 
 // Fixed-point weight round_half_even(256 * L^alpha); L^alpha evaluated with
@@ -399,6 +532,12 @@ extern "C" fs_status fs_balance_fbs(const int32_t* uih_len, int64_t S, int32_t n
   int launches = 0;
   if (S == 0) {
     fill_i64_kernel<<<1, kThreads, 0, st>>>(rank_offsets, int64_t(n) + 1, 0);
+    count_launch(1);
+    return launch_status();
+  }
+  if (S <= kFbsSmallMax) {  // one block: sort and deal in shared memory
+    cudaFuncSetAttribute(fbs_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kFbsSmallSmem));
+    fbs_small_kernel<<<1, kFbsSmallThreads, kFbsSmallSmem, st>>>(uih_len, int32_t(S), n, perm, rank_offsets, err);
     count_launch(1);
     return launch_status();
   }

@@ -49,10 +49,15 @@ extern "C" fs_status fs_bucketize_rowwise(const int64_t* ids, int64_t T, const i
   radix::PassWs P;
   if (!radix::carve_pass_ws(T, n, cur, P)) return FS_ERR_WORKSPACE;
   const int64_t block = (num_rows + n - 1) / n;
-  SrcShard src{ids, num_rows, block, 1.0f / static_cast<float>(block), n};
   int launches = 0;
   if (T > 0) {
-    radix::run_pass(src, DstShardMajor{sm_ids, pos}, 0, 0, n, nullptr, T, P, err, st, &launches);
+    if (num_rows < (int64_t(1) << 32)) {  // rows fit 32 bits: the lighter staging
+      const shard::SrcShard32 src{ids, num_rows, block, 1.0f / static_cast<float>(block), n};
+      radix::run_pass(src, DstShardMajor{sm_ids, pos}, 0, 0, n, nullptr, T, P, err, st, &launches);
+    } else {
+      const SrcShard src{ids, num_rows, block, 1.0f / static_cast<float>(block), n};
+      radix::run_pass(src, DstShardMajor{sm_ids, pos}, 0, 0, n, nullptr, T, P, err, st, &launches);
+    }
   } else {
     if (cudaMemsetAsync(P.digit_base, 0, size_t(n) * sizeof(uint32_t), st) != cudaSuccess) return FS_ERR_CUDA;
   }

@@ -40,12 +40,168 @@ __global__ void __launch_bounds__(kThreads) mark_kernel(const int64_t* ids_t, in
   }
 }
 
+// Row marking through a shared-memory window of the bitmap.  Block b takes
+// the IDs [b * chunk, (b + 1) * chunk) in sub-chunks of kMarkSub; per
+// sub-chunk the block finds the range of rows it touches, and when that range
+// fits the window (kWinWords bitmap words: 409,600 rows) the bits are set in
+// shared memory; the window's dirty words are OR-ed into the global bitmap
+// only when a sub-chunk falls outside it, and at the end.  IDs in shard-major
+// order (grouped by row range) stay inside one window for a whole shard, so
+// the global bitmap sees one OR per dirty word instead of a load (and often
+// an atomic) per ID.  A sub-chunk whose rows span more than the window is
+// marked straight in global memory (load, then atomic where the bit is
+// missing).  The result is the same set of bits either way.
+constexpr int kMarkThreads = 256;
+constexpr int kMarkItems = 8;  // per thread per sub-chunk; the next sub-chunk's 8 are in flight meanwhile
+constexpr int kMarkSub = kMarkThreads * kMarkItems;
+constexpr int kWinWords = 12800;  // 51.2 KB: four blocks per SM
+constexpr size_t kMarkSmem = size_t(kWinWords) * sizeof(uint32_t);
+
+__device__ __forceinline__ void block_min_max(int64_t& lo, int64_t& hi, int64_t* s_lo, int64_t* s_hi) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const int64_t a = __shfl_xor_sync(0xffffffffu, lo, o), b = __shfl_xor_sync(0xffffffffu, hi, o);
+    lo = a < lo ? a : lo;
+    hi = b > hi ? b : hi;
+  }
+  if (lane == 0) {
+    s_lo[warp] = lo;
+    s_hi[warp] = hi;
+  }
+  __syncthreads();
+  lo = s_lo[0];
+  hi = s_hi[0];
+  for (int w = 1; w < nw; ++w) {
+    lo = s_lo[w] < lo ? s_lo[w] : lo;
+    hi = s_hi[w] > hi ? s_hi[w] : hi;
+  }
+  __syncthreads();  // s_lo / s_hi are free again
+}
+
+__global__ void __launch_bounds__(kMarkThreads, 4) mark_window_kernel(const int64_t* __restrict__ ids, int64_t T,
+                                                                     int64_t chunk, int64_t R, uint32_t* bm,
+                                                                     int32_t* err) {
+  extern __shared__ uint32_t win[];  // [kWinWords]
+  __shared__ int64_t s_lo[kMarkThreads / 32], s_hi[kMarkThreads / 32];
+  for (int j = threadIdx.x; j < kWinWords; j += kMarkThreads) win[j] = 0u;
+  __syncthreads();
+  const int64_t c0 = int64_t(blockIdx.x) * chunk;
+  const int64_t c1 = (c0 + chunk < T) ? c0 + chunk : T;
+  // block-uniform window state: base word (-1: no window), dirty words [dlo, dhi] relative to it
+  int64_t base = -1, dlo = kWinWords, dhi = -1;
+  auto flush = [&]() {
+    if (base >= 0)
+      for (int64_t w = dlo + threadIdx.x; w <= dhi; w += kMarkThreads) {
+        const uint32_t v = win[w];
+        if (v) {
+          atomicOr(bm + base + w, v);
+          win[w] = 0u;
+        }
+      }
+    dlo = kWinWords;
+    dhi = -1;
+  };
+  int64_t nx[kMarkItems];  // the next sub-chunk's IDs, loaded while this one is marked
+  auto load = [&](int64_t s0) {
+#pragma unroll
+    for (int i = 0; i < kMarkItems; ++i) {
+      const int64_t j = s0 + int64_t(i) * kMarkThreads + threadIdx.x;
+      nx[i] = j < c1 ? __ldcs(ids + j) : -1;
+    }
+  };
+  if (c0 < c1) load(c0);
+  for (int64_t s0 = c0; s0 < c1; s0 += kMarkSub) {
+    int64_t id[kMarkItems];
+#pragma unroll
+    for (int i = 0; i < kMarkItems; ++i) id[i] = nx[i];
+    if (s0 + kMarkSub < c1) load(s0 + kMarkSub);
+    int64_t lo = INT64_MAX, hi = -1;
+#pragma unroll
+    for (int i = 0; i < kMarkItems; ++i) {
+      const int64_t j = s0 + int64_t(i) * kMarkThreads + threadIdx.x;
+      if (id[i] < 0 || id[i] >= R) {
+        if (j < c1) set_err(err, FS_ERR_ID_RANGE);
+        id[i] = -1;
+        continue;
+      }
+      lo = id[i] < lo ? id[i] : lo;
+      hi = id[i] > hi ? id[i] : hi;
+    }
+    block_min_max(lo, hi, s_lo, s_hi);  // (also orders the previous sub-chunk's window updates before a flush)
+    if (hi < 0) continue;               // no valid ID in this sub-chunk
+    const int64_t lw = lo >> 5, hw = hi >> 5;
+    if (!(base >= 0 && lw >= base && hw < base + kWinWords)) {
+      flush();
+      __syncthreads();
+      // the new window leaves a quarter of its slack below this sub-chunk's rows and the rest
+      // above (IDs grouped by row range move upwards), so later sub-chunks of the same range fit
+      const int64_t slack = kWinWords - 1 - (hw - lw);
+      base = slack >= 0 ? (lw - slack / 4 > 0 ? lw - slack / 4 : 0) : -1;
+    }
+    if (base >= 0) {
+      // test before set: a Zipf-hot row's later IDs find their bit set and skip the atomic
+      // (same-word shared atomics of one warp would serialize)
+      uint32_t cur[kMarkItems];
+#pragma unroll
+      for (int i = 0; i < kMarkItems; ++i) cur[i] = id[i] >= 0 ? win[(id[i] >> 5) - base] : ~0u;
+#pragma unroll
+      for (int i = 0; i < kMarkItems; ++i) {
+        const uint32_t bit = 1u << (uint32_t(id[i]) & 31u);
+        if (id[i] >= 0 && (cur[i] & bit) == 0) atomicOr(win + ((id[i] >> 5) - base), bit);
+      }
+      dlo = (lw - base) < dlo ? (lw - base) : dlo;
+      dhi = (hw - base) > dhi ? (hw - base) : dhi;
+    } else {
+      // rows too spread for the window: every word loaded first, then an atomic where the bit
+      // is missing (a stale word only costs a redundant atomic)
+      uint32_t cur[kMarkItems];
+#pragma unroll
+      for (int i = 0; i < kMarkItems; ++i) cur[i] = id[i] >= 0 ? bm[uint64_t(id[i]) >> 5] : ~0u;
+#pragma unroll
+      for (int i = 0; i < kMarkItems; ++i) {
+        const uint32_t bit = 1u << (uint32_t(id[i]) & 31u);
+        if (id[i] >= 0 && (cur[i] & bit) == 0) atomicOr(bm + (uint64_t(id[i]) >> 5), bit);
+      }
+    }
+  }
+  __syncthreads();
+  flush();
+}
+
+// Blocks of the windowed mark: four per SM, each a contiguous chunk of the IDs.
+void launch_mark_window(const int64_t* ids, int64_t T, int64_t R, uint32_t* bm, int32_t* err, cudaStream_t st) {
+  if (T <= 0) return;
+  int64_t grid = int64_t(sm_count()) * 4;
+  int64_t chunk = (T + grid - 1) / grid;
+  if (chunk < kMarkSub) chunk = kMarkSub;
+  grid = (T + chunk - 1) / chunk;
+  cudaFuncSetAttribute(mark_window_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kMarkSmem));
+  mark_window_kernel<<<unsigned(grid), kMarkThreads, kMarkSmem, st>>>(ids, T, chunk, R, bm, err);
+}
+
 // Three counters packed in one 64-bit word, 21 bits each (a tile holds at most
 // kWordsPerTile * 32 = 65536 rows per counter).
 __device__ __forceinline__ uint64_t pack3(uint32_t a, uint32_t b, uint32_t c) {
   return uint64_t(a) | (uint64_t(b) << 21) | (uint64_t(c) << 42);
 }
 __device__ __forceinline__ uint32_t unpack3(uint64_t v, int k) { return uint32_t((v >> (21 * k)) & 0x1FFFFFu); }
+
+// Position of the r-th (0-based) set bit of w (w has more than r set bits):
+// halves, quarters ... of the word chosen by population counts.
+__device__ __forceinline__ int nth_set_bit(uint32_t w, int r) {
+  int pos = 0;
+#pragma unroll
+  for (int half = 16; half >= 1; half >>= 1) {
+    const int c = __popc(w & ((1u << half) - 1u));
+    if (r >= c) {
+      r -= c;
+      w >>= half;
+      pos += half;
+    }
+  }
+  return pos;
+}
 
 __global__ void __launch_bounds__(kThreads) compact_kernel(const uint32_t* bm_t, const uint32_t* bm_next, int64_t nwords,
                                                            int64_t R, int32_t n, int64_t block, int64_t* co,
@@ -56,10 +212,13 @@ __global__ void __launch_bounds__(kThreads) compact_kernel(const uint32_t* bm_t,
   __shared__ uint64_t tmp[32];
   __shared__ int64_t s_tile;
   __shared__ int64_t s_excl[3];
+  __shared__ uint32_t wpre[kWordsPerTile];   // per word of the tile: the list's set bits in earlier words
+  __shared__ uint32_t wbits[kWordsPerTile];  // per word: the list's bits
   if (threadIdx.x == 0) s_tile = atomicAdd(tile_counter, 1);
   __syncthreads();
   const int64_t tile = s_tile;
-  const int64_t w0 = tile * kWordsPerTile + int64_t(threadIdx.x) * kWordsPerThread;
+  const int64_t tw0 = tile * kWordsPerTile;  // the tile's first word
+  const int64_t w0 = tw0 + int64_t(threadIdx.x) * kWordsPerThread;
   uint32_t m[3][kWordsPerThread];
   uint32_t c[3] = {0, 0, 0};
 #pragma unroll
@@ -87,35 +246,52 @@ __global__ void __launch_bounds__(kThreads) compact_kernel(const uint32_t* bm_t,
   __syncthreads();
   int64_t* lists[3] = {co, ex_t, ex_next};
   int64_t* offs[3] = {co_off, ex_t_off, ex_next_off};
-  const int64_t last_word = nwords - 1;
+  const int64_t row0 = tw0 * 32;                                           // the tile's first row
+  const int64_t row_end = (tw0 + kWordsPerTile) * 32 < R ? (tw0 + kWordsPerTile) * 32 : R;
+  const bool last_tile = tw0 + kWordsPerTile >= nwords;
 #pragma unroll
   for (int k = 0; k < 3; ++k) {
-    int64_t at = s_excl[k] + int64_t(unpack3(ex, k));
+    // words and their in-tile prefixes to shared memory
+    uint32_t run = unpack3(ex, k);
+#pragma unroll
     for (int i = 0; i < kWordsPerThread; ++i) {
-      const int64_t w = w0 + i;
-      if (w >= nwords) break;
-      uint32_t bits = m[k][i];
-      // shard boundaries k_s * block that fall inside this word (rows < R)
-      const int64_t row0 = w * 32;
-      int64_t s_lo = (row0 + block - 1) / block;
-      for (int64_t s = s_lo; s <= n && s * block < row0 + 32 && s * block < R; ++s) {
-        const uint32_t below = uint32_t(s * block - row0);
-        offs[k][s] = at + __popc(bits & ((below == 0) ? 0u : (0xFFFFFFFFu >> (32 - below))));
-      }
-      while (bits) {
-        const int b = __ffs(bits) - 1;
-        bits &= bits - 1;
-        if (at < cap) lists[k][at] = row0 + b;
-        ++at;
-      }
-      if (w == last_word) {
-        counts[k] = at;
-        if (at > cap) set_err(err, FS_ERR_CAPACITY);
-        // boundaries at or beyond R hold the full list length
-        int64_t s_first = (R + block - 1) / block;
-        for (int64_t s = s_first; s <= n; ++s) offs[k][s] = at;
-      }
+      wpre[threadIdx.x * kWordsPerThread + i] = run;
+      wbits[threadIdx.x * kWordsPerThread + i] = m[k][i];
+      run += __popc(m[k][i]);
     }
+    __syncthreads();
+    const uint32_t cnt = unpack3(tot, k);
+    const int64_t base = s_excl[k];
+    int64_t* list = lists[k];
+    // entry j of the tile's run of list k: the word holding it by binary search on the
+    // prefixes, then its set bit by rank; consecutive threads write consecutive entries
+    for (uint32_t j = threadIdx.x; j < cnt; j += kThreads) {
+      int lo = 0, hi = kWordsPerTile - 1;  // the last word whose prefix is <= j
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (wpre[mid] <= j) lo = mid; else hi = mid - 1;
+      }
+      const int bit = nth_set_bit(wbits[lo], int(j - wpre[lo]));
+      const int64_t at = base + j;
+      if (at < cap) list[at] = row0 + int64_t(lo) * 32 + bit;
+    }
+    // shard boundaries s * block inside [row0, row_end): rows of the list below them
+    const int64_t s_first = (row0 + block - 1) / block;
+    for (int64_t s = s_first + threadIdx.x; s <= n && s * block < row_end; s += kThreads) {
+      const int64_t rel = s * block - row0;
+      const int wi = int(rel >> 5), below = int(rel & 31);
+      offs[k][s] = base + wpre[wi] + __popc(wbits[wi] & ((below == 0) ? 0u : (0xFFFFFFFFu >> (32 - below))));
+    }
+    if (last_tile) {
+      const int64_t total = base + cnt;
+      if (threadIdx.x == 0) {
+        counts[k] = total;
+        if (total > cap) set_err(err, FS_ERR_CAPACITY);
+      }
+      // boundaries at or beyond R hold the full list length
+      for (int64_t s = (R + block - 1) / block + threadIdx.x; s <= n; s += kThreads) offs[k][s] = total;
+    }
+    __syncthreads();  // wpre / wbits are rewritten for the next list
   }
 }
 
@@ -267,7 +443,7 @@ extern "C" fs_status fs_row_bitmap(const int64_t* ids, int64_t T, int64_t num_ro
   if (cudaMemsetAsync(bitmap, 0, fs_row_bitmap_words(num_rows) * sizeof(uint32_t), st) != cudaSuccess)
     return FS_ERR_CUDA;
   if (T > 0) {
-    mark_kernel<<<grid_for(T), kThreads, 0, st>>>(ids, T, nullptr, 0, num_rows, bitmap, nullptr, err);
+    launch_mark_window(ids, T, num_rows, bitmap, err, st);
     count_launch(1);
   }
   return launch_status();

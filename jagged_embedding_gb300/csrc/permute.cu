@@ -233,7 +233,7 @@ __global__ void __launch_bounds__(kThreads) permute_seg_copy_kernel(const int64_
 }
 
 // Fused permute + bucketize, kernel 2: blocks take chunks of
-// radix::kChunkTiles consecutive output tiles (kCopyTile == radix::kTile IDs
+// 1 << cshift consecutive output tiles (the counting pass's chunk size) (kCopyTile == radix::kTile IDs
 // each) and copy them like permute_copy_kernel; every ID written is counted
 // in its shard's bin, giving the counting pass's counts[tile][shard] (exclusive
 // within the chunk) and chunk_sums[chunk][shard].  Tiles past the output (up
@@ -243,7 +243,8 @@ static_assert(kCopyTile == radix::kTile, "a copy tile is a counting tile");
 __global__ void __launch_bounds__(kThreads) permute_count_kernel(
     const int64_t* values, const int64_t* out_offsets, const int64_t* src_start, const int32_t* first_sample,
     int64_t S, int64_t capacity, int64_t* out_values, const int64_t* rank_offsets, int32_t n, int64_t* rank_id_offsets,
-    int32_t* err, shard::SrcShard sh, uint32_t* counts, uint32_t* chunk_sums, int64_t ntiles_cap, int64_t* T_out) {
+    int32_t* err, shard::SrcShard sh, uint32_t* counts, uint32_t* chunk_sums, int64_t ntiles_cap, int cshift,
+    int64_t* T_out) {
   __shared__ uint32_t hist[radix::kMaxBins];
   const int nb = sh.n;
   if (blockIdx.x == 0) {
@@ -267,8 +268,8 @@ __global__ void __launch_bounds__(kThreads) permute_count_kernel(
   uint32_t run[radix::kPerT];
 #pragma unroll
   for (int q = 0; q < radix::kPerT; ++q) run[q] = 0;
-  for (int c = 0; c < radix::kChunkTiles; ++c) {
-    const int64_t t = int64_t(blockIdx.x) * radix::kChunkTiles + c;
+  for (int c = 0; c < (1 << cshift); ++c) {
+    const int64_t t = (int64_t(blockIdx.x) << cshift) + c;
     if (t >= ntiles_cap) break;
     for (int d = threadIdx.x; d < nb; d += kThreads) hist[d] = 0;
     __syncthreads();
@@ -508,18 +509,28 @@ extern "C" fs_status fs_permute_bucketize(const int64_t* offsets, const int64_t*
         offsets, S, PermArray{perm}, out_offsets, src_start, first_sample, L.copy_tiles, capacity,
         reinterpret_cast<uint64_t*>(zero + 256), reinterpret_cast<int*>(zero), err, spin_limit(), debug_skip_tile());
     const int64_t nchunks = radix::num_chunks(P.ntiles);
+    const int cs = radix::chunk_shift(P.ntiles);
     permute_count_kernel<<<unsigned(nchunks), kThreads, 0, st>>>(values, out_offsets, src_start, first_sample, S,
                                                                  capacity, out_values, rank_offsets, n,
                                                                  rank_id_offsets, err, sh, P.counts, P.chunk,
-                                                                 P.ntiles, T_out);
+                                                                 P.ntiles, cs, T_out);
     radix::chunk_scan_kernel<<<unsigned((n + 31) / 32), radix::kScanThreads, 0, st>>>(P.chunk, nchunks, n, P.totals);
     radix::digit_base_kernel<<<1, radix::kThreads, 0, st>>>(P.totals, n, P.digit_base, P.n_valid);
     const radix::PlainTiles tiles{T_out, 0, P.digit_base};
-    const size_t smem = radix::downsweep_smem_bytes<int64_t>();
-    auto down = radix::downsweep_kernel<shard::SrcShard, shard::DstShardMajor, radix::PlainTiles>;
-    radix::set_smem(down, smem);
-    down<<<unsigned(P.ntiles), radix::kThreads, smem, st>>>(sh, shard::DstShardMajor{sm_ids, pos}, tiles, 0, 0, n,
-                                                            P.counts, P.chunk);
+    if (num_rows < (int64_t(1) << 32)) {  // rows fit 32 bits: the lighter staging (same shard of every ID)
+      const shard::SrcShard32 sh32{out_values, num_rows, block, sh.inv_block, n};
+      const size_t smem = radix::downsweep_smem_bytes<uint32_t>();
+      auto down = radix::downsweep_kernel<shard::SrcShard32, shard::DstShardMajor, radix::PlainTiles>;
+      radix::set_smem(down, smem);
+      down<<<unsigned(P.ntiles), radix::kDownThreads, smem, st>>>(sh32, shard::DstShardMajor{sm_ids, pos}, tiles, 0, 0,
+                                                                  n, P.counts, P.chunk, cs);
+    } else {
+      const size_t smem = radix::downsweep_smem_bytes<int64_t>();
+      auto down = radix::downsweep_kernel<shard::SrcShard, shard::DstShardMajor, radix::PlainTiles>;
+      radix::set_smem(down, smem);
+      down<<<unsigned(P.ntiles), radix::kDownThreads, smem, st>>>(sh, shard::DstShardMajor{sm_ids, pos}, tiles, 0, 0, n,
+                                                              P.counts, P.chunk, cs);
+    }
     launches = 5;
   }
   shard::shard_offsets_kernel<<<1, kThreads, 0, st>>>(P.digit_base, n, 0, T_out, shard_offsets);

@@ -2,7 +2,7 @@
 // Merrill & Grimshaw, "High Performance and Scalable Radix Sorting", 2011).
 //
 // One pass over the items of [0, count) keyed by one digit:
-//   1. upsweep:    one block per chunk of kChunkTiles tiles of kTile items;
+//   1. upsweep:    one block per chunk of 4 or 16 tiles of kTile items;
 //                  per tile, the count of every digit value, written as the
 //                  exclusive prefix over the chunk's earlier tiles
 //                  (counts[tile][digit]); per chunk, the digit totals;
@@ -32,6 +32,7 @@
 
 #include "fs_common.cuh"
 
+
 namespace fs {
 namespace radix {
 
@@ -40,11 +41,19 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kItems = 16;
 constexpr int kTile = kThreads * kItems;  // 4096 items per tile
 constexpr int kMaxBins = 1024;
-constexpr int kChunkTiles = 16;  // tiles per upsweep block
+// Tiles per counting (upsweep) block: 16, or 4 for passes of fewer than
+// kSmallPassTiles tiles, so that a mid-size pass (a few thousand tiles) still
+// gives every SM several blocks.  A pass's chunk size follows from its tile
+// count alone (chunk_shift), so every kernel and workspace size of the pass
+// agrees on it.
+constexpr int64_t kSmallPassTiles = 16384;
+constexpr int chunk_shift(int64_t ntiles) { return ntiles < kSmallPassTiles ? 2 : 4; }
 constexpr int kPerT = kMaxBins / kThreads;  // digits per thread
 
 constexpr int64_t num_tiles(int64_t count) { return (count + kTile - 1) / kTile; }
-constexpr int64_t num_chunks(int64_t ntiles) { return (ntiles + kChunkTiles - 1) / kChunkTiles; }
+constexpr int64_t num_chunks(int64_t ntiles) {
+  return (ntiles + (int64_t(1) << chunk_shift(ntiles)) - 1) >> chunk_shift(ntiles);
+}
 
 
 // Index, inside its tile, of item i of lane `lane` in warp `warp` (warp-striped,
@@ -91,6 +100,7 @@ struct PlainTiles {
 struct SegTiles {
   const int64_t* seg_off;     // [nseg + 1]
   const int64_t* tile_base;   // [nseg + 1]
+  const int32_t* tile_seg;    // [tiles]: the tile's segment, -1 past the last (seg_map_kernel)
   const uint32_t* seg_base;   // [nseg][nb]
   const uint32_t* group_base; // [2][nseg]
   int32_t nseg;
@@ -98,15 +108,11 @@ struct SegTiles {
   int32_t group_shift;
   __device__ __forceinline__ TileSpan span(int64_t t) const {
     TileSpan r{0, 0, 0};
-    if (t >= tile_base[nseg]) return r;
-    int lo = 0, hi = nseg - 1;  // the last segment whose first tile is <= t (skips empty segments)
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (tile_base[mid] <= t) lo = mid; else hi = mid - 1;
-    }
-    r.seg = lo;
-    r.start = seg_off[lo] + (t - tile_base[lo]) * kTile;
-    const int64_t left = seg_off[lo + 1] - r.start;
+    const int s = __ldg(tile_seg + t);  // one load instead of a search over tile_base
+    if (s < 0) return r;
+    r.seg = s;
+    r.start = __ldg(seg_off + s) + (t - __ldg(tile_base + s)) * kTile;
+    const int64_t left = __ldg(seg_off + s + 1) - r.start;
     r.count = int32_t(left < kTile ? (left < 0 ? 0 : left) : kTile);
     return r;
   }
@@ -116,7 +122,7 @@ struct SegTiles {
 };
 
 // ------------------------------------------------------------------ upsweep
-// Block c: tiles [c * kChunkTiles, ...) one after another.  Per tile, one
+// Block c: tiles [c << cshift, (c + 1) << cshift) one after another.  Per tile, one
 // block-wide histogram (all item loads issued first, then one shared-memory
 // increment per item); counts[tile][d] = this chunk's count of d before the
 // tile; chunk_sums[c][d] = the chunk's count of d.  Empty tiles count nothing
@@ -124,15 +130,15 @@ struct SegTiles {
 template <class Src, class Tiles>
 __global__ void __launch_bounds__(kThreads) upsweep_kernel(Src src, Tiles tiles, int shift, int bits, int nb,
                                                            uint32_t* counts, uint32_t* chunk_sums, int64_t ntiles,
-                                                           int32_t* err) {
+                                                           int cshift, int32_t* err) {
   __shared__ uint32_t hist[kMaxBins];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t chunk = blockIdx.x;
   uint32_t run[kPerT];
 #pragma unroll
   for (int j = 0; j < kPerT; ++j) run[j] = 0;
-  for (int c = 0; c < kChunkTiles; ++c) {
-    const int64_t tile = chunk * kChunkTiles + c;
+  for (int c = 0; c < (1 << cshift); ++c) {
+    const int64_t tile = (chunk << cshift) + c;
     if (tile >= ntiles) break;
     const TileSpan sp = tiles.span(tile);
     for (int j = threadIdx.x; j < nb; j += kThreads) hist[j] = 0;
@@ -236,6 +242,22 @@ static __global__ void __launch_bounds__(kThreads) digit_base_kernel(const uint3
 }
 
 // ------------------------------------------------------------------ downsweep
+// Block shape of the downsweep: kDownThreads threads, kDownItems items each
+// (one tile of kTile items).  Measured alternatives (512 threads x 8 items,
+// 16-bit warp counts) were no faster on the large-table passes.
+constexpr int kDownThreads = kThreads;
+constexpr int kDownItems = kTile / kDownThreads;
+constexpr int kDownWarps = kDownThreads / 32;
+constexpr int kDownPerT = kMaxBins / kDownThreads;  // digits per thread
+static_assert(kDownThreads * kDownItems == kTile && kDownPerT >= 1, "downsweep shape");
+using HistT = uint32_t;
+#ifndef FS_BALLOT_MAX_BITS
+#define FS_BALLOT_MAX_BITS 8  // widest digit the multisplit matches by ballots
+#endif
+
+// Index, inside its tile, of the downsweep's item i of lane `lane` in warp `warp`.
+__device__ __forceinline__ int down_index(int warp, int i, int lane) { return warp * 32 * kDownItems + i * 32 + lane; }
+
 // Shared memory: the per-warp digit counts during ranking, then (same space)
 // the staged keys and values in tile order; behind them the tile's digit
 // counts (later each run's output offset minus its tile-local start), the
@@ -243,7 +265,7 @@ static __global__ void __launch_bounds__(kThreads) digit_base_kernel(const uint3
 template <class KeyT>
 constexpr size_t downsweep_smem_bytes() {
   size_t stage = size_t(kTile) * (sizeof(KeyT) + sizeof(uint32_t));
-  size_t hist = size_t(kWarps) * kMaxBins * sizeof(uint32_t);
+  size_t hist = size_t(kDownWarps) * kMaxBins * sizeof(HistT);
   size_t un = stage > hist ? stage : hist;
   return un + 2 * kMaxBins * sizeof(uint32_t) + 64 * sizeof(uint32_t);
 }
@@ -261,15 +283,17 @@ struct DownBlocks<Src, decltype(void(Src::kMinBlocks))> {
 };
 
 template <class Src, class Dst, class Tiles>
-__global__ void __launch_bounds__(kThreads, DownBlocks<Src>::value) downsweep_kernel(Src src, Dst dst, Tiles tiles, int shift, int bits,
-                                                                int nb, const uint32_t* counts,
-                                                                const uint32_t* chunk_base) {
+__global__ void __launch_bounds__(kDownThreads, DownBlocks<Src>::value) downsweep_kernel(Src src, Dst dst, Tiles tiles,
+                                                                                     int shift, int bits, int nb,
+                                                                                     const uint32_t* counts,
+                                                                                     const uint32_t* chunk_base,
+                                                                                     int cshift) {
   using KeyT = typename Src::Key;
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  uint32_t* warp_hist = reinterpret_cast<uint32_t*>(smem_raw);  // [kWarps][nb] (ranking)
-  KeyT* stage_k = reinterpret_cast<KeyT*>(smem_raw);            // [kTile]      (staging)
+  HistT* warp_hist = reinterpret_cast<HistT*>(smem_raw);  // [kDownWarps][nb] (ranking)
+  KeyT* stage_k = reinterpret_cast<KeyT*>(smem_raw);      // [kTile]          (staging)
   constexpr size_t stage_bytes = size_t(kTile) * (sizeof(KeyT) + sizeof(uint32_t));
-  constexpr size_t hist_bytes = size_t(kWarps) * kMaxBins * sizeof(uint32_t);
+  constexpr size_t hist_bytes = size_t(kDownWarps) * kMaxBins * sizeof(HistT);
   constexpr size_t un = stage_bytes > hist_bytes ? stage_bytes : hist_bytes;
   uint32_t* stage_v = reinterpret_cast<uint32_t*>(smem_raw + size_t(kTile) * sizeof(KeyT));
   uint32_t* run_off = reinterpret_cast<uint32_t*>(smem_raw + un);  // tile counts, then output offset - local start
@@ -283,11 +307,11 @@ __global__ void __launch_bounds__(kThreads, DownBlocks<Src>::value) downsweep_ke
 
   // this tile's offset inside every digit run: loaded first, so that these
   // reads overlap the item loads and the ranking below
-  uint32_t my_off[kPerT];
+  uint32_t my_off[kDownPerT];
 #pragma unroll
-  for (int i = 0; i < kPerT; ++i) {
-    const int d = threadIdx.x + i * kThreads;
-    my_off[i] = d < nb ? __ldg(counts + tile * nb + d) + __ldg(chunk_base + (tile / kChunkTiles) * nb + d) +
+  for (int i = 0; i < kDownPerT; ++i) {
+    const int d = threadIdx.x + i * kDownThreads;
+    my_off[i] = d < nb ? __ldg(counts + tile * nb + d) + __ldg(chunk_base + (tile >> cshift) * nb + d) +
                              tiles.base(sp.seg, d)
                        : 0u;
   }
@@ -295,60 +319,77 @@ __global__ void __launch_bounds__(kThreads, DownBlocks<Src>::value) downsweep_ke
   // per item: the key, one packed word (digit in bits 20..31, rank / local
   // position in bits 0..19) and, only for sources whose value is not the item
   // index, the value
-  KeyT key[kItems];
-  uint32_t val[Src::kIndexValue ? 1 : kItems];
-  uint32_t pk[kItems];
+  KeyT key[kDownItems];
+  uint32_t val[Src::kIndexValue ? 1 : kDownItems];
+  uint32_t pk[kDownItems];
   constexpr uint32_t kSkipPk = 0xFFF00000u;
   {
-    typename Src::Raw raw[kItems];
+    typename Src::Raw raw[kDownItems];
 #pragma unroll
-    for (int i = 0; i < kItems; ++i) {
-      const int l = local_index(warp, i, lane);
+    for (int i = 0; i < kDownItems; ++i) {
+      const int l = down_index(warp, i, lane);
       if (l < sp.count) raw[i] = src.template fetch<true>(sp.start + l);
     }
     if constexpr (Src::kFetch2) {
 #pragma unroll
-      for (int i = 0; i < kItems; ++i)
-        if (local_index(warp, i, lane) < sp.count) src.template fetch2<true>(raw[i]);
+      for (int i = 0; i < kDownItems; ++i)
+        if (down_index(warp, i, lane) < sp.count) src.template fetch2<true>(raw[i]);
     }
 #pragma unroll
-    for (int i = 0; i < kItems; ++i) {
-      const int l = local_index(warp, i, lane);
+    for (int i = 0; i < kDownItems; ++i) {
+      const int l = down_index(warp, i, lane);
       uint32_t v = 0;
       const bool ok = l < sp.count && src.make(raw[i], sp.start + l, sp.seg, key[i], v, nullptr);
       if constexpr (!Src::kIndexValue) val[i] = v;
       pk[i] = ok ? (src.digit(key[i], shift, bits, sp.seg) << 20) : kSkipPk;
     }
   }
-  for (int j = threadIdx.x; j < kWarps * nb; j += kThreads) warp_hist[j] = 0;
+  for (int j = threadIdx.x; j < kDownWarps * nb; j += kDownThreads) warp_hist[j] = 0u;
   __syncthreads();
 
   // warp-level multisplit, slot by slot (slot order = item order)
-  uint32_t* wh = warp_hist + warp * nb;
+  HistT* wh = warp_hist + warp * nb;
+  // lanes with the same digit: for digits of at most 8 bits one ballot per
+  // digit bit (faster there than match.any: the 256-shard bucketize pass
+  // 3.36 -> 3.07 ms on 303M IDs), wider digits by match.any (10-bit passes
+  // were slower with ballots)
+  const int dbits = nb > 1 ? 32 - __clz(nb - 1) : 1;  // every digit is below nb
+  const bool by_ballot = dbits <= FS_BALLOT_MAX_BITS;
 #pragma unroll
-  for (int i = 0; i < kItems; ++i) {
+  for (int i = 0; i < kDownItems; ++i) {
     const uint32_t d = pk[i] >> 20;
     const bool skip = pk[i] == kSkipPk;
-    const unsigned peers = __match_any_sync(0xffffffffu, pk[i]);
+    unsigned peers;
+    if (by_ballot) {
+      const unsigned sk = __ballot_sync(0xffffffffu, skip);  // skipped items match each other only
+      peers = skip ? sk : ~sk;
+      for (int b = 0; b < dbits; ++b) {
+        const bool on = (d >> b) & 1u;
+        const unsigned m = __ballot_sync(0xffffffffu, on);
+        peers &= on ? m : ~m;
+      }
+    } else {
+      peers = __match_any_sync(0xffffffffu, pk[i]);
+    }
     const unsigned lt = __popc(peers & lanemask_lt());
-    const uint32_t b = skip ? 0u : wh[d];
+    const uint32_t b = skip ? 0u : uint32_t(wh[d]);
     if (!skip) pk[i] |= b + lt;
     __syncwarp();
-    if (!skip && lt == 0) wh[d] = b + __popc(peers);
+    if (!skip && lt == 0) wh[d] = HistT(b + __popc(peers));
     __syncwarp();
   }
   __syncthreads();
 
   // exclusive over warps per digit, tile totals
 #pragma unroll
-  for (int i = 0; i < kPerT; ++i) {
-    const int d = threadIdx.x + i * kThreads;
+  for (int i = 0; i < kDownPerT; ++i) {
+    const int d = threadIdx.x + i * kDownThreads;
     if (d < nb) {
       uint32_t run = 0;
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
+      for (int w = 0; w < kDownWarps; ++w) {
         const uint32_t c = warp_hist[w * nb + d];
-        warp_hist[w * nb + d] = run;
+        warp_hist[w * nb + d] = HistT(run);
         run += c;
       }
       run_off[d] = run;
@@ -356,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, DownBlocks<Src>::value) downsweep_ke
   }
   __syncthreads();
   {
-    constexpr int kPer = kMaxBins / kThreads;  // digits per thread
+    constexpr int kPer = kMaxBins / kDownThreads;  // digits per thread
     const int d0 = threadIdx.x * kPer;
     uint32_t v[kPer], sum = 0;
 #pragma unroll
@@ -377,30 +418,30 @@ __global__ void __launch_bounds__(kThreads, DownBlocks<Src>::value) downsweep_ke
   // each run's output position minus its tile-local start: staged item j of
   // digit d goes to run_off[d] + j (positions < 2^31, exact modulo 2^32)
 #pragma unroll
-  for (int i = 0; i < kPerT; ++i) {
-    const int d = threadIdx.x + i * kThreads;
+  for (int i = 0; i < kDownPerT; ++i) {
+    const int d = threadIdx.x + i * kDownThreads;
     if (d < nb) run_off[d] = my_off[i] - local_start[d];
   }
 #pragma unroll
-  for (int i = 0; i < kItems; ++i)
+  for (int i = 0; i < kDownItems; ++i)
     if (pk[i] != kSkipPk) {
       const uint32_t d = pk[i] >> 20;
-      pk[i] = (d << 20) | (local_start[d] + warp_hist[warp * nb + d] + (pk[i] & 0xFFFFFu));  // tile-local position
+      pk[i] = (d << 20) | (local_start[d] + uint32_t(warp_hist[warp * nb + d]) + (pk[i] & 0xFFFFFu));  // tile-local position
     }
   const uint32_t nvalid = scratch[40];
   __syncthreads();  // warp_hist is dead; its space becomes the staging area
 #pragma unroll
-  for (int i = 0; i < kItems; ++i)
+  for (int i = 0; i < kDownItems; ++i)
     if (pk[i] != kSkipPk) {
       const uint32_t at = pk[i] & 0xFFFFFu;
       stage_k[at] = key[i];
       if constexpr (Src::kIndexValue)  // digit and tile-local index: no digit to recompute below
-        stage_v[at] = ((pk[i] >> 20) << 12) | uint32_t(local_index(warp, i, lane));
+        stage_v[at] = ((pk[i] >> 20) << 12) | uint32_t(down_index(warp, i, lane));
       else
         stage_v[at] = val[i];
     }
   __syncthreads();
-  for (uint32_t j = threadIdx.x; j < nvalid; j += kThreads) {
+  for (uint32_t j = threadIdx.x; j < nvalid; j += kDownThreads) {
     const KeyT k = stage_k[j];
     const uint32_t sv = stage_v[j];
     if constexpr (Src::kIndexValue) {
@@ -494,23 +535,25 @@ void run_pass(const Src& src, const Dst& dst, int shift, int bits, int nb, const
   }
   const int64_t nchunks = num_chunks(P.ntiles);
   const PlainTiles tiles{count_dev, count_host, P.digit_base};
+  const int cs = chunk_shift(P.ntiles);
   upsweep_kernel<Src, PlainTiles><<<unsigned(nchunks), kThreads, 0, st>>>(src, tiles, shift, bits, nb, P.counts,
-                                                                          P.chunk, P.ntiles, err);
+                                                                          P.chunk, P.ntiles, cs, err);
   chunk_scan_kernel<<<unsigned((nb + 31) / 32), kScanThreads, 0, st>>>(P.chunk, nchunks, nb, P.totals);
   digit_base_kernel<<<1, kThreads, 0, st>>>(P.totals, nb, P.digit_base, P.n_valid);
   const size_t smem = downsweep_smem_bytes<typename Src::Key>();
   set_smem(downsweep_kernel<Src, Dst, PlainTiles>, smem);
-  downsweep_kernel<Src, Dst, PlainTiles><<<unsigned(P.ntiles), kThreads, smem, st>>>(src, dst, tiles, shift, bits, nb,
-                                                                                     P.counts, P.chunk);
+  downsweep_kernel<Src, Dst, PlainTiles><<<unsigned(P.ntiles), kDownThreads, smem, st>>>(src, dst, tiles, shift, bits, nb,
+                                                                                     P.counts, P.chunk, cs);
   *launches += 4;
 }
 
 // ------------------------------------------------------------------ segment-aligned passes
 // Passes that sort every segment of an array already grouped into segments
 // (the update's sort of shard-major IDs: one segment per shard), under
-// SegTiles.  One pass = upsweep, chunk scan, seg_base_kernel (the digit
-// bases of every segment), seg_offsets_kernel (the group bases, and the
-// segments and tiles of the pass's output for the next pass), downsweep.
+// SegTiles.  One pass = seg_map_kernel (each tile's segment), upsweep, chunk
+// scan, seg_base_kernel (the digit bases of every segment), seg_offsets_kernel
+// (the group bases, and the segments and tiles of the pass's output for the
+// next pass), downsweep.
 constexpr int kSegThreads = 1024;  // segments handled by one block: nseg <= kSegThreads
 
 // Segment offsets of the input, made safe to tile: seg_off[s] = the running
@@ -558,7 +601,7 @@ static __global__ void __launch_bounds__(kSegThreads) seg_tiles_kernel(const int
 // segment's items in group g.
 static __global__ void __launch_bounds__(kThreads) seg_base_kernel(const uint32_t* counts, const uint32_t* chunk_base,
                                                               const uint32_t* totals, const int64_t* tile_base,
-                                                              int32_t nseg, int nb, int group_shift,
+                                                              int32_t nseg, int nb, int group_shift, int cshift,
                                                               uint32_t* seg_base, uint32_t* gtot) {
   __shared__ uint32_t tmp[32];
   __shared__ uint32_t g0;
@@ -566,7 +609,7 @@ static __global__ void __launch_bounds__(kThreads) seg_base_kernel(const uint32_
   const int64_t tiles = tile_base[nseg];
   const int64_t f0 = tile_base[s], f1 = tile_base[s + 1];
   auto G = [&](int64_t f, int d) -> uint32_t {
-    return f < tiles ? counts[f * nb + d] + chunk_base[(f / kChunkTiles) * nb + d] : totals[d];
+    return f < tiles ? counts[f * nb + d] + chunk_base[(f >> cshift) * nb + d] : totals[d];
   };
   constexpr int kPer = kMaxBins / kThreads;
   const int d0 = threadIdx.x * kPer;  // contiguous digits per thread: the scan runs in digit order
@@ -632,6 +675,29 @@ static __global__ void __launch_bounds__(kSegThreads) seg_offsets_kernel(const u
   }
 }
 
+// tile_seg[t] = the segment owning tile t of a segment-aligned tiling (the
+// last segment whose first tile is <= t, so empty segments own none), -1 for
+// tiles past the last segment's; the search runs over tile_base staged in
+// shared memory, so the passes' tiles find their segment with one load.
+static __global__ void __launch_bounds__(kSegThreads) seg_map_kernel(const int64_t* tile_base, int32_t nseg,
+                                                                    int64_t max_tiles, int32_t* tile_seg) {
+  __shared__ int64_t tb[kSegThreads + 1];
+  for (int s = threadIdx.x; s <= nseg; s += blockDim.x) tb[s] = tile_base[s];
+  __syncthreads();
+  const int64_t t = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (t >= max_tiles) return;
+  if (t >= tb[nseg]) {
+    tile_seg[t] = -1;
+    return;
+  }
+  int lo = 0, hi = nseg - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (tb[mid] <= t) lo = mid; else hi = mid - 1;
+  }
+  tile_seg[t] = lo;
+}
+
 // Scratch of the segment-aligned passes over up to `count` items in nseg segments.
 struct SegWs {
   int32_t nseg = 0;
@@ -644,6 +710,7 @@ struct SegWs {
   uint32_t* group_base = nullptr;  // [2][nseg]
   int64_t* seg_off[2] = {nullptr, nullptr};    // [nseg + 1] each: a pass's input segments
   int64_t* tile_base[2] = {nullptr, nullptr};  // [nseg + 1] each
+  int32_t* tile_seg = nullptr;                 // [max_tiles]: the current pass's tile -> segment map
 };
 
 constexpr int64_t seg_max_tiles(int64_t count, int32_t nseg) { return num_tiles(count) + nseg; }
@@ -661,6 +728,7 @@ inline void take_seg_ws(int64_t count, int32_t nseg, Ws& ws, SegWs* W) {
   int64_t* so1 = ws.template take<int64_t>(size_t(nseg) + 1);
   int64_t* tb0 = ws.template take<int64_t>(size_t(nseg) + 1);
   int64_t* tb1 = ws.template take<int64_t>(size_t(nseg) + 1);
+  int32_t* ts = ws.template take<int32_t>(size_t(mt));
   if (W) {
     W->nseg = nseg;
     W->max_tiles = mt;
@@ -674,6 +742,7 @@ inline void take_seg_ws(int64_t count, int32_t nseg, Ws& ws, SegWs* W) {
     W->seg_off[1] = so1;
     W->tile_base[0] = tb0;
     W->tile_base[1] = tb1;
+    W->tile_seg = ts;
   }
 }
 
@@ -684,20 +753,23 @@ template <class Src, class Dst>
 void run_seg_pass(const Src& src, const Dst& dst, int shift, int bits, int group_shift, const SegWs& W, int in,
                   int64_t* n_valid, int64_t* n_first, int32_t* err, cudaStream_t st, int* launches) {
   const int nb = 1 << bits;
-  const SegTiles tiles{W.seg_off[in], W.tile_base[in], W.seg_base, W.group_base, W.nseg, nb, group_shift};
+  const SegTiles tiles{W.seg_off[in], W.tile_base[in], W.tile_seg, W.seg_base, W.group_base, W.nseg, nb, group_shift};
   const int64_t nchunks = num_chunks(W.max_tiles);
+  const int cs = chunk_shift(W.max_tiles);
+  seg_map_kernel<<<unsigned((W.max_tiles + kSegThreads - 1) / kSegThreads), kSegThreads, 0, st>>>(
+      W.tile_base[in], W.nseg, W.max_tiles, W.tile_seg);
   upsweep_kernel<Src, SegTiles><<<unsigned(nchunks), kThreads, 0, st>>>(src, tiles, shift, bits, nb, W.counts,
-                                                                        W.chunk, W.max_tiles, err);
+                                                                        W.chunk, W.max_tiles, cs, err);
   chunk_scan_kernel<<<unsigned((nb + 31) / 32), kScanThreads, 0, st>>>(W.chunk, nchunks, nb, W.totals);
   seg_base_kernel<<<unsigned(W.nseg), kThreads, 0, st>>>(W.counts, W.chunk, W.totals, W.tile_base[in], W.nseg, nb,
-                                                          group_shift, W.seg_base, W.gtot);
+                                                          group_shift, cs, W.seg_base, W.gtot);
   seg_offsets_kernel<<<1, kSegThreads, 0, st>>>(W.gtot, W.nseg, W.group_base, W.seg_off[1 - in],
                                                 W.tile_base[1 - in], n_valid, n_first);
   const size_t smem = downsweep_smem_bytes<typename Src::Key>();
   set_smem(downsweep_kernel<Src, Dst, SegTiles>, smem);
-  downsweep_kernel<Src, Dst, SegTiles><<<unsigned(W.max_tiles), kThreads, smem, st>>>(src, dst, tiles, shift, bits, nb,
-                                                                                      W.counts, W.chunk);
-  *launches += 5;
+  downsweep_kernel<Src, Dst, SegTiles><<<unsigned(W.max_tiles), kDownThreads, smem, st>>>(src, dst, tiles, shift, bits, nb,
+                                                                                      W.counts, W.chunk, cs);
+  *launches += 6;
 }
 
 // LSD sort of (uint32 key, uint32 value) pairs drawn from Src0 (the items of

@@ -43,11 +43,51 @@ struct SrcShard {
   }
 };
 
+// The same source with the IDs staged as 32-bit rows, for tables of fewer
+// than 2^32 rows: the staging takes half the shared memory and the keys half
+// the registers, so the downsweep fits four blocks per SM instead of three.
+// An ID outside [0, R) is staged as 0 (below) or R (at or above), which has
+// the shard SrcShard gives the original ID (the counting pass may use either
+// source); the call reports FS_ERR_ID_RANGE, and that entry's shard-major copy
+// is then the clamped value.
+struct SrcShard32 {
+  using Key = uint32_t;
+  static constexpr bool kIndexValue = true;  // value = item index
+  static constexpr int kMinBlocks = 4;
+  static constexpr bool kFetch2 = false;
+  const int64_t* ids;
+  int64_t R;  // < 2^32
+  int64_t block;
+  float inv_block;
+  int32_t n;
+  using Raw = int64_t;
+  template <bool>
+  __device__ __forceinline__ Raw fetch(int64_t i) const { return __ldcs(ids + i); }
+  __device__ __forceinline__ bool make(Raw id, int64_t i, int, Key& key, uint32_t& val, int32_t* err) const {
+    key = id < 0 ? 0u : (id >= R ? uint32_t(R) : uint32_t(id));
+    val = static_cast<uint32_t>(i);
+    if (err && (id < 0 || id >= R)) set_err(err, FS_ERR_ID_RANGE);
+    return true;
+  }
+  __device__ __forceinline__ uint32_t digit(Key key, int, int, int) const {
+    if (key == 0) return 0;
+    if (int64_t(key) >= R) return uint32_t(n - 1);
+    int64_t q = static_cast<int64_t>(__float2uint_rz(__fmul_rz(__uint2float_rz(key), inv_block)));
+    if (q * block > int64_t(key)) --q;
+    if ((q + 1) * block <= int64_t(key)) ++q;
+    return q >= n ? uint32_t(n - 1) : uint32_t(q);
+  }
+};
+
 struct DstShardMajor {
   int64_t* sm_ids;
   int32_t* pos;
   __device__ __forceinline__ void store(int64_t o, int64_t key, uint32_t val) const {
     __stcs(sm_ids + o, key);
+    __stcs(pos + o, static_cast<int32_t>(val));
+  }
+  __device__ __forceinline__ void store(int64_t o, uint32_t key, uint32_t val) const {
+    __stcs(sm_ids + o, int64_t(key));
     __stcs(pos + o, static_cast<int32_t>(val));
   }
 };

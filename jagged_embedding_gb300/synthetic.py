@@ -136,11 +136,14 @@ def _zipf_cdf(R: int, s: float, device) -> torch.Tensor:
     key = (R, s, str(device))
     c = _cdf_cache.get(key)
     if c is None:
-        k = torch.arange(1, R + 1, dtype=torch.float64, device=device)
+        # summed on the host, in order: a device scan may associate the fp64 sum
+        # differently from run to run, which would move IDs at CDF boundaries
+        k = torch.arange(1, R + 1, dtype=torch.float64)
         c = torch.cumsum(k.pow_(-s), 0)
         c /= c[-1].clone()
         _cdf_cache.clear()  # keep at most one table resident
-        _cdf_cache[key] = c
+        _cdf_cache[key] = c.to(device)
+        c = _cdf_cache[key]
     return c
 
 

@@ -22,6 +22,9 @@ op is one of
   gather-sorted -- the same IDs and table as gather: fs_emb_sort_rows once, then fs_emb_gather_sorted and
                fs_emb_gather each timed alone (median of reps calls, CUDA events), with the bandwidth of
                the algorithmic bytes (8 + 256 per ID, 256 per distinct row)
+  bitmap    -- fs_row_bitmap of T bounded-Zipf(1.0) IDs over R rows, in the shard-major order the pipeline
+               marks them in (fs_bucketize_rowwise into 256 row-range shards first); prints the median
+               time and the bandwidth of the IDs read
   autotune  -- VBS AutoTune with T samples over R logical ranks (lognormal(7, 1.6) lengths up to 16384,
                alpha 1.5, length-sorted cut): fs_vbs_autotune, fs_balance_vbs_tuned and the plain
                fs_balance_vbs, each timed alone (median of reps calls, CUDA events)
@@ -47,7 +50,7 @@ SHARDS = 256
 
 def main(argv) -> int:
     if len(argv) < 3 or argv[0] not in ("gather", "backward", "backward-bf16", "bucketize", "transpose",
-                                        "autotune", "gather-sorted", "prep", "sorted-step"):
+                                        "autotune", "gather-sorted", "prep", "sorted-step", "bitmap"):
         print(__doc__)
         return 2
     op, T, R = argv[0], int(argv[1]), int(argv[2])
@@ -66,6 +69,8 @@ def main(argv) -> int:
     ids = synthetic.zipf_rows(R, 1.0, T, g, dev)
     if op == "sorted-step":
         return _sorted_step(ids, T, R, reps, dev, g, err)
+    if op == "bitmap":
+        return _bitmap(ids, T, R, reps, dev, err)
     if op == "gather-sorted":
         return _gather_sorted(ids, T, R, reps, dev, g, err)
     if op == "gather":
@@ -205,6 +210,18 @@ def _sorted_step(ids, T, R, reps, dev, g, err):
     print(f"sorted-step T={T} R={R} U={U}: sort {t_sort:.3f} ms, gather {t_gather:.3f} ms "
           f"({gb / t_gather / 1e6:.0f} GB/s), update {t_update:.3f} ms ({ub / t_update / 1e6:.0f} GB/s) "
           f"(median of {reps}); algorithmic bytes gather {gb}, update {ub}")
+    return 0
+
+
+def _bitmap(ids, T, R, reps, dev, err):
+    reps = max(reps, 5)
+    rio = torch.linspace(0, T, SHARDS + 1, device=dev).round().to(torch.int64)
+    sm, _, _, _, e0 = B.fs_bucketize_rowwise(ids, rio, R)
+    B.check(e0, "bitmap bucketize")
+    bm = torch.empty(int(B.lib().fs_row_bitmap_words(R)), dtype=torch.int32, device=dev)
+    t = _median_ms(lambda: B.fs_row_bitmap(sm, R, bitmap=bm, err=err), reps)
+    B.check(err, "bitmap")
+    print(f"bitmap T={T} R={R}: {t:.3f} ms, {8 * T / t / 1e6:.0f} GB/s of IDs read (median of {reps})")
     return 0
 
 
