@@ -499,9 +499,12 @@ __global__ void __launch_bounds__(kThreads, MINB) reduce_kernel(const uint32_t* 
 // Shared-memory ring of the bulk-copy reduce: per warp kRingStages stages of
 // BR gradient rows each (BR * RB <= 2 KB), the mbarriers in front.
 constexpr int kRingStages = 4;
+#ifndef FS_RING_ROWS
+#define FS_RING_ROWS 8  // most gradient rows per ring stage
+#endif
 template <int RB>
 struct Ring {
-  static constexpr int BR = (2048 / RB) < 8 ? (2048 / RB) : 8;  // rows per stage
+  static constexpr int BR = (2048 / RB) < FS_RING_ROWS ? (2048 / RB) : FS_RING_ROWS;  // rows per stage
   static constexpr int SPC = 32 / BR;                            // stages per 32-entry batch of keys
   static constexpr int kStageBytes = BR * RB;
   static constexpr int kWarpBytes = 128 + kRingStages * kStageBytes;

@@ -18,7 +18,7 @@ namespace fs {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kWordsPerThread = 8;
+constexpr int kWordsPerThread = 2;  // 512 words (16384 rows) per compact tile: a 10M-row table gives 611 tiles
 constexpr int kWordsPerTile = kThreads * kWordsPerThread;
 
 __global__ void __launch_bounds__(kThreads) mark_kernel(const int64_t* ids_t, int64_t T_t, const int64_t* ids_next,
@@ -181,7 +181,7 @@ void launch_mark_window(const int64_t* ids, int64_t T, int64_t R, uint32_t* bm, 
 }
 
 // Three counters packed in one 64-bit word, 21 bits each (a tile holds at most
-// kWordsPerTile * 32 = 65536 rows per counter).
+// kWordsPerTile * 32 rows per counter).
 __device__ __forceinline__ uint64_t pack3(uint32_t a, uint32_t b, uint32_t c) {
   return uint64_t(a) | (uint64_t(b) << 21) | (uint64_t(c) << 42);
 }

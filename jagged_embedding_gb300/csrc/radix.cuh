@@ -195,9 +195,21 @@ static __global__ void __launch_bounds__(kScanThreads) chunk_scan_kernel(uint32_
   const int d = blockIdx.x * 32 + lane;
   const int64_t per = (nchunks + 31) / 32;
   const int64_t c0 = w * per, c1 = (c0 + per < nchunks) ? c0 + per : nchunks;
+  // (both walks over a warp's chunks keep 8 loads in flight: the chunk counts
+  // sit in L2, and one dependent load per chunk would set the pace)
+  constexpr int kB = 8;
   uint32_t s = 0;
-  if (d < nb)
-    for (int64_t c = c0; c < c1; ++c) s += chunk_sums[c * nb + d];
+  if (d < nb) {
+    int64_t c = c0;
+    for (; c + kB <= c1; c += kB) {
+      uint32_t v[kB];
+#pragma unroll
+      for (int k = 0; k < kB; ++k) v[k] = chunk_sums[(c + k) * nb + d];
+#pragma unroll
+      for (int k = 0; k < kB; ++k) s += v[k];
+    }
+    for (; c < c1; ++c) s += chunk_sums[c * nb + d];
+  }
   part[w][lane] = s;
   __syncthreads();
   if (w == 0) {
@@ -211,12 +223,24 @@ static __global__ void __launch_bounds__(kScanThreads) chunk_scan_kernel(uint32_
   }
   __syncthreads();
   uint32_t run = part[w][lane];
-  if (d < nb)
-    for (int64_t c = c0; c < c1; ++c) {
+  if (d < nb) {
+    int64_t c = c0;
+    for (; c + kB <= c1; c += kB) {
+      uint32_t v[kB];
+#pragma unroll
+      for (int k = 0; k < kB; ++k) v[k] = chunk_sums[(c + k) * nb + d];
+#pragma unroll
+      for (int k = 0; k < kB; ++k) {
+        chunk_sums[(c + k) * nb + d] = run;
+        run += v[k];
+      }
+    }
+    for (; c < c1; ++c) {
       const uint32_t v = chunk_sums[c * nb + d];
       chunk_sums[c * nb + d] = run;
       run += v;
     }
+  }
 }
 
 // Exclusive scan of the digit totals; *n_valid = their sum.
