@@ -112,34 +112,33 @@ struct SrcRows {
 };
 
 #ifndef FS_SHARD_SORT_MINB
-#define FS_SHARD_SORT_MINB 3
+#define FS_SHARD_SORT_MINB 4
 #endif
 #ifndef FS_SHARD_SORT2_MINB
 #define FS_SHARD_SORT2_MINB 4
 #endif
 
 // Sources of the per-shard sort (fs_emb_sort_rows_sharded).  Pass 1 reads the
-// shard-major IDs, their batch-major positions and collision flags; the key is
-// the same (phase bit | row) as SrcRows's and the value the position; the
-// digit is the low `bits` bits of the row's offset inside its shard (the
-// tile's segment).  An ID outside [0, R), outside the tile's shard, or with a
-// flag above 1 is dropped (the first two set the error word).  The flag comes
-// from a per-entry mask (kRowBits false) or from the row bitmap of the
-// collision rows (kRowBits true: one bitmap word per entry, read after the
-// IDs are in; in shard-major order a tile's words lie in its shard's stretch
-// of the bitmap).  The digit does not depend on the flag; a bitmap flag is
-// always 0 or 1, so the upsweep skips the bitmap (a mask byte above 1 drops
-// the entry, so the upsweep reads the mask).
+// shard-major IDs and their collision flags; the key is the same (phase bit |
+// row) as SrcRows's and the value the entry's index, which the sink turns
+// into its batch-major position (DstGatherPos) when it writes the entry, so
+// no position waits in registers through the ranking (four blocks per SM fit
+// where three did); the digit is the low `bits` bits of the row's offset
+// inside its shard (the tile's segment).  An ID outside [0, R), outside the
+// tile's shard, or with a flag above 1 is dropped (the first two set the
+// error word).  The flag comes from a per-entry mask (kRowBits false) or from
+// the row bitmap of the collision rows (kRowBits true: one bitmap word per
+// entry, read after the IDs are in; in shard-major order a tile's words lie in
+// its shard's stretch of the bitmap).  The digit does not depend on the flag;
+// a bitmap flag is always 0 or 1, so the upsweep skips the bitmap (a mask byte
+// above 1 drops the entry, so the upsweep reads the mask).
 template <bool kRowBits>
 struct SrcShardRows {
   using Key = uint32_t;
-  static constexpr bool kIndexValue = false;
+  static constexpr bool kIndexValue = true;  // value = entry index (DstGatherPos reads its position)
   static constexpr bool kFetch2 = kRowBits;
-  // three loads per item in flight (ID, position, flag): the downsweep keeps
-  // them without spilling on the register budget of 3 blocks per SM
   static constexpr int kMinBlocks = FS_SHARD_SORT_MINB;
   const int64_t* sm_ids;
-  const int32_t* pos;
   const uint8_t* is_co;     // per shard-major entry (kRowBits false); null: one phase
   const uint32_t* co_rows;  // collision rows (kRowBits true)
   int64_t R;
@@ -148,14 +147,12 @@ struct SrcShardRows {
   uint32_t row_mask;
   struct Raw {
     int64_t id;
-    uint32_t p;
     uint32_t m;
   };
   template <bool kVal>
   __device__ __forceinline__ Raw fetch(int64_t i) const {
     Raw r;
     r.id = __ldcs(sm_ids + i);
-    r.p = kVal ? uint32_t(__ldcs(pos + i)) : 0u;
     // (the upsweep needs the mask too: a flag above 1 drops the entry there as well)
     r.m = (!kRowBits && is_co) ? uint32_t(__ldcs(is_co + i)) : 0u;
     return r;
@@ -169,7 +166,7 @@ struct SrcShardRows {
       }
     }
   }
-  __device__ __forceinline__ bool make(const Raw& r, int64_t, int seg, Key& key, uint32_t& val, int32_t* err) const {
+  __device__ __forceinline__ bool make(const Raw& r, int64_t i, int seg, Key& key, uint32_t& val, int32_t* err) const {
     if (r.m > 1) return false;
     if (r.id < 0 || r.id >= R) {
       if (err) set_err(err, FS_ERR_ID_RANGE);
@@ -181,7 +178,7 @@ struct SrcShardRows {
       return false;
     }
     key = uint32_t(r.id) | ((kRowBits || is_co) ? (uint32_t(1 - r.m) << kb) : 0u);
-    val = r.p;
+    val = uint32_t(i);
     return true;
   }
   __device__ __forceinline__ uint32_t digit(Key key, int shift, int bits, int seg) const {
@@ -190,27 +187,42 @@ struct SrcShardRows {
   }
 };
 
+// Sink of pass 1: the key, and the batch-major position of the entry whose
+// index the downsweep hands over.
+template <class PosT>
+struct DstGatherPos {
+  uint32_t* k;
+  uint32_t* v;
+  const PosT* pos;
+  __device__ __forceinline__ void store(int64_t o, uint32_t key, uint32_t idx) const {
+    k[o] = key;
+    v[o] = uint32_t(__ldg(pos + idx));
+  }
+};
+
 // Pass 2 of the per-shard sort: pass 1's (key, position) pairs; the digit is
 // (phase bit, next `lbits` bits of the offset in the shard), the phase bit
-// being the group (collision rows of every shard before exclusive ones).
+// being the group (collision rows of every shard before exclusive ones).  As
+// in pass 1 the value handed to the sink is the entry's index, and the sink
+// (DstGatherPos over pass 1's positions) copies the position when it writes
+// the entry.
 struct SrcShardRows2 {
   using Key = uint32_t;
-  static constexpr bool kIndexValue = false;
+  static constexpr bool kIndexValue = true;
   static constexpr bool kFetch2 = false;
   static constexpr int kMinBlocks = FS_SHARD_SORT2_MINB;
   const uint32_t* k;
-  const uint32_t* v;
   int64_t block;
   int kb;
   uint32_t row_mask;
   int lbits;       // bits of the shard offset this pass sorts
   bool two_phase;  // the key's bit kb is the phase
-  using Raw = uint2;
-  template <bool kVal>
-  __device__ __forceinline__ Raw fetch(int64_t i) const { return make_uint2(__ldcs(k + i), kVal ? __ldcs(v + i) : 0u); }
-  __device__ __forceinline__ bool make(const Raw& r, int64_t, int, Key& key, uint32_t& val, int32_t*) const {
-    key = r.x;
-    val = r.y;
+  using Raw = uint32_t;
+  template <bool>
+  __device__ __forceinline__ Raw fetch(int64_t i) const { return __ldcs(k + i); }
+  __device__ __forceinline__ bool make(Raw r, int64_t i, int, Key& key, uint32_t& val, int32_t*) const {
+    key = r;
+    val = uint32_t(i);
     return true;
   }
   __device__ __forceinline__ uint32_t digit(Key key, int shift, int, int seg) const {
@@ -499,12 +511,12 @@ __global__ void __launch_bounds__(kThreads, MINB) reduce_kernel(const uint32_t* 
 // Shared-memory ring of the bulk-copy reduce: per warp kRingStages stages of
 // BR gradient rows each (BR * RB <= 2 KB), the mbarriers in front.
 constexpr int kRingStages = 4;
-#ifndef FS_RING_ROWS
-#define FS_RING_ROWS 8  // most gradient rows per ring stage
-#endif
+// Most gradient rows per ring stage (stages of 4 rows, four blocks per SM:
+// no faster on the bf16 table, 0.5% slower on the f32 one).
+constexpr int kRingRows = 8;
 template <int RB>
 struct Ring {
-  static constexpr int BR = (2048 / RB) < FS_RING_ROWS ? (2048 / RB) : FS_RING_ROWS;  // rows per stage
+  static constexpr int BR = (2048 / RB) < kRingRows ? (2048 / RB) : kRingRows;  // rows per stage
   static constexpr int SPC = 32 / BR;                            // stages per 32-entry batch of keys
   static constexpr int kStageBytes = BR * RB;
   static constexpr int kWarpBytes = 128 + kRingStages * kStageBytes;
@@ -1251,16 +1263,16 @@ extern "C" fs_status fs_emb_sort_rows_sharded(int64_t num_rows, int32_t dim, fs_
   int launches = 1;
   radix::seg_tiles_kernel<<<1, radix::kSegThreads, 0, st>>>(shard_offsets, n, T, W.seg_off[0], W.tile_base[0], err);
   if (two && co_rows) {
-    const SrcShardRows<true> s1{sm_ids, pos, nullptr, co_rows, num_rows, P.block, B.kb, B.row_mask};
-    radix::run_seg_pass(s1, radix::DstU32{k1, v1}, 0, P.b1, P.b1, W, 0, B.W.pass.n_valid, nullptr, err, st,
+    const SrcShardRows<true> s1{sm_ids, nullptr, co_rows, num_rows, P.block, B.kb, B.row_mask};
+    radix::run_seg_pass(s1, DstGatherPos<int32_t>{k1, v1, pos}, 0, P.b1, P.b1, W, 0, B.W.pass.n_valid, nullptr, err, st,
                         &launches);
   } else {
-    const SrcShardRows<false> s1{sm_ids, pos, two ? is_co : nullptr, nullptr, num_rows, P.block, B.kb, B.row_mask};
-    radix::run_seg_pass(s1, radix::DstU32{k1, v1}, 0, P.b1, P.b1, W, 0, B.W.pass.n_valid, nullptr, err, st,
+    const SrcShardRows<false> s1{sm_ids, two ? is_co : nullptr, nullptr, num_rows, P.block, B.kb, B.row_mask};
+    radix::run_seg_pass(s1, DstGatherPos<int32_t>{k1, v1, pos}, 0, P.b1, P.b1, W, 0, B.W.pass.n_valid, nullptr, err, st,
                         &launches);
   }
-  const SrcShardRows2 s2{k1, v1, P.block, B.kb, B.row_mask, P.lb2, two};
-  radix::run_seg_pass(s2, radix::DstU32{B.sk, B.sv}, P.b1, P.lb2 + P.ph, P.lb2, W, 1, B.W.pass.n_valid,
+  const SrcShardRows2 s2{k1, P.block, B.kb, B.row_mask, P.lb2, two};
+  radix::run_seg_pass(s2, DstGatherPos<uint32_t>{B.sk, B.sv, v1}, P.b1, P.lb2 + P.ph, P.lb2, W, 1, B.W.pass.n_valid,
                       two ? B.n_first : nullptr, nullptr, st, &launches);
   count_launch(launches);
   return launch_status();

@@ -57,13 +57,12 @@ constexpr int kMarkSub = kMarkThreads * kMarkItems;
 constexpr int kWinWords = 12800;  // 51.2 KB: four blocks per SM
 constexpr size_t kMarkSmem = size_t(kWinWords) * sizeof(uint32_t);
 
-__device__ __forceinline__ void block_min_max(int64_t& lo, int64_t& hi, int64_t* s_lo, int64_t* s_hi) {
+__device__ __forceinline__ void block_min_max(uint32_t& lo, uint32_t& hi, uint32_t* s_lo, uint32_t* s_hi) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
-    const int64_t a = __shfl_xor_sync(0xffffffffu, lo, o), b = __shfl_xor_sync(0xffffffffu, hi, o);
-    lo = a < lo ? a : lo;
-    hi = b > hi ? b : hi;
+    lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+    hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
   }
   if (lane == 0) {
     s_lo[warp] = lo;
@@ -73,26 +72,29 @@ __device__ __forceinline__ void block_min_max(int64_t& lo, int64_t& hi, int64_t*
   lo = s_lo[0];
   hi = s_hi[0];
   for (int w = 1; w < nw; ++w) {
-    lo = s_lo[w] < lo ? s_lo[w] : lo;
-    hi = s_hi[w] > hi ? s_hi[w] : hi;
+    lo = min(lo, s_lo[w]);
+    hi = max(hi, s_hi[w]);
   }
   __syncthreads();  // s_lo / s_hi are free again
 }
 
+// Rows are below num_rows <= 2^32, so the per-ID work is 32-bit: an ID is
+// checked once in 64 bits, then handled as its row; window positions are
+// 32-bit word indices (rows / 32 < 2^27).
 __global__ void __launch_bounds__(kMarkThreads, 4) mark_window_kernel(const int64_t* __restrict__ ids, int64_t T,
                                                                      int64_t chunk, int64_t R, uint32_t* bm,
                                                                      int32_t* err) {
   extern __shared__ uint32_t win[];  // [kWinWords]
-  __shared__ int64_t s_lo[kMarkThreads / 32], s_hi[kMarkThreads / 32];
+  __shared__ uint32_t s_lo[kMarkThreads / 32], s_hi[kMarkThreads / 32];
   for (int j = threadIdx.x; j < kWinWords; j += kMarkThreads) win[j] = 0u;
   __syncthreads();
   const int64_t c0 = int64_t(blockIdx.x) * chunk;
   const int64_t c1 = (c0 + chunk < T) ? c0 + chunk : T;
   // block-uniform window state: base word (-1: no window), dirty words [dlo, dhi] relative to it
-  int64_t base = -1, dlo = kWinWords, dhi = -1;
+  int32_t base = -1, dlo = kWinWords, dhi = -1;
   auto flush = [&]() {
     if (base >= 0)
-      for (int64_t w = dlo + threadIdx.x; w <= dhi; w += kMarkThreads) {
+      for (int32_t w = dlo + int32_t(threadIdx.x); w <= dhi; w += kMarkThreads) {
         const uint32_t v = win[w];
         if (v) {
           atomicOr(bm + base + w, v);
@@ -104,39 +106,39 @@ __global__ void __launch_bounds__(kMarkThreads, 4) mark_window_kernel(const int6
   };
   int64_t nx[kMarkItems];  // the next sub-chunk's IDs, loaded while this one is marked
   auto load = [&](int64_t s0) {
+    const int64_t* p = ids + s0 + threadIdx.x;
+    const int64_t left = c1 - s0 - int64_t(threadIdx.x);  // this thread's items of the sub-chunk: i * kMarkThreads < left
 #pragma unroll
-    for (int i = 0; i < kMarkItems; ++i) {
-      const int64_t j = s0 + int64_t(i) * kMarkThreads + threadIdx.x;
-      nx[i] = j < c1 ? __ldcs(ids + j) : -1;
-    }
+    for (int i = 0; i < kMarkItems; ++i) nx[i] = int64_t(i) * kMarkThreads < left ? __ldcs(p + i * kMarkThreads) : -1;
   };
   if (c0 < c1) load(c0);
   for (int64_t s0 = c0; s0 < c1; s0 += kMarkSub) {
-    int64_t id[kMarkItems];
-#pragma unroll
-    for (int i = 0; i < kMarkItems; ++i) id[i] = nx[i];
-    if (s0 + kMarkSub < c1) load(s0 + kMarkSub);
-    int64_t lo = INT64_MAX, hi = -1;
+    uint32_t row[kMarkItems];
+    unsigned ok = 0;  // bit i: item i is a valid ID
+    uint32_t lo = 0xFFFFFFFFu, hi = 0;
+    const int64_t left = c1 - s0 - int64_t(threadIdx.x);
 #pragma unroll
     for (int i = 0; i < kMarkItems; ++i) {
-      const int64_t j = s0 + int64_t(i) * kMarkThreads + threadIdx.x;
-      if (id[i] < 0 || id[i] >= R) {
-        if (j < c1) set_err(err, FS_ERR_ID_RANGE);
-        id[i] = -1;
-        continue;
+      const int64_t id = nx[i];
+      row[i] = uint32_t(id);
+      if (id >= 0 && id < R) {
+        ok |= 1u << i;
+        lo = min(lo, row[i]);
+        hi = max(hi, row[i]);
+      } else if (int64_t(i) * kMarkThreads < left) {
+        set_err(err, FS_ERR_ID_RANGE);
       }
-      lo = id[i] < lo ? id[i] : lo;
-      hi = id[i] > hi ? id[i] : hi;
     }
+    if (s0 + kMarkSub < c1) load(s0 + kMarkSub);
     block_min_max(lo, hi, s_lo, s_hi);  // (also orders the previous sub-chunk's window updates before a flush)
-    if (hi < 0) continue;               // no valid ID in this sub-chunk
-    const int64_t lw = lo >> 5, hw = hi >> 5;
+    if (lo > hi) continue;              // no valid ID in this sub-chunk
+    const int32_t lw = int32_t(lo >> 5), hw = int32_t(hi >> 5);
     if (!(base >= 0 && lw >= base && hw < base + kWinWords)) {
       flush();
       __syncthreads();
       // the new window leaves a quarter of its slack below this sub-chunk's rows and the rest
       // above (IDs grouped by row range move upwards), so later sub-chunks of the same range fit
-      const int64_t slack = kWinWords - 1 - (hw - lw);
+      const int32_t slack = kWinWords - 1 - (hw - lw);
       base = slack >= 0 ? (lw - slack / 4 > 0 ? lw - slack / 4 : 0) : -1;
     }
     if (base >= 0) {
@@ -144,24 +146,24 @@ __global__ void __launch_bounds__(kMarkThreads, 4) mark_window_kernel(const int6
       // (same-word shared atomics of one warp would serialize)
       uint32_t cur[kMarkItems];
 #pragma unroll
-      for (int i = 0; i < kMarkItems; ++i) cur[i] = id[i] >= 0 ? win[(id[i] >> 5) - base] : ~0u;
+      for (int i = 0; i < kMarkItems; ++i) cur[i] = (ok >> i) & 1u ? win[int32_t(row[i] >> 5) - base] : ~0u;
 #pragma unroll
       for (int i = 0; i < kMarkItems; ++i) {
-        const uint32_t bit = 1u << (uint32_t(id[i]) & 31u);
-        if (id[i] >= 0 && (cur[i] & bit) == 0) atomicOr(win + ((id[i] >> 5) - base), bit);
+        const uint32_t bit = 1u << (row[i] & 31u);
+        if ((cur[i] & bit) == 0) atomicOr(win + (int32_t(row[i] >> 5) - base), bit);
       }
-      dlo = (lw - base) < dlo ? (lw - base) : dlo;
-      dhi = (hw - base) > dhi ? (hw - base) : dhi;
+      dlo = min(dlo, lw - base);
+      dhi = max(dhi, hw - base);
     } else {
       // rows too spread for the window: every word loaded first, then an atomic where the bit
       // is missing (a stale word only costs a redundant atomic)
       uint32_t cur[kMarkItems];
 #pragma unroll
-      for (int i = 0; i < kMarkItems; ++i) cur[i] = id[i] >= 0 ? bm[uint64_t(id[i]) >> 5] : ~0u;
+      for (int i = 0; i < kMarkItems; ++i) cur[i] = (ok >> i) & 1u ? bm[row[i] >> 5] : ~0u;
 #pragma unroll
       for (int i = 0; i < kMarkItems; ++i) {
-        const uint32_t bit = 1u << (uint32_t(id[i]) & 31u);
-        if (id[i] >= 0 && (cur[i] & bit) == 0) atomicOr(bm + (uint64_t(id[i]) >> 5), bit);
+        const uint32_t bit = 1u << (row[i] & 31u);
+        if ((cur[i] & bit) == 0) atomicOr(bm + (row[i] >> 5), bit);
       }
     }
   }

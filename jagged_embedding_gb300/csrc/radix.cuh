@@ -275,9 +275,7 @@ constexpr int kDownWarps = kDownThreads / 32;
 constexpr int kDownPerT = kMaxBins / kDownThreads;  // digits per thread
 static_assert(kDownThreads * kDownItems == kTile && kDownPerT >= 1, "downsweep shape");
 using HistT = uint32_t;
-#ifndef FS_BALLOT_MAX_BITS
-#define FS_BALLOT_MAX_BITS 8  // widest digit the multisplit matches by ballots
-#endif
+constexpr int kBallotMaxBits = 8;  // widest digit the multisplit matches by ballots
 
 // Index, inside its tile, of the downsweep's item i of lane `lane` in warp `warp`.
 __device__ __forceinline__ int down_index(int warp, int i, int lane) { return warp * 32 * kDownItems + i * 32 + lane; }
@@ -378,7 +376,7 @@ __global__ void __launch_bounds__(kDownThreads, DownBlocks<Src>::value) downswee
   // 3.36 -> 3.07 ms on 303M IDs), wider digits by match.any (10-bit passes
   // were slower with ballots)
   const int dbits = nb > 1 ? 32 - __clz(nb - 1) : 1;  // every digit is below nb
-  const bool by_ballot = dbits <= FS_BALLOT_MAX_BITS;
+  const bool by_ballot = dbits <= kBallotMaxBits;
 #pragma unroll
   for (int i = 0; i < kDownItems; ++i) {
     const uint32_t d = pk[i] >> 20;

@@ -25,6 +25,9 @@ op is one of
   bitmap    -- fs_row_bitmap of T bounded-Zipf(1.0) IDs over R rows, in the shard-major order the pipeline
                marks them in (fs_bucketize_rowwise into 256 row-range shards first); prints the median
                time and the bandwidth of the IDs read
+  collision -- fs_collision_split_bitmaps of two batches of T bounded-Zipf(1.0) IDs over R rows (their row
+               bitmaps built first, no masks): the compact of the collision / exclusive lists with
+               256 shard offsets; prints the median time and the list lengths
   autotune  -- VBS AutoTune with T samples over R logical ranks (lognormal(7, 1.6) lengths up to 16384,
                alpha 1.5, length-sorted cut): fs_vbs_autotune, fs_balance_vbs_tuned and the plain
                fs_balance_vbs, each timed alone (median of reps calls, CUDA events)
@@ -50,7 +53,7 @@ SHARDS = 256
 
 def main(argv) -> int:
     if len(argv) < 3 or argv[0] not in ("gather", "backward", "backward-bf16", "bucketize", "transpose",
-                                        "autotune", "gather-sorted", "prep", "sorted-step", "bitmap"):
+                                        "autotune", "gather-sorted", "prep", "sorted-step", "bitmap", "collision"):
         print(__doc__)
         return 2
     op, T, R = argv[0], int(argv[1]), int(argv[2])
@@ -71,6 +74,8 @@ def main(argv) -> int:
         return _sorted_step(ids, T, R, reps, dev, g, err)
     if op == "bitmap":
         return _bitmap(ids, T, R, reps, dev, err)
+    if op == "collision":
+        return _collision(ids, synthetic.zipf_rows(R, 1.0, T, g, dev), T, R, reps, dev, err)
     if op == "gather-sorted":
         return _gather_sorted(ids, T, R, reps, dev, g, err)
     if op == "gather":
@@ -222,6 +227,23 @@ def _bitmap(ids, T, R, reps, dev, err):
     t = _median_ms(lambda: B.fs_row_bitmap(sm, R, bitmap=bm, err=err), reps)
     B.check(err, "bitmap")
     print(f"bitmap T={T} R={R}: {t:.3f} ms, {8 * T / t / 1e6:.0f} GB/s of IDs read (median of {reps})")
+    return 0
+
+
+def _collision(a, b, T, R, reps, dev, err):
+    reps = max(reps, 5)
+    n = SHARDS
+    bma, _ = B.fs_row_bitmap(a, R, err=err)
+    bmb, _ = B.fs_row_bitmap(b, R, err=err)
+    cap = min(2 * T, R)
+    out = {k: torch.empty(cap, dtype=torch.int64, device=dev) for k in ("co", "ex_t", "ex_next")}
+    out.update({"counts": torch.zeros(3, dtype=torch.int64, device=dev)})
+    out.update({k: torch.empty(n + 1, dtype=torch.int64, device=dev) for k in ("co_off", "ex_t_off", "ex_next_off")})
+    ws = B.workspace(B.lib().fs_collision_split_bitmaps_workspace_size(R), dev)
+    t = _median_ms(lambda: B.fs_collision_split_bitmaps(a, bma, b, bmb, R, n, out, cap, err=err, ws=ws,
+                                                        want_t_mask=False, want_next_mask=False), reps)
+    B.check(err, "collision")
+    print(f"collision T={T} R={R}: {t:.3f} ms, lists {out['counts'].tolist()} (median of {reps})")
     return 0
 
 
