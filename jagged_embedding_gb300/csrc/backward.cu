@@ -980,8 +980,10 @@ bool carve_bwd(int64_t T, int64_t R, int32_t dim, fs_phase phase, void* ws, size
 // sort) sets FS_ERR_BAD_OFFSETS and is skipped.
 constexpr int kGatherThreads = 256;
 
+// (three blocks per SM: 85 registers hold the U row loads and the next
+// iteration's entries; at four blocks the spills cost more than the extra warps)
 template <int VPR>
-__global__ void __launch_bounds__(kGatherThreads) gather_sorted_kernel(const int4* __restrict__ table, int64_t R,
+__global__ void __launch_bounds__(kGatherThreads, 3) gather_sorted_kernel(const int4* __restrict__ table, int64_t R,
                                                                        const uint32_t* __restrict__ keys,
                                                                        const uint32_t* __restrict__ pos,
                                                                        const int64_t* __restrict__ n_dev, int64_t T,
@@ -996,15 +998,26 @@ __global__ void __launch_bounds__(kGatherThreads) gather_sorted_kernel(const int
   const int lane = threadIdx.x & 31;
   const int sub = lane / VPR, c = lane % VPR;
   const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
-  for (int64_t e0 = ((int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5) * RPW; e0 < n; e0 += nwarps * RPW) {
-    uint32_t my_row = 0, my_pos = 0xFFFFFFFFu;  // position all ones: no entry
-    if (lane < RPW && e0 + lane < n) {
-      my_row = __ldcs(keys + e0 + lane) & row_mask;
-      my_pos = __ldcs(pos + e0 + lane);
-      if (int64_t(my_row) >= R || int64_t(my_pos) >= T) {
-        set_err(err, FS_ERR_BAD_OFFSETS);
-        my_pos = 0xFFFFFFFFu;
-      }
+  const int64_t stride = nwarps * RPW;
+  // the keys and positions of the warp's next iteration are loaded before the
+  // current iteration's rows, so the entry stream's latency overlaps them
+  uint32_t nk = 0, np = 0xFFFFFFFFu;
+  auto load_entries = [&](int64_t e) {
+    nk = 0;
+    np = 0xFFFFFFFFu;  // position all ones: no entry
+    if (lane < RPW && e + lane < n) {
+      nk = __ldcs(keys + e + lane);
+      np = __ldcs(pos + e + lane);
+    }
+  };
+  int64_t e0 = ((int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5) * RPW;
+  load_entries(e0);
+  for (; e0 < n; e0 += stride) {
+    uint32_t my_row = nk & row_mask, my_pos = np;
+    load_entries(e0 + stride);
+    if (my_pos != 0xFFFFFFFFu && (int64_t(my_row) >= R || int64_t(my_pos) >= T)) {
+      set_err(err, FS_ERR_BAD_OFFSETS);
+      my_pos = 0xFFFFFFFFu;
     }
     int4 v[U];
     uint32_t p[U];

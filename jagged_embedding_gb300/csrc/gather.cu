@@ -116,8 +116,10 @@ __global__ void __launch_bounds__(kThreads) gather_word_kernel(const uint32_t* _
 // per lane; whole rows are written to their scattered positions.  An ID out of
 // range sets FS_ERR_ID_RANGE, a position out of [0, T) FS_ERR_BAD_OFFSETS;
 // either entry is skipped.
+// (three blocks per SM, as the row-sorted gather: room for the row loads and
+// the next iteration's entries)
 template <int VPR>
-__global__ void __launch_bounds__(kThreads) gather_scatter_kernel(const int4* __restrict__ table, int64_t R,
+__global__ void __launch_bounds__(kThreads, 3) gather_scatter_kernel(const int4* __restrict__ table, int64_t R,
                                                                   const int64_t* __restrict__ sm_ids,
                                                                   const int32_t* __restrict__ pos, int64_t T,
                                                                   int4* __restrict__ out, int32_t* err) {
@@ -128,12 +130,27 @@ __global__ void __launch_bounds__(kThreads) gather_scatter_kernel(const int4* __
   const int lane = threadIdx.x & 31;
   const int sub = lane / VPR, c = lane % VPR;
   const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
-  for (int64_t e0 = ((int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5) * RPW; e0 < T; e0 += nwarps * RPW) {
-    int64_t my_id = -1;
-    int32_t my_pos = -1;
-    if (lane < RPW && e0 + lane < T) {
-      my_id = __ldcs(sm_ids + e0 + lane);
-      my_pos = __ldcs(pos + e0 + lane);
+  const int64_t stride = nwarps * RPW;
+  // the IDs and positions of the warp's next iteration are loaded before the
+  // current iteration's rows, so the entry stream's latency overlaps them
+  int64_t nid = -1;
+  int32_t npos = -1;
+  auto load_entries = [&](int64_t e) {
+    nid = -1;
+    npos = -1;
+    if (lane < RPW && e + lane < T) {
+      nid = __ldcs(sm_ids + e + lane);
+      npos = __ldcs(pos + e + lane);
+    }
+  };
+  int64_t e0 = ((int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5) * RPW;
+  load_entries(e0);
+  for (; e0 < T; e0 += stride) {
+    int64_t my_id = nid;
+    const int32_t my_pos = npos;
+    const bool live = lane < RPW && e0 + lane < T;
+    load_entries(e0 + stride);
+    if (live) {
       if (my_id < 0 || my_id >= R) {
         set_err(err, FS_ERR_ID_RANGE);
         my_id = -1;

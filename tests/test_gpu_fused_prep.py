@@ -45,6 +45,7 @@ def _perm(L, n, kind):
     (2000, 8, 100_000, 5.0, 1.2, 2048, "fbs", 0.1),          # some empty samples
     (777, 1, 50_000, 4.0, 1.0, 1000, "fbs", 0.0),            # one rank, ragged tail
     (4096, 1024, 3_000_000, 4.0, 1.5, 4096, "fbs", 0.0),     # the most shards
+    (1024, 64, (1 << 33) + 7, 5.0, 1.2, 2048, "fbs", 0.0),    # rows beyond 2^32: 64-bit staging
     (16, 4, 1000, 1.0, 0.5, 10, "vbs", 0.0),                 # a few IDs
 ])
 def test_fused_prep_matches_oracle_and_two_calls(S, n, R, mu, sigma, lmax, kind, empty):

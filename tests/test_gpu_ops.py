@@ -813,3 +813,20 @@ def test_sorted_calls_refuse_partial_phases_and_misalignment():
     with pytest.raises(B.FsError) as e:                                    # workspace too small
         B.fs_emb_gather_sorted(Wd, T, ws[:16])
     assert e.value.code == 5
+
+
+@pytest.mark.parametrize("n,R,T", [(256, (1 << 33) + 12_345, 300_000), (7, (1 << 32) + 1, 50_001)])
+def test_bucketize_tables_of_2_32_rows_or_more(n, R, T):
+    """Tables of 2^32 rows or more keep the 64-bit staging (rows do not fit 32 bits); same parity."""
+    rng = np.random.default_rng(n + 11)
+    ids = rng.integers(0, R, T).astype(np.int64)
+    ids[: T // 10] = rng.integers((1 << 32) - 5, min(R, (1 << 32) + 5), T // 10)   # rows around 2^32
+    cuts = np.sort(rng.integers(0, T + 1, n - 1))
+    rio = np.concatenate([[0], cuts, [T]]).astype(np.int64)
+    sm, pos, splits, so, err = B.fs_bucketize_rowwise(torch.from_numpy(ids).to(DEV), torch.from_numpy(rio).to(DEV), R)
+    _check(err)
+    sm_ref, pos_ref, splits_ref, so_ref = oracle.bucketize_rowwise(ids, rio, n, R)
+    assert np.array_equal(to_np(sm), sm_ref)
+    assert np.array_equal(to_np(pos), pos_ref)
+    assert np.array_equal(to_np(splits), splits_ref)
+    assert np.array_equal(to_np(so), so_ref)
