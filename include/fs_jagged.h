@@ -78,7 +78,9 @@ typedef enum {
  *   uih_len      [S]   int32, >= 0 (negative -> FS_ERR_INVALID_ARG in *err)
  *   perm         [S]   int32 out: perm[new position] = g
  *   rank_offsets [n+1] int64 out: rank r owns new positions [ro[r], ro[r+1])
- * S in [0, 2^31), n >= 1.
+ * S in [0, 2^31), n >= 1.  Up to 16384 samples are sorted and dealt by one
+ * block in shared memory (the workspace is not touched then); larger batches
+ * use device-wide radix passes in the workspace.
  * ---------------------------------------------------------------------- */
 size_t fs_balance_fbs_workspace_size(int64_t S, int32_t n);
 fs_status fs_balance_fbs(const int32_t* uih_len, int64_t S, int32_t n, int32_t* perm, int64_t* rank_offsets,

@@ -1014,8 +1014,9 @@ __global__ void __launch_bounds__(kGatherThreads, 3) gather_sorted_kernel(const 
   load_entries(e0);
   for (; e0 < n; e0 += stride) {
     uint32_t my_row = nk & row_mask, my_pos = np;
+    const bool live = lane < RPW && e0 + lane < n;
     load_entries(e0 + stride);
-    if (my_pos != 0xFFFFFFFFu && (int64_t(my_row) >= R || int64_t(my_pos) >= T)) {
+    if (live && (int64_t(my_row) >= R || int64_t(my_pos) >= T)) {
       set_err(err, FS_ERR_BAD_OFFSETS);
       my_pos = 0xFFFFFFFFu;
     }
