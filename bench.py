@@ -530,6 +530,28 @@ def kernel_hash(call="gather", sorted_gather=False):
     return h.hexdigest()[:16]
 
 
+def gpu_numa_cpus(dev):
+    """(node, CPUs) of the host NUMA node the GPU is attached to, or None when the host does not say."""
+    try:
+        import torch
+        p = torch.cuda.get_device_properties(dev)
+        bus = "%04x:%02x:%02x.0" % (p.pci_domain_id, p.pci_bus_id, p.pci_device_id)
+        with open(f"/sys/bus/pci/devices/{bus}/numa_node") as f:
+            node = int(f.read())
+        if node < 0:
+            return None
+        with open(f"/sys/devices/system/node/node{node}/cpulist") as f:
+            cl = f.read().strip()
+        cpus = set()
+        for part in cl.split(","):
+            a, _, b = part.partition("-")
+            cpus.update(range(int(a), int(b or a) + 1))
+        cpus &= os.sched_getaffinity(0)
+        return (node, cpus) if cpus else None
+    except Exception:
+        return None
+
+
 def run_e2e(w, pipe, batches, grads, K, W, dev, ws, times=None):
     """Same steps, inputs copied from pinned host memory inside the timed region.
 
@@ -543,9 +565,19 @@ def run_e2e(w, pipe, batches, grads, K, W, dev, ws, times=None):
 
     from jagged_embedding_gb300 import binding as B
 
-    host = []
-    for b in batches:
-        host.append({k: (v.cpu().pin_memory() if torch.is_tensor(v) else v) for k, v in b.items()})
+    # pinned host copies of the batches, their pages placed (first touch) on the NUMA node the GPU is
+    # attached to when the host has more than one
+    numa = gpu_numa_cpus(dev)
+    old_aff = os.sched_getaffinity(0)
+    if numa:
+        os.sched_setaffinity(0, numa[1])
+    try:
+        host = []
+        for b in batches:
+            host.append({k: (v.cpu().pin_memory() if torch.is_tensor(v) else v) for k, v in b.items()})
+    finally:
+        if numa:
+            os.sched_setaffinity(0, old_aff)
     max_S1 = max(h["offsets"].numel() for h in host)
     max_T = pipe.max_T
     ring = [{"uih_len": torch.empty(max_S1 - 1, dtype=torch.int32, device=dev),
@@ -641,6 +673,7 @@ def run_e2e(w, pipe, batches, grads, K, W, dev, ws, times=None):
     ids_all, secs_max = aggregate(ids, secs, ws, dev)
     return {"value": ids_all / secs_max, "unit": "IDs/s", "h2d_bytes_per_step": h2d_bytes / K,
             "d2h_bytes_per_step": 32, "h2d_copy_ms_last": [round(x, 3) for x in copy_ms],
+            "host_numa_node": numa[0] if numa else None,
             "note": "batch IDs + lengths + offsets from pinned host memory, "
                     "copy of batch i+2 overlapped with step i; gradients device-resident; "
                     "h2d_copy_ms_last: durations of the last timed copies (a step waits for its batch's copy)"}
