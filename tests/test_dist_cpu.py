@@ -94,3 +94,33 @@ def test_step_times_are_seeded_and_slow_every_fourth_rank():
     assert not torch.equal(a, synthetic.step_times(w, 3))
     slow, fast = a[::4].double().mean(), torch.cat([a[1::4], a[2::4], a[3::4]]).double().mean()
     assert 1.4 < float(slow / fast) < 1.6
+
+
+def test_recorded_traffic_only_for_the_sources_it_was_taken_on(tmp_path, monkeypatch):
+    """A DRAM traffic record is printed only while the call's kernel sources hash to the recorded value."""
+    import json
+    import bench
+    src = tmp_path / "jagged_embedding_gb300" / "csrc"
+    src.mkdir(parents=True)
+    for name in ("backward.cu", "radix.cuh", "bulk.cuh", "gather.cu"):
+        (src / name).write_text(f"// {name}\n")
+    (tmp_path / "profiles").mkdir()
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    rec = {"gather/large-table-full-step": {"kernel_hash": bench.kernel_hash("gather", True), "bytes_per_launch": 7},
+           "update/large-table-full-step": {"kernel_hash": bench.kernel_hash("update", True), "bytes_per_launch": 9}}
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(rec))
+    assert bench.recorded_traffic("gather", "large-table-full-step", True) == 7
+    assert bench.recorded_traffic("update", "large-table-full-step", True) == 9
+    assert bench.recorded_traffic("gather", "mid-full-step", True) is None         # no record for that workload
+    (src / "backward.cu").write_text("// changed\n")                             # the gather and update kernels' file
+    assert bench.recorded_traffic("gather", "large-table-full-step", True) is None
+    assert bench.recorded_traffic("update", "large-table-full-step", True) is None
+    (src / "backward.cu").write_text("// backward.cu\n")
+    (src / "bulk.cuh").write_text("// changed\n")                                # the update's only
+    assert bench.recorded_traffic("gather", "large-table-full-step", True) == 7
+    assert bench.recorded_traffic("update", "large-table-full-step", True) is None
+
+
+def test_gpu_numa_node_without_a_device_is_none():
+    import bench
+    assert bench.gpu_numa_cpus(0) is None or isinstance(bench.gpu_numa_cpus(0)[1], set)
