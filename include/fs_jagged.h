@@ -464,6 +464,9 @@ fs_status fs_emb_sort_rows_sharded(int64_t num_rows, int32_t dim, fs_dtype dtype
  * fs_set_spin_limit: polls before a bounded inter-block wait gives up with
  *   FS_ERR_TIMEOUT (default 1<<22, roughly a second); a wait for a bulk copy
  *   of gradient rows gives up after polls * 256 ns.  Applies to later calls.
+ *   The Python binding applies the environment variable FS_SPIN_LIMIT (a
+ *   positive integer) when it loads the library.
+ * fs_get_spin_limit: the limit in force.
  * fs_launch_count: kernels this library has launched in this process.
  * fs_debug_skip_publish: test hook for the bounded waits.  Tile `tile` of the
  *   single-pass scans (VBS weights, permute offsets, collision compaction)
@@ -476,6 +479,7 @@ fs_status fs_emb_sort_rows_sharded(int64_t num_rows, int32_t dim, fs_dtype dtype
 fs_status fs_check(const int32_t* err, fs_stream_t stream);
 const char* fs_status_string(fs_status s);
 void fs_set_spin_limit(int64_t polls);
+int64_t fs_get_spin_limit(void);
 void fs_debug_skip_publish(int64_t tile);
 int64_t fs_launch_count(void);
 const char* fs_version(void);

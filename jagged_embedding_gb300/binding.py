@@ -40,7 +40,7 @@ EXPORTS = [
     "fs_emb_backward_adagrad_workspace_size", "fs_emb_backward_adagrad", "fs_emb_sort_rows",
     "fs_emb_gather_sorted", "fs_emb_update_sorted", "fs_emb_sort_rows_sharded_workspace_size",
     "fs_emb_sort_rows_sharded", "fs_check", "fs_status_string",
-    "fs_set_spin_limit", "fs_debug_skip_publish", "fs_launch_count", "fs_version",
+    "fs_set_spin_limit", "fs_get_spin_limit", "fs_debug_skip_publish", "fs_launch_count", "fs_version",
 ]
 
 
@@ -99,6 +99,7 @@ def lib():
         "fs_check": ([P, P], C.c_int),
         "fs_status_string": ([C.c_int], C.c_char_p),
         "fs_set_spin_limit": ([i64], None),
+        "fs_get_spin_limit": ([], i64),
         "fs_debug_skip_publish": ([i64], None),
         "fs_launch_count": ([], i64),
         "fs_version": ([], C.c_char_p),
@@ -107,6 +108,15 @@ def lib():
         fn = getattr(L, name)
         fn.argtypes = args
         fn.restype = res
+    env = os.environ.get("FS_SPIN_LIMIT")
+    if env:  # bounded waits: polls before giving up with FS_ERR_TIMEOUT
+        try:
+            polls = int(env)
+        except ValueError:
+            raise FsError(1, f"FS_SPIN_LIMIT={env!r} is not an integer") from None
+        if polls < 1:
+            raise FsError(1, f"FS_SPIN_LIMIT={env!r} must be positive")
+        L.fs_set_spin_limit(polls)
     _lib = L
     return L
 
@@ -165,6 +175,10 @@ def launch_count():
 
 def set_spin_limit(polls):
     lib().fs_set_spin_limit(int(polls))
+
+
+def spin_limit():
+    return int(lib().fs_get_spin_limit())
 
 
 def debug_skip_publish(tile):

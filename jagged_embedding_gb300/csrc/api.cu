@@ -59,6 +59,8 @@ extern "C" const char* fs_status_string(fs_status s) {
 
 extern "C" void fs_set_spin_limit(int64_t polls) { fs::g_spin_limit.store(polls < 1 ? 1 : polls); }
 
+extern "C" int64_t fs_get_spin_limit(void) { return fs::g_spin_limit.load(); }
+
 extern "C" void fs_debug_skip_publish(int64_t tile) { fs::g_skip_tile.store(tile); }
 
 extern "C" int64_t fs_launch_count(void) { return fs::g_launches.load(); }

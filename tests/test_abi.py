@@ -168,3 +168,32 @@ def test_profiling_cases_print_usage_without_arguments():
     import profile_cases
     assert profile_cases.main([]) == 2
     assert profile_cases.main(["nosuchop", "1", "1"]) == 2
+
+
+def _spin_limit_in_child(env_value):
+    import subprocess
+    import sys
+    env = dict(os.environ)
+    env.pop("FS_SPIN_LIMIT", None)
+    if env_value is not None:
+        env["FS_SPIN_LIMIT"] = env_value
+    code = ("from jagged_embedding_gb300 import binding as B\n"
+            "try:\n    print(B.spin_limit())\nexcept B.FsError as e:\n    print('error', e.code)\n")
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr
+    return r.stdout.split()
+
+
+def test_spin_limit_from_the_environment():
+    """FS_SPIN_LIMIT sets the bounded waits' poll limit when the binding loads the library."""
+    assert _spin_limit_in_child(None) == [str(1 << 22)]
+    assert _spin_limit_in_child("12345") == ["12345"]
+    assert _spin_limit_in_child("0") == ["error", "1"]
+    assert _spin_limit_in_child("many") == ["error", "1"]
+    L = B.lib()
+    before = L.fs_get_spin_limit()
+    try:
+        L.fs_set_spin_limit(-5)                     # clamped to one poll
+        assert L.fs_get_spin_limit() == 1
+    finally:
+        L.fs_set_spin_limit(before)
