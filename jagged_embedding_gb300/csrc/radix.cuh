@@ -385,7 +385,11 @@ __global__ void __launch_bounds__(kDownThreads, DownBlocks<Src>::value) downswee
     if (by_ballot) {
       const unsigned sk = __ballot_sync(0xffffffffu, skip);  // skipped items match each other only
       peers = skip ? sk : ~sk;
-      for (int b = 0; b < dbits; ++b) {
+      // all kBallotMaxBits bits, unrolled: a kept digit is below nb, so its
+      // bits from dbits up are zero, and those ballots change no kept lane's
+      // peers (the skip ballot already set the skipped lanes apart)
+#pragma unroll
+      for (int b = 0; b < kBallotMaxBits; ++b) {
         const bool on = (d >> b) & 1u;
         const unsigned m = __ballot_sync(0xffffffffu, on);
         peers &= on ? m : ~m;
