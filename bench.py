@@ -33,6 +33,7 @@ if ROOT not in sys.path:
 METRIC = "jagged IDs/s (balance+bucketize+collision+gather+update); % of HBM roofline"
 DEFAULT_WORKLOAD = "large-table-full-step"
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 7900.0  # the vendor's HBM3e figure for GB300 (context beside the measured peak)
 
 
 # --------------------------------------------------------------------------- helpers
@@ -44,6 +45,16 @@ def measured_peaks():
             d = json.load(f)
         return float(d.get("hbm_gbs", FALLBACK_HBM_GBS)), "measured"
     return FALLBACK_HBM_GBS, "fallback"
+
+
+def step_roofline(by_stage, K, secs, hbm_gbs):
+    """Whole-step roofline keys of the result line: bytes per step by stage (summed over the K timed
+    steps in `by_stage`), and the fraction of the measured and of the nominal HBM bandwidth."""
+    total = sum(by_stage.values())
+    return {"hbm_roofline_frac_step": total / secs / (hbm_gbs * 1e9),
+            "hbm_nominal_frac_step": total / secs / (NOMINAL_HBM_GBS * 1e9),
+            "algorithmic_bytes_per_step": total / K,
+            "algorithmic_bytes_per_step_by_stage": {k: v / K for k, v in by_stage.items()}}
 
 
 def algorithmic_bytes(w, S, T, U, R, n_cand=0, masks=False):
@@ -420,13 +431,14 @@ def run_gpu(args):
         del out
     torch.cuda.synchronize()
     hbm_gbs, peak_kind = measured_peaks()
-    step_bytes = 0.0
+    by_stage = {}
     gbytes = 0.0
     ubytes = 0.0
     for t in step_batches:
         n_cand = int(batches[t]["cand_offsets"][-1]) if w.composite else 0
         bb = algorithmic_bytes(w, w.S, Ts[t], U[t], w.R, n_cand, masks=prio)
-        step_bytes += sum(bb.values())
+        for k, v in bb.items():
+            by_stage[k] = by_stage.get(k, 0.0) + v
         gbytes += gather_bytes(w, Ts[t], U[t])
         ubytes += bb.get("backward", 0.0)
     gbytes /= K
@@ -463,8 +475,7 @@ def run_gpu(args):
         "metric": METRIC, "value": value, "unit": "IDs/s", "n_gpus": ws, "steps": K, "warmup": W,
         "ms_per_step": 1000.0 * secs_max / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": f"int64/{w.dtype}", "data": "synthetic", "config": cfg,
-        "hbm_roofline_frac_step": step_bytes / secs / (hbm_gbs * 1e9),
-        "algorithmic_bytes_per_step": step_bytes / K,
+        **step_roofline(by_stage, K, secs, hbm_gbs),
         "roofline": None, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clk,
     }
     if not prio:

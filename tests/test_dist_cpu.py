@@ -84,6 +84,24 @@ def test_algorithmic_bytes_autotune_and_config():
     assert bench.algorithmic_bytes(big, big.S, 10, 3, big.R)["backward"] == 264 * 10 + 520 * 3
 
 
+def test_step_roofline_keys():
+    import bench
+    from jagged_embedding_gb300 import synthetic
+    w = synthetic.WORKLOADS["large-table-full-step"]
+    by_stage = {}
+    for T, U in ((3.0e8, 3.7e7), (3.1e8, 3.8e7)):      # two timed steps
+        for k, v in bench.algorithmic_bytes(w, w.S, T, U, w.R).items():
+            by_stage[k] = by_stage.get(k, 0.0) + v
+    total = sum(by_stage.values())
+    secs = 0.08
+    r = bench.step_roofline(by_stage, 2, secs, 6666.6)
+    assert r["algorithmic_bytes_per_step"] == total / 2
+    assert abs(sum(r["algorithmic_bytes_per_step_by_stage"].values()) - total / 2) <= 1e-6 * total
+    assert set(r["algorithmic_bytes_per_step_by_stage"]) == {"prep", "collision", "gather", "backward"}
+    assert r["hbm_roofline_frac_step"] == total / secs / 6666.6e9
+    assert abs(r["hbm_nominal_frac_step"] / r["hbm_roofline_frac_step"] - 6666.6 / 7900.0) < 1e-12
+
+
 def test_step_times_are_seeded_and_slow_every_fourth_rank():
     import torch
 
